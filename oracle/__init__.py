@@ -1,0 +1,17 @@
+"""CPU oracle for the dequant-GEMV path (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference legs may import this package.  The CUDA library never calls it and
+shares no code with it.
+"""
+from .ggml_oracle import (  # noqa: F401
+    fp16_bits_to_f64,
+    q8_0_dequant,
+    q4k_scales_mins,
+    q4k_dequant,
+    gemv,
+    silu,
+    swiglu,
+    ffn_residual,
+    gemm_batch,
+)

@@ -1,0 +1,367 @@
+"""Pins for the CPU oracle: each check ties it to something other than itself.
+
+* IEEE binary16 decoding: exhaustive against numpy's float16, plus hand-worked
+  values from the binary16 definition (tests/golden/fp16_special_values.txt).
+* Q8_0 dequant: hand-built blocks with closed-form values (column mapping,
+  sign, extremes -128/127, negative scale).
+* Q4_K dequant: hand-worked scale/min byte patterns
+  (tests/golden/q4k_scale_fields.txt), a field-wise encoder written from the
+  layout description (round trip), one-hot scale/min superblocks that light
+  exactly one sub-block, and a nibble-order pattern.
+* GEMV: one-hot x extracts a column of a non-square W (catches transposes);
+  exact rational (fractions.Fraction) dot products on tiny shapes; linearity.
+* SwiGLU / FFN: silu identities and closed forms; one-hot W_up rows; W_down = 0
+  gives the residual exactly; identity W_down gives residual + mid.
+* Batch GEMM: M = 1 equals the GEMV; permuting X rows permutes Y rows.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from conftest import GOLDEN
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+# ---------------------------------------------------------------- fp16 decode
+
+def test_fp16_decoder_exhaustive_against_numpy():
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = oracle.fp16_bits_to_f64(bits)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # signed zeros keep their sign
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_fp16_decoder_golden_values():
+    rows = []
+    with open(os.path.join(GOLDEN, "fp16_special_values.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            b, v = line.split()
+            rows.append((int(b, 16), float(v)))
+    got = oracle.fp16_bits_to_f64(np.array([b for b, _ in rows], dtype=np.uint16))
+    for (b, v), g in zip(rows, got):
+        if math.isnan(v):
+            assert math.isnan(g), hex(b)
+        else:
+            assert g == v and math.copysign(1, g) == math.copysign(1, v), (hex(b), g, v)
+
+
+# ---------------------------------------------------------------- Q8_0
+
+def _q8_block(d_bits: int, q):
+    q = np.asarray(q, dtype=np.int64)
+    assert q.shape == (32,)
+    return np.concatenate([[d_bits & 0xFF, d_bits >> 8], (q & 0xFF)]).astype(np.uint8)
+
+
+def test_q8_0_unit_scale_block():
+    # d = 1.0 (0x3c00), q[k] = k - 16  ->  weight k = k - 16
+    blk = _q8_block(0x3C00, np.arange(32) - 16)
+    w = oracle.q8_0_dequant(blk[None, :], 1, 32)
+    assert w.dtype == np.float32
+    assert np.array_equal(w[0], np.arange(32, dtype=np.float32) - 16)
+
+
+def test_q8_0_full_int8_range_power_of_two_scale():
+    # d = 2^-10 (0x1400); q runs over all of int8 including -128 -> q * 2^-10 exactly
+    qs = np.arange(-128, 128)
+    row = np.concatenate([_q8_block(0x1400, qs[32 * b: 32 * b + 32]) for b in range(8)])
+    w = oracle.q8_0_dequant(row[None, :], 1, 256)
+    assert np.array_equal(w[0], (qs * 2.0 ** -10).astype(np.float32))
+
+
+def test_q8_0_column_mapping_and_sign():
+    # 2 rows x 64 cols; block b of row r has its own scale; element k of block b is column 32b+k
+    scales = {(0, 0): (0x3C00, 1.0), (0, 1): (0x4000, 2.0), (1, 0): (0xBC00, -1.0), (1, 1): (0x3800, 0.5)}
+    rows = []
+    for r in range(2):
+        blocks = []
+        for b in range(2):
+            q = (np.arange(32) + 1) * (1 if b == 0 else -1) + 10 * r
+            blocks.append(_q8_block(scales[(r, b)][0], q))
+        rows.append(np.concatenate(blocks))
+    w = oracle.q8_0_dequant(np.stack(rows), 2, 64)
+    for r in range(2):
+        for b in range(2):
+            q = (np.arange(32) + 1) * (1 if b == 0 else -1) + 10 * r
+            assert np.array_equal(w[r, 32 * b: 32 * b + 32], (scales[(r, b)][1] * q).astype(np.float32))
+
+
+def test_q8_0_extremes_exact():
+    # largest |d| and |q|: 65504 * -128 is exact in f32
+    blk = _q8_block(0x7BFF, np.array([-128, 127] + [0] * 30))
+    w = oracle.q8_0_dequant(blk[None, :], 1, 32)
+    assert w[0, 0] == np.float32(-8384512.0) and w[0, 1] == np.float32(65504.0 * 127)
+
+
+# ---------------------------------------------------------------- Q4_K
+
+def _golden_scale_rows():
+    out = []
+    with open(os.path.join(GOLDEN, "q4k_scale_fields.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            b, sc, m = [p.strip() for p in line.split("|")]
+            out.append((np.array([int(t, 16) for t in b.split()], dtype=np.uint8),
+                        [int(t) for t in sc.split()], [int(t) for t in m.split()]))
+    return out
+
+
+@pytest.mark.parametrize("row", range(20))
+def test_q4k_scale_fields_golden(row):
+    b, sc, m = _golden_scale_rows()[row]
+    got_sc, got_m = oracle.q4k_scales_mins(b[None, :])
+    assert list(got_sc[0]) == sc and list(got_m[0]) == m
+
+
+def _encode_scale_fields(sc, m):
+    """Field-wise encoder written from the placement description (not by inverting the decoder)."""
+    out = [0] * 12
+    for j in range(8):
+        if j < 4:
+            out[j] |= sc[j] & 63
+            out[4 + j] |= m[j] & 63
+        else:
+            lo_sc, hi_sc = sc[j] & 15, sc[j] >> 4
+            lo_m, hi_m = m[j] & 15, m[j] >> 4
+            out[8 + (j - 4)] |= lo_sc | (lo_m << 4)
+            out[j - 4] |= hi_sc << 6
+            out[4 + (j - 4)] |= hi_m << 6
+    return np.array(out, dtype=np.uint8)
+
+
+def test_q4k_scale_fields_roundtrip_random():
+    rng = np.random.default_rng(1234)
+    for _ in range(500):
+        sc = rng.integers(0, 64, 8)
+        m = rng.integers(0, 64, 8)
+        got_sc, got_m = oracle.q4k_scales_mins(_encode_scale_fields(sc, m)[None, :])
+        assert np.array_equal(got_sc[0], sc) and np.array_equal(got_m[0], m)
+
+
+def _q4k_superblock(d_bits, dmin_bits, scales12, qs128):
+    return np.concatenate([[d_bits & 0xFF, d_bits >> 8, dmin_bits & 0xFF, dmin_bits >> 8],
+                           scales12, qs128]).astype(np.uint8)
+
+
+def _nibble_pattern():
+    # byte i: low nibble = i % 16, high nibble = 15 - i % 16
+    i = np.arange(128)
+    return ((i % 16) | ((15 - i % 16) << 4)).astype(np.uint8)
+
+
+def _expected_q_of_pattern():
+    q = np.empty(256, dtype=np.int64)
+    for c in range(4):
+        for l in range(32):
+            q[64 * c + l] = (32 * c + l) % 16
+            q[64 * c + 32 + l] = 15 - (32 * c + l) % 16
+    return q
+
+
+@pytest.mark.parametrize("j", range(8))
+@pytest.mark.parametrize("v", [1, 37, 63])
+def test_q4k_one_hot_scale_lights_one_subblock(j, v):
+    sc = [0] * 8
+    sc[j] = v
+    sb = _q4k_superblock(0x3C00, 0x3C00, _encode_scale_fields(sc, [0] * 8), _nibble_pattern())
+    w = oracle.q4k_dequant(sb[None, :], 1, 256)[0]
+    q = _expected_q_of_pattern()
+    expect = np.zeros(256)
+    expect[32 * j: 32 * j + 32] = v * q[32 * j: 32 * j + 32]
+    assert np.array_equal(w, expect.astype(np.float32))
+
+
+@pytest.mark.parametrize("j", range(8))
+def test_q4k_one_hot_min_lights_one_subblock(j):
+    m = [0] * 8
+    m[j] = 63
+    # d = 1, dmin = 0.5, all scales 0  ->  weight = -0.5 * 63 in sub-block j, 0 elsewhere
+    sb = _q4k_superblock(0x3C00, 0x3800, _encode_scale_fields([0] * 8, m), _nibble_pattern())
+    w = oracle.q4k_dequant(sb[None, :], 1, 256)[0]
+    expect = np.zeros(256)
+    expect[32 * j: 32 * j + 32] = -0.5 * 63
+    assert np.array_equal(w, expect.astype(np.float32))
+
+
+def test_q4k_nibble_order_and_formula():
+    # all sc = 1, m = 2, d = 2, dmin = 0.25: weight = 2*q - 0.5 with q from the pattern
+    sb = _q4k_superblock(0x4000, 0x3400, _encode_scale_fields([1] * 8, [2] * 8), _nibble_pattern())
+    w = oracle.q4k_dequant(sb[None, :], 1, 256)[0]
+    assert np.array_equal(w, (2.0 * _expected_q_of_pattern() - 0.5).astype(np.float32))
+
+
+def test_q4k_multi_superblock_rows():
+    # 2 rows x 2 superblocks with distinct d: superblock s of row r covers columns 256s..256s+255
+    d_bits = [[0x3C00, 0x4000], [0x3800, 0xBC00]]
+    d_val = [[1.0, 2.0], [0.5, -1.0]]
+    rows = []
+    for r in range(2):
+        rows.append(np.concatenate([
+            _q4k_superblock(d_bits[r][s], 0x0000, _encode_scale_fields([3] * 8, [0] * 8), _nibble_pattern())
+            for s in range(2)]))
+    w = oracle.q4k_dequant(np.stack(rows), 2, 512)
+    q = _expected_q_of_pattern()
+    for r in range(2):
+        for s in range(2):
+            assert np.array_equal(w[r, 256 * s: 256 * s + 256], (d_val[r][s] * 3 * q).astype(np.float32))
+
+
+def test_q4k_subtraction_rounds_once_in_f32():
+    # a = d*sc*q and b = dmin*m chosen so that a - b needs more than 24 bits:
+    # d = 2^-14 (0x0400), sc = 63, q = 15 -> a = 945 * 2^-14; dmin = 65504 (0x7bff), m = 63
+    sc = [63] * 8
+    m = [63] * 8
+    qs = np.full(128, 0xFF, dtype=np.uint8)
+    sb = _q4k_superblock(0x0400, 0x7BFF, _encode_scale_fields(sc, m), qs)
+    w = oracle.q4k_dequant(sb[None, :], 1, 256)[0]
+    a = Fraction(945, 2 ** 14)
+    b = Fraction(65504 * 63)
+    expect = _round_to_f32(a - b)
+    assert Fraction(float(expect)) != a - b              # the difference is not representable
+    assert np.all(w == expect)
+
+
+def _round_to_f32(fr: Fraction) -> np.float32:
+    """Round an exact rational to the nearest f32 (ties to even), by comparing exact distances."""
+    f = np.float32(float(fr))
+    best = None
+    for c in (np.nextafter(f, np.float32(-np.inf)), f, np.nextafter(f, np.float32(np.inf))):
+        dist = abs(Fraction(float(c)) - fr)
+        even = (int(np.array(c).view(np.uint32)) & 1) == 0
+        key = (dist, not even)
+        if best is None or key < best[0]:
+            best = (key, c)
+    return best[1]
+
+
+# ---------------------------------------------------------------- GEMV
+
+def _small_q8(n_out, n_in, seed):
+    return oracle.q8_0_dequant(synth.q8_0_blocks(np.random.default_rng(seed), n_out, n_in), n_out, n_in)
+
+
+def _small_q4k(n_out, n_in, seed):
+    return oracle.q4k_dequant(synth.q4k_blocks(np.random.default_rng(seed), n_out, n_in), n_out, n_in)
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4k"])
+def test_gemv_one_hot_extracts_column(fmt):
+    n_out, n_in = (5, 96) if fmt == "q8_0" else (3, 512)
+    w = _small_q8(n_out, n_in, 7) if fmt == "q8_0" else _small_q4k(n_out, n_in, 7)
+    for k in [0, 1, n_in // 2 + 3, n_in - 1]:
+        x = np.zeros((1, n_in), np.float32)
+        x[0, k] = 1.0
+        y, a = oracle.gemv(w, x)
+        assert np.array_equal(y[0], w[:, k].astype(np.float64))
+        assert np.array_equal(a[0], np.abs(w[:, k]).astype(np.float64))
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4k"])
+def test_gemv_exact_rational_tiny(fmt):
+    n_out, n_in = (3, 64) if fmt == "q8_0" else (2, 256)
+    w = _small_q8(n_out, n_in, 11) if fmt == "q8_0" else _small_q4k(n_out, n_in, 11)
+    x = synth.activations(np.random.default_rng(3), 2, n_in)
+    y, a = oracle.gemv(w, x)
+    for b in range(2):
+        for r in range(n_out):
+            exact = sum(Fraction(float(w[r, k])) * Fraction(float(x[b, k])) for k in range(n_in))
+            exact_a = sum(abs(Fraction(float(w[r, k])) * Fraction(float(x[b, k]))) for k in range(n_in))
+            assert abs(Fraction(y[b, r]) - exact) <= Fraction(exact_a) * Fraction(1, 2 ** 45)
+            assert abs(Fraction(a[b, r]) - exact_a) <= Fraction(exact_a) * Fraction(1, 2 ** 45)
+
+
+def test_gemv_linearity():
+    w = _small_q8(17, 160, 5)
+    rng = np.random.default_rng(9)
+    x1 = synth.activations(rng, 1, 160)
+    x2 = synth.activations(rng, 1, 160)
+    y1, a1 = oracle.gemv(w, x1)
+    y2, a2 = oracle.gemv(w, x2)
+    y12, _ = oracle.gemv(w, 2.0 * x1.astype(np.float64) - 0.5 * x2.astype(np.float64))
+    assert np.all(np.abs(y12 - (2.0 * y1 - 0.5 * y2)) <= 1e-12 * (2 * a1 + 0.5 * a2))
+
+
+def test_gemv_batch_rows_are_independent():
+    w = _small_q4k(4, 256, 2)
+    x = synth.activations(np.random.default_rng(4), 3, 256)
+    yb, ab = oracle.gemv(w, x)
+    for b in range(3):
+        y, a = oracle.gemv(w, x[b:b + 1])
+        assert np.array_equal(yb[b], y[0]) and np.array_equal(ab[b], a[0])
+
+
+# ---------------------------------------------------------------- SwiGLU / FFN
+
+def test_silu_closed_forms():
+    z = np.array([0.0, math.log(3.0), -math.log(3.0), 40.0, -800.0, 1.0])
+    s = oracle.silu(z)
+    assert s[0] == 0.0
+    assert abs(s[1] - 0.75 * math.log(3.0)) <= 1e-15          # sigmoid(ln 3) = 3/4
+    assert abs(s[2] + 0.25 * math.log(3.0)) <= 1e-15          # sigmoid(-ln 3) = 1/4
+    assert abs(s[3] - 40.0) <= 40.0 * 1e-15
+    assert s[4] <= 0.0 and abs(s[4]) < 1e-300
+    # silu(z) - silu(-z) = z for any z
+    zz = np.linspace(-30, 30, 601)
+    assert np.all(np.abs(oracle.silu(zz) - oracle.silu(-zz) - zz) <= 1e-13 * (1 + np.abs(zz)))
+
+
+def test_swiglu_one_hot_up_rows():
+    n_ff, n_embd = 8, 256
+    wg = _small_q4k(n_ff, n_embd, 21)
+    wu = np.zeros((n_ff, n_embd), np.float32)
+    cols = [5, 0, 255, 17, 100, 3, 64, 128]
+    for i, k in enumerate(cols):
+        wu[i, k] = 1.0
+    x = synth.activations(np.random.default_rng(22), 1, n_embd)
+    s = oracle.swiglu(wg, wu, x)
+    g, _ = oracle.gemv(wg, x)
+    for i, k in enumerate(cols):
+        gi = g[0, i]
+        assert s["u"][0, i] == float(x[0, k])
+        assert abs(s["mid"][0, i] - gi / (1.0 + math.exp(-gi)) * float(x[0, k])) <= 1e-15 * abs(gi * x[0, k]) + 1e-300
+
+
+def test_ffn_zero_down_gives_residual_exactly():
+    n_embd, n_ff = 256, 512
+    wg, wu = _small_q4k(n_ff, n_embd, 31), _small_q4k(n_ff, n_embd, 32)
+    wd = np.zeros((n_embd, n_ff), np.float32)
+    x, res = (synth.activations(np.random.default_rng(s), 1, n_embd) for s in (33, 34))
+    o = oracle.ffn_residual(wg, wu, wd, x, res)
+    assert np.array_equal(o["out"], res.astype(np.float64))
+
+
+def test_ffn_identity_down_gives_residual_plus_mid():
+    n = 256
+    wg, wu = _small_q4k(n, n, 41), _small_q4k(n, n, 42)
+    wd = np.eye(n, dtype=np.float32)
+    x, res = (synth.activations(np.random.default_rng(s), 1, n) for s in (43, 44))
+    o = oracle.ffn_residual(wg, wu, wd, x, res)
+    assert np.array_equal(o["out"], res.astype(np.float64) + o["mid"])
+
+
+# ---------------------------------------------------------------- batch GEMM
+
+def test_gemm_batch_m1_equals_gemv_and_permutes_rows():
+    w = _small_q8(24, 128, 51)
+    x = synth.activations(np.random.default_rng(52), 9, 128)
+    y, a = oracle.gemm_batch(w, x)
+    y1, _ = oracle.gemv(w, x[4:5])
+    assert np.array_equal(y[4], y1[0])
+    perm = np.random.default_rng(53).permutation(9)
+    yp, ap = oracle.gemm_batch(w, x[perm])
+    assert np.array_equal(yp, y[perm]) and np.array_equal(ap, a[perm])
