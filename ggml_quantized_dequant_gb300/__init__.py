@@ -1,0 +1,200 @@
+"""Python binding of the qdq CUDA library (libqdq.so): argument marshalling only.
+
+Every function here takes torch CUDA tensors (or raw device pointers as ints),
+passes their addresses, sizes and the current CUDA stream to the C ABI declared
+in ``include/qdq.h``, and raises :class:`QdqError` on a non-zero status.  All
+arithmetic runs in the CUDA kernels; there is no CPU path.  The library is
+built in-tree by ``__graft_entry__.build()`` (or ``python -m
+ggml_quantized_dequant_gb300._build``); loading fails loudly if it is absent.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqdq.so")
+
+QDQ_OK = 0
+QDQ_ERR_NULL = -1
+QDQ_ERR_DIMS = -2
+QDQ_ERR_ALIGN = -3
+QDQ_ERR_UNSUPPORTED = -4
+QDQ_ERR_CUDA = -5
+QDQ_ERR_ALIAS = -6
+QDQ_MAX_GEMV_BATCH = 8
+QDQ_MAX_GEMV_N_IN = 49152
+QDQ_OPT_PDL = 1
+QDQ_OPT_L2_PREFETCH = 2
+QDQ_OPT_CTAS_PER_SM = 3
+
+_c_int, _c_size, _c_vp, _c_char_p = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_char_p
+
+# name -> (restype, argtypes); mirrors include/qdq.h
+SIGNATURES = {
+    "qdq_status_string": (_c_char_p, [_c_int]),
+    "qdq_last_cuda_error": (_c_int, []),
+    "qdq_version": (_c_char_p, []),
+    "qdq_q8_0_packed_bytes": (_c_size, [_c_int, _c_int]),
+    "qdq_q4k_packed_bytes": (_c_size, [_c_int, _c_int]),
+    "qdq_q8_0_pack": (_c_int, [_c_vp, _c_vp, _c_int, _c_int, _c_vp]),
+    "qdq_q4k_pack": (_c_int, [_c_vp, _c_vp, _c_int, _c_int, _c_vp]),
+    "qdq_q8_0_dequant": (_c_int, [_c_vp, _c_vp, _c_int, _c_int, _c_vp]),
+    "qdq_q4k_dequant": (_c_int, [_c_vp, _c_vp, _c_int, _c_int, _c_vp]),
+    "qdq_q8_0_gemv": (_c_int, [_c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_vp]),
+    "qdq_q4k_gemv": (_c_int, [_c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_vp]),
+    "qdq_q4k_swiglu": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_vp]),
+    "qdq_q4k_ffn_residual": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                      _c_int, _c_int, _c_int, _c_vp]),
+    "qdq_q8_0_gemm_batch_workspace_bytes": (_c_size, [_c_int, _c_int]),
+    "qdq_q8_0_gemm_batch": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_vp]),
+    "qdq_pipeline_timeouts": (_c_int, []),
+    "qdq_set_option": (_c_int, [_c_int, _c_int]),
+}
+
+_lib = None
+
+
+class QdqError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        msg = "%s failed: %s" % (fn, status_string(status))
+        if status == QDQ_ERR_CUDA and _lib is not None:
+            msg += " (cudaError %d)" % _lib.qdq_last_cuda_error()
+        super().__init__(msg)
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libqdq.so (once) and declare every entry point's signature."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError("libqdq.so is not built (%s); run __graft_entry__.build()" % p)
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def lib() -> ctypes.CDLL:
+    return load()
+
+
+def status_string(status: int) -> str:
+    if _lib is None:
+        return str(status)
+    return _lib.qdq_status_string(int(status)).decode()
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return int(t.data_ptr())
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream) or None
+    if isinstance(stream, int):
+        return stream or None
+    return int(stream.cuda_stream) or None
+
+
+def _check(name: str, status: int):
+    if status != QDQ_OK:
+        raise QdqError(name, status)
+
+
+# ---------------------------------------------------------------- C-ABI mirrors
+
+def q8_0_packed_bytes(n_out: int, n_in: int) -> int:
+    return int(lib().qdq_q8_0_packed_bytes(n_out, n_in))
+
+
+def q4k_packed_bytes(n_out: int, n_in: int) -> int:
+    return int(lib().qdq_q4k_packed_bytes(n_out, n_in))
+
+
+def q8_0_pack(ggml, packed, n_out: int, n_in: int, stream=None):
+    _check("qdq_q8_0_pack", lib().qdq_q8_0_pack(_ptr(ggml), _ptr(packed), n_out, n_in, _stream(stream)))
+
+
+def q4k_pack(ggml, packed, n_out: int, n_in: int, stream=None):
+    _check("qdq_q4k_pack", lib().qdq_q4k_pack(_ptr(ggml), _ptr(packed), n_out, n_in, _stream(stream)))
+
+
+def q8_0_dequant(W, out, n_out: int, n_in: int, stream=None):
+    _check("qdq_q8_0_dequant", lib().qdq_q8_0_dequant(_ptr(W), _ptr(out), n_out, n_in, _stream(stream)))
+
+
+def q4k_dequant(W, out, n_out: int, n_in: int, stream=None):
+    _check("qdq_q4k_dequant", lib().qdq_q4k_dequant(_ptr(W), _ptr(out), n_out, n_in, _stream(stream)))
+
+
+def q8_0_gemv(W, x, y, n_out: int, n_in: int, batch: int = 1, stream=None):
+    _check("qdq_q8_0_gemv", lib().qdq_q8_0_gemv(_ptr(W), _ptr(x), _ptr(y), n_out, n_in, batch, _stream(stream)))
+
+
+def q4k_gemv(W, x, y, n_out: int, n_in: int, batch: int = 1, stream=None):
+    _check("qdq_q4k_gemv", lib().qdq_q4k_gemv(_ptr(W), _ptr(x), _ptr(y), n_out, n_in, batch, _stream(stream)))
+
+
+def q4k_swiglu(Wg, Wu, x, mid, n_ff: int, n_embd: int, batch: int = 1, stream=None):
+    _check("qdq_q4k_swiglu", lib().qdq_q4k_swiglu(_ptr(Wg), _ptr(Wu), _ptr(x), _ptr(mid), n_ff, n_embd, batch,
+                                                  _stream(stream)))
+
+
+def q4k_ffn_residual(Wg, Wu, Wd, x, residual, out, mid_workspace, n_embd: int, n_ff: int, batch: int = 1,
+                     stream=None):
+    _check("qdq_q4k_ffn_residual",
+           lib().qdq_q4k_ffn_residual(_ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(x), _ptr(residual), _ptr(out),
+                                      _ptr(mid_workspace), n_embd, n_ff, batch, _stream(stream)))
+
+
+def q8_0_gemm_batch_workspace_bytes(M: int, n_in: int) -> int:
+    return int(lib().qdq_q8_0_gemm_batch_workspace_bytes(M, n_in))
+
+
+def q8_0_gemm_batch(W, X, Y, workspace, n_out: int, n_in: int, M: int, stream=None):
+    _check("qdq_q8_0_gemm_batch", lib().qdq_q8_0_gemm_batch(_ptr(W), _ptr(X), _ptr(Y), _ptr(workspace), n_out,
+                                                            n_in, M, _stream(stream)))
+
+
+def pipeline_timeouts() -> int:
+    return int(lib().qdq_pipeline_timeouts())
+
+
+def set_option(key: int, value: int) -> int:
+    r = int(lib().qdq_set_option(key, value))
+    if r < 0:
+        raise QdqError("qdq_set_option", r)
+    return r
+
+
+# ---------------------------------------------------------------- upload helpers
+# (device memory comes from torch; the repack itself runs in the CUDA kernels)
+
+def upload_q8_0(ggml_bytes, n_out: int, n_in: int, device="cuda", stream=None):
+    """Copy raw GGML Q8_0 bytes (numpy uint8 or torch) to the device and repack them; returns the packed tensor."""
+    import torch
+    raw = torch.as_tensor(ggml_bytes, dtype=torch.uint8).reshape(-1).to(device)
+    packed = torch.empty(q8_0_packed_bytes(n_out, n_in), dtype=torch.uint8, device=device)
+    q8_0_pack(raw, packed, n_out, n_in, stream)
+    return packed
+
+
+def upload_q4k(ggml_bytes, n_out: int, n_in: int, device="cuda", stream=None):
+    """Copy raw GGML Q4_K bytes (numpy uint8 or torch) to the device and repack them; returns the packed tensor."""
+    import torch
+    raw = torch.as_tensor(ggml_bytes, dtype=torch.uint8).reshape(-1).to(device)
+    packed = torch.empty(q4k_packed_bytes(n_out, n_in), dtype=torch.uint8, device=device)
+    q4k_pack(raw, packed, n_out, n_in, stream)
+    return packed

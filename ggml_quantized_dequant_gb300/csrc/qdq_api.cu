@@ -1,0 +1,256 @@
+// C-ABI boundary of the qdq library: argument validation, status codes and
+// dispatch to the kernel launchers.  Nothing here touches tensor data; every
+// arithmetic step runs in the CUDA kernels.
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "qdq_internal.cuh"
+
+namespace qdq {
+
+namespace {
+thread_local int g_last_cuda_error = 0;
+std::atomic<int> g_opt_pdl{1};
+std::atomic<int> g_opt_l2_prefetch{1};
+std::atomic<int> g_opt_ctas_per_sm{1};
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_dev_once[kMaxDevices];
+DeviceInfo g_dev_info[kMaxDevices];
+cudaError_t g_dev_err[kMaxDevices];
+
+std::mutex g_smem_mu;
+struct SmemEntry {
+  const void *func;
+  int device;
+  int bytes;
+};
+std::vector<SmemEntry> g_smem;
+}  // namespace
+
+int opt_pdl() { return g_opt_pdl.load(std::memory_order_relaxed); }
+int opt_l2_prefetch() { return g_opt_l2_prefetch.load(std::memory_order_relaxed); }
+int opt_ctas_per_sm() { return g_opt_ctas_per_sm.load(std::memory_order_relaxed); }
+
+int fail_cuda(cudaError_t e) {
+  g_last_cuda_error = int(e);
+  return QDQ_ERR_CUDA;
+}
+
+cudaError_t device_info(DeviceInfo *out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::call_once(g_dev_once[dev], [dev]() {
+    DeviceInfo di{};
+    cudaError_t err = cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (err == cudaSuccess)
+      err = cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (err == cudaSuccess)
+      err = cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (err == cudaSuccess)
+      err = cudaDeviceGetAttribute(&di.reserved_smem_per_block, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    g_dev_info[dev] = di;
+    g_dev_err[dev] = err;
+  });
+  *out = g_dev_info[dev];
+  return g_dev_err[dev];
+}
+
+size_t gemv_smem_bytes(const DeviceInfo &di, size_t need) {
+  if (!opt_pdl()) return need;
+  const int per_sm = opt_ctas_per_sm() + 1;  // this kernel's CTAs + one of the next kernel
+  long cap = long(di.smem_per_sm) / per_sm - di.reserved_smem_per_block;
+  if (cap > di.max_smem_optin) cap = di.max_smem_optin;
+  return size_t(cap) > need ? size_t(cap) : need;
+}
+
+cudaError_t allow_dynamic_smem(const void *func, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_smem_mu);
+  for (SmemEntry &s : g_smem) {
+    if (s.func == func && s.device == dev) {
+      if (s.bytes >= bytes) return cudaSuccess;
+      e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      if (e == cudaSuccess) s.bytes = bytes;
+      return e;
+    }
+  }
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) g_smem.push_back({func, dev, bytes});
+  return e;
+}
+
+}  // namespace qdq
+
+using namespace qdq;
+
+namespace {
+
+bool dims_q8(int n_out, int n_in) { return n_out > 0 && n_in > 0 && (n_in % 32) == 0; }
+bool dims_q4k(int n_out, int n_in) { return n_out > 0 && n_in > 0 && (n_in % 256) == 0; }
+
+size_t q8_bytes(int n_out, int n_in) { return size_t(n_out) * size_t(n_in / 32) * 34; }
+size_t q4k_bytes(int n_out, int n_in) { return size_t(n_out) * size_t(n_in / 256) * 144; }
+
+int check_gemv_common(const void *W, const float *x, const float *y, int n_out, int n_in, int batch,
+                      size_t w_bytes) {
+  if (!W || !x || !y) return QDQ_ERR_NULL;
+  if (batch < 1 || batch > QDQ_MAX_GEMV_BATCH) return QDQ_ERR_DIMS;
+  if (n_in > QDQ_MAX_GEMV_N_IN) return QDQ_ERR_UNSUPPORTED;
+  if (!aligned(W, 16) || !aligned(x, 16) || !aligned(y, 4)) return QDQ_ERR_ALIGN;
+  const size_t yb = size_t(batch) * n_out * 4, xb = size_t(batch) * n_in * 4;
+  if (overlaps(y, yb, W, w_bytes) || overlaps(y, yb, x, xb)) return QDQ_ERR_ALIAS;
+  return QDQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *qdq_status_string(int status) {
+  switch (status) {
+    case QDQ_OK: return "QDQ_OK";
+    case QDQ_ERR_NULL: return "QDQ_ERR_NULL: a required pointer is NULL";
+    case QDQ_ERR_DIMS: return "QDQ_ERR_DIMS: bad dimension";
+    case QDQ_ERR_ALIGN: return "QDQ_ERR_ALIGN: pointer misaligned";
+    case QDQ_ERR_UNSUPPORTED: return "QDQ_ERR_UNSUPPORTED: shape not handled by this build";
+    case QDQ_ERR_CUDA: return "QDQ_ERR_CUDA: CUDA runtime error (see qdq_last_cuda_error)";
+    case QDQ_ERR_ALIAS: return "QDQ_ERR_ALIAS: output overlaps an input";
+    default: return "unknown qdq status";
+  }
+}
+
+int qdq_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char *qdq_version(void) { return "qdq 0.1 sm_103a"; }
+
+int qdq_set_option(int key, int value) {
+  switch (key) {
+    case QDQ_OPT_PDL:
+      if (value != 0 && value != 1) return QDQ_ERR_DIMS;
+      return g_opt_pdl.exchange(value);
+    case QDQ_OPT_L2_PREFETCH:
+      if (value != 0 && value != 1) return QDQ_ERR_DIMS;
+      return g_opt_l2_prefetch.exchange(value);
+    case QDQ_OPT_CTAS_PER_SM:
+      if (value < 1 || value > 4) return QDQ_ERR_DIMS;
+      return g_opt_ctas_per_sm.exchange(value);
+    default: return QDQ_ERR_DIMS;
+  }
+}
+
+size_t qdq_q8_0_packed_bytes(int n_out, int n_in) { return dims_q8(n_out, n_in) ? q8_bytes(n_out, n_in) : 0; }
+size_t qdq_q4k_packed_bytes(int n_out, int n_in) { return dims_q4k(n_out, n_in) ? q4k_bytes(n_out, n_in) : 0; }
+
+int qdq_q8_0_pack(const void *ggml, void *packed, int n_out, int n_in, cudaStream_t stream) {
+  if (!ggml || !packed) return QDQ_ERR_NULL;
+  if (!dims_q8(n_out, n_in)) return QDQ_ERR_DIMS;
+  if (!aligned(packed, 16)) return QDQ_ERR_ALIGN;
+  const size_t n = q8_bytes(n_out, n_in);
+  if (overlaps(ggml, n, packed, n)) return QDQ_ERR_ALIAS;
+  return launch_q8_0_pack(ggml, packed, n_out, n_in, stream);
+}
+
+int qdq_q4k_pack(const void *ggml, void *packed, int n_out, int n_in, cudaStream_t stream) {
+  if (!ggml || !packed) return QDQ_ERR_NULL;
+  if (!dims_q4k(n_out, n_in)) return QDQ_ERR_DIMS;
+  if (!aligned(packed, 16)) return QDQ_ERR_ALIGN;
+  const size_t n = q4k_bytes(n_out, n_in);
+  if (overlaps(ggml, n, packed, n)) return QDQ_ERR_ALIAS;
+  return launch_q4k_pack(ggml, packed, n_out, n_in, stream);
+}
+
+int qdq_q8_0_dequant(const void *W, float *out, int n_out, int n_in, cudaStream_t stream) {
+  if (!W || !out) return QDQ_ERR_NULL;
+  if (!dims_q8(n_out, n_in)) return QDQ_ERR_DIMS;
+  if (!aligned(W, 16) || !aligned(out, 4)) return QDQ_ERR_ALIGN;
+  if (overlaps(out, size_t(n_out) * n_in * 4, W, q8_bytes(n_out, n_in))) return QDQ_ERR_ALIAS;
+  return launch_q8_0_dequant(W, out, n_out, n_in, stream);
+}
+
+int qdq_q4k_dequant(const void *W, float *out, int n_out, int n_in, cudaStream_t stream) {
+  if (!W || !out) return QDQ_ERR_NULL;
+  if (!dims_q4k(n_out, n_in)) return QDQ_ERR_DIMS;
+  if (!aligned(W, 16) || !aligned(out, 4)) return QDQ_ERR_ALIGN;
+  if (overlaps(out, size_t(n_out) * n_in * 4, W, q4k_bytes(n_out, n_in))) return QDQ_ERR_ALIAS;
+  return launch_q4k_dequant(W, out, n_out, n_in, stream);
+}
+
+int qdq_q8_0_gemv(const void *W, const float *x, float *y, int n_out, int n_in, int batch,
+                  cudaStream_t stream) {
+  if (!dims_q8(n_out, n_in)) return (!W || !x || !y) ? QDQ_ERR_NULL : QDQ_ERR_DIMS;
+  const int rc = check_gemv_common(W, x, y, n_out, n_in, batch, q8_bytes(n_out, n_in));
+  if (rc != QDQ_OK) return rc;
+  return launch_q8_0_gemv(W, x, y, n_out, n_in, batch, stream);
+}
+
+int qdq_q4k_gemv(const void *W, const float *x, float *y, int n_out, int n_in, int batch,
+                 cudaStream_t stream) {
+  if (!dims_q4k(n_out, n_in)) return (!W || !x || !y) ? QDQ_ERR_NULL : QDQ_ERR_DIMS;
+  const int rc = check_gemv_common(W, x, y, n_out, n_in, batch, q4k_bytes(n_out, n_in));
+  if (rc != QDQ_OK) return rc;
+  return launch_q4k_gemv(0, W, nullptr, x, nullptr, y, n_out, n_in, batch, stream);
+}
+
+int qdq_q4k_swiglu(const void *Wg, const void *Wu, const float *x, float *mid, int n_ff, int n_embd,
+                   int batch, cudaStream_t stream) {
+  if (!Wg || !Wu || !x || !mid) return QDQ_ERR_NULL;
+  if (!dims_q4k(n_ff, n_embd)) return QDQ_ERR_DIMS;
+  int rc = check_gemv_common(Wg, x, mid, n_ff, n_embd, batch, q4k_bytes(n_ff, n_embd));
+  if (rc != QDQ_OK) return rc;
+  if (!aligned(Wu, 16)) return QDQ_ERR_ALIGN;
+  if (overlaps(mid, size_t(batch) * n_ff * 4, Wu, q4k_bytes(n_ff, n_embd))) return QDQ_ERR_ALIAS;
+  return launch_q4k_gemv(1, Wg, Wu, x, nullptr, mid, n_ff, n_embd, batch, stream);
+}
+
+int qdq_q4k_ffn_residual(const void *Wg, const void *Wu, const void *Wd, const float *x,
+                         const float *residual, float *out, float *mid, int n_embd, int n_ff, int batch,
+                         cudaStream_t stream) {
+  if (!Wg || !Wu || !Wd || !x || !residual || !out || !mid) return QDQ_ERR_NULL;
+  if (!dims_q4k(n_ff, n_embd) || !dims_q4k(n_embd, n_ff)) return QDQ_ERR_DIMS;
+  if (batch < 1 || batch > QDQ_MAX_GEMV_BATCH) return QDQ_ERR_DIMS;
+  if (n_embd > QDQ_MAX_GEMV_N_IN || n_ff > QDQ_MAX_GEMV_N_IN) return QDQ_ERR_UNSUPPORTED;
+  if (!aligned(Wg, 16) || !aligned(Wu, 16) || !aligned(Wd, 16) || !aligned(x, 16) ||
+      !aligned(mid, 16) || !aligned(residual, 4) || !aligned(out, 4))
+    return QDQ_ERR_ALIGN;
+  const size_t wgb = q4k_bytes(n_ff, n_embd), wdb = q4k_bytes(n_embd, n_ff);
+  const size_t eb = size_t(batch) * n_embd * 4, fb = size_t(batch) * n_ff * 4;
+  // mid may overlap nothing; out may only coincide exactly with residual
+  if (overlaps(mid, fb, Wg, wgb) || overlaps(mid, fb, Wu, wgb) || overlaps(mid, fb, Wd, wdb) ||
+      overlaps(mid, fb, x, eb) || overlaps(mid, fb, residual, eb) || overlaps(mid, fb, out, eb))
+    return QDQ_ERR_ALIAS;
+  if (overlaps(out, eb, Wg, wgb) || overlaps(out, eb, Wu, wgb) || overlaps(out, eb, Wd, wdb) ||
+      overlaps(out, eb, x, eb))
+    return QDQ_ERR_ALIAS;
+  if (out != residual && overlaps(out, eb, residual, eb)) return QDQ_ERR_ALIAS;
+  int rc = launch_q4k_gemv(1, Wg, Wu, x, nullptr, mid, n_ff, n_embd, batch, stream);
+  if (rc != QDQ_OK) return rc;
+  return launch_q4k_gemv(2, Wd, nullptr, mid, residual, out, n_embd, n_ff, batch, stream);
+}
+
+size_t qdq_q8_0_gemm_batch_workspace_bytes(int M, int n_in) {
+  if (M < 1 || n_in < 1) return 0;
+  return size_t(M) * size_t(n_in) * 2;
+}
+
+int qdq_q8_0_gemm_batch(const void *W, const float *X, float *Y, void *workspace, int n_out, int n_in,
+                        int M, cudaStream_t stream) {
+  if (!W || !X || !Y || !workspace) return QDQ_ERR_NULL;
+  if (!dims_q8(n_out, n_in) || M < 1) return QDQ_ERR_DIMS;
+  if ((n_in % 64) != 0 || (n_out % 128) != 0) return QDQ_ERR_UNSUPPORTED;
+  if (!aligned(W, 16) || !aligned(X, 16) || !aligned(Y, 16) || !aligned(workspace, 128))
+    return QDQ_ERR_ALIGN;
+  const size_t wb = q8_bytes(n_out, n_in), xb = size_t(M) * n_in * 4, yb = size_t(M) * n_out * 4;
+  const size_t ws = qdq_q8_0_gemm_batch_workspace_bytes(M, n_in);
+  if (overlaps(Y, yb, W, wb) || overlaps(Y, yb, X, xb) || overlaps(Y, yb, workspace, ws) ||
+      overlaps(workspace, ws, W, wb) || overlaps(workspace, ws, X, xb))
+    return QDQ_ERR_ALIAS;
+  return launch_q8_0_gemm_batch(W, X, Y, workspace, n_out, n_in, M, stream);
+}
+
+}  // extern "C"

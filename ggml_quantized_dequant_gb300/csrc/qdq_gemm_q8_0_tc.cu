@@ -1,0 +1,451 @@
+// Batch-prefill Q8_0 GEMM on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// "Module cuda_lane", Goal: prefer tensor-core dense matmul for batch
+// prefill-shaped GEMMs; "weight_cache.rs", try_cuda_batch_gemv: hidden is
+// packed batch x n_in, weight is row-major n_out x n_in (GGML rows), out is
+// batch x n_out.  The reference densifies the weights on the host, pads every
+// dimension to 16 and transposes for a WMMA kernel; here the quantised weights
+// stay on the device and are dequantised tile by tile in shared memory, and
+// ragged token counts are masked instead of padded.
+//
+// Computation (per output element):  Y[m, r] = sum_k bf16(X[m, k]) * bf16(d[r, k/32] * q[r, k])
+// with f32 accumulation.  d*q is exact in f32 and rounded once to bf16; X is
+// rounded once to bf16 by a small conversion kernel that runs first.
+//
+// Tiling ("swap AB"): the MMA's M dimension is 128 weight rows (n_out), its N
+// dimension is the token tile (16..256), K steps by 64 per pipeline stage.
+// One CTA = one (128-row, token-tile, K-range) tile; K is split across CTAs
+// when the tile count alone cannot fill the SMs, and split partial sums are
+// added into Y with f32 atomics (Y zeroed by the conversion kernel first).
+//
+// Warp roles (192 threads):
+//   warps 0-3  dequantise: thread t owns weight row t of the tile; it reads
+//              the 64 int8 quants of that row (TMA-staged, 64-byte swizzle),
+//              scales them by the row's two fp16 block scales and writes the
+//              bf16 row into the A tile in the 128-byte-swizzled K-major
+//              layout the tensor core reads; after the last stage the same
+//              warps read the accumulator out of TMEM and store Y;
+//   warp 4     TMA producer: int8 weight tile (128 x 64) and bf16 activation
+//              tile (N x 64, 128-byte swizzle) per stage;
+//   warp 5     allocates TMEM, and one lane issues tcgen05.mma (K = 16 each)
+//              and tcgen05.commit to release each stage.
+// Every mbarrier wait is bounded by a wall-clock limit; a wait that runs out
+// counts a pipeline timeout (qdq_pipeline_timeouts) and the CTA winds down
+// instead of hanging.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <mutex>
+
+#include "qdq_internal.cuh"
+
+namespace qdq {
+
+__device__ unsigned int g_pipeline_timeouts = 0;
+
+namespace {
+
+constexpr int BM = 128;  // weight rows per tile (MMA M)
+constexpr int BK = 64;   // K per stage (128 bytes of bf16: one swizzle span)
+constexpr int kDequantWarps = 4;
+constexpr int kThreads = 32 * (kDequantWarps + 2);
+constexpr uint32_t kQTileBytes = BM * BK;      // int8 weight tile
+constexpr uint32_t kATileBytes = BM * BK * 2;  // bf16 weight tile
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---- mbarrier ---------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase with the given parity; false if the wall-clock limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(a, parity)) return true;
+    if ((i & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// ---- TMA ----------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, int x, int y, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---- tcgen05 --------------------------------------------------------------------
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major operand tile in the canonical
+// 128-byte-swizzle layout: rows of 128 bytes (64 bf16 along K), groups of 8
+// rows 1024 bytes apart, 16-byte chunk c of row r stored at chunk c ^ (r % 8).
+// Fields: start address >> 4 (bits 0-13), leading byte offset >> 4 (16-29,
+// unused for this layout), stride byte offset >> 4 (32-45), descriptor
+// version 1 (46-47), swizzle mode 2 = 128-byte (61-63).
+__device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr) {
+  return uint64_t((saddr >> 4) & 0x3FFFu) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
+         (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+// Instruction descriptor, kind::f16: f32 accumulator (bits 4-5 = 1), A and B
+// bf16 (bits 7-9 = 1, 10-12 = 1), both K-major, N >> 3 at bits 17-22,
+// M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
+}
+
+template <int N>
+struct GemmCfg {
+  static constexpr int kStages = N >= 256 ? 3 : 4;
+  static constexpr uint32_t kBTileBytes = uint32_t(N) * 128;
+  static constexpr uint32_t kStageBytes = kQTileBytes + kATileBytes + kBTileBytes;
+  static constexpr uint32_t kTmemCols = N < 32 ? 32 : N;
+  static constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + 256;
+};
+
+template <int N>
+__global__ void __launch_bounds__(kThreads, 1)
+    q8_0_gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_x,
+                        const uint8_t *__restrict__ W, float *__restrict__ Y, int n_out, int n_in, int M,
+                        int kb_per_split, int atomic_out) {
+  using C = GemmCfg<N>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + S * C::kStageBytes);
+  uint64_t *aready = full + S;
+  uint64_t *empty = aready + S;
+  uint64_t *accum = empty + S;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
+  __shared__ int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile_n = blockIdx.x, tile_m = blockIdx.y;
+  const int nkb = n_in / BK;
+  const int kb0 = blockIdx.z * kb_per_split;
+  const int kb1 = min(kb0 + kb_per_split, nkb);
+  const int nk = kb1 - kb0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&aready[s], kDequantWarps * 32);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accum, 1);
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kDequantWarps + 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  pdl_launch_dependents();
+
+  if (warp == kDequantWarps) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
+      const int npre = nk < S ? nk : S;
+      // weights do not depend on the previous kernel: start them before the wait
+      for (int i = 0; i < npre; ++i) {
+        mbar_arrive_expect_tx(&full[i], kQTileBytes + C::kBTileBytes);
+        tma_load_2d(smem + i * C::kStageBytes, &tm_q, (kb0 + i) * BK, tile_n * BM, &full[i]);
+      }
+      pdl_wait();
+      for (int i = 0; i < npre; ++i)
+        tma_load_2d(smem + i * C::kStageBytes + kQTileBytes + kATileBytes, &tm_x, (kb0 + i) * BK, tile_m * N,
+                    &full[i]);
+      int issued = npre;
+      for (int i = npre; i < nk; ++i) {
+        const int s = i % S;
+        if (!mbar_wait(&empty[s], ((i / S) + 1) & 1)) {
+          s_abort = 1;
+          break;
+        }
+        uint8_t *st = smem + s * C::kStageBytes;
+        mbar_arrive_expect_tx(&full[s], kQTileBytes + C::kBTileBytes);
+        tma_load_2d(st, &tm_q, (kb0 + i) * BK, tile_n * BM, &full[s]);
+        tma_load_2d(st + kQTileBytes + kATileBytes, &tm_x, (kb0 + i) * BK, tile_m * N, &full[s]);
+        issued = i + 1;
+      }
+      // never leave with copies in flight: wait (bounded) for the last loads issued
+      for (int i = issued - S < 0 ? 0 : issued - S; i < issued; ++i) mbar_wait(&full[i % S], (i / S) & 1);
+    } else {
+      pdl_wait();
+    }
+  } else if (warp == kDequantWarps + 1) {
+    // ---------------- MMA issuer ----------------
+    pdl_wait();
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, N);
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % S;
+        if (!mbar_wait(&aready[s], (i / S) & 1) || !mbar_wait(&full[s], (i / S) & 1)) {
+          s_abort = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(smem + s * C::kStageBytes + kQTileBytes);
+        const uint32_t b_base = a_base + kATileBytes;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)
+          umma_bf16(tmem, desc_kmajor_sw128(a_base + 32 * k), desc_kmajor_sw128(b_base + 32 * k), idesc,
+                    (i | k) != 0);
+        umma_commit(&empty[s]);
+      }
+      umma_commit(accum);
+    }
+  } else {
+    // ---------------- dequantise, then epilogue ----------------
+    pdl_wait();
+    const int row = threadIdx.x;  // 0..127 = weight row within the tile = TMEM lane
+    const int grow = tile_n * BM + row;
+    const uint32_t *d32 = reinterpret_cast<const uint32_t *>(W + int64_t(n_out) * n_in) + int64_t(grow) * (n_in / BK);
+    uint32_t dnext = __ldg(d32 + kb0);
+    bool ok = true;
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % S;
+      const uint32_t dcur = dnext;
+      if (i + 1 < nk) dnext = __ldg(d32 + kb0 + i + 1);
+      if (!mbar_wait(&full[s], (i / S) & 1)) {
+        s_abort = 1;
+        ok = false;
+        break;
+      }
+      const uint8_t *qt = smem + s * C::kStageBytes;
+      uint8_t *at = smem + s * C::kStageBytes + kQTileBytes;
+      const int qsw = (row >> 1) & 3;  // 64-byte swizzle of the TMA-written int8 tile
+      const __half2 dh = *reinterpret_cast<const __half2 *>(&dcur);
+      const float2 dd = __half22float2(dh);  // block scales for K 0..31 and 32..63
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint4 qv = *reinterpret_cast<const uint4 *>(qt + row * 64 + ((c ^ qsw) << 4));
+        const float dsc = c < 2 ? dd.x : dd.y;
+        const f2 dpair = f2_make(dsc, dsc);
+        const uint32_t words[4] = {qv.x, qv.y, qv.z, qv.w};
+        uint32_t packed[8];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          f2 q01, q23;
+          s8x4_to_f2(words[w], q01, q23);
+          float a0, a1, a2, a3;
+          f2_split(f2_mul(q01, dpair), a0, a1);
+          f2_split(f2_mul(q23, dpair), a2, a3);
+          const __nv_bfloat162 p01 = __floats2bfloat162_rn(a0, a1);
+          const __nv_bfloat162 p23 = __floats2bfloat162_rn(a2, a3);
+          packed[2 * w] = *reinterpret_cast<const uint32_t *>(&p01);
+          packed[2 * w + 1] = *reinterpret_cast<const uint32_t *>(&p23);
+        }
+        // 16 quants -> two 16-byte bf16 chunks (K 16c..16c+7 and 16c+8..16c+15)
+        const int c0 = 2 * c, c1 = 2 * c + 1;
+        *reinterpret_cast<uint4 *>(at + row * 128 + ((c0 ^ (row & 7)) << 4)) =
+            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        *reinterpret_cast<uint4 *>(at + row * 128 + ((c1 ^ (row & 7)) << 4)) =
+            make_uint4(packed[4], packed[5], packed[6], packed[7]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(&aready[s]);
+    }
+    if (ok && mbar_wait(accum, 0)) {
+      tc_fence_after();
+      const uint32_t lane_base = uint32_t(warp * 32) << 16;
+      const int m0 = tile_m * N;
+#pragma unroll 1
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld16(tmem + lane_base + uint32_t(c0), r);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int m = m0 + c0 + j;
+          if (m < M) {
+            float *dst = Y + int64_t(m) * n_out + grow;
+            if (atomic_out) atomicAdd(dst, __uint_as_float(r[j]));
+            else *dst = __uint_as_float(r[j]);
+          }
+        }
+      }
+    } else {
+      s_abort = 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && s_abort) atomicAdd(&g_pipeline_timeouts, 1u);
+  if (warp == kDequantWarps + 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// X (f32, M x n_in) -> bf16 workspace; optionally zero Y for split-K accumulation.
+__global__ void __launch_bounds__(256) x_to_bf16_kernel(const float4 *__restrict__ X, uint2 *__restrict__ xb,
+                                                        int64_t n4, float4 *__restrict__ Yz, int64_t nz4) {
+  pdl_launch_dependents();
+  pdl_wait();  // the workspace and Y may still be in use by the previous kernel
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n4; i += stride) {
+    const float4 v = X[i];
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+    xb[i] = make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
+  }
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < nz4; i += stride)
+    Yz[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+cudaError_t get_encoder() {
+  std::call_once(g_encode_once, []() {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode ? cudaSuccess : cudaErrorNotSupported;
+}
+
+bool encode_2d(CUtensorMap *tm, CUtensorMapDataType dt, void *base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(tm, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int N>
+int launch_tile(const uint8_t *W, const float *X, float *Y, void *ws, int n_out, int n_in, int M, cudaStream_t s,
+                const DeviceInfo &di) {
+  using C = GemmCfg<N>;
+  CUtensorMap tm_q, tm_x;
+  if (!encode_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t *>(W), uint64_t(n_in), uint64_t(n_out),
+                 uint64_t(n_in), BK, BM, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws, uint64_t(n_in), uint64_t(M), uint64_t(n_in) * 2, BK,
+                 N, CU_TENSOR_MAP_SWIZZLE_128B))
+    return QDQ_ERR_UNSUPPORTED;
+
+  const int ntile_n = n_out / BM;
+  const int ntile_m = (M + N - 1) / N;
+  const int nkb = n_in / BK;
+  const int tiles = ntile_n * ntile_m;
+  int split = di.sm_count / tiles;
+  if (split < 1) split = 1;
+  if (split > nkb) split = nkb;
+  const int kb_per = (nkb + split - 1) / split;
+  split = (nkb + kb_per - 1) / kb_per;  // every split gets at least one K block
+
+  // conversion (+ zeroing of Y when partial sums are accumulated)
+  const int64_t n4 = int64_t(M) * n_in / 4;
+  const int64_t nz4 = split > 1 ? int64_t(M) * n_out / 4 : 0;
+  int cgrid = int((n4 + 255) / 256);
+  if (cgrid > di.sm_count * 8) cgrid = di.sm_count * 8;
+  if (cgrid < 1) cgrid = 1;
+  cudaError_t e = launch(x_to_bf16_kernel, dim3(cgrid), dim3(256), 0, s, reinterpret_cast<const float4 *>(X),
+                         static_cast<uint2 *>(ws), n4, reinterpret_cast<float4 *>(Y), nz4);
+  if (e != cudaSuccess) return fail_cuda(e);
+
+  auto kern = q8_0_gemm_tc_kernel<N>;
+  e = allow_dynamic_smem(reinterpret_cast<const void *>(kern), int(C::kSmemBytes));
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = launch(kern, dim3(ntile_n, ntile_m, split), dim3(kThreads), C::kSmemBytes, s, tm_q, tm_x, W, Y, n_out, n_in,
+             M, kb_per, split > 1 ? 1 : 0);
+  return e == cudaSuccess ? QDQ_OK : fail_cuda(e);
+}
+
+}  // namespace
+
+int launch_q8_0_gemm_batch(const void *Wv, const float *X, float *Y, void *ws, int n_out, int n_in, int M,
+                           cudaStream_t s) {
+  DeviceInfo di;
+  cudaError_t e = device_info(&di);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = get_encoder();
+  if (e != cudaSuccess) return fail_cuda(e);
+  const uint8_t *W = static_cast<const uint8_t *>(Wv);
+  if (M <= 16) return launch_tile<16>(W, X, Y, ws, n_out, n_in, M, s, di);
+  if (M <= 32) return launch_tile<32>(W, X, Y, ws, n_out, n_in, M, s, di);
+  if (M <= 64) return launch_tile<64>(W, X, Y, ws, n_out, n_in, M, s, di);
+  if (M <= 128) return launch_tile<128>(W, X, Y, ws, n_out, n_in, M, s, di);
+  return launch_tile<256>(W, X, Y, ws, n_out, n_in, M, s, di);
+}
+
+}  // namespace qdq
+
+extern "C" int qdq_pipeline_timeouts(void) {
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, qdq::g_pipeline_timeouts, sizeof(v)) != cudaSuccess) return -1;
+  if (cudaMemcpyToSymbol(qdq::g_pipeline_timeouts, &zero, sizeof(zero)) != cudaSuccess) return -1;
+  return int(v);
+}

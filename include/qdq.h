@@ -1,0 +1,174 @@
+/*
+ * qdq.h -- GB300 (sm_103a) dequantize-and-multiply kernels for GGML Q8_0 / Q4_K
+ * weight matrices against f32 activations (the token-decode hot path).
+ *
+ * Sources (rustdoc pages of the qualia_core_db crate):
+ *   "Module cuda_lane", Functions:
+ *     q8_0_gemv_oracle_into / try_q8_0_cuda_gemv   -> qdq_q8_0_gemv
+ *     try_q4k_soa_gemv                              -> qdq_q4k_gemv
+ *     try_q4k_soa_fused_swiglu                      -> qdq_q4k_swiglu
+ *     try_q4k_soa_ffn_block / _ffn_block_residual   -> qdq_q4k_ffn_residual
+ *     preload_q4k_soa_weights (one-time upload)     -> qdq_q8_0_pack / qdq_q4k_pack
+ *   "Module cuda_lane", Goal (batch prefill-shaped GEMMs on tensor cores) and
+ *   "weight_cache.rs", try_cuda_batch_gemv          -> qdq_q8_0_gemm_batch
+ *
+ * Conventions for every call
+ *   - W is row-major n_out x n_in (rows = outputs, the GGML convention).
+ *     Activations are packed batch x n_in f32, outputs batch x n_out f32
+ *     ("weight_cache.rs", try_cuda_batch_gemv doc comment).
+ *   - All data pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates, frees or keeps a pointer after a call returns.
+ *   - Every compute call is asynchronous and stream-ordered on `stream`
+ *     (0 = the legacy default stream); nothing synchronises the host.
+ *   - Calls return QDQ_OK or a negative status.  On any error nothing has been
+ *     launched and every output buffer is untouched.  There is no fallback
+ *     path: an unsupported shape is an error, never a silent slower route.
+ *   - Kernels are launched with programmatic dependent launch: a kernel may
+ *     start streaming its own weights while the previous kernel on the stream
+ *     finishes, but it reads activations only after that kernel completed.
+ *
+ * Block formats (GGML, little-endian)
+ *   Q8_0: 34-byte block per 32 weights: fp16 d, then int8 q[32]; w = d*q.
+ *   Q4_K: 144-byte superblock per 256 weights: fp16 d, fp16 dmin, 12 bytes of
+ *         eight 6-bit scales sc_j and eight 6-bit mins m_j, 128 bytes of 4-bit
+ *         quants; sub-block j = weights 32j..32j+31; w = d*sc_j*q - dmin*m_j.
+ *
+ * Packed (device) formats -- produced once by qdq_*_pack, same byte count as
+ * the GGML input, laid out as planes so that every kernel load is a 16-byte
+ * aligned vector load:
+ *   Q8_0 packed: [ q plane: n_out*n_in int8, row-major ]
+ *                [ d plane: n_out*(n_in/32) fp16, row-major ]
+ *   Q4_K packed: [ q plane: n_out*(n_in/2) bytes; weight e of a row is nibble
+ *                  (e & 1) (0 = low) of byte e/2 ]
+ *                [ header plane: n_out*(n_in/256) records of 16 bytes:
+ *                  word0 = d | dmin << 16 (fp16 bits); words 1..3 form a
+ *                  96-bit little-endian field with sc_j at bits 12j..12j+5
+ *                  and m_j at bits 12j+6..12j+11 ]
+ */
+#ifndef QDQ_H
+#define QDQ_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes --------------------------------------------------------- */
+#define QDQ_OK               0
+#define QDQ_ERR_NULL        -1  /* a required pointer is NULL */
+#define QDQ_ERR_DIMS        -2  /* a dimension is <= 0, not a whole number of blocks, or out of range */
+#define QDQ_ERR_ALIGN       -3  /* a pointer does not meet the stated alignment */
+#define QDQ_ERR_UNSUPPORTED -4  /* valid arguments this build does not handle (e.g. n_in too large) */
+#define QDQ_ERR_CUDA        -5  /* a CUDA runtime call failed; see qdq_last_cuda_error() */
+#define QDQ_ERR_ALIAS       -6  /* an output overlaps an input it may not overlap */
+
+/* Human-readable name of a status code (static string). */
+const char *qdq_status_string(int status);
+/* cudaError_t of the most recent QDQ_ERR_CUDA returned on the calling thread (0 if none). */
+int qdq_last_cuda_error(void);
+/* Library version string (static). */
+const char *qdq_version(void);
+
+/* ---- limits --------------------------------------------------------------- */
+/* Largest supported batch for the GEMV-family calls. */
+#define QDQ_MAX_GEMV_BATCH 8
+/* Largest supported n_in for the GEMV-family calls (activations are staged in
+ * shared memory: batch_group * n_in * 4 bytes per CTA). */
+#define QDQ_MAX_GEMV_N_IN 49152
+
+/* ---- one-time repack (the pages' preload step) ----------------------------
+ * "Module cuda_lane", Functions: preload_q4k_soa_weights -- bulk upload once
+ * at plan build.  Converts a row-major GGML matrix already resident on the
+ * device into the packed planes above.  `ggml` and `packed` are device
+ * pointers; `packed` must hold qdq_*_packed_bytes(n_out, n_in) bytes, be
+ * 16-byte aligned and must not overlap `ggml`.  Q8_0 needs n_in % 32 == 0,
+ * Q4_K needs n_in % 256 == 0.
+ */
+size_t qdq_q8_0_packed_bytes(int n_out, int n_in);   /* n_out*n_in/32*34, 0 on bad dims */
+size_t qdq_q4k_packed_bytes(int n_out, int n_in);    /* n_out*n_in/256*144, 0 on bad dims */
+int qdq_q8_0_pack(const void *ggml, void *packed, int n_out, int n_in, cudaStream_t stream);
+int qdq_q4k_pack(const void *ggml, void *packed, int n_out, int n_in, cudaStream_t stream);
+
+/* ---- dequantisation (verification aid) ------------------------------------
+ * Writes the f32 weights of a packed matrix, row-major n_out x n_in, into
+ * `out` (4-byte aligned).  Q8_0: d*q (exact in f32).  Q4_K: the single f32
+ * rounding of d*sc_j*q - dmin*m_j.  Same block definitions as above.
+ */
+int qdq_q8_0_dequant(const void *W, float *out, int n_out, int n_in, cudaStream_t stream);
+int qdq_q4k_dequant(const void *W, float *out, int n_out, int n_in, cudaStream_t stream);
+
+/* ---- GEMV: y[b, r] = sum_k w[r, k] * x[b, k] -------------------------------
+ * "Module cuda_lane", Functions: try_q8_0_cuda_gemv, q8_0_gemv_oracle_into,
+ * try_q4k_soa_gemv.  W: packed (16-byte aligned).  x: batch x n_in f32,
+ * 16-byte aligned.  y: batch x n_out f32, 4-byte aligned, must not overlap W
+ * or x.  1 <= batch <= QDQ_MAX_GEMV_BATCH.  f32 accumulation; the error
+ * against the exact sum stays far below 1e-5 * sum_k |w[r,k]| |x[b,k]|.
+ */
+int qdq_q8_0_gemv(const void *W, const float *x, float *y,
+                  int n_out, int n_in, int batch, cudaStream_t stream);
+int qdq_q4k_gemv(const void *W, const float *x, float *y,
+                 int n_out, int n_in, int batch, cudaStream_t stream);
+
+/* ---- fused SwiGLU expansion -------------------------------------------------
+ * "Module cuda_lane", Functions: try_q4k_soa_fused_swiglu:
+ *   mid[b, i] = silu(gate_i . x_b) * (up_i . x_b),  silu(z) = z / (1 + e^-z),
+ * one kernel reading x once for both Q4_K matrices.  Wg, Wu: packed Q4_K
+ * n_ff x n_embd.  x: batch x n_embd (16-byte aligned).  mid: batch x n_ff,
+ * must not overlap any input.
+ */
+int qdq_q4k_swiglu(const void *Wg, const void *Wu, const float *x, float *mid,
+                   int n_ff, int n_embd, int batch, cudaStream_t stream);
+
+/* ---- FFN block with on-device residual --------------------------------------
+ * "Module cuda_lane", Functions: try_q4k_soa_ffn_block_residual:
+ *   out = residual + W_down . swiglu(W_gate x, W_up x)
+ * (pre-norm-free: x is used as given).  Two kernels on `stream`; `mid` stays
+ * on the device.  Wg, Wu: packed Q4_K n_ff x n_embd; Wd: packed Q4_K
+ * n_embd x n_ff.  x, residual, out: batch x n_embd.  mid_workspace: caller-
+ * owned batch x n_ff f32 scratch, 16-byte aligned, overwritten.  out may be
+ * exactly `residual` (in-place residual add) but may not overlap anything else.
+ */
+int qdq_q4k_ffn_residual(const void *Wg, const void *Wu, const void *Wd,
+                         const float *x, const float *residual, float *out,
+                         float *mid_workspace, int n_embd, int n_ff, int batch,
+                         cudaStream_t stream);
+
+/* ---- batch-prefill GEMM on tensor cores -----------------------------------
+ * "Module cuda_lane", Goal (tensor-core GEMM for batch prefill-shaped work)
+ * and "weight_cache.rs", try_cuda_batch_gemv (hidden packed batch x n_in,
+ * W row-major n_out x n_in, out batch x n_out; the reference pads to 16 and
+ * trims, this call masks instead):
+ *   Y[m, r] = sum_k bf16(X[m, k]) * bf16(w[r, k])   (f32 accumulation)
+ * W: packed Q8_0 (16-byte aligned).  X: M x n_in f32 (16-byte aligned).
+ * Y: M x n_out f32 (16-byte aligned), must not overlap W, X or workspace.
+ * workspace: caller-owned scratch of qdq_q8_0_gemm_batch_workspace_bytes(M,
+ * n_in) bytes, 128-byte aligned, overwritten (X rounded to bf16).
+ * Requires n_in % 64 == 0 and n_out % 128 == 0; M >= 1 (tail masked).
+ * Error against the exact sum: <= 4e-3 * sum_k |w[r,k]| |X[m,k]|.
+ */
+size_t qdq_q8_0_gemm_batch_workspace_bytes(int M, int n_in);
+int qdq_q8_0_gemm_batch(const void *W, const float *X, float *Y, void *workspace,
+                        int n_out, int n_in, int M, cudaStream_t stream);
+
+/* ---- pipeline health -------------------------------------------------------
+ * Every wait inside the tensor-core pipeline is bounded (2 s wall clock); a
+ * wait that runs out makes its CTA stop early instead of hanging, and counts
+ * here.  Returns the count since the previous call and resets it (-1 on a
+ * CUDA error).  Synchronous: it waits for the device.
+ */
+int qdq_pipeline_timeouts(void);
+
+/* ---- launch options (same work, different launch shape; for measurement) -- */
+#define QDQ_OPT_PDL          1  /* 1 (default): programmatic dependent launch on; 0: plain launches */
+#define QDQ_OPT_L2_PREFETCH  2  /* 1 (default): each CTA bulk-prefetches its weight rows into L2 first */
+#define QDQ_OPT_CTAS_PER_SM  3  /* GEMV CTAs per SM, 1..4 (default 1) */
+/* Sets a process-wide option; returns the previous value, or QDQ_ERR_DIMS for a bad key/value. */
+int qdq_set_option(int key, int value);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QDQ_H */

@@ -54,10 +54,10 @@ def q8_0_blocks(rng: np.random.Generator, n_out: int, n_in: int,
         raise ValueError("n_in must be a multiple of 32 for Q8_0")
     nb = n_in // Q8_0_BLOCK_ELEMS
     d = rng.uniform(d_range[0], d_range[1], size=(n_out, nb))
-    q = rng.integers(q_range[0], q_range[1] + 1, size=(n_out, nb, Q8_0_BLOCK_ELEMS), dtype=np.int16)
+    q = rng.integers(q_range[0], q_range[1] + 1, size=(n_out, nb, Q8_0_BLOCK_ELEMS), dtype=np.int8)
     out = np.empty((n_out, nb, Q8_0_BLOCK_BYTES), dtype=np.uint8)
     out[..., 0:2] = _fp16_le_bytes(d)
-    out[..., 2:] = q.astype(np.int8).view(np.uint8)
+    out[..., 2:] = q.view(np.uint8)
     return out.reshape(n_out, nb * Q8_0_BLOCK_BYTES)
 
 

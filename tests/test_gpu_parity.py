@@ -1,0 +1,331 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Bars (stated in the workload definition):
+* dequantised weights: bit-exact (compared as raw f32 bits);
+* GEMV / SwiGLU / FFN: |y - y_ref| <= 1e-5 * sum|w||x| (FFN / SwiGLU with the
+  propagated bound of tests/_bounds.py);
+* tensor-core batch GEMM: |Y - Y_ref| <= 4e-3 * sum|w||x| against the fp64
+  oracle on the unrounded activations.
+Shapes cover several tiles plus ragged tails, batch 1..8, and the full
+workload sizes in the launch configuration the bench times.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from _bounds import ffn_bound, gemv_excess, swiglu_eps
+
+pytestmark = pytest.mark.gpu
+
+
+def _dev():
+    import torch
+    return torch.device("cuda")
+
+
+def _t(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).to(_dev())
+
+
+def _nan(*shape):
+    import torch
+    return torch.full(shape, float("nan"), dtype=torch.float32, device=_dev())
+
+
+def _np(t):
+    import torch
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+# ------------------------------------------------------------------ dequant
+
+@pytest.mark.parametrize("n_out,n_in", [(256, 512), (3, 96), (37, 1056), (8192, 3072)])
+def test_q8_0_dequant_bit_exact(cuda_lib, n_out, n_in):
+    qdq = cuda_lib
+    wb = synth.q8_0_blocks(np.random.default_rng(n_out * 7 + n_in), n_out, n_in)
+    W = qdq.upload_q8_0(wb, n_out, n_in)
+    out = _nan(n_out, n_in)
+    qdq.q8_0_dequant(W, out, n_out, n_in)
+    ref = oracle.q8_0_dequant(wb, n_out, n_in)
+    assert np.array_equal(_np(out).view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("n_out,n_in", [(3, 256), (37, 768), (8192, 3072)])
+def test_q4k_dequant_bit_exact(cuda_lib, n_out, n_in):
+    qdq = cuda_lib
+    wb = synth.q4k_blocks(np.random.default_rng(n_out * 5 + n_in), n_out, n_in)
+    W = qdq.upload_q4k(wb, n_out, n_in)
+    out = _nan(n_out, n_in)
+    qdq.q4k_dequant(W, out, n_out, n_in)
+    ref = oracle.q4k_dequant(wb, n_out, n_in)
+    assert np.array_equal(_np(out).view(np.uint32), ref.view(np.uint32))
+
+
+def test_q4k_dequant_extreme_scales_bit_exact(cuda_lib):
+    # largest dmin and smallest d: the f32 subtraction has to round
+    qdq = cuda_lib
+    wb = synth.q4k_blocks(np.random.default_rng(3), 16, 512, d_range=(6e-5, 6e-5), dmin_range=(6e4, 6e4))
+    W = qdq.upload_q4k(wb, 16, 512)
+    out = _nan(16, 512)
+    qdq.q4k_dequant(W, out, 16, 512)
+    assert np.array_equal(_np(out).view(np.uint32), oracle.q4k_dequant(wb, 16, 512).view(np.uint32))
+
+
+# ------------------------------------------------------------------ GEMV
+
+Q8_SHAPES = [(256, 512, 1), (1, 32, 1), (3, 96, 1), (157, 800, 1), (300, 4096, 3), (64, 512, 8),
+             (33, 8192, 8), (1000, 1024, 2)]
+
+
+@pytest.mark.parametrize("n_out,n_in,batch", Q8_SHAPES)
+def test_q8_0_gemv_parity(cuda_lib, n_out, n_in, batch):
+    qdq = cuda_lib
+    rng = np.random.default_rng(n_out + 3 * n_in + batch)
+    wb = synth.q8_0_blocks(rng, n_out, n_in)
+    x = synth.activations(rng, batch, n_in)
+    W = qdq.upload_q8_0(wb, n_out, n_in)
+    y = _nan(batch, n_out)
+    qdq.q8_0_gemv(W, _t(x), y, n_out, n_in, batch)
+    y_ref, a = oracle.gemv(oracle.q8_0_dequant(wb, n_out, n_in), x)
+    assert gemv_excess(_np(y), y_ref, a) <= 1.0
+
+
+def test_q8_0_gemv_config0_seed0(cuda_lib):
+    qdq = cuda_lib
+    wb, x = synth.config0()
+    W = qdq.upload_q8_0(wb, 256, 512)
+    y = _nan(1, 256)
+    qdq.q8_0_gemv(W, _t(x), y, 256, 512, 1)
+    y_ref, a = oracle.gemv(oracle.q8_0_dequant(wb, 256, 512), x)
+    assert gemv_excess(_np(y), y_ref, a) <= 1.0
+
+
+@pytest.mark.parametrize("which", ["up", "down"])
+def test_q8_0_gemv_full_size(cuda_lib, which):
+    qdq = cuda_lib
+    if which == "up":
+        n_out, n_in, wb, x = 8192, 3072, synth.config1_up(0), synth.config1_x()
+    else:
+        n_out, n_in, wb = 3072, 8192, synth.config1_down(0)
+        x = synth.activations(synth.rng_for(1, 3), 1, 8192)
+    W = qdq.upload_q8_0(wb, n_out, n_in)
+    y = _nan(1, n_out)
+    qdq.q8_0_gemv(W, _t(x), y, n_out, n_in, 1)
+    y_ref, a = oracle.gemv(oracle.q8_0_dequant(wb, n_out, n_in), x)
+    assert gemv_excess(_np(y), y_ref, a) <= 1.0
+
+
+def test_q8_0_gemv_extreme_quants(cuda_lib):
+    # q = -128 and +127, negative and large scales
+    qdq = cuda_lib
+    n_out, n_in = 40, 256
+    wb = synth.q8_0_blocks(np.random.default_rng(5), n_out, n_in, d_range=(-3e4, 3e4), q_range=(-128, 127))
+    blk = wb.reshape(n_out, n_in // 32, 34)
+    blk[::2, :, 2:] = np.uint8(0x80)  # every other row all -128
+    x = synth.activations(np.random.default_rng(6), 2, n_in)
+    W = qdq.upload_q8_0(wb, n_out, n_in)
+    y = _nan(2, n_out)
+    qdq.q8_0_gemv(W, _t(x), y, n_out, n_in, 2)
+    y_ref, a = oracle.gemv(oracle.q8_0_dequant(wb, n_out, n_in), x)
+    assert gemv_excess(_np(y), y_ref, a) <= 1.0
+
+
+def test_gemv_zero_x_gives_exact_zero(cuda_lib):
+    qdq = cuda_lib
+    wb = synth.q8_0_blocks(np.random.default_rng(8), 64, 512)
+    W = qdq.upload_q8_0(wb, 64, 512)
+    y = _nan(1, 64)
+    qdq.q8_0_gemv(W, _t(np.zeros((1, 512), np.float32)), y, 64, 512, 1)
+    assert np.all(_np(y) == 0.0)
+
+
+Q4_SHAPES = [(1, 256, 1), (5, 512, 1), (157, 2048, 1), (300, 3072, 4), (64, 512, 8), (33, 8192, 8),
+             (1000, 1280, 2)]
+
+
+@pytest.mark.parametrize("n_out,n_in,batch", Q4_SHAPES)
+def test_q4k_gemv_parity(cuda_lib, n_out, n_in, batch):
+    qdq = cuda_lib
+    rng = np.random.default_rng(n_out + 5 * n_in + batch)
+    wb = synth.q4k_blocks(rng, n_out, n_in)
+    x = synth.activations(rng, batch, n_in)
+    W = qdq.upload_q4k(wb, n_out, n_in)
+    y = _nan(batch, n_out)
+    qdq.q4k_gemv(W, _t(x), y, n_out, n_in, batch)
+    y_ref, a = oracle.gemv(oracle.q4k_dequant(wb, n_out, n_in), x)
+    assert gemv_excess(_np(y), y_ref, a) <= 1.0
+
+
+def test_q4k_gemv_full_size_config2(cuda_lib):
+    qdq = cuda_lib
+    wb, x = synth.config2_w(0), synth.config2_x()
+    W = qdq.upload_q4k(wb, 8192, 3072)
+    y = _nan(1, 8192)
+    qdq.q4k_gemv(W, _t(x), y, 8192, 3072, 1)
+    y_ref, a = oracle.gemv(oracle.q4k_dequant(wb, 8192, 3072), x)
+    assert gemv_excess(_np(y), y_ref, a) <= 1.0
+
+
+def test_q4k_gemv_cancelling_weights(cuda_lib):
+    # d*sc*q close to dmin*m for most weights: sum|w||x| is small relative to the
+    # separate terms, the hard case for the factored sub-block sum
+    qdq = cuda_lib
+    n_out, n_in = 64, 1024
+    rng = np.random.default_rng(11)
+    wb = synth.q4k_blocks(rng, n_out, n_in, d_range=(1e-2, 1e-2), dmin_range=(1e-2, 1e-2))
+    sb = wb.reshape(n_out, n_in // 256, 144)
+    # every sc_j = 4 and m_j = 32 (bytes 0..3: sc 4; bytes 4..7: m 32 plus the top bits 2 of
+    # m_4..7; bytes 8..11: low nibbles sc 4, m 0), d == dmin, so a quant of 8 gives exactly 0
+    sb[..., 4:16] = np.array([4, 4, 4, 4, 160, 160, 160, 160, 4, 4, 4, 4], dtype=np.uint8)
+    sb[..., 16:] = np.where(rng.random(sb[..., 16:].shape) < 0.8, 0x88, sb[..., 16:]).astype(np.uint8)
+    x = synth.activations(rng, 1, n_in)
+    W = qdq.upload_q4k(wb, n_out, n_in)
+    y = _nan(1, n_out)
+    qdq.q4k_gemv(W, _t(x), y, n_out, n_in, 1)
+    w = oracle.q4k_dequant(wb, n_out, n_in)
+    y_ref, a = oracle.gemv(w, x)
+    assert gemv_excess(_np(y), y_ref, a) <= 1.0
+
+
+# ------------------------------------------------------------------ SwiGLU / FFN
+
+@pytest.mark.parametrize("n_ff,n_embd,batch", [(512, 256, 1), (1000, 512, 3), (8192, 3072, 1)])
+def test_q4k_swiglu_parity(cuda_lib, n_ff, n_embd, batch):
+    qdq = cuda_lib
+    rng = np.random.default_rng(n_ff + n_embd + batch)
+    g, u = synth.q4k_blocks(rng, n_ff, n_embd), synth.q4k_blocks(rng, n_ff, n_embd)
+    x = synth.activations(rng, batch, n_embd)
+    Wg, Wu = qdq.upload_q4k(g, n_ff, n_embd), qdq.upload_q4k(u, n_ff, n_embd)
+    mid = _nan(batch, n_ff)
+    qdq.q4k_swiglu(Wg, Wu, _t(x), mid, n_ff, n_embd, batch)
+    s = oracle.swiglu(oracle.q4k_dequant(g, n_ff, n_embd), oracle.q4k_dequant(u, n_ff, n_embd), x)
+    err = np.abs(_np(mid) - s["mid"])
+    assert np.all(err <= swiglu_eps(s))
+
+
+def _ffn_case(qdq, n_embd, n_ff, batch, seed, in_place=False, layer=None):
+    if layer is not None:
+        g, u, d = synth.config3_layer(layer)
+        x, res = synth.config3_x_residual()
+    else:
+        rng = np.random.default_rng(seed)
+        g, u, d = (synth.q4k_blocks(rng, n_ff, n_embd), synth.q4k_blocks(rng, n_ff, n_embd),
+                   synth.q4k_blocks(rng, n_embd, n_ff))
+        x, res = synth.activations(rng, batch, n_embd), synth.activations(rng, batch, n_embd)
+    Wg, Wu, Wd = qdq.upload_q4k(g, n_ff, n_embd), qdq.upload_q4k(u, n_ff, n_embd), qdq.upload_q4k(d, n_embd, n_ff)
+    mid = _nan(batch, n_ff)
+    res_d = _t(res)
+    out = res_d if in_place else _nan(batch, n_embd)
+    qdq.q4k_ffn_residual(Wg, Wu, Wd, _t(x), res_d, out, mid, n_embd, n_ff, batch)
+    wd = oracle.q4k_dequant(d, n_embd, n_ff)
+    o = oracle.ffn_residual(oracle.q4k_dequant(g, n_ff, n_embd), oracle.q4k_dequant(u, n_ff, n_embd), wd, x, res)
+    err = np.abs(_np(out) - o["out"])
+    assert np.all(err <= ffn_bound(o, wd))
+    assert np.all(np.abs(_np(mid) - o["mid"]) <= swiglu_eps(o))
+
+
+@pytest.mark.parametrize("n_embd,n_ff,batch", [(256, 512, 1), (512, 1280, 2), (768, 2048, 5)])
+def test_q4k_ffn_residual_parity(cuda_lib, n_embd, n_ff, batch):
+    _ffn_case(cuda_lib, n_embd, n_ff, batch, seed=n_embd + n_ff + batch)
+
+
+def test_q4k_ffn_residual_in_place(cuda_lib):
+    _ffn_case(cuda_lib, 512, 1024, 2, seed=99, in_place=True)
+
+
+def test_q4k_ffn_residual_full_size_config3(cuda_lib):
+    _ffn_case(cuda_lib, 3072, 8192, 1, seed=0, layer=0)
+
+
+# ------------------------------------------------------------------ batch GEMM (tensor cores)
+
+def _gemm_case(qdq, n_out, n_in, M, wb=None, X=None, sample_rows=None, seed=0):
+    import torch
+    rng = np.random.default_rng(seed)
+    if wb is None:
+        wb = synth.q8_0_blocks(rng, n_out, n_in)
+    if X is None:
+        X = synth.activations(rng, M, n_in)
+    W = qdq.upload_q8_0(wb, n_out, n_in)
+    Y = _nan(M, n_out)
+    ws = torch.empty(qdq.q8_0_gemm_batch_workspace_bytes(M, n_in), dtype=torch.uint8, device=_dev())
+    qdq.q8_0_gemm_batch(W, _t(X), Y, ws, n_out, n_in, M)
+    Yh = _np(Y)
+    rows = np.arange(M) if sample_rows is None else sample_rows
+    Y_ref, A = oracle.gemm_batch(oracle.q8_0_dequant(wb, n_out, n_in), X[rows])
+    assert gemv_excess(Yh[rows], Y_ref, A, rel=4e-3) <= 1.0
+    assert qdq.pipeline_timeouts() == 0
+
+
+@pytest.mark.parametrize("M", [1, 16, 20, 64, 100, 200, 257, 512])
+def test_q8_0_gemm_batch_parity_small(cuda_lib, M):
+    _gemm_case(cuda_lib, 256, 512, M, seed=M)
+
+
+@pytest.mark.parametrize("n_out,n_in,M", [(384, 1024, 33), (128, 64, 16), (1024, 2048, 130)])
+def test_q8_0_gemm_batch_parity_shapes(cuda_lib, n_out, n_in, M):
+    _gemm_case(cuda_lib, n_out, n_in, M, seed=n_out + M)
+
+
+@pytest.mark.parametrize("kind", [0, 1])
+@pytest.mark.parametrize("M", [16, 64, 512])
+def test_q8_0_gemm_batch_full_size_config4(cuda_lib, kind, M):
+    n_out, n_in = (8192, 3072) if kind == 0 else (3072, 8192)
+    sample = None if M <= 64 else np.random.default_rng(M).choice(M, 12, replace=False)
+    _gemm_case(cuda_lib, n_out, n_in, M, wb=synth.config4_w(kind), X=synth.config4_x(kind, M),
+               sample_rows=sample)
+
+
+def test_q8_0_gemm_batch_m1_matches_gemv_within_bf16_bound(cuda_lib):
+    qdq = cuda_lib
+    import torch
+    wb, x = synth.config0()
+    W = qdq.upload_q8_0(wb, 256, 512)
+    y = _nan(1, 256)
+    Y = _nan(1, 256)
+    qdq.q8_0_gemv(W, _t(x), y, 256, 512, 1)
+    ws = torch.empty(qdq.q8_0_gemm_batch_workspace_bytes(1, 512), dtype=torch.uint8, device=_dev())
+    qdq.q8_0_gemm_batch(W, _t(x), Y, ws, 256, 512, 1)
+    _, a = oracle.gemv(oracle.q8_0_dequant(wb, 256, 512), x)
+    assert np.all(np.abs(_np(Y) - _np(y)) <= 4e-3 * a)
+
+
+# ------------------------------------------------------------------ launch options, errors
+
+def test_launch_options_do_not_change_results(cuda_lib):
+    qdq = cuda_lib
+    rng = np.random.default_rng(21)
+    wb = synth.q4k_blocks(rng, 700, 2048)
+    x = synth.activations(rng, 1, 2048)
+    W = qdq.upload_q4k(wb, 700, 2048)
+    outs = []
+    for pdl, pf in [(1, 1), (0, 0), (1, 0), (0, 1)]:
+        old_pdl = qdq.set_option(qdq.QDQ_OPT_PDL, pdl)
+        old_pf = qdq.set_option(qdq.QDQ_OPT_L2_PREFETCH, pf)
+        y = _nan(1, 700)
+        qdq.q4k_gemv(W, _t(x), y, 700, 2048, 1)
+        outs.append(_np(y))
+        qdq.set_option(qdq.QDQ_OPT_PDL, old_pdl)
+        qdq.set_option(qdq.QDQ_OPT_L2_PREFETCH, old_pf)
+    for o in outs[1:]:
+        assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32))
+
+
+def test_error_leaves_outputs_untouched(cuda_lib):
+    qdq = cuda_lib
+    import torch
+    wb = synth.q8_0_blocks(np.random.default_rng(1), 64, 256)
+    W = qdq.upload_q8_0(wb, 64, 256)
+    x = _t(synth.activations(np.random.default_rng(2), 1, 256))
+    y = _nan(1, 64)
+    with pytest.raises(qdq.QdqError) as e:
+        qdq.q8_0_gemv(W, int(x.data_ptr()) + 4, y, 64, 256, 1)   # misaligned x
+    assert e.value.status == qdq.QDQ_ERR_ALIGN
+    with pytest.raises(qdq.QdqError) as e:
+        qdq.q8_0_gemv(W, x, y, 64, 256, 9)                        # batch too large
+    assert e.value.status == qdq.QDQ_ERR_DIMS
+    assert np.all(np.isnan(_np(y)))
+    torch.cuda.synchronize()

@@ -1,0 +1,130 @@
+"""Host-side checks of the C-ABI library that need no GPU.
+
+* the shared library loads and exports every function ``include/qdq.h``
+  declares, and the Python binding declares a signature for each of them;
+* argument validation: NULL pointers, bad dimensions, misaligned pointers and
+  aliasing outputs are rejected with the documented status before anything
+  touches CUDA (fake, never-dereferenced addresses are enough here);
+* the packed-size helpers return the GGML byte counts.
+"""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qdq.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from ggml_quantized_dequant_gb300 import _build
+    import ggml_quantized_dequant_gb300 as qdq
+    _build.build()
+    return qdq.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(qdq_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ["qdq_q8_0_gemv", "qdq_q4k_gemv", "qdq_q4k_swiglu", "qdq_q4k_ffn_residual",
+                 "qdq_q8_0_gemm_batch", "qdq_q8_0_pack", "qdq_q4k_pack"]:
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported_and_bound(lib):
+    import ggml_quantized_dequant_gb300 as qdq
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in qdq.SIGNATURES, name
+
+
+def test_no_cuda_symbols_in_signatures_are_torch_types():
+    # the C ABI uses plain pointers and sizes only
+    src = open(HEADER).read()
+    assert "torch" not in src.lower().replace("torch types", "")
+
+
+GOOD = 0x10000000  # a 256-byte aligned fake device address (never dereferenced)
+
+
+def test_packed_sizes(lib):
+    assert lib.qdq_q8_0_packed_bytes(8192, 3072) == 8192 * 3072 // 32 * 34
+    assert lib.qdq_q4k_packed_bytes(8192, 3072) == 8192 * 3072 // 256 * 144
+    assert lib.qdq_q8_0_packed_bytes(4, 33) == 0
+    assert lib.qdq_q4k_packed_bytes(4, 300) == 0
+    assert lib.qdq_q8_0_packed_bytes(0, 32) == 0
+    assert lib.qdq_q8_0_gemm_batch_workspace_bytes(16, 3072) == 16 * 3072 * 2
+
+
+def test_gemv_argument_validation(lib):
+    import ggml_quantized_dequant_gb300 as qdq
+    W, x, y = GOOD, GOOD + (1 << 28), GOOD + (2 << 28)
+    assert lib.qdq_q8_0_gemv(None, x, y, 64, 64, 1, None) == qdq.QDQ_ERR_NULL
+    assert lib.qdq_q8_0_gemv(W, x, y, 64, 48, 1, None) == qdq.QDQ_ERR_DIMS      # n_in % 32
+    assert lib.qdq_q8_0_gemv(W, x, y, 0, 64, 1, None) == qdq.QDQ_ERR_DIMS
+    assert lib.qdq_q8_0_gemv(W, x, y, 64, 64, 0, None) == qdq.QDQ_ERR_DIMS      # batch 0
+    assert lib.qdq_q8_0_gemv(W, x, y, 64, 64, 9, None) == qdq.QDQ_ERR_DIMS      # batch > 8
+    assert lib.qdq_q8_0_gemv(W + 8, x, y, 64, 64, 1, None) == qdq.QDQ_ERR_ALIGN
+    assert lib.qdq_q8_0_gemv(W, x + 4, y, 64, 64, 1, None) == qdq.QDQ_ERR_ALIGN
+    assert lib.qdq_q8_0_gemv(W, x, y + 2, 64, 64, 1, None) == qdq.QDQ_ERR_ALIGN
+    assert lib.qdq_q8_0_gemv(W, x, W + 64, 64, 64, 1, None) == qdq.QDQ_ERR_ALIAS  # y inside W
+    assert lib.qdq_q8_0_gemv(W, x, x, 64, 64, 1, None) == qdq.QDQ_ERR_ALIAS
+    assert lib.qdq_q8_0_gemv(W, x, y, 64, 1 << 20, 1, None) == qdq.QDQ_ERR_UNSUPPORTED
+    assert lib.qdq_q4k_gemv(W, x, y, 64, 128, 1, None) == qdq.QDQ_ERR_DIMS       # n_in % 256
+    assert lib.qdq_q4k_gemv(W, None, y, 64, 256, 1, None) == qdq.QDQ_ERR_NULL
+
+
+def test_swiglu_and_ffn_validation(lib):
+    import ggml_quantized_dequant_gb300 as qdq
+    Wg, Wu, Wd = GOOD, GOOD + (1 << 28), GOOD + (2 << 28)
+    x, res, out, mid = GOOD + (3 << 28), GOOD + (4 << 28), GOOD + (5 << 28), GOOD + (6 << 28)
+    assert lib.qdq_q4k_swiglu(Wg, None, x, mid, 512, 256, 1, None) == qdq.QDQ_ERR_NULL
+    assert lib.qdq_q4k_swiglu(Wg, Wu, x, mid, 512, 255, 1, None) == qdq.QDQ_ERR_DIMS
+    assert lib.qdq_q4k_swiglu(Wg, Wu + 4, x, mid, 512, 256, 1, None) == qdq.QDQ_ERR_ALIGN
+    assert lib.qdq_q4k_swiglu(Wg, Wu, x, Wu + 16, 512, 256, 1, None) == qdq.QDQ_ERR_ALIAS
+    args = dict(n_embd=256, n_ff=512, batch=1)
+    f = lambda *p: lib.qdq_q4k_ffn_residual(*p, args["n_embd"], args["n_ff"], args["batch"], None)  # noqa: E731
+    assert f(Wg, Wu, Wd, x, res, out, None) == qdq.QDQ_ERR_NULL
+    assert f(Wg, Wu, Wd, x, res, out, mid + 4) == qdq.QDQ_ERR_ALIGN
+    assert f(Wg, Wu, Wd, x, res, out, x) == qdq.QDQ_ERR_ALIAS            # mid overlaps x
+    assert f(Wg, Wu, Wd, x, res, res + 4, mid) == qdq.QDQ_ERR_ALIAS      # partial overlap with residual
+    assert f(Wg, Wu, Wd, x, res, x, mid) == qdq.QDQ_ERR_ALIAS            # out over x
+    assert lib.qdq_q4k_ffn_residual(Wg, Wu, Wd, x, res, out, mid, 256, 500, 1, None) == qdq.QDQ_ERR_DIMS
+    assert lib.qdq_q4k_ffn_residual(Wg, Wu, Wd, x, res, out, mid, 256, 512, 9, None) == qdq.QDQ_ERR_DIMS
+
+
+def test_gemm_validation(lib):
+    import ggml_quantized_dequant_gb300 as qdq
+    W, X, Y, ws = GOOD, GOOD + (1 << 28), GOOD + (2 << 28), GOOD + (3 << 28)
+    assert lib.qdq_q8_0_gemm_batch(W, X, Y, None, 256, 512, 16, None) == qdq.QDQ_ERR_NULL
+    assert lib.qdq_q8_0_gemm_batch(W, X, Y, ws, 256, 512, 0, None) == qdq.QDQ_ERR_DIMS
+    assert lib.qdq_q8_0_gemm_batch(W, X, Y, ws, 256, 480, 16, None) == qdq.QDQ_ERR_UNSUPPORTED  # n_in % 64
+    assert lib.qdq_q8_0_gemm_batch(W, X, Y, ws, 200, 512, 16, None) == qdq.QDQ_ERR_UNSUPPORTED  # n_out % 128
+    assert lib.qdq_q8_0_gemm_batch(W, X, Y, ws + 64, 256, 512, 16, None) == qdq.QDQ_ERR_ALIGN
+    assert lib.qdq_q8_0_gemm_batch(W, X, X, ws, 256, 512, 16, None) == qdq.QDQ_ERR_ALIAS
+
+
+def test_pack_validation(lib):
+    import ggml_quantized_dequant_gb300 as qdq
+    assert lib.qdq_q8_0_pack(GOOD, None, 4, 32, None) == qdq.QDQ_ERR_NULL
+    assert lib.qdq_q8_0_pack(GOOD, GOOD + 8, 4, 32, None) == qdq.QDQ_ERR_ALIGN
+    assert lib.qdq_q8_0_pack(GOOD, GOOD + 16, 4, 32, None) == qdq.QDQ_ERR_ALIAS
+    assert lib.qdq_q4k_pack(GOOD, GOOD + (1 << 20), 4, 100, None) == qdq.QDQ_ERR_DIMS
+
+
+def test_options_and_strings(lib):
+    import ggml_quantized_dequant_gb300 as qdq
+    assert lib.qdq_set_option(99, 1) == qdq.QDQ_ERR_DIMS
+    assert lib.qdq_set_option(qdq.QDQ_OPT_CTAS_PER_SM, 9) == qdq.QDQ_ERR_DIMS
+    prev = lib.qdq_set_option(qdq.QDQ_OPT_PDL, 0)
+    assert prev in (0, 1)
+    assert lib.qdq_set_option(qdq.QDQ_OPT_PDL, prev) == 0
+    assert b"QDQ_ERR_ALIAS" in lib.qdq_status_string(qdq.QDQ_ERR_ALIAS)
+    assert lib.qdq_last_cuda_error() == 0
+    assert b"sm_103a" in lib.qdq_version()
