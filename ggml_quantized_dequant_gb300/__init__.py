@@ -27,6 +27,8 @@ QDQ_MAX_GEMV_N_IN = 49152
 QDQ_OPT_PDL = 1
 QDQ_OPT_L2_PREFETCH = 2
 QDQ_OPT_CTAS_PER_SM = 3
+QDQ_OPT_XS_GROUPS = 4
+QDQ_OPT_XS_STAGES = 5
 
 _c_int, _c_size, _c_vp, _c_char_p = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_char_p
 

@@ -14,6 +14,8 @@ thread_local int g_last_cuda_error = 0;
 std::atomic<int> g_opt_pdl{1};
 std::atomic<int> g_opt_l2_prefetch{1};
 std::atomic<int> g_opt_ctas_per_sm{1};
+std::atomic<int> g_opt_xs_groups{0};
+std::atomic<int> g_opt_xs_stages{0};
 
 constexpr int kMaxDevices = 64;
 std::once_flag g_dev_once[kMaxDevices];
@@ -32,6 +34,8 @@ std::vector<SmemEntry> g_smem;
 int opt_pdl() { return g_opt_pdl.load(std::memory_order_relaxed); }
 int opt_l2_prefetch() { return g_opt_l2_prefetch.load(std::memory_order_relaxed); }
 int opt_ctas_per_sm() { return g_opt_ctas_per_sm.load(std::memory_order_relaxed); }
+int opt_xs_groups() { return g_opt_xs_groups.load(std::memory_order_relaxed); }
+int opt_xs_stages() { return g_opt_xs_stages.load(std::memory_order_relaxed); }
 
 int fail_cuda(cudaError_t e) {
   g_last_cuda_error = int(e);
@@ -140,6 +144,12 @@ int qdq_set_option(int key, int value) {
     case QDQ_OPT_CTAS_PER_SM:
       if (value < 1 || value > 4) return QDQ_ERR_DIMS;
       return g_opt_ctas_per_sm.exchange(value);
+    case QDQ_OPT_XS_GROUPS:
+      if (value < 0 || value > 16) return QDQ_ERR_DIMS;
+      return g_opt_xs_groups.exchange(value);
+    case QDQ_OPT_XS_STAGES:
+      if (value < 0 || value > 16) return QDQ_ERR_DIMS;
+      return g_opt_xs_stages.exchange(value);
     default: return QDQ_ERR_DIMS;
   }
 }

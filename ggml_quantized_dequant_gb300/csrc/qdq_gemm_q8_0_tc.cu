@@ -18,16 +18,17 @@
 // when the tile count alone cannot fill the SMs, and split partial sums are
 // added into Y with f32 atomics (Y zeroed by the conversion kernel first).
 //
-// Warp roles (192 threads):
-//   warps 0-3  dequantise: thread t owns weight row t of the tile; it reads
-//              the 64 int8 quants of that row (TMA-staged, 64-byte swizzle),
-//              scales them by the row's two fp16 block scales and writes the
-//              bf16 row into the A tile in the 128-byte-swizzled K-major
-//              layout the tensor core reads; after the last stage the same
-//              warps read the accumulator out of TMEM and store Y;
-//   warp 4     TMA producer: int8 weight tile (128 x 64) and bf16 activation
+// Warp roles (576 threads):
+//   warps 0-15 dequantise: four threads per weight row of the tile, each
+//              taking 16 of the row's 64 int8 quants (TMA-staged, 64-byte
+//              swizzle), scaling them by their fp16 block scale and writing
+//              the bf16 values into the A tile in the 128-byte-swizzled
+//              K-major layout the tensor core reads; after the last stage the
+//              same warps read the accumulator out of TMEM (warp w reads TMEM
+//              lanes 32*(w%4).. and every fourth 16-column chunk) and store Y;
+//   warp 16    TMA producer: int8 weight tile (128 x 64) and bf16 activation
 //              tile (N x 64, 128-byte swizzle) per stage;
-//   warp 5     allocates TMEM, and one lane issues tcgen05.mma (K = 16 each)
+//   warp 17    allocates TMEM, and one lane issues tcgen05.mma (K = 16 each)
 //              and tcgen05.commit to release each stage.
 // Every mbarrier wait is bounded by a wall-clock limit; a wait that runs out
 // counts a pipeline timeout (qdq_pipeline_timeouts) and the CTA winds down
@@ -48,54 +49,11 @@ namespace {
 
 constexpr int BM = 128;  // weight rows per tile (MMA M)
 constexpr int BK = 64;   // K per stage (128 bytes of bf16: one swizzle span)
-constexpr int kDequantWarps = 4;
+constexpr int kDequantWarps = 16;                 // 4 per SM sub-partition: hides ALU latency
+constexpr int kThreadsPerRow = kDequantWarps / 4;  // dequant threads per weight row
 constexpr int kThreads = 32 * (kDequantWarps + 2);
 constexpr uint32_t kQTileBytes = BM * BK;      // int8 weight tile
 constexpr uint32_t kATileBytes = BM * BK * 2;  // bf16 weight tile
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// ---- mbarrier ---------------------------------------------------------------
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Wait for the phase with the given parity; false if the wall-clock limit ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-  const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
-  const unsigned long long t0 = global_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(a, parity)) return true;
-    if ((i & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
-
 // ---- TMA ----------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, int x, int y, uint64_t *bar) {
   asm volatile(
@@ -169,8 +127,9 @@ template <int N>
 __global__ void __launch_bounds__(kThreads, 1)
     q8_0_gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_x,
                         const uint8_t *__restrict__ W, float *__restrict__ Y, int n_out, int n_in, int M,
-                        int kb_per_split, int atomic_out) {
+                        int kb_per_split, int atomic_out, const Magic mg_param) {
   using C = GemmCfg<N>;
+  const Magic mg = lane_magic(mg_param);
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -264,11 +223,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- dequantise, then epilogue ----------------
     pdl_wait();
-    const int row = threadIdx.x;  // 0..127 = weight row within the tile = TMEM lane
+    const int row = threadIdx.x & (BM - 1);  // weight row within the tile = TMEM lane
+    const int part = threadIdx.x >> 7;       // which 16 of the row's 64 quants
     const int grow = tile_n * BM + row;
     const uint32_t *d32 = reinterpret_cast<const uint32_t *>(W + int64_t(n_out) * n_in) + int64_t(grow) * (n_in / BK);
     uint32_t dnext = __ldg(d32 + kb0);
     bool ok = true;
+    const int qsw = (row >> 1) & 3;  // 64-byte swizzle of the TMA-written int8 tile
     for (int i = 0; i < nk; ++i) {
       const int s = i % S;
       const uint32_t dcur = dnext;
@@ -280,25 +241,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint8_t *qt = smem + s * C::kStageBytes;
       uint8_t *at = smem + s * C::kStageBytes + kQTileBytes;
-      const int qsw = (row >> 1) & 3;  // 64-byte swizzle of the TMA-written int8 tile
       const __half2 dh = *reinterpret_cast<const __half2 *>(&dcur);
-      const float2 dd = __half22float2(dh);  // block scales for K 0..31 and 32..63
+      const float dsc = part < 2 ? __low2float(dh) : __high2float(dh);  // block scale of K 32*(part/2)..
+      const float2 dpair = f2(dsc, dsc);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cq = 0; cq < 4 / kThreadsPerRow; ++cq) {
+        const int c = part * (4 / kThreadsPerRow) + cq;  // 16-byte quant chunk (K 16c..16c+15)
         const uint4 qv = *reinterpret_cast<const uint4 *>(qt + row * 64 + ((c ^ qsw) << 4));
-        const float dsc = c < 2 ? dd.x : dd.y;
-        const f2 dpair = f2_make(dsc, dsc);
         const uint32_t words[4] = {qv.x, qv.y, qv.z, qv.w};
         uint32_t packed[8];
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-          f2 q01, q23;
-          s8x4_to_f2(words[w], q01, q23);
-          float a0, a1, a2, a3;
-          f2_split(f2_mul(q01, dpair), a0, a1);
-          f2_split(f2_mul(q23, dpair), a2, a3);
-          const __nv_bfloat162 p01 = __floats2bfloat162_rn(a0, a1);
-          const __nv_bfloat162 p23 = __floats2bfloat162_rn(a2, a3);
+          float2 q01, q23;
+          s8x4_to_f2(words[w], mg, q01, q23);
+          const float2 a01 = __fmul2_rn(q01, dpair), a23 = __fmul2_rn(q23, dpair);  // exact: d*q fits in f32
+          const __nv_bfloat162 p01 = __float22bfloat162_rn(a01);
+          const __nv_bfloat162 p23 = __float22bfloat162_rn(a23);
           packed[2 * w] = *reinterpret_cast<const uint32_t *>(&p01);
           packed[2 * w + 1] = *reinterpret_cast<const uint32_t *>(&p23);
         }
@@ -314,17 +272,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok && mbar_wait(accum, 0)) {
       tc_fence_after();
-      const uint32_t lane_base = uint32_t(warp * 32) << 16;
+      const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
       const int m0 = tile_m * N;
 #pragma unroll 1
-      for (int c0 = 0; c0 < N; c0 += 16) {
+      for (int c0 = (warp >> 2) * 16; c0 < N; c0 += 16 * (kDequantWarps / 4)) {
         uint32_t r[16];
         tmem_ld16(tmem + lane_base + uint32_t(c0), r);
+        const int erow = tile_n * BM + (warp & 3) * 32 + lane;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int m = m0 + c0 + j;
           if (m < M) {
-            float *dst = Y + int64_t(m) * n_out + grow;
+            float *dst = Y + int64_t(m) * n_out + erow;
             if (atomic_out) atomicAdd(dst, __uint_as_float(r[j]));
             else *dst = __uint_as_float(r[j]);
           }
@@ -420,7 +379,7 @@ int launch_tile(const uint8_t *W, const float *X, float *Y, void *ws, int n_out,
   e = allow_dynamic_smem(reinterpret_cast<const void *>(kern), int(C::kSmemBytes));
   if (e != cudaSuccess) return fail_cuda(e);
   e = launch(kern, dim3(ntile_n, ntile_m, split), dim3(kThreads), C::kSmemBytes, s, tm_q, tm_x, W, Y, n_out, n_in,
-             M, kb_per, split > 1 ? 1 : 0);
+             M, kb_per, split > 1 ? 1 : 0, make_magic());
   return e == cudaSuccess ? QDQ_OK : fail_cuda(e);
 }
 
@@ -443,9 +402,16 @@ int launch_q8_0_gemm_batch(const void *Wv, const float *X, float *Y, void *ws, i
 
 }  // namespace qdq
 
-extern "C" int qdq_pipeline_timeouts(void) {
+namespace qdq {
+int read_gemm_timeouts() {
   unsigned int v = 0, zero = 0;
-  if (cudaMemcpyFromSymbol(&v, qdq::g_pipeline_timeouts, sizeof(v)) != cudaSuccess) return -1;
-  if (cudaMemcpyToSymbol(qdq::g_pipeline_timeouts, &zero, sizeof(zero)) != cudaSuccess) return -1;
+  if (cudaMemcpyFromSymbol(&v, g_pipeline_timeouts, sizeof(v)) != cudaSuccess) return -1;
+  if (cudaMemcpyToSymbol(g_pipeline_timeouts, &zero, sizeof(zero)) != cudaSuccess) return -1;
   return int(v);
+}
+}  // namespace qdq
+
+extern "C" int qdq_pipeline_timeouts(void) {
+  const int a = qdq::read_gemm_timeouts(), b = qdq::read_xs_timeouts();
+  return (a < 0 || b < 0) ? -1 : a + b;
 }

@@ -14,7 +14,9 @@
 //
 // Design (HBM-bound, like the Q8_0 kernel): one CTA per SM over a contiguous
 // row range, L2 bulk prefetch of that range before the programmatic-launch
-// wait, x and X_j in shared memory, two rows per warp task.  Lane l handles
+// wait, x and X_j in shared memory, two rows per warp task (gate and up row of
+// the same output for SwiGLU), tasks x lane-iterations split evenly across the
+// warps, P iterations of loads in flight per lane.  Lane l handles
 // sub-blocks l, l+32, ... of a row: 16 bytes of packed nibbles (weight e of
 // the sub-block in nibble e&1 of byte e/2) with one 128-bit load, and the
 // 16-byte header record of its superblock (d, dmin and the twelve-bit
@@ -34,45 +36,42 @@ constexpr int kWarps = kThreads / 32;
 
 enum Mode { kPlain = 0, kSwiglu = 1, kResidual = 2 };
 
-// Eight nibbles of `w` (weights 0..7 of a word) -> four exact float pairs.
-__device__ __forceinline__ void u4x8_to_f2(uint32_t w, f2 q[4]) {
-  const f2 bias01 = f2_make(-8388608.0f, -524288.0f);   // -2^23, -2^19
-  const f2 bias23 = f2_make(-32768.0f, -2048.0f);       // -2^15, -2^11
-  const uint32_t h = w >> 16;
-  q[0] = f2_add(f2_from_u32((w & 0x000Fu) | 0x4B000000u, (w & 0x00F0u) | 0x49000000u), bias01);
-  q[1] = f2_add(f2_from_u32((w & 0x0F00u) | 0x47000000u, (w & 0xF000u) | 0x45000000u), bias23);
-  q[2] = f2_add(f2_from_u32((h & 0x000Fu) | 0x4B000000u, (h & 0x00F0u) | 0x49000000u), bias01);
-  q[3] = f2_add(f2_from_u32((h & 0x0F00u) | 0x47000000u, (h & 0xF000u) | 0x45000000u), bias23);
-}
+// x staging: sub-block J (32 floats) of batch row b at float offset
+// (b * nsb + J) * kXStride, followed by its sum X_J in the next float; the
+// 144-byte stride puts the 16-byte reads of eight consecutive sub-blocks in
+// eight different bank groups (9J mod 8 = J mod 8), with no index math.
+constexpr int kXStride = 36;
 
 // (D, M) = (d*sc_j, dmin*m_j) for this lane's sub-block j from a header record.
-// `sel`/`sh` pick the 12-bit field j of the 96-bit field in words y, z, w.
-__device__ __forceinline__ f2 q4k_scale_pair(const uint4 h, int sel, int sh) {
-  const uint32_t lo = sel == 0 ? h.y : (sel == 1 ? h.z : h.w);
-  const uint32_t hi = sel == 0 ? h.z : h.w;
+// Field j (sc in bits 0-5, m in bits 6-11) starts at bit 12j of words y,z,w:
+// lanes j < 3 read it from (y, z), 3 <= j < 6 from (z, w), j >= 6 from w.
+__device__ __forceinline__ float2 q4k_scale_pair(const uint4 h, bool g0, bool g1, int sh, const Magic &k) {
+  const uint32_t lo = g0 ? h.y : (g1 ? h.z : h.w);
+  const uint32_t hi = g0 ? h.z : h.w;
   const uint32_t v = __funnelshift_r(lo, hi, sh);
-  // sc in bits 0..5 -> 2^23 + sc;  m in bits 6..11 -> 2^17 + m
-  const f2 scm = f2_add(f2_from_u32((v & 0x3Fu) | 0x4B000000u, (v & 0xFC0u) | 0x48000000u),
-                        f2_make(-8388608.0f, -131072.0f));
-  const __half2 dd = *reinterpret_cast<const __half2 *>(&h.x);
-  const float2 df = __half22float2(dd);  // (d, dmin)
-  return f2_mul(f2_make(df.x, df.y), scm);
+  // sc -> 2^23 + sc;  m (bits 6..11) -> 2^17 + m
+  const float2 scm = q4k_field_to_f2(v, k);
+  const float2 dd = __half22float2(*reinterpret_cast<const __half2 *>(&h.x));  // (d, dmin)
+  return __fmul2_rn(dd, scm);
 }
 
-template <int NB, int MODE>
+template <int NB, int MODE, int P>
 __global__ void __launch_bounds__(kThreads) q4k_gemv_kernel(const uint8_t *__restrict__ W,
                                                             const uint8_t *__restrict__ W2,
                                                             const float *__restrict__ x,
                                                             const float *residual, float *y, int n_out,
-                                                            int n_in, int l2_prefetch) {
+                                                            int n_in, int l2_prefetch, const Magic mg_param) {
   extern __shared__ float4 smem4[];
+  const Magic mg = lane_magic(mg_param);
   constexpr int kRowsPerTask = MODE == kSwiglu ? 1 : 2;  // output rows per warp task
+  constexpr int kOut = MODE == kSwiglu ? 2 : 1;          // sums per output row
   const int nsb = n_in >> 5;                              // sub-blocks per row
   const int64_t q_bytes = int64_t(n_out) * (n_in >> 1);
   const int64_t q_row = n_in >> 1;
   const int64_t h_row = int64_t(n_in >> 8) * 16;
   const int r_begin = int(int64_t(blockIdx.x) * n_out / gridDim.x);
   const int r_end = int(int64_t(blockIdx.x + 1) * n_out / gridDim.x);
+  const int nrows = r_end - r_begin;
 
   if (l2_prefetch && threadIdx.x == 0) {
     prefetch_range_l2(W, q_bytes, r_begin * q_row, r_end * q_row);
@@ -83,157 +82,172 @@ __global__ void __launch_bounds__(kThreads) q4k_gemv_kernel(const uint8_t *__res
     }
   }
   pdl_launch_dependents();
-  pdl_wait();
-
-  float4 *xs = smem4;                                                   // NB * nsb lines of 8 chunks
-  float *xsum = reinterpret_cast<float *>(smem4 + size_t(NB) * nsb * 8);  // NB * nsb sums
-  {
-    const float4 *x4 = reinterpret_cast<const float4 *>(x);
-    const int n4 = NB * nsb * 8;
-    for (int i = threadIdx.x; i < n4; i += kThreads) xs[swz_chunk(i >> 3, i & 7)] = x4[i];
-  }
-  __syncthreads();
-  for (int l = threadIdx.x; l < NB * nsb; l += kThreads) {
-    float s = 0.f;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const float4 v = xs[swz_chunk(l, c)];
-      s += (v.x + v.y) + (v.z + v.w);
-    }
-    xsum[l] = s;
-  }
-  __syncthreads();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j = lane & 7;  // sub-block index within the superblock, fixed per lane
-  const int sel = (12 * j) >> 5, sh = (12 * j) & 31;
-  const int ntask = (r_end - r_begin + kRowsPerTask - 1) / kRowsPerTask;
+  const bool g0 = j < 3, g1 = j < 6;
+  const int sh = (12 * j) & 31;
+  const int itpt = (nsb + 31) >> 5;  // lane iterations per task ("units")
+  const int ntask = (nrows + kRowsPerTask - 1) / kRowsPerTask;
+  const int total = ntask * itpt;
+  // balanced contiguous unit ranges; never shorter than a task, so at most two
+  // warps add into any output (two commuting shared-memory adds: deterministic)
+  int per = (total + kWarps - 1) / kWarps;
+  if (per < itpt) per = itpt;
+  const int k0 = min(warp * per, total);
+  const int k1 = min(k0 + per, total);
 
-  for (int task = warp; task < ntask; task += kWarps) {
-    const int r0 = r_begin + task * kRowsPerTask;
-    const uint8_t *qrow[2];
-    const uint8_t *hrow[2];
-    if (MODE == kSwiglu) {
-      qrow[0] = W + r0 * q_row;
-      hrow[0] = W + q_bytes + r0 * h_row;
-      qrow[1] = W2 + r0 * q_row;
-      hrow[1] = W2 + q_bytes + r0 * h_row;
-    } else {
+  // load cursor with per-task row pointers; the weight ring is filled before
+  // waiting on the previous kernel, which only x depends on
+  int lt = k0 / itpt, li = k0 - lt * itpt;
+  const uint8_t *lq[2];
+  const uint8_t *lh[2];
+  auto set_rows = [&]() {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const uint8_t *base = (MODE == kSwiglu && r == 1) ? W2 : W;
+      const int row = MODE == kSwiglu ? r_begin + lt : r_begin + min(2 * lt + r, nrows - 1);
+      lq[r] = base + row * q_row + lane * 16;
+      lh[r] = base + q_bytes + row * h_row + (lane >> 3) * 16;
+    }
+  };
+  uint4 qb[P][2], hb[P][2];
+  auto load = [&](int slot) {
+    if (lane + 32 * li < nsb) {
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        const int row = min(r0 + r, r_end - 1);  // a missing last row re-reads the previous one; result dropped
-        qrow[r] = W + row * q_row;
-        hrow[r] = W + q_bytes + row * h_row;
+        qb[slot][r] = ldg_stream(lq[r] + li * 512);
+        hb[slot][r] = ldg_stream(lh[r] + li * 64);
       }
     }
-    f2 acc[2][NB];
-    float accm[2][NB];
+    if (++li == itpt) {
+      li = 0;
+      ++lt;
+      set_rows();
+    }
+  };
+  if (k0 < k1) {
+    set_rows();
+#pragma unroll
+    for (int p = 0; p < P; ++p)
+      if (k0 + p < k1) load(p);
+  }
+
+  pdl_wait();
+  float *xs = reinterpret_cast<float *>(smem4);
+  float *ysm = xs + size_t(NB) * nsb * kXStride;  // [kOut][nrows][NB]
+  {
+    const float4 *x4 = reinterpret_cast<const float4 *>(x);
+    for (int i = threadIdx.x; i < NB * nsb * 8; i += kThreads)
+      *reinterpret_cast<float4 *>(xs + (i >> 3) * kXStride + (i & 7) * 4) = x4[i];
+    for (int i = threadIdx.x; i < kOut * nrows * NB; i += kThreads) ysm[i] = 0.f;
+  }
+  __syncthreads();
+  for (int l = threadIdx.x; l < NB * nsb; l += kThreads) {
+    const float *xl = xs + l * kXStride;
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float4 v = *reinterpret_cast<const float4 *>(xl + 4 * c);
+      s += (v.x + v.y) + (v.z + v.w);
+    }
+    xs[l * kXStride + 32] = s;
+  }
+  __syncthreads();
+
+  if (k0 < k1) {
+    int ct = k0 / itpt, ci = k0 - ct * itpt;  // compute cursor
+    float2 acc[2][NB];
 #pragma unroll
     for (int r = 0; r < 2; ++r)
 #pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        acc[r][b] = f2_make(0.f, 0.f);
-        accm[r][b] = 0.f;
-      }
+      for (int b = 0; b < NB; ++b) acc[r][b] = f2(0.f, 0.f);
 
-    int J = lane;
-    uint4 qv[2], hv[2];
-    if (J < nsb) {
+    for (int kb = k0; kb < k1; kb += P) {
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        qv[r] = ldg_stream(qrow[r] + int64_t(J) * 16);
-        hv[r] = ldg_stream(hrow[r] + int64_t(J >> 3) * 16);
-      }
-    }
-    while (J < nsb) {
-      const int nx = J + 32;
-      uint4 qn[2], hn[2];
-      if (nx < nsb) {
+      for (int p = 0; p < P; ++p) {
+        const int k = kb + p;
+        if (k < k1) {
+          const int J = lane + 32 * ci;
+          if (J < nsb) {
+            float2 DM[2];
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          qn[r] = ldg_stream(qrow[r] + int64_t(nx) * 16);
-          hn[r] = ldg_stream(hrow[r] + int64_t(nx >> 3) * 16);
-        }
-      }
-      f2 DM[2];
+            for (int r = 0; r < 2; ++r) DM[r] = q4k_scale_pair(hb[p][r], g0, g1, sh, mg);
+            float2 S[2][NB], T[2][NB];  // two independent chains per row
 #pragma unroll
-      for (int r = 0; r < 2; ++r) DM[r] = q4k_scale_pair(hv[r], sel, sh);
-
-      f2 S[2][NB];
+            for (int r = 0; r < 2; ++r)
 #pragma unroll
-      for (int r = 0; r < 2; ++r)
+              for (int b = 0; b < NB; ++b) S[r][b] = T[r][b] = f2(0.f, 0.f);
+            const float *xj = xs + J * kXStride;
 #pragma unroll
-        for (int b = 0; b < NB; ++b) S[r][b] = f2_make(0.f, 0.f);
+            for (int wd = 0; wd < 4; ++wd) {
+              float2 q[2][4];
 #pragma unroll
-      for (int wd = 0; wd < 4; ++wd) {
-        f2 q[2][4];
+              for (int r = 0; r < 2; ++r) {
+                const uint32_t w = wd == 0 ? qb[p][r].x : wd == 1 ? qb[p][r].y : wd == 2 ? qb[p][r].z : qb[p][r].w;
+                u4x8_to_f2(w, mg, q[r]);
+              }
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const uint32_t w = wd == 0 ? qv[r].x : wd == 1 ? qv[r].y : wd == 2 ? qv[r].z : qv[r].w;
-          u4x8_to_f2(w, q[r]);
-        }
+              for (int b = 0; b < NB; ++b) {
+                const float4 xa = *reinterpret_cast<const float4 *>(xj + b * nsb * kXStride + 8 * wd);
+                const float4 xb = *reinterpret_cast<const float4 *>(xj + b * nsb * kXStride + 8 * wd + 4);
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          const int line = b * nsb + J;
-          const float4 xa = xs[swz_chunk(line, 2 * wd)];
-          const float4 xb = xs[swz_chunk(line, 2 * wd + 1)];
-          const f2 x01 = f2_make(xa.x, xa.y), x23 = f2_make(xa.z, xa.w);
-          const f2 x45 = f2_make(xb.x, xb.y), x67 = f2_make(xb.z, xb.w);
+                for (int r = 0; r < 2; ++r) {
+                  S[r][b] = __ffma2_rn(q[r][0], f2(xa.x, xa.y), S[r][b]);
+                  T[r][b] = __ffma2_rn(q[r][1], f2(xa.z, xa.w), T[r][b]);
+                  S[r][b] = __ffma2_rn(q[r][2], f2(xb.x, xb.y), S[r][b]);
+                  T[r][b] = __ffma2_rn(q[r][3], f2(xb.z, xb.w), T[r][b]);
+                }
+              }
+            }
 #pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            S[r][b] = f2_fma(q[r][0], x01, S[r][b]);
-            S[r][b] = f2_fma(q[r][1], x23, S[r][b]);
-            S[r][b] = f2_fma(q[r][2], x45, S[r][b]);
-            S[r][b] = f2_fma(q[r][3], x67, S[r][b]);
+            for (int b = 0; b < NB; ++b) {
+              const float xsum = xj[b * nsb * kXStride + 32];
+#pragma unroll
+              for (int r = 0; r < 2; ++r) {
+                // (acc.x, acc.y) += (D * S.x, D * S.y - M * X_J)
+                const float2 t = __ffma2_rn(f2(DM[r].x, DM[r].x), __fadd2_rn(S[r][b], T[r][b]), acc[r][b]);
+                acc[r][b] = f2(t.x, fmaf(-DM[r].y, xsum, t.y));
+              }
+            }
           }
-        }
-      }
+          if (k + P < k1) load(p);
+          if (++ci == itpt || k + 1 == k1) {  // this warp's share of task ct is complete
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        float D, M;
-        f2_split(DM[r], D, M);
+            for (int r = 0; r < 2; ++r) {
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          acc[r][b] = f2_fma(f2_make(D, D), S[r][b], acc[r][b]);
-          accm[r][b] = fmaf(-M, xsum[b * nsb + J], accm[r][b]);
-        }
-      }
-      if (nx < nsb) {
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          qv[r] = qn[r];
-          hv[r] = hn[r];
-        }
-      }
-      J = nx;
-    }
-
-    float v[2][NB];
-#pragma unroll
-    for (int r = 0; r < 2; ++r)
-#pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        float lo, hi;
-        f2_split(acc[r][b], lo, hi);
-        v[r][b] = warp_sum((lo + hi) + accm[r][b]);
-      }
-    if (lane == 0) {
-#pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        if (MODE == kSwiglu) {
-          const float g = v[0][b], u = v[1][b];
-          y[int64_t(b) * n_out + r0] = g / (1.0f + expf(-g)) * u;
-        } else {
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const int row = r0 + r;
-            if (row < r_end) {
-              const int64_t o = int64_t(b) * n_out + row;
-              y[o] = MODE == kResidual ? residual[o] + v[r][b] : v[r][b];
+              for (int b = 0; b < NB; ++b) {
+                const float v = warp_sum(acc[r][b].x + acc[r][b].y);
+                if (lane == 0) {
+                  if (MODE == kSwiglu) {
+                    atomicAdd(&ysm[(r * nrows + ct) * NB + b], v);
+                  } else if (2 * ct + r < nrows) {
+                    atomicAdd(&ysm[(2 * ct + r) * NB + b], v);
+                  }
+                }
+                acc[r][b] = f2(0.f, 0.f);
+              }
+            }
+            if (ci == itpt) {
+              ci = 0;
+              ++ct;
             }
           }
         }
       }
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < nrows * NB; i += kThreads) {
+    const int row = i / NB, b = i - row * NB;
+    const int64_t o = int64_t(b) * n_out + r_begin + row;
+    if (MODE == kSwiglu) {
+      const float g = ysm[i], u = ysm[nrows * NB + i];
+      y[o] = g / (1.0f + expf(-g)) * u;
+    } else if (MODE == kResidual) {
+      y[o] = residual[o] + ysm[i];
+    } else {
+      y[o] = ysm[i];
     }
   }
 }
@@ -242,18 +256,20 @@ template <int NB, int MODE>
 int launch_nb(const uint8_t *W, const uint8_t *W2, const float *x, const float *residual, float *y,
               int n_out, int n_in, cudaStream_t s, const DeviceInfo &di) {
   const int nsb = n_in >> 5;
-  const size_t smem = gemv_smem_bytes(di, size_t(NB) * nsb * (8 * sizeof(float4) + sizeof(float)));
-  auto kern = q4k_gemv_kernel<NB, MODE>;
+  const int rows_per_task = MODE == kSwiglu ? 1 : 2;
+  const int grid = gemv_grid(di, n_out, rows_per_task);
+  const int max_rows = (n_out + grid - 1) / grid;
+  const int outs = MODE == kSwiglu ? 2 : 1;
+  const size_t smem = gemv_smem_bytes(
+      di, size_t(NB) * nsb * kXStride * sizeof(float) + size_t(outs) * max_rows * NB * sizeof(float));
+  constexpr int P = NB <= 2 ? 4 : 2;  // loads in flight per lane
+  auto kern = q4k_gemv_kernel<NB, MODE, P>;
   if (smem > 48 * 1024) {
     const cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(kern), int(smem));
     if (e != cudaSuccess) return fail_cuda(e);
   }
-  const int rows_per_task = MODE == kSwiglu ? 1 : 2;
-  int grid = di.sm_count * opt_ctas_per_sm();
-  const int max_grid = (n_out + rows_per_task - 1) / rows_per_task;
-  if (grid > max_grid) grid = max_grid;
   const cudaError_t e = launch(kern, dim3(grid), dim3(kThreads), smem, s, W, W2, x, residual, y, n_out,
-                               n_in, opt_l2_prefetch());
+                               n_in, opt_l2_prefetch(), make_magic());
   return e == cudaSuccess ? QDQ_OK : fail_cuda(e);
 }
 
@@ -276,14 +292,19 @@ int dispatch(int nb, const uint8_t *W, const uint8_t *W2, const float *x, const 
 
 int launch_q4k_gemv(int mode, const void *Wv, const void *W2v, const float *x, const float *residual,
                     float *y, int n_out, int n_in, int batch, cudaStream_t s) {
+  if (gemv_xs_supported(n_in, batch, 1)) return launch_gemv_xs(1, mode, Wv, W2v, x, residual, y, n_out, n_in, s);
   DeviceInfo di;
   const cudaError_t e = device_info(&di);
   if (e != cudaSuccess) return fail_cuda(e);
   const uint8_t *W = static_cast<const uint8_t *>(Wv);
   const uint8_t *W2 = static_cast<const uint8_t *>(W2v);
   const int budget = di.max_smem_optin < 200 * 1024 ? di.max_smem_optin : 200 * 1024;
-  const int per_row = (n_in >> 5) * int(8 * sizeof(float4) + sizeof(float));
-  int per = budget / per_row;
+  const int rows_per_task = mode == kSwiglu ? 1 : 2;
+  const int grid = gemv_grid(di, n_out, rows_per_task);
+  const int max_rows = (n_out + grid - 1) / grid;
+  const int per_batch = (n_in >> 5) * kXStride * int(sizeof(float)) +
+                        (mode == kSwiglu ? 2 : 1) * max_rows * int(sizeof(float));
+  int per = budget / per_batch;
   if (per < 1) return QDQ_ERR_UNSUPPORTED;
   if (per > QDQ_MAX_GEMV_BATCH) per = QDQ_MAX_GEMV_BATCH;
   for (int b0 = 0; b0 < batch; b0 += per) {

@@ -1,0 +1,387 @@
+// Batch-1 dequant-GEMV fast path: "x-stationary" consumers fed by a bulk-copy
+// weight pipeline in shared memory.
+//
+// "Module cuda_lane", Functions: try_q8_0_cuda_gemv / q8_0_gemv_oracle_into
+// (Q8_0 GEMV), try_q4k_soa_gemv (Q4_K GEMV), try_q4k_soa_fused_swiglu
+// (out[i] = silu(gate_i . x) * (up_i . x)), try_q4k_soa_ffn_block_residual
+// (out = residual + W_down . mid).  Token decode multiplies one activation
+// vector by every weight matrix, so this is the path the decode loop takes.
+//
+// Layout of the work:
+//  * a row of n_in weights is cut into nblk = n_in / 32 column blocks (one Q8_0
+//    block, or one Q4_K sub-block); lane l of "slice" warp s owns block
+//    32 s + l for the whole kernel and keeps its 32 activations in registers,
+//    so WPR = ceil(nblk / 32) slice warps cover a row and x never goes through
+//    shared memory;
+//  * a CTA owns a contiguous range of output rows (one CTA per SM).  A
+//    producer warp streams them in stages of 4 rows -- quant bytes and scale
+//    (Q8_0 d) or header (Q4_K) bytes, each a contiguous range of its plane --
+//    with 1-D bulk async copies into a ring of stages in shared memory.  The
+//    weights do not depend on the previous kernel, so the ring is filled
+//    before the previous kernel has finished (programmatic dependent launch);
+//  * the slice warps form G groups; group g consumes stages g, g+G, ...  For
+//    each stage a lane reads its block of the 4 rows, and a recursive-halving
+//    butterfly reduces the 4 per-lane partial sums across the warp (lane 8k
+//    ends with row k's warp total).  The WPR slice totals of a row are added
+//    in fixed order at the end, so results are deterministic.
+// SwiGLU streams gate and up rows as pairs (a stage = 2 output rows, each
+// with its gate row and its up row) and combines them in the epilogue.
+// Every pipeline wait is bounded; a wait that runs out is counted
+// (qdq_pipeline_timeouts) and the CTA winds down instead of hanging.
+#include "qdq_internal.cuh"
+
+namespace qdq {
+
+__device__ unsigned int g_xs_timeouts = 0;
+
+namespace {
+
+constexpr int kStageRows = 4;    // virtual rows per stage = butterfly width
+constexpr int kMaxThreads = 544;  // up to 16 consumer warps + the producer
+
+enum Fmt { kQ8 = 0, kQ4 = 1 };
+enum Epi { kPlain = 0, kSwiglu = 1, kResidual = 2 };
+
+// Reduce v[0..3] (one partial per row per lane) over the warp; afterwards lane
+// 8k holds the warp total of row k.
+__device__ __forceinline__ void butterfly4(float v[kStageRows], int lane) {
+  {
+    const bool up = lane & 16;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float send = up ? v[i] : v[i + 2];
+      const float keep = up ? v[i + 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+  }
+  {
+    const bool up = lane & 8;
+    const float send = up ? v[0] : v[1];
+    const float keep = up ? v[1] : v[0];
+    v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 4);
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
+struct XsArgs {
+  const uint8_t *W;   // packed matrix (gate for SwiGLU)
+  const uint8_t *W2;  // up matrix (SwiGLU only)
+  const float *x;
+  const float *residual;
+  float *y;
+  int n_out;        // output rows
+  int n_in;
+  int wpr;          // slice warps per row
+  int groups;       // consumer groups per CTA
+  int sg;           // ring slots per consumer group (the ring holds groups * sg stages)
+  int stage_bytes;  // bytes per ring stage (multiple of 128)
+  int l2_prefetch;
+};
+
+template <int FMT, int EPI>
+__global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, const Magic mg_param) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int kV = EPI == kSwiglu ? 2 : 1;  // virtual rows per output row
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ncw = a.wpr * a.groups;  // consumer warps; warp ncw is the producer
+  const int n_in = a.n_in;
+  const int G = a.groups, SG = a.sg, S = G * SG;  // slots: group g owns g*SG .. g*SG+SG-1
+
+  const int r0 = int(int64_t(blockIdx.x) * a.n_out / gridDim.x);
+  const int r1 = int(int64_t(blockIdx.x + 1) * a.n_out / gridDim.x);
+  const int nv = (r1 - r0) * kV;                     // virtual rows of this CTA
+  const int nst = (nv + kStageRows - 1) / kStageRows;  // stages
+
+  const int64_t q_row = FMT == kQ8 ? int64_t(n_in) : int64_t(n_in >> 1);                  // quant bytes per row
+  const int64_t s_row = FMT == kQ8 ? int64_t(n_in >> 4) : int64_t(n_in >> 8) * 16;      // scale/header bytes per row
+  const int64_t q_bytes = int64_t(a.n_out) * q_row;
+
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + size_t(S) * a.stage_bytes);
+  uint64_t *empty = full + S;
+  float *psum = reinterpret_cast<float *>(empty + S);  // [nv][wpr]
+  __shared__ int s_abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], a.wpr);
+    }
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+
+  if (warp == ncw) {
+    // ---------------- producer: weights only, so no wait on the previous kernel ----------------
+    // Stage t goes to group g = t % G, which consumes its stages in order i = t / G
+    // from its own slots g*SG + i % SG; a slot is refilled only after that group
+    // released it, so no wait can ever see a phase that is two fills old.
+    if (lane == 0) {
+      if (a.l2_prefetch) {
+        prefetch_range_l2(a.W, q_bytes, r0 * q_row, r1 * q_row);
+        prefetch_range_l2(a.W + q_bytes, int64_t(a.n_out) * s_row, r0 * s_row, r1 * s_row);
+        if (EPI == kSwiglu) {
+          prefetch_range_l2(a.W2, q_bytes, r0 * q_row, r1 * q_row);
+          prefetch_range_l2(a.W2 + q_bytes, int64_t(a.n_out) * s_row, r0 * s_row, r1 * s_row);
+        }
+      }
+      int issued = 0;
+      for (int t = 0; t < nst; ++t) {
+        const int i = t / G;
+        const int s = (t % G) * SG + i % SG;
+        if (i >= SG && !mbar_wait(&empty[s], ((i / SG) + 1) & 1)) {
+          s_abort = 1;
+          break;
+        }
+        uint8_t *stq = smem + size_t(s) * a.stage_bytes;
+        uint8_t *sts = stq + kStageRows * q_row;
+        const int rr = r0 + t * (kStageRows / kV);     // first output row of the stage
+        const int nr = min(kStageRows / kV, r1 - rr);  // output rows in the stage
+        mbar_arrive_expect_tx(&full[s], uint32_t(kV * nr * (q_row + s_row)));
+        bulk_copy_g2s(stq, a.W + rr * q_row, uint32_t(nr * q_row), &full[s]);
+        bulk_copy_g2s(sts, a.W + q_bytes + rr * s_row, uint32_t(nr * s_row), &full[s]);
+        if (EPI == kSwiglu) {  // up rows go to slots 2, 3
+          bulk_copy_g2s(stq + 2 * q_row, a.W2 + rr * q_row, uint32_t(nr * q_row), &full[s]);
+          bulk_copy_g2s(sts + 2 * s_row, a.W2 + q_bytes + rr * s_row, uint32_t(nr * s_row), &full[s]);
+        }
+        issued = t + 1;
+      }
+      // never exit with copies in flight: wait for the last fill of every slot
+      for (int t = issued - S < 0 ? 0 : issued - S; t < issued; ++t) {
+        const int i = t / G;
+        mbar_wait(&full[(t % G) * SG + i % SG], (i / SG) & 1);
+      }
+    }
+  } else {
+    // ---------------- consumers ----------------
+    const int slice = warp % a.wpr, grp = warp / a.wpr;
+    const int blk = slice * 32 + lane;
+    const bool valid = blk < (n_in >> 5);
+    const Magic mg = lane_magic(mg_param);
+    pdl_wait();  // activations come from the previous kernel
+    float2 xr[16];  // activation pairs, kept as aligned register pairs for the packed FMAs
+    float xsum = 0.f;
+    if (valid) {
+      const float4 *xp = reinterpret_cast<const float4 *>(a.x + blk * 32);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const float4 v = __ldg(xp + c);
+        xr[2 * c] = f2(v.x, v.y);
+        xr[2 * c + 1] = f2(v.z, v.w);
+      }
+      if constexpr (FMT == kQ4) {
+        float2 t = f2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) t = __fadd2_rn(t, xr[c]);
+        xsum = t.x + t.y;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) xr[k] = f2(0.f, 0.f);
+    }
+    // Q4_K: this lane's 12-bit (sc, m) field lives at bit 12 j of header words 1..3
+    const int j = lane & 7;
+    const bool g0 = j < 3, g1 = j < 6;
+    const int sh = (12 * j) & 31;
+    // a lane past the end of the row reads block 0 (finite data) against x = 0
+    const int bq = valid ? blk : 0;
+    const int qoff = FMT == kQ8 ? bq * 32 : bq * 16;
+    const int soff = FMT == kQ8 ? bq * 2 : (bq >> 3) * 16;
+    // byte offsets of this lane's data for the 4 rows of a stage (the same in every stage);
+    // SwiGLU: virtual rows gate r, up r, gate r+1, up r+1 sit in slots 0, 2, 1, 3
+    int qofs[kStageRows], sofs[kStageRows];
+#pragma unroll
+    for (int k = 0; k < kStageRows; ++k) {
+      const int slot = EPI == kSwiglu ? ((k & 1) << 1) | (k >> 1) : k;
+      qofs[k] = int(slot * q_row) + qoff;
+      sofs[k] = int(kStageRows * q_row + slot * s_row) + soff;
+    }
+
+    int s = grp * SG;      // this group's current slot and the parity of its fill:
+    uint32_t parity = 0;   // tracked incrementally (no division in the loop)
+    for (int t = grp; t < nst; t += G) {
+      if (!mbar_wait(&full[s], parity)) {
+        s_abort = 1;
+        break;
+      }
+      const uint8_t *stq = smem + size_t(s) * a.stage_bytes;
+      float part[kStageRows];
+      // All four rows' loads first, then their arithmetic interleaved word by word:
+      // eight independent accumulation chains per lane.  Rows past the end of the
+      // last stage compute from stale shared memory and are dropped; the butterfly
+      // never mixes rows, so they cannot touch the kept sums.
+      if constexpr (FMT == kQ8) {
+        uint4 qa[kStageRows], qb[kStageRows];
+        float dv[kStageRows];
+#pragma unroll
+        for (int k = 0; k < kStageRows; ++k) {
+          qa[k] = *reinterpret_cast<const uint4 *>(stq + qofs[k]);
+          qb[k] = *reinterpret_cast<const uint4 *>(stq + qofs[k] + 16);
+          dv[k] = __half2float(*reinterpret_cast<const __half *>(stq + sofs[k]));
+        }
+        float2 s0[kStageRows], s1[kStageRows];
+#pragma unroll
+        for (int k = 0; k < kStageRows; ++k) s0[k] = s1[k] = f2(0.f, 0.f);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+          for (int k = 0; k < kStageRows; ++k) {
+            const uint32_t w = kk == 0 ? qa[k].x : kk == 1 ? qa[k].y : kk == 2 ? qa[k].z : kk == 3 ? qa[k].w
+                             : kk == 4 ? qb[k].x : kk == 5 ? qb[k].y : kk == 6 ? qb[k].z : qb[k].w;
+            float2 q01, q23;
+            s8x4_to_f2(w, mg, q01, q23);
+            s0[k] = __ffma2_rn(q01, xr[2 * kk], s0[k]);
+            s1[k] = __ffma2_rn(q23, xr[2 * kk + 1], s1[k]);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < kStageRows; ++k) {
+          const float2 st = __fadd2_rn(s0[k], s1[k]);
+          part[k] = dv[k] * (st.x + st.y);
+        }
+      } else {
+        uint4 q[kStageRows], h[kStageRows];
+#pragma unroll
+        for (int k = 0; k < kStageRows; ++k) {
+          q[k] = *reinterpret_cast<const uint4 *>(stq + qofs[k]);
+          h[k] = *reinterpret_cast<const uint4 *>(stq + sofs[k]);
+        }
+        float2 DM[kStageRows];
+#pragma unroll
+        for (int k = 0; k < kStageRows; ++k) {
+          const uint32_t lo = g0 ? h[k].y : (g1 ? h[k].z : h[k].w);
+          const uint32_t hi = g0 ? h[k].z : h[k].w;
+          const uint32_t f = __funnelshift_r(lo, hi, sh);
+          const float2 scm = q4k_field_to_f2(f, mg);  // (sc, m)
+          DM[k] = __fmul2_rn(__half22float2(*reinterpret_cast<const __half2 *>(&h[k].x)), scm);  // (d sc, dmin m)
+        }
+        float2 s0[kStageRows], s1[kStageRows];
+#pragma unroll
+        for (int k = 0; k < kStageRows; ++k) s0[k] = s1[k] = f2(0.f, 0.f);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+          for (int k = 0; k < kStageRows; ++k) {
+            const uint32_t w = kk == 0 ? q[k].x : kk == 1 ? q[k].y : kk == 2 ? q[k].z : q[k].w;
+            float2 qq[4];
+            u4x8_to_f2(w, mg, qq);
+            s0[k] = __ffma2_rn(qq[0], xr[4 * kk], s0[k]);
+            s1[k] = __ffma2_rn(qq[1], xr[4 * kk + 1], s1[k]);
+            s0[k] = __ffma2_rn(qq[2], xr[4 * kk + 2], s0[k]);
+            s1[k] = __ffma2_rn(qq[3], xr[4 * kk + 3], s1[k]);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < kStageRows; ++k) {
+          const float2 st = __fadd2_rn(s0[k], s1[k]);
+          part[k] = fmaf(DM[k].x, st.x + st.y, -DM[k].y * xsum);  // d sc_j sum(q x) - dmin m_j sum(x)
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done reading the stage
+      if (++s == (grp + 1) * SG) {
+        s = grp * SG;
+        parity ^= 1u;
+      }
+      butterfly4(part, lane);
+      if ((lane & 7) == 0) {
+        const int v = t * kStageRows + (lane >> 3);
+        if (v < nv) psum[v * a.wpr + slice] = part[0];
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && s_abort) atomicAdd(&g_xs_timeouts, 1u);
+  // epilogue: add the slice totals of each row in fixed order
+  const int nreal = r1 - r0;
+  for (int r = threadIdx.x; r < nreal; r += blockDim.x) {
+    if (EPI == kSwiglu) {
+      // stage t holds output rows 2t, 2t+1 as virtual rows (gate 2t, up 2t, gate 2t+1, up 2t+1)
+      const float *pg = psum + (2 * r) * a.wpr;
+      const float *pu = psum + (2 * r + 1) * a.wpr;
+      float g = 0.f, u = 0.f;
+      for (int s = 0; s < a.wpr; ++s) {
+        g += pg[s];
+        u += pu[s];
+      }
+      a.y[r0 + r] = g / (1.0f + expf(-g)) * u;
+    } else {
+      float v = 0.f;
+      const float *ps = psum + r * a.wpr;
+      for (int s = 0; s < a.wpr; ++s) v += ps[s];
+      a.y[r0 + r] = EPI == kResidual ? a.residual[r0 + r] + v : v;
+    }
+  }
+}
+
+template <int FMT, int EPI>
+int launch_xs(const uint8_t *W, const uint8_t *W2, const float *x, const float *residual, float *y, int n_out,
+              int n_in, cudaStream_t s, const DeviceInfo &di) {
+  XsArgs a;
+  a.W = W;
+  a.W2 = W2;
+  a.x = x;
+  a.residual = residual;
+  a.y = y;
+  a.n_out = n_out;
+  a.n_in = n_in;
+  a.wpr = ((n_in >> 5) + 31) / 32;
+  a.groups = a.wpr >= 12 ? 1 : 12 / a.wpr;  // about 12 consumer warps
+  if (opt_xs_groups() > 0) a.groups = opt_xs_groups();
+  if (32 * (a.wpr * a.groups + 1) > kMaxThreads) return QDQ_ERR_UNSUPPORTED;
+  a.l2_prefetch = opt_l2_prefetch();
+  const int64_t q_row = FMT == kQ8 ? n_in : n_in / 2;
+  const int64_t s_row = FMT == kQ8 ? n_in / 16 : (n_in / 256) * 16;
+  a.stage_bytes = int((kStageRows * (q_row + s_row) + 127) / 128 * 128);
+  int grid = di.sm_count * opt_ctas_per_sm();
+  if (grid > n_out) grid = n_out;
+  const int max_rows = (n_out + grid - 1) / grid;
+  const size_t psum_bytes = size_t(max_rows) * (EPI == kSwiglu ? 2 : 1) * a.wpr * sizeof(float);
+  // ring: about half an SM's shared memory, so the next kernel's CTA fits beside this one
+  const long budget = long(di.smem_per_sm) / 2 - di.reserved_smem_per_block - long(psum_bytes) - 1024;
+  int sg = int(budget / (long(a.stage_bytes) * a.groups));
+  if (sg > 8) sg = 8;
+  if (sg < 2) sg = 2;
+  if (opt_xs_stages() > 0) sg = opt_xs_stages();
+  a.sg = sg;
+  const int stages = a.groups * sg;
+  const size_t smem = size_t(stages) * a.stage_bytes + 2 * stages * sizeof(uint64_t) + psum_bytes;
+  if (smem > size_t(di.max_smem_optin)) return QDQ_ERR_UNSUPPORTED;
+  auto kern = gemv_xs_kernel<FMT, EPI>;
+  const cudaError_t e0 = allow_dynamic_smem(reinterpret_cast<const void *>(kern), int(smem));
+  if (e0 != cudaSuccess) return fail_cuda(e0);
+  const cudaError_t e = launch(kern, dim3(grid), dim3(32 * (a.wpr * a.groups + 1)), smem, s, a, make_magic());
+  return e == cudaSuccess ? QDQ_OK : fail_cuda(e);
+}
+
+}  // namespace
+
+bool gemv_xs_supported(int n_in, int batch, int fmt_q4k) {
+  // one 32-weight block per lane and at most 16 slice warps per row; stage copies of
+  // the Q8_0 scale plane start on 16-byte boundaries only when n_in % 256 == 0
+  return batch == 1 && (n_in >> 5) <= 32 * 16 && (fmt_q4k || n_in % 256 == 0);
+}
+
+int launch_gemv_xs(int fmt_q4k, int mode, const void *W, const void *W2, const float *x, const float *residual,
+                   float *y, int n_out, int n_in, cudaStream_t s) {
+  DeviceInfo di;
+  const cudaError_t e = device_info(&di);
+  if (e != cudaSuccess) return fail_cuda(e);
+  const uint8_t *w = static_cast<const uint8_t *>(W), *w2 = static_cast<const uint8_t *>(W2);
+  if (!fmt_q4k) return launch_xs<kQ8, kPlain>(w, w2, x, residual, y, n_out, n_in, s, di);
+  if (mode == 1) return launch_xs<kQ4, kSwiglu>(w, w2, x, residual, y, n_out, n_in, s, di);
+  if (mode == 2) return launch_xs<kQ4, kResidual>(w, w2, x, residual, y, n_out, n_in, s, di);
+  return launch_xs<kQ4, kPlain>(w, w2, x, residual, y, n_out, n_in, s, di);
+}
+
+int read_xs_timeouts() {
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_xs_timeouts, sizeof(v)) != cudaSuccess) return -1;
+  if (cudaMemcpyToSymbol(g_xs_timeouts, &zero, sizeof(zero)) != cudaSuccess) return -1;
+  return int(v);
+}
+
+}  // namespace qdq

@@ -12,6 +12,13 @@ namespace qdq {
 
 // ---------------------------------------------------------------- host side
 
+// Process-wide launch options (see QDQ_OPT_* in qdq.h).
+int opt_pdl();
+int opt_l2_prefetch();
+int opt_ctas_per_sm();
+int opt_xs_groups();
+int opt_xs_stages();
+
 // Per-device facts queried once (SM count, opt-in shared memory).
 struct DeviceInfo {
   int sm_count;
@@ -25,13 +32,17 @@ struct DeviceInfo {
 // CTAs plus one CTA of the next kernel but no more -- so the next kernel's
 // weight prefetch runs exactly one kernel ahead instead of flooding L2.
 size_t gemv_smem_bytes(const DeviceInfo &di, size_t need);
+
+// Grid of a streaming GEMV: CTAs-per-SM x SMs, but no more CTAs than tasks of
+// `rows_per_task` output rows.
+inline int gemv_grid(const DeviceInfo &di, int n_out, int rows_per_task) {
+  const int g = di.sm_count * opt_ctas_per_sm();
+  const int max_g = (n_out + rows_per_task - 1) / rows_per_task;
+  return g < max_g ? g : max_g;
+}
 // Returns 0 and fills `out` for the current device, or a cudaError_t.
 cudaError_t device_info(DeviceInfo *out);
 
-// Process-wide launch options (see QDQ_OPT_* in qdq.h).
-int opt_pdl();
-int opt_l2_prefetch();
-int opt_ctas_per_sm();
 
 // Records a CUDA error for qdq_last_cuda_error() and returns QDQ_ERR_CUDA.
 int fail_cuda(cudaError_t e);
@@ -75,6 +86,15 @@ int launch_q8_0_gemv(const void *W, const float *x, float *y, int n_out, int n_i
 // mode 2: y = residual + W x.
 int launch_q4k_gemv(int mode, const void *W, const void *W2, const float *x, const float *residual,
                     float *y, int n_out, int n_in, int batch, cudaStream_t s);
+// Batch-1 "x-stationary" GEMV fast path (qdq_gemv_xs.cu); fmt_q4k 0 = Q8_0,
+// 1 = Q4_K with mode 0/1/2 as launch_q4k_gemv.
+bool gemv_xs_supported(int n_in, int batch, int fmt_q4k);
+int launch_gemv_xs(int fmt_q4k, int mode, const void *W, const void *W2, const float *x, const float *residual,
+                   float *y, int n_out, int n_in, cudaStream_t s);
+// Pipeline-timeout counters of the translation units that run bounded waits:
+// each returns its count since the last call and resets it (-1 on CUDA error).
+int read_gemm_timeouts();
+int read_xs_timeouts();
 int launch_q8_0_gemm_batch(const void *W, const float *X, float *Y, void *workspace, int n_out,
                            int n_in, int M, cudaStream_t s);
 
@@ -106,6 +126,62 @@ __device__ __forceinline__ void prefetch_range_l2(const uint8_t *base, uint64_t 
   }
 }
 
+// ---- shared-memory pipelines (mbarrier + bulk async copies) -----------------
+// Every wait is bounded by a wall-clock limit: a wait that runs out returns
+// false and the caller winds its CTA down instead of hanging.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---- mbarrier ---------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase with the given parity; false if the wall-clock limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(a, parity)) return true;
+    if ((i & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// 1-D bulk async copy global -> shared, completing on an mbarrier (16-byte
+// aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 // 128-bit read-only load that does not allocate in L1 (streamed weights).
 __device__ __forceinline__ uint4 ldg_stream(const void *p) {
   uint4 v;
@@ -115,59 +191,94 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p) {
   return v;
 }
 
-// Packed f32x2 arithmetic (sm_100+): two lanes per instruction.
-struct f2 {
-  unsigned long long v;
+// Packed f32x2 arithmetic (sm_100+ builtins): two floats per instruction.
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+__device__ __forceinline__ float2 f2_bits(uint32_t a, uint32_t b) {
+  return make_float2(__uint_as_float(a), __uint_as_float(b));
+}
+
+// Exact small-integer -> f32 conversions without conversion instructions.  A
+// value v placed in mantissa bits [p, p+k) of a float whose exponent makes bit
+// p worth 1 reads as 2^(23-p) + v; subtracting 2^(23-p) (a packed f32x2 add)
+// leaves v exactly.  Each select is one LOP3 with the mask as an immediate and
+// the exponent pattern in a per-lane register: a LOP3 cannot take two uniform
+// operands, so patterns kept in uniform registers would cost a move per use.
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t c) {  // (a & MASK) | c
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(c));
+  return d;
+}
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t lop3_sel_xor(uint32_t a, uint32_t c) {  // MASK ? (a ^ c) : c
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "n"(MASK), "r"(c));
+  return d;
+}
+
+// Exponent patterns (and the matching subtraction constants), passed as kernel
+// parameters and moved into per-lane registers once per thread (lane_magic).
+struct Magic {
+  uint32_t s8_0, s8_1;                // Q8_0: byte 0 / byte 1 of a half, sign bit flipped: 2^23, 2^15 (+128)
+  uint32_t u4_0, u4_1, u4_2, u4_3;    // Q4_K: nibble 0..3 of a half: 2^23, 2^19, 2^15, 2^11
+  uint32_t sc, m;                     // Q4_K header: 6-bit scale at bit 0 (2^23), 6-bit min at bit 6 (2^17)
+  float2 b_s8, b_u4_01, b_u4_23, b_scm;  // subtraction constants
 };
-__device__ __forceinline__ f2 f2_make(float a, float b) {
-  f2 r;
-  asm("mov.b64 %0, {%1,%2};" : "=l"(r.v) : "f"(a), "f"(b));
-  return r;
+inline Magic make_magic() {
+  Magic k;
+  k.s8_0 = 0x4B000080u;
+  k.s8_1 = 0x47008000u;
+  k.u4_0 = 0x4B000000u;
+  k.u4_1 = 0x49000000u;
+  k.u4_2 = 0x47000000u;
+  k.u4_3 = 0x45000000u;
+  k.sc = 0x4B000000u;
+  k.m = 0x48000000u;
+  k.b_s8 = make_float2(-8388736.0f, -32896.0f);     // -(2^23 + 128), -(2^15 + 128)
+  k.b_u4_01 = make_float2(-8388608.0f, -524288.0f);  // -2^23, -2^19
+  k.b_u4_23 = make_float2(-32768.0f, -2048.0f);      // -2^15, -2^11
+  k.b_scm = make_float2(-8388608.0f, -131072.0f);    // -2^23, -2^17
+  return k;
 }
-__device__ __forceinline__ f2 f2_from_u32(uint32_t a, uint32_t b) {
-  f2 r;
-  asm("mov.b64 %0, {%1,%2};" : "=l"(r.v) : "r"(a), "r"(b));
-  return r;
-}
-__device__ __forceinline__ void f2_split(f2 a, float &lo, float &hi) {
-  asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
-}
-__device__ __forceinline__ f2 f2_add(f2 a, f2 b) {
-  f2 r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
-  return r;
-}
-__device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
-  f2 r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
-  return r;
-}
-__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
-  f2 r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+__device__ __forceinline__ uint32_t lane_reg(uint32_t v) { return __shfl_sync(0xffffffffu, v, threadIdx.x & 31); }
+__device__ __forceinline__ float lane_regf(float v) { return __shfl_sync(0xffffffffu, v, threadIdx.x & 31); }
+__device__ __forceinline__ Magic lane_magic(const Magic &k) {
+  Magic r;
+  r.s8_0 = lane_reg(k.s8_0);
+  r.s8_1 = lane_reg(k.s8_1);
+  r.u4_0 = lane_reg(k.u4_0);
+  r.u4_1 = lane_reg(k.u4_1);
+  r.u4_2 = lane_reg(k.u4_2);
+  r.u4_3 = lane_reg(k.u4_3);
+  r.sc = lane_reg(k.sc);
+  r.m = lane_reg(k.m);
+  r.b_s8 = f2(lane_regf(k.b_s8.x), lane_regf(k.b_s8.y));
+  r.b_u4_01 = f2(lane_regf(k.b_u4_01.x), lane_regf(k.b_u4_01.y));
+  r.b_u4_23 = f2(lane_regf(k.b_u4_23.x), lane_regf(k.b_u4_23.y));
+  r.b_scm = f2(lane_regf(k.b_scm.x), lane_regf(k.b_scm.y));
   return r;
 }
 
 // Four signed int8 in `w` -> exact floats as two pairs (q0,q1), (q2,q3).
-// A byte placed in mantissa bits [p, p+8) of a float whose exponent makes bit
-// p worth 1 reads as 2^(23-p) + (byte ^ 0x80); one packed subtraction of the
-// constants 2^(23-p) + 128 leaves q exactly (no conversion instructions).
-__device__ __forceinline__ void s8x4_to_f2(uint32_t w, f2 &q01, f2 &q23) {
-  const f2 bias = f2_make(-8388736.0f, -32896.0f);  // -(2^23 + 128), -(2^15 + 128)
+__device__ __forceinline__ void s8x4_to_f2(uint32_t w, const Magic &k, float2 &q01, float2 &q23) {
   const uint32_t hi = w >> 16;
-  const uint32_t a = ((w ^ 0x80u) & 0xFFu) | 0x4B000000u;      // 2^23 + (q0 + 128)
-  const uint32_t b = ((w ^ 0x8000u) & 0xFF00u) | 0x47000000u;  // 2^15 + (q1 + 128)
-  const uint32_t c = ((hi ^ 0x80u) & 0xFFu) | 0x4B000000u;
-  const uint32_t d = ((hi ^ 0x8000u) & 0xFF00u) | 0x47000000u;
-  q01 = f2_add(f2_from_u32(a, b), bias);
-  q23 = f2_add(f2_from_u32(c, d), bias);
+  q01 = __fadd2_rn(f2_bits(lop3_sel_xor<0x000000FFu>(w, k.s8_0), lop3_sel_xor<0x0000FF00u>(w, k.s8_1)), k.b_s8);
+  q23 = __fadd2_rn(f2_bits(lop3_sel_xor<0x000000FFu>(hi, k.s8_0), lop3_sel_xor<0x0000FF00u>(hi, k.s8_1)), k.b_s8);
 }
 
-// Activation staging in shared memory: rows of floats cut into 128-byte lines
-// of eight 16-byte chunks; chunk c of line l is stored at position c ^ (l & 7),
-// so the eight lanes of one 128-bit shared-memory phase that read the same
-// chunk of eight consecutive lines hit eight different bank groups.
-__device__ __forceinline__ int swz_chunk(int line, int chunk) { return (line << 3) | (chunk ^ (line & 7)); }
+// Eight unsigned nibbles of `w` (nibble i = bits 4i..4i+3) -> four exact float pairs.
+__device__ __forceinline__ void u4x8_to_f2(uint32_t w, const Magic &k, float2 q[4]) {
+  const uint32_t h = w >> 16;
+  q[0] = __fadd2_rn(f2_bits(lop3_and_or<0x000Fu>(w, k.u4_0), lop3_and_or<0x00F0u>(w, k.u4_1)), k.b_u4_01);
+  q[1] = __fadd2_rn(f2_bits(lop3_and_or<0x0F00u>(w, k.u4_2), lop3_and_or<0xF000u>(w, k.u4_3)), k.b_u4_23);
+  q[2] = __fadd2_rn(f2_bits(lop3_and_or<0x000Fu>(h, k.u4_0), lop3_and_or<0x00F0u>(h, k.u4_1)), k.b_u4_01);
+  q[3] = __fadd2_rn(f2_bits(lop3_and_or<0x0F00u>(h, k.u4_2), lop3_and_or<0xF000u>(h, k.u4_3)), k.b_u4_23);
+}
+
+// Q4_K header field (sc in bits 0..5, m in bits 6..11) -> (sc, m) as floats.
+__device__ __forceinline__ float2 q4k_field_to_f2(uint32_t f, const Magic &k) {
+  return __fadd2_rn(f2_bits(lop3_and_or<0x3Fu>(f, k.sc), lop3_and_or<0xFC0u>(f, k.m)), k.b_scm);
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -329,3 +329,32 @@ def test_error_leaves_outputs_untouched(cuda_lib):
     assert e.value.status == qdq.QDQ_ERR_DIMS
     assert np.all(np.isnan(_np(y)))
     torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------ batch-1 pipeline shapes
+
+@pytest.mark.parametrize("groups,slots", [(1, 1), (1, 2), (2, 1), (3, 4), (5, 2), (4, 3)])
+def test_batch1_pipeline_shapes(cuda_lib, groups, slots):
+    # the batch-1 kernels stream weights through per-group shared-memory rings;
+    # every (consumer groups, slots per group) shape must give the same sums
+    qdq = cuda_lib
+    rng = np.random.default_rng(100 + 10 * groups + slots)
+    wq = synth.q8_0_blocks(rng, 600, 3072)
+    g, u = synth.q4k_blocks(rng, 600, 3072), synth.q4k_blocks(rng, 600, 3072)
+    x = synth.activations(rng, 1, 3072)
+    Wq, Wg, Wu = qdq.upload_q8_0(wq, 600, 3072), qdq.upload_q4k(g, 600, 3072), qdq.upload_q4k(u, 600, 3072)
+    old_g = qdq.set_option(qdq.QDQ_OPT_XS_GROUPS, groups)
+    old_s = qdq.set_option(qdq.QDQ_OPT_XS_STAGES, slots)
+    try:
+        y, mid = _nan(1, 600), _nan(1, 600)
+        qdq.q8_0_gemv(Wq, _t(x), y, 600, 3072, 1)
+        qdq.q4k_swiglu(Wg, Wu, _t(x), mid, 600, 3072, 1)
+        yh, mh = _np(y), _np(mid)
+    finally:
+        qdq.set_option(qdq.QDQ_OPT_XS_GROUPS, old_g)
+        qdq.set_option(qdq.QDQ_OPT_XS_STAGES, old_s)
+    y_ref, a = oracle.gemv(oracle.q8_0_dequant(wq, 600, 3072), x)
+    assert gemv_excess(yh, y_ref, a) <= 1.0
+    s = oracle.swiglu(oracle.q4k_dequant(g, 600, 3072), oracle.q4k_dequant(u, 600, 3072), x)
+    assert np.all(np.abs(mh - s["mid"]) <= swiglu_eps(s))
+    assert qdq.pipeline_timeouts() == 0
