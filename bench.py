@@ -53,6 +53,31 @@ def measured_peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
+def kernel_sources_digest() -> str:
+    """sha256 over the CUDA sources and the public header, in name order (identifies one build)."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "ggml_quantized_dequant_gb300", "csrc")
+    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc) if f.endswith((".cu", ".cuh")))
+    for path in files + [os.path.join(ROOT, "include", "qdq.h")]:
+        h.update(os.path.basename(path).encode())
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(case: str):
+    """DRAM bytes per launch that ncu measured for `case`, or None if not captured for these sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f).get(case)
+    if not d or d.get("sources_sha256") != kernel_sources_digest():
+        return None
+    return float(d["dram_bytes_per_launch"])
+
+
 def job_value(units_per_rank: float, world: int, t_max_s: float) -> float:
     """Whole-job throughput: every rank processed `units_per_rank`; the job took the slowest rank's time."""
     return units_per_rank * world / t_max_s
@@ -356,9 +381,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                    "timing": "CUDA graph of one step (56 launches, programmatic dependent launch), "
                              "replayed; CUDA events on the replay stream",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "kernel": "q8_0_gemv_kernel<1>", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": "gemv_xs_kernel<0, 0> (Q8_0 batch-1 GEMV)", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": args.traffic, "peak_source": peaks["source"],
+                     "traffic": args.traffic if args.traffic is not None else recorded_traffic("q8_0_gemv"),
+                     "peak_source": peaks["source"],
                      "bytes_per_launch": bytes_per_launch},
         "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": N_EMBD * 4, "d2h_bytes_per_step": N_EMBD * 4,
                 "steps": e2e_steps, "ms_per_step": e2e_dt / e2e_steps * 1e3,
@@ -457,6 +483,60 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
     return rows
 
 
+def run_profile_case(case: str):
+    """A few eager calls of one hot-path op on its full-size matrices (one set, no graph, no JSON line).
+
+    For profilers: the weights are one matrix set (tens of MB), so a capture with many passes stays
+    small; each call reads its weights cold when the profiler flushes the caches between passes.
+    """
+    import torch
+    import synth
+    import ggml_quantized_dequant_gb300 as qdq
+    from ggml_quantized_dequant_gb300 import _build
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (there is no CPU path)")
+    _build.build()
+    qdq.load()
+    dev = torch.device("cuda")
+    calls = 5
+    if case == "q8_0_gemv":
+        W = qdq.upload_q8_0(synth.config1_up(0), N_FF, N_EMBD, device=dev)
+        x = torch.from_numpy(synth.config1_x()).to(dev)
+        y = torch.empty((1, N_FF), device=dev)
+        fn = lambda: qdq.q8_0_gemv(W, x, y, N_FF, N_EMBD, 1)
+    elif case == "q4k_gemv":
+        W = qdq.upload_q4k(synth.config2_w(0), N_FF, N_EMBD, device=dev)
+        x = torch.from_numpy(synth.config2_x()).to(dev)
+        y = torch.empty((1, N_FF), device=dev)
+        fn = lambda: qdq.q4k_gemv(W, x, y, N_FF, N_EMBD, 1)
+    elif case == "q4k_ffn":
+        g, u, d = synth.config3_layer(0)
+        Wg, Wu = qdq.upload_q4k(g, N_FF, N_EMBD, device=dev), qdq.upload_q4k(u, N_FF, N_EMBD, device=dev)
+        Wd = qdq.upload_q4k(d, N_EMBD, N_FF, device=dev)
+        xh, rh = synth.config3_x_residual()
+        x, r = torch.from_numpy(xh).to(dev), torch.from_numpy(rh).to(dev)
+        out = torch.empty_like(r)
+        mid = torch.empty((1, N_FF), device=dev)
+        fn = lambda: qdq.q4k_ffn_residual(Wg, Wu, Wd, x, r, out, mid, N_EMBD, N_FF, 1)
+    elif case.startswith("q8_0_gemm_M"):
+        M = int(case[len("q8_0_gemm_M"):])
+        W = qdq.upload_q8_0(synth.config4_w(0, 0), N_FF, N_EMBD, device=dev)
+        X = torch.from_numpy(synth.config4_x(0, M)).to(dev)
+        Y = torch.empty((M, N_FF), device=dev)
+        ws = torch.empty(qdq.q8_0_gemm_batch_workspace_bytes(M, N_EMBD), dtype=torch.uint8, device=dev)
+        fn = lambda: qdq.q8_0_gemm_batch(W, X, Y, ws, N_FF, N_EMBD, M)
+    else:
+        raise SystemExit("unknown --profile case %r" % case)
+    for _ in range(calls):
+        fn()
+    torch.cuda.synchronize()
+    if qdq.pipeline_timeouts() != 0:
+        raise SystemExit("pipeline wait timed out")
+    print("profile case %s: %d calls done" % (case, calls))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -469,7 +549,12 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per launch of the dominant kernel, if captured for this build")
+    ap.add_argument("--profile", default=None, metavar="CASE",
+                    help="run a few calls of one op for a profiler and exit: q8_0_gemv, q4k_gemv, q4k_ffn, "
+                         "q8_0_gemm_M<M>")
     args = ap.parse_args(argv)
+    if args.profile:
+        return run_profile_case(args.profile)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 

@@ -329,7 +329,10 @@ int launch_xs(const uint8_t *W, const uint8_t *W2, const float *x, const float *
   a.n_out = n_out;
   a.n_in = n_in;
   a.wpr = ((n_in >> 5) + 31) / 32;
-  a.groups = a.wpr >= 12 ? 1 : 12 / a.wpr;  // about 12 consumer warps
+  // about 9 consumer warps: with the producer, two CTAs (this kernel's and the
+  // next one's) fit in an SM's registers, so the next kernel's weights stream in
+  // while this one computes
+  a.groups = a.wpr >= 9 ? 1 : 9 / a.wpr;
   if (opt_xs_groups() > 0) a.groups = opt_xs_groups();
   if (32 * (a.wpr * a.groups + 1) > kMaxThreads) return QDQ_ERR_UNSUPPORTED;
   a.l2_prefetch = opt_l2_prefetch();
