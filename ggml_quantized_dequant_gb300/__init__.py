@@ -22,6 +22,8 @@ QDQ_ERR_ALIGN = -3
 QDQ_ERR_UNSUPPORTED = -4
 QDQ_ERR_CUDA = -5
 QDQ_ERR_ALIAS = -6
+QDQ_ERR_SCRATCH = -7
+QDQ_NOALLOC_FFN_MAX_MID = 262144
 QDQ_MAX_GEMV_BATCH = 8
 QDQ_MAX_GEMV_N_IN = 49152
 QDQ_OPT_PDL = 1
@@ -48,6 +50,8 @@ SIGNATURES = {
     "qdq_q4k_swiglu": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_vp]),
     "qdq_q4k_ffn_residual": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
                                       _c_int, _c_int, _c_int, _c_vp]),
+    "qdq_q4k_ffn_residual_noalloc": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                              _c_int, _c_int, _c_int, _c_vp]),
     "qdq_q8_0_gemm_batch_workspace_bytes": (_c_size, [_c_int, _c_int]),
     "qdq_q8_0_gemm_batch": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_vp]),
     "qdq_pipeline_timeouts": (_c_int, []),
@@ -159,6 +163,17 @@ def q4k_ffn_residual(Wg, Wu, Wd, x, residual, out, mid_workspace, n_embd: int, n
     _check("qdq_q4k_ffn_residual",
            lib().qdq_q4k_ffn_residual(_ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(x), _ptr(residual), _ptr(out),
                                       _ptr(mid_workspace), n_embd, n_ff, batch, _stream(stream)))
+
+
+def q4k_ffn_residual_noalloc(Wg, Wu, Wd, x, residual, out, n_embd: int, n_ff: int, batch: int = 1, stream=None):
+    """The FFN block with its intermediate vector in the library's fixed device array (no allocation).
+
+    For callers that may not allocate device memory.  batch * n_ff must not exceed
+    QDQ_NOALLOC_FFN_MAX_MID; calls that overlap on the GPU share the array and race.
+    """
+    _check("qdq_q4k_ffn_residual_noalloc",
+           lib().qdq_q4k_ffn_residual_noalloc(_ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(x), _ptr(residual), _ptr(out),
+                                              n_embd, n_ff, batch, _stream(stream)))
 
 
 def q8_0_gemm_batch_workspace_bytes(M: int, n_in: int) -> int:

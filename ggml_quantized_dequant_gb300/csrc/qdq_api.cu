@@ -125,6 +125,7 @@ const char *qdq_status_string(int status) {
     case QDQ_ERR_UNSUPPORTED: return "QDQ_ERR_UNSUPPORTED: shape not handled by this build";
     case QDQ_ERR_CUDA: return "QDQ_ERR_CUDA: CUDA runtime error (see qdq_last_cuda_error)";
     case QDQ_ERR_ALIAS: return "QDQ_ERR_ALIAS: output overlaps an input";
+    case QDQ_ERR_SCRATCH: return "QDQ_ERR_SCRATCH: request exceeds the fixed scratch array (batch * n_ff)";
     default: return "unknown qdq status";
   }
 }

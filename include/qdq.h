@@ -63,6 +63,7 @@ extern "C" {
 #define QDQ_ERR_UNSUPPORTED -4  /* valid arguments this build does not handle (e.g. n_in too large) */
 #define QDQ_ERR_CUDA        -5  /* a CUDA runtime call failed; see qdq_last_cuda_error() */
 #define QDQ_ERR_ALIAS       -6  /* an output overlaps an input it may not overlap */
+#define QDQ_ERR_SCRATCH     -7  /* the request does not fit the library's fixed scratch array */
 
 /* Human-readable name of a status code (static string). */
 const char *qdq_status_string(int status);
@@ -134,6 +135,25 @@ int qdq_q4k_ffn_residual(const void *Wg, const void *Wu, const void *Wd,
                          const float *x, const float *residual, float *out,
                          float *mid_workspace, int n_embd, int n_ff, int batch,
                          cudaStream_t stream);
+
+/* ---- FFN block without caller scratch (allocates nothing) -------------------
+ * No counterpart on the reference pages: an addition for callers that may not
+ * allocate device memory -- e.g. a plug-in whose host application owns all GPU
+ * memory through its own pool, or a decode loop that must not pay for
+ * cudaMalloc/cudaFree.  Same operation, arguments and error behaviour as
+ * qdq_q4k_ffn_residual, but `mid` lives in a fixed device array inside the
+ * library (QDQ_NOALLOC_FFN_MAX_MID floats, 1 MiB, held by every GPU that loads
+ * the library until the process exits); nothing is allocated.
+ *   - batch * n_ff > QDQ_NOALLOC_FFN_MAX_MID returns QDQ_ERR_SCRATCH.
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the one array: calls that overlap on the GPU (other
+ *     streams, other threads) race on it and must be serialised by the caller.
+ */
+#define QDQ_NOALLOC_FFN_MAX_MID 262144
+int qdq_q4k_ffn_residual_noalloc(const void *Wg, const void *Wu, const void *Wd,
+                                 const float *x, const float *residual, float *out,
+                                 int n_embd, int n_ff, int batch, cudaStream_t stream);
 
 /* ---- batch-prefill GEMM on tensor cores -----------------------------------
  * "Module cuda_lane", Goal (tensor-core GEMM for batch prefill-shaped work)
