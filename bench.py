@@ -53,15 +53,21 @@ def measured_peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
-def kernel_sources_digest() -> str:
-    """sha256 over the CUDA sources and the public header, in name order (identifies one build)."""
+# CUDA sources that define each profiled kernel (a recorded counter is stale once any of them changes)
+KERNEL_SOURCES = {
+    "q8_0_gemv": ["qdq_gemv_xs.cu", "qdq_internal.cuh"],
+    "q4k_ffn": ["qdq_gemv_xs.cu", "qdq_internal.cuh"],
+}
+
+
+def kernel_sources_digest(case: str) -> str:
+    """sha256 over the CUDA sources of one profiled kernel, in the listed order."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ggml_quantized_dequant_gb300", "csrc")
-    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc) if f.endswith((".cu", ".cuh")))
-    for path in files + [os.path.join(ROOT, "include", "qdq.h")]:
-        h.update(os.path.basename(path).encode())
-        with open(path, "rb") as f:
+    for name in KERNEL_SOURCES[case]:
+        h.update(name.encode())
+        with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
@@ -73,7 +79,7 @@ def recorded_traffic(case: str):
         return None
     with open(p) as f:
         d = json.load(f).get(case)
-    if not d or d.get("sources_sha256") != kernel_sources_digest():
+    if not d or d.get("sources_sha256") != kernel_sources_digest(case):
         return None
     return float(d["dram_bytes_per_launch"])
 
