@@ -12,7 +12,7 @@ namespace qdq {
 namespace {
 thread_local int g_last_cuda_error = 0;
 std::atomic<int> g_opt_pdl{1};
-std::atomic<int> g_opt_l2_prefetch{1};
+std::atomic<int> g_opt_l2_prefetch{0};
 std::atomic<int> g_opt_ctas_per_sm{1};
 std::atomic<int> g_opt_xs_groups{0};
 std::atomic<int> g_opt_xs_stages{0};
@@ -56,6 +56,8 @@ cudaError_t device_info(DeviceInfo *out) {
       err = cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
     if (err == cudaSuccess)
       err = cudaDeviceGetAttribute(&di.reserved_smem_per_block, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (err == cudaSuccess)
+      err = cudaDeviceGetAttribute(&di.regs_per_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
     g_dev_info[dev] = di;
     g_dev_err[dev] = err;
   });

@@ -28,6 +28,9 @@
 // with its gate row and its up row) and combines them in the epilogue.
 // Every pipeline wait is bounded; a wait that runs out is counted
 // (qdq_pipeline_timeouts) and the CTA winds down instead of hanging.
+#include <mutex>
+#include <vector>
+
 #include "qdq_internal.cuh"
 
 namespace qdq {
@@ -77,6 +80,7 @@ struct XsArgs {
   int groups;       // consumer groups per CTA
   int sg;           // ring slots per consumer group (the ring holds groups * sg stages)
   int stage_bytes;  // bytes per ring stage (multiple of 128)
+  int xbuf_offset;  // shared-memory offset of the staged activations (used when groups > 1)
   int l2_prefetch;
 };
 
@@ -91,8 +95,12 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
 
   const int r0 = int(int64_t(blockIdx.x) * a.n_out / gridDim.x);
   const int r1 = int(int64_t(blockIdx.x + 1) * a.n_out / gridDim.x);
-  const int nv = (r1 - r0) * kV;                     // virtual rows of this CTA
-  const int nst = (nv + kStageRows - 1) / kStageRows;  // stages
+  const int nreal = r1 - r0;
+  // Group g owns the output rows [gbeg(g), gbeg(g + 1)) of this CTA, so the groups
+  // finish together (a partial last stage per group, not a whole stage of imbalance).
+  auto gbeg = [&](int g) { return r0 + g * nreal / G; };
+  auto gstages = [&](int g) { return ((gbeg(g + 1) - gbeg(g)) * kV + kStageRows - 1) / kStageRows; };
+  constexpr int kRowsPerStage = kStageRows / kV;
 
   const int64_t q_row = FMT == kQ8 ? int64_t(n_in) : int64_t(n_in >> 1);                  // quant bytes per row
   const int64_t s_row = FMT == kQ8 ? int64_t(n_in >> 4) : int64_t(n_in >> 8) * 16;      // scale/header bytes per row
@@ -100,7 +108,8 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
 
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + size_t(S) * a.stage_bytes);
   uint64_t *empty = full + S;
-  float *psum = reinterpret_cast<float *>(empty + S);  // [nv][wpr]
+  float *psum = reinterpret_cast<float *>(empty + S);  // [virtual rows][wpr]
+  float *xbuf = reinterpret_cast<float *>(smem + a.xbuf_offset);  // n_in floats when G > 1
   __shared__ int s_abort;
 
   if (threadIdx.x == 0) {
@@ -116,9 +125,10 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
 
   if (warp == ncw) {
     // ---------------- producer: weights only, so no wait on the previous kernel ----------------
-    // Stage t goes to group g = t % G, which consumes its stages in order i = t / G
-    // from its own slots g*SG + i % SG; a slot is refilled only after that group
-    // released it, so no wait can ever see a phase that is two fills old.
+    // Round i issues stage i of every group that has one.  Group g consumes its
+    // stages in order from its own slots g*SG + i % SG; a slot is refilled only
+    // after that group released it, so no wait can ever see a phase that is two
+    // fills old.
     if (lane == 0) {
       if (a.l2_prefetch) {
         prefetch_range_l2(a.W, q_bytes, r0 * q_row, r1 * q_row);
@@ -128,31 +138,37 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
           prefetch_range_l2(a.W2 + q_bytes, int64_t(a.n_out) * s_row, r0 * s_row, r1 * s_row);
         }
       }
-      int issued = 0;
-      for (int t = 0; t < nst; ++t) {
-        const int i = t / G;
-        const int s = (t % G) * SG + i % SG;
-        if (i >= SG && !mbar_wait(&empty[s], ((i / SG) + 1) & 1)) {
-          s_abort = 1;
-          break;
+      int rounds = 0;
+      for (int g = 0; g < G; ++g) rounds = max(rounds, gstages(g));
+      int stop_i = rounds, stop_g = 0;  // first stage not issued, if the loop stopped early
+      for (int i = 0; i < rounds && stop_i == rounds; ++i) {
+        for (int g = 0; g < G; ++g) {
+          if (i >= gstages(g)) continue;
+          const int s = g * SG + i % SG;
+          if (i >= SG && !mbar_wait(&empty[s], ((i / SG) + 1) & 1)) {
+            s_abort = 1;
+            stop_i = i;
+            stop_g = g;
+            break;
+          }
+          uint8_t *stq = smem + size_t(s) * a.stage_bytes;
+          uint8_t *sts = stq + kStageRows * q_row;
+          const int rr = gbeg(g) + i * kRowsPerStage;           // first output row of the stage
+          const int nr = min(kRowsPerStage, gbeg(g + 1) - rr);  // output rows in the stage
+          mbar_arrive_expect_tx(&full[s], uint32_t(kV * nr * (q_row + s_row)));
+          bulk_copy_g2s(stq, a.W + rr * q_row, uint32_t(nr * q_row), &full[s]);
+          bulk_copy_g2s(sts, a.W + q_bytes + rr * s_row, uint32_t(nr * s_row), &full[s]);
+          if (EPI == kSwiglu) {  // up rows go to slots 2, 3
+            bulk_copy_g2s(stq + 2 * q_row, a.W2 + rr * q_row, uint32_t(nr * q_row), &full[s]);
+            bulk_copy_g2s(sts + 2 * s_row, a.W2 + q_bytes + rr * s_row, uint32_t(nr * s_row), &full[s]);
+          }
         }
-        uint8_t *stq = smem + size_t(s) * a.stage_bytes;
-        uint8_t *sts = stq + kStageRows * q_row;
-        const int rr = r0 + t * (kStageRows / kV);     // first output row of the stage
-        const int nr = min(kStageRows / kV, r1 - rr);  // output rows in the stage
-        mbar_arrive_expect_tx(&full[s], uint32_t(kV * nr * (q_row + s_row)));
-        bulk_copy_g2s(stq, a.W + rr * q_row, uint32_t(nr * q_row), &full[s]);
-        bulk_copy_g2s(sts, a.W + q_bytes + rr * s_row, uint32_t(nr * s_row), &full[s]);
-        if (EPI == kSwiglu) {  // up rows go to slots 2, 3
-          bulk_copy_g2s(stq + 2 * q_row, a.W2 + rr * q_row, uint32_t(nr * q_row), &full[s]);
-          bulk_copy_g2s(sts + 2 * s_row, a.W2 + q_bytes + rr * s_row, uint32_t(nr * s_row), &full[s]);
-        }
-        issued = t + 1;
       }
       // never exit with copies in flight: wait for the last fill of every slot
-      for (int t = issued - S < 0 ? 0 : issued - S; t < issued; ++t) {
-        const int i = t / G;
-        mbar_wait(&full[(t % G) * SG + i % SG], (i / SG) & 1);
+      for (int g = 0; g < G; ++g) {
+        const int issued = stop_i == rounds ? gstages(g) : min(gstages(g), stop_i + (g < stop_g ? 1 : 0));
+        for (int i = issued - SG < 0 ? 0 : issued - SG; i < issued; ++i)
+          mbar_wait(&full[g * SG + i % SG], (i / SG) & 1);
       }
     }
   } else {
@@ -161,14 +177,30 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
     const int blk = slice * 32 + lane;
     const bool valid = blk < (n_in >> 5);
     const Magic mg = lane_magic(mg_param);
-    pdl_wait();  // activations come from the previous kernel
+    // Activations come from the previous kernel.  One warp waits for it; the
+    // others sleep on a named barrier instead of polling beside the CTA that
+    // is still computing on this SM.  The second wait returns at once and
+    // gives every consumer thread the dependency's memory visibility.
+    if (warp == 0) pdl_wait();
+    named_bar_sync(1, 32 * ncw);
+    pdl_wait();
+    // With several groups every slice of x is needed by G warps: stage it through
+    // shared memory once instead of fetching it G times from L2.
+    const float *xsrc = a.x;
+    if (G > 1) {
+      const float4 *src = reinterpret_cast<const float4 *>(a.x);
+      float4 *dst = reinterpret_cast<float4 *>(xbuf);
+      for (int c = threadIdx.x; c < (n_in >> 2); c += 32 * ncw) dst[c] = __ldg(src + c);
+      named_bar_sync(1, 32 * ncw);
+      xsrc = xbuf;
+    }
     float2 xr[16];  // activation pairs, kept as aligned register pairs for the packed FMAs
     float xsum = 0.f;
     if (valid) {
-      const float4 *xp = reinterpret_cast<const float4 *>(a.x + blk * 32);
+      const float4 *xp = reinterpret_cast<const float4 *>(xsrc + blk * 32);
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const float4 v = __ldg(xp + c);
+        const float4 v = xp[c];
         xr[2 * c] = f2(v.x, v.y);
         xr[2 * c + 1] = f2(v.z, v.w);
       }
@@ -200,9 +232,12 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
       sofs[k] = int(kStageRows * q_row + slot * s_row) + soff;
     }
 
+    const int rbeg = gbeg(grp) - r0;                 // this group's first local output row
+    const int vend = (gbeg(grp + 1) - r0) * kV;      // end of its virtual rows
+    const int nst = gstages(grp);
     int s = grp * SG;      // this group's current slot and the parity of its fill:
     uint32_t parity = 0;   // tracked incrementally (no division in the loop)
-    for (int t = grp; t < nst; t += G) {
+    for (int t = 0; t < nst; ++t) {
       if (!mbar_wait(&full[s], parity)) {
         s_abort = 1;
         break;
@@ -288,18 +323,17 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
       }
       butterfly4(part, lane);
       if ((lane & 7) == 0) {
-        const int v = t * kStageRows + (lane >> 3);
-        if (v < nv) psum[v * a.wpr + slice] = part[0];
+        const int v = rbeg * kV + t * kStageRows + (lane >> 3);  // local virtual row
+        if (v < vend) psum[v * a.wpr + slice] = part[0];
       }
     }
   }
   __syncthreads();
   if (threadIdx.x == 0 && s_abort) atomicAdd(&g_xs_timeouts, 1u);
   // epilogue: add the slice totals of each row in fixed order
-  const int nreal = r1 - r0;
   for (int r = threadIdx.x; r < nreal; r += blockDim.x) {
     if (EPI == kSwiglu) {
-      // stage t holds output rows 2t, 2t+1 as virtual rows (gate 2t, up 2t, gate 2t+1, up 2t+1)
+      // local output row r is virtual row 2r (gate) and 2r + 1 (up)
       const float *pg = psum + (2 * r) * a.wpr;
       const float *pu = psum + (2 * r + 1) * a.wpr;
       float g = 0.f, u = 0.f;
@@ -317,6 +351,24 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
   }
 }
 
+// Registers per thread of a kernel (queried once per kernel).
+cudaError_t kernel_regs(const void *func, int *regs) {
+  static std::mutex mu;
+  static std::vector<std::pair<const void *, int>> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto &c : cache)
+    if (c.first == func) {
+      *regs = c.second;
+      return cudaSuccess;
+    }
+  cudaFuncAttributes fa;
+  const cudaError_t e = cudaFuncGetAttributes(&fa, func);
+  if (e != cudaSuccess) return e;
+  cache.emplace_back(func, fa.numRegs);
+  *regs = fa.numRegs;
+  return cudaSuccess;
+}
+
 template <int FMT, int EPI>
 int launch_xs(const uint8_t *W, const uint8_t *W2, const float *x, const float *residual, float *y, int n_out,
               int n_in, cudaStream_t s, const DeviceInfo &di) {
@@ -329,10 +381,17 @@ int launch_xs(const uint8_t *W, const uint8_t *W2, const float *x, const float *
   a.n_out = n_out;
   a.n_in = n_in;
   a.wpr = ((n_in >> 5) + 31) / 32;
-  // about 9 consumer warps: with the producer, two CTAs (this kernel's and the
-  // next one's) fit in an SM's registers, so the next kernel's weights stream in
-  // while this one computes
-  a.groups = a.wpr >= 9 ? 1 : 9 / a.wpr;
+  auto kern = gemv_xs_kernel<FMT, EPI>;
+  // As many consumer groups as fit in half an SM's registers together with the
+  // producer warp, so that the next kernel's CTA fits beside this one and its
+  // weights stream in while this one computes.
+  int regs = 0;
+  const cudaError_t er = kernel_regs(reinterpret_cast<const void *>(kern), &regs);
+  if (er != cudaSuccess) return fail_cuda(er);
+  const int warps_half_sm = di.regs_per_sm / 2 / (((regs + 7) / 8) * 8 * 32);
+  a.groups = (warps_half_sm - 1) / a.wpr;
+  if (a.groups > (kMaxThreads / 32 - 1) / a.wpr) a.groups = (kMaxThreads / 32 - 1) / a.wpr;
+  if (a.groups < 1) a.groups = 1;
   if (opt_xs_groups() > 0) a.groups = opt_xs_groups();
   if (32 * (a.wpr * a.groups + 1) > kMaxThreads) return QDQ_ERR_UNSUPPORTED;
   a.l2_prefetch = opt_l2_prefetch();
@@ -343,17 +402,20 @@ int launch_xs(const uint8_t *W, const uint8_t *W2, const float *x, const float *
   if (grid > n_out) grid = n_out;
   const int max_rows = (n_out + grid - 1) / grid;
   const size_t psum_bytes = size_t(max_rows) * (EPI == kSwiglu ? 2 : 1) * a.wpr * sizeof(float);
+  const size_t xbuf_bytes = a.groups > 1 ? size_t(n_in) * sizeof(float) : 0;
   // ring: about half an SM's shared memory, so the next kernel's CTA fits beside this one
-  const long budget = long(di.smem_per_sm) / 2 - di.reserved_smem_per_block - long(psum_bytes) - 1024;
+  const long budget =
+      long(di.smem_per_sm) / 2 - di.reserved_smem_per_block - long(psum_bytes) - long(xbuf_bytes) - 1024;
   int sg = int(budget / (long(a.stage_bytes) * a.groups));
   if (sg > 8) sg = 8;
   if (sg < 2) sg = 2;
   if (opt_xs_stages() > 0) sg = opt_xs_stages();
   a.sg = sg;
   const int stages = a.groups * sg;
-  const size_t smem = size_t(stages) * a.stage_bytes + 2 * stages * sizeof(uint64_t) + psum_bytes;
+  const size_t psum_end = size_t(stages) * a.stage_bytes + 2 * stages * sizeof(uint64_t) + psum_bytes;
+  a.xbuf_offset = int((psum_end + 15) / 16 * 16);
+  const size_t smem = size_t(a.xbuf_offset) + xbuf_bytes;
   if (smem > size_t(di.max_smem_optin)) return QDQ_ERR_UNSUPPORTED;
-  auto kern = gemv_xs_kernel<FMT, EPI>;
   const cudaError_t e0 = allow_dynamic_smem(reinterpret_cast<const void *>(kern), int(smem));
   if (e0 != cudaSuccess) return fail_cuda(e0);
   const cudaError_t e = launch(kern, dim3(grid), dim3(32 * (a.wpr * a.groups + 1)), smem, s, a, make_magic());

@@ -25,6 +25,7 @@ struct DeviceInfo {
   int max_smem_optin;
   int smem_per_sm;
   int reserved_smem_per_block;
+  int regs_per_sm;
 };
 
 // Dynamic shared memory for a streaming GEMV CTA: at least `need`, and when
@@ -106,6 +107,10 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 // Wait until every prerequisite grid has completed and its writes are visible.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Named barrier over `threads` threads (a multiple of 32); barrier 0 is __syncthreads.
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 // Bulk L2 prefetch of [p, p+bytes): p and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes) {

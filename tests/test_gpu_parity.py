@@ -333,6 +333,35 @@ def test_error_leaves_outputs_untouched(cuda_lib):
 
 # ------------------------------------------------------------------ batch-1 pipeline shapes
 
+@pytest.mark.parametrize("n_out,groups", [(2053, 0), (2053, 3), (1001, 2), (1001, 5), (152 * 9 + 151, 0)])
+def test_batch1_uneven_group_rows(cuda_lib, n_out, groups):
+    # rows of a CTA are split between its consumer groups; uneven splits end each
+    # group with a partial stage, which must neither be lost nor spill into the next group
+    qdq = cuda_lib
+    rng = np.random.default_rng(n_out + 7 * groups)
+    wq = synth.q8_0_blocks(rng, n_out, 3072)
+    g, u, d = synth.q4k_blocks(rng, n_out, 3072), synth.q4k_blocks(rng, n_out, 3072), synth.q4k_blocks(rng, n_out, 3072)
+    x, res = synth.activations(rng, 1, 3072), synth.activations(rng, 1, n_out)
+    Wq, Wg, Wu, Wd = (qdq.upload_q8_0(wq, n_out, 3072), qdq.upload_q4k(g, n_out, 3072),
+                      qdq.upload_q4k(u, n_out, 3072), qdq.upload_q4k(d, n_out, 3072))
+    old_g = qdq.set_option(qdq.QDQ_OPT_XS_GROUPS, groups)
+    try:
+        y, mid, y4 = _nan(1, n_out), _nan(1, n_out), _nan(1, n_out)
+        qdq.q8_0_gemv(Wq, _t(x), y, n_out, 3072, 1)
+        qdq.q4k_swiglu(Wg, Wu, _t(x), mid, n_out, 3072, 1)
+        qdq.q4k_gemv(Wd, _t(x), y4, n_out, 3072, 1)
+        yh, mh, y4h = _np(y), _np(mid), _np(y4)
+    finally:
+        qdq.set_option(qdq.QDQ_OPT_XS_GROUPS, old_g)
+    y_ref, a = oracle.gemv(oracle.q8_0_dequant(wq, n_out, 3072), x)
+    assert gemv_excess(yh, y_ref, a) <= 1.0
+    s = oracle.swiglu(oracle.q4k_dequant(g, n_out, 3072), oracle.q4k_dequant(u, n_out, 3072), x)
+    assert np.all(np.abs(mh - s["mid"]) <= swiglu_eps(s))
+    y4_ref, a4 = oracle.gemv(oracle.q4k_dequant(d, n_out, 3072), x)
+    assert gemv_excess(y4h, y4_ref, a4) <= 1.0
+    assert qdq.pipeline_timeouts() == 0
+
+
 @pytest.mark.parametrize("groups,slots", [(1, 1), (1, 2), (2, 1), (3, 4), (5, 2), (4, 3)])
 def test_batch1_pipeline_shapes(cuda_lib, groups, slots):
     # the batch-1 kernels stream weights through per-group shared-memory rings;
