@@ -80,7 +80,6 @@ struct XsArgs {
   int groups;       // consumer groups per CTA
   int sg;           // ring slots per consumer group (the ring holds groups * sg stages)
   int stage_bytes;  // bytes per ring stage (multiple of 128)
-  int xbuf_offset;  // shared-memory offset of the staged activations (used when groups > 1)
   int l2_prefetch;
 };
 
@@ -109,7 +108,6 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + size_t(S) * a.stage_bytes);
   uint64_t *empty = full + S;
   float *psum = reinterpret_cast<float *>(empty + S);  // [virtual rows][wpr]
-  float *xbuf = reinterpret_cast<float *>(smem + a.xbuf_offset);  // n_in floats when G > 1
   __shared__ int s_abort;
 
   if (threadIdx.x == 0) {
@@ -184,23 +182,13 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
     if (warp == 0) pdl_wait();
     named_bar_sync(1, 32 * ncw);
     pdl_wait();
-    // With several groups every slice of x is needed by G warps: stage it through
-    // shared memory once instead of fetching it G times from L2.
-    const float *xsrc = a.x;
-    if (G > 1) {
-      const float4 *src = reinterpret_cast<const float4 *>(a.x);
-      float4 *dst = reinterpret_cast<float4 *>(xbuf);
-      for (int c = threadIdx.x; c < (n_in >> 2); c += 32 * ncw) dst[c] = __ldg(src + c);
-      named_bar_sync(1, 32 * ncw);
-      xsrc = xbuf;
-    }
     float2 xr[16];  // activation pairs, kept as aligned register pairs for the packed FMAs
     float xsum = 0.f;
     if (valid) {
-      const float4 *xp = reinterpret_cast<const float4 *>(xsrc + blk * 32);
+      const float4 *xp = reinterpret_cast<const float4 *>(a.x + blk * 32);
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const float4 v = xp[c];
+        const float4 v = __ldg(xp + c);
         xr[2 * c] = f2(v.x, v.y);
         xr[2 * c + 1] = f2(v.z, v.w);
       }
@@ -382,14 +370,17 @@ int launch_xs(const uint8_t *W, const uint8_t *W2, const float *x, const float *
   a.n_in = n_in;
   a.wpr = ((n_in >> 5) + 31) / 32;
   auto kern = gemv_xs_kernel<FMT, EPI>;
-  // As many consumer groups as fit in half an SM's registers together with the
-  // producer warp, so that the next kernel's CTA fits beside this one and its
-  // weights stream in while this one computes.
+  // About 6 (Q8_0) or 9 (Q4_K, twice the weights per byte) consumer warps:
+  // measured best on 3072 <-> 8192 decode chains.  More warps add contention
+  // without adding throughput.  The groups must also fit in half an SM's
+  // registers together with the producer warp, so that the next kernel's CTA
+  // fits beside this one and its weights stream in while this one computes.
   int regs = 0;
   const cudaError_t er = kernel_regs(reinterpret_cast<const void *>(kern), &regs);
   if (er != cudaSuccess) return fail_cuda(er);
   const int warps_half_sm = di.regs_per_sm / 2 / (((regs + 7) / 8) * 8 * 32);
-  a.groups = (warps_half_sm - 1) / a.wpr;
+  a.groups = (FMT == kQ8 ? 6 : 9) / a.wpr;
+  if (a.groups > (warps_half_sm - 1) / a.wpr) a.groups = (warps_half_sm - 1) / a.wpr;
   if (a.groups > (kMaxThreads / 32 - 1) / a.wpr) a.groups = (kMaxThreads / 32 - 1) / a.wpr;
   if (a.groups < 1) a.groups = 1;
   if (opt_xs_groups() > 0) a.groups = opt_xs_groups();
@@ -402,19 +393,20 @@ int launch_xs(const uint8_t *W, const uint8_t *W2, const float *x, const float *
   if (grid > n_out) grid = n_out;
   const int max_rows = (n_out + grid - 1) / grid;
   const size_t psum_bytes = size_t(max_rows) * (EPI == kSwiglu ? 2 : 1) * a.wpr * sizeof(float);
-  const size_t xbuf_bytes = a.groups > 1 ? size_t(n_in) * sizeof(float) : 0;
-  // ring: about half an SM's shared memory, so the next kernel's CTA fits beside this one
-  const long budget =
-      long(di.smem_per_sm) / 2 - di.reserved_smem_per_block - long(psum_bytes) - long(xbuf_bytes) - 1024;
+  // ring: about half an SM's shared memory, so the next kernel's CTA fits beside
+  // this one; at least two slots per group, so drop groups that would not fit
+  const long budget = long(di.smem_per_sm) / 2 - di.reserved_smem_per_block - long(psum_bytes) - 1024;
+  if (opt_xs_groups() == 0) {
+    const int g_smem = int(budget / (2L * a.stage_bytes));
+    if (a.groups > g_smem) a.groups = g_smem < 1 ? 1 : g_smem;
+  }
   int sg = int(budget / (long(a.stage_bytes) * a.groups));
   if (sg > 8) sg = 8;
   if (sg < 2) sg = 2;
   if (opt_xs_stages() > 0) sg = opt_xs_stages();
   a.sg = sg;
   const int stages = a.groups * sg;
-  const size_t psum_end = size_t(stages) * a.stage_bytes + 2 * stages * sizeof(uint64_t) + psum_bytes;
-  a.xbuf_offset = int((psum_end + 15) / 16 * 16);
-  const size_t smem = size_t(a.xbuf_offset) + xbuf_bytes;
+  const size_t smem = size_t(stages) * a.stage_bytes + 2 * stages * sizeof(uint64_t) + psum_bytes;
   if (smem > size_t(di.max_smem_optin)) return QDQ_ERR_UNSUPPORTED;
   const cudaError_t e0 = allow_dynamic_smem(reinterpret_cast<const void *>(kern), int(smem));
   if (e0 != cudaSuccess) return fail_cuda(e0);
