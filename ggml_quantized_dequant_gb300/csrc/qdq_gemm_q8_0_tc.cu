@@ -116,7 +116,8 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
 
 template <int N>
 struct GemmCfg {
-  static constexpr int kStages = N >= 256 ? 3 : 4;
+  // as many stages as fit in 227 KB: more weight bytes in flight per SM
+  static constexpr int kStages = N >= 256 ? 4 : N >= 128 ? 5 : N >= 64 ? 6 : 8;
   static constexpr uint32_t kBTileBytes = uint32_t(N) * 128;
   static constexpr uint32_t kStageBytes = kQTileBytes + kATileBytes + kBTileBytes;
   static constexpr uint32_t kTmemCols = N < 32 ? 32 : N;
@@ -222,18 +223,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------- dequantise, then epilogue ----------------
-    pdl_wait();
+    // The weights do not depend on the previous kernel, so dequantisation starts
+    // at once; only the epilogue (which writes Y) waits for it.
     const int row = threadIdx.x & (BM - 1);  // weight row within the tile = TMEM lane
     const int part = threadIdx.x >> 7;       // which 16 of the row's 64 quants
     const int grow = tile_n * BM + row;
     const uint32_t *d32 = reinterpret_cast<const uint32_t *>(W + int64_t(n_out) * n_in) + int64_t(grow) * (n_in / BK);
-    uint32_t dnext = __ldg(d32 + kb0);
+    // block scales (one u32 = two fp16 per K block) are fetched four stages ahead
+    uint32_t dq0 = nk > 0 ? __ldg(d32 + kb0) : 0u, dq1 = nk > 1 ? __ldg(d32 + kb0 + 1) : 0u;
+    uint32_t dq2 = nk > 2 ? __ldg(d32 + kb0 + 2) : 0u, dq3 = nk > 3 ? __ldg(d32 + kb0 + 3) : 0u;
     bool ok = true;
     const int qsw = (row >> 1) & 3;  // 64-byte swizzle of the TMA-written int8 tile
     for (int i = 0; i < nk; ++i) {
       const int s = i % S;
-      const uint32_t dcur = dnext;
-      if (i + 1 < nk) dnext = __ldg(d32 + kb0 + i + 1);
+      const uint32_t dcur = dq0;
+      dq0 = dq1;
+      dq1 = dq2;
+      dq2 = dq3;
+      dq3 = i + 4 < nk ? __ldg(d32 + kb0 + i + 4) : 0u;
       if (!mbar_wait(&full[s], (i / S) & 1)) {
         s_abort = 1;
         ok = false;
@@ -270,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(&aready[s]);
     }
+    pdl_wait();
     if (ok && mbar_wait(accum, 0)) {
       tc_fence_after();
       const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
