@@ -41,6 +41,7 @@ namespace {
 
 constexpr int kStageRows = 4;    // virtual rows per stage = butterfly width
 constexpr int kMaxThreads = 544;  // up to 16 consumer warps + the producer
+constexpr int kMaxGroups = 16;    // consumer groups per CTA (one slice warp per group at least)
 
 enum Fmt { kQ8 = 0, kQ4 = 1 };
 enum Epi { kPlain = 0, kSwiglu = 1, kResidual = 2 };
@@ -136,19 +137,23 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
           prefetch_range_l2(a.W2 + q_bytes, int64_t(a.n_out) * s_row, r0 * s_row, r1 * s_row);
         }
       }
-      int rounds = 0;
-      for (int g = 0; g < G; ++g) rounds = max(rounds, gstages(g));
-      int stop_i = rounds, stop_g = 0;  // first stage not issued, if the loop stopped early
-      for (int i = 0; i < rounds && stop_i == rounds; ++i) {
+      // Issue each group's stages in order as soon as that group frees a slot, never
+      // blocking on one group while another could be fed.
+      int next[kMaxGroups];  // next stage to issue, per group
+      int remaining = 0;
+      for (int g = 0; g < G; ++g) {
+        next[g] = 0;
+        remaining += gstages(g);
+      }
+      unsigned long long idle_since = global_ns();
+      uint32_t idle_spins = 0;
+      while (remaining > 0) {
+        bool progress = false;
         for (int g = 0; g < G; ++g) {
+          const int i = next[g];
           if (i >= gstages(g)) continue;
           const int s = g * SG + i % SG;
-          if (i >= SG && !mbar_wait(&empty[s], ((i / SG) + 1) & 1)) {
-            s_abort = 1;
-            stop_i = i;
-            stop_g = g;
-            break;
-          }
+          if (i >= SG && !mbar_test(&empty[s], ((i / SG) + 1) & 1)) continue;
           uint8_t *stq = smem + size_t(s) * a.stage_bytes;
           uint8_t *sts = stq + kStageRows * q_row;
           const int rr = gbeg(g) + i * kRowsPerStage;           // first output row of the stage
@@ -160,14 +165,25 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
             bulk_copy_g2s(stq + 2 * q_row, a.W2 + rr * q_row, uint32_t(nr * q_row), &full[s]);
             bulk_copy_g2s(sts + 2 * s_row, a.W2 + q_bytes + rr * s_row, uint32_t(nr * s_row), &full[s]);
           }
+          next[g] = i + 1;
+          --remaining;
+          progress = true;
+        }
+        if (progress) {
+          idle_spins = 0;
+          idle_since = global_ns();
+        } else {
+          if ((++idle_spins & 255u) == 0 && global_ns() - idle_since > kWaitLimitNs) {
+            s_abort = 1;  // no slot came free within the limit: stop issuing
+            break;
+          }
+          __nanosleep(64);  // leave the issue slots to the consumers while no slot is free
         }
       }
       // never exit with copies in flight: wait for the last fill of every slot
-      for (int g = 0; g < G; ++g) {
-        const int issued = stop_i == rounds ? gstages(g) : min(gstages(g), stop_i + (g < stop_g ? 1 : 0));
-        for (int i = issued - SG < 0 ? 0 : issued - SG; i < issued; ++i)
+      for (int g = 0; g < G; ++g)
+        for (int i = next[g] - SG < 0 ? 0 : next[g] - SG; i < next[g]; ++i)
           mbar_wait(&full[g * SG + i % SG], (i / SG) & 1);
-      }
     }
   } else {
     // ---------------- consumers ----------------
@@ -231,6 +247,13 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
         break;
       }
       const uint8_t *stq = smem + size_t(s) * a.stage_bytes;
+      // The stage's bytes are in registers once the loads below are issued: the
+      // arrive (a release) orders those reads before the slot is refilled, so the
+      // producer can start the next copy while this warp computes.
+      auto release = [&](int slot) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+      };
       float part[kStageRows];
       // All four rows' loads first, then their arithmetic interleaved word by word:
       // eight independent accumulation chains per lane.  Rows past the end of the
@@ -245,6 +268,7 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
           qb[k] = *reinterpret_cast<const uint4 *>(stq + qofs[k] + 16);
           dv[k] = __half2float(*reinterpret_cast<const __half *>(stq + sofs[k]));
         }
+        release(s);
         float2 s0[kStageRows], s1[kStageRows];
 #pragma unroll
         for (int k = 0; k < kStageRows; ++k) s0[k] = s1[k] = f2(0.f, 0.f);
@@ -272,6 +296,7 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
           q[k] = *reinterpret_cast<const uint4 *>(stq + qofs[k]);
           h[k] = *reinterpret_cast<const uint4 *>(stq + sofs[k]);
         }
+        release(s);
         float2 DM[kStageRows];
 #pragma unroll
         for (int k = 0; k < kStageRows; ++k) {
@@ -303,8 +328,6 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
           part[k] = fmaf(DM[k].x, st.x + st.y, -DM[k].y * xsum);  // d sc_j sum(q x) - dmin m_j sum(x)
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done reading the stage
       if (++s == (grp + 1) * SG) {
         s = grp * SG;
         parity ^= 1u;
