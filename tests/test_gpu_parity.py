@@ -265,7 +265,8 @@ def test_q8_0_gemm_batch_parity_small(cuda_lib, M):
     _gemm_case(cuda_lib, 256, 512, M, seed=M)
 
 
-@pytest.mark.parametrize("n_out,n_in,M", [(384, 1024, 33), (128, 64, 16), (1024, 2048, 130)])
+@pytest.mark.parametrize("n_out,n_in,M", [(384, 1024, 33), (128, 64, 16), (1024, 2048, 130), (256, 320, 40),
+                                           (128, 448, 17), (512, 192, 300)])
 def test_q8_0_gemm_batch_parity_shapes(cuda_lib, n_out, n_in, M):
     _gemm_case(cuda_lib, n_out, n_in, M, seed=n_out + M)
 
