@@ -129,14 +129,6 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
     // after that group released it, so no wait can ever see a phase that is two
     // fills old.
     if (lane == 0) {
-      if (a.l2_prefetch) {
-        prefetch_range_l2(a.W, q_bytes, r0 * q_row, r1 * q_row);
-        prefetch_range_l2(a.W + q_bytes, int64_t(a.n_out) * s_row, r0 * s_row, r1 * s_row);
-        if (EPI == kSwiglu) {
-          prefetch_range_l2(a.W2, q_bytes, r0 * q_row, r1 * q_row);
-          prefetch_range_l2(a.W2 + q_bytes, int64_t(a.n_out) * s_row, r0 * s_row, r1 * s_row);
-        }
-      }
       // Issue each group's stages in order as soon as that group frees a slot, never
       // blocking on one group while another could be fed.
       int next[kMaxGroups];  // next stage to issue, per group
@@ -147,6 +139,7 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
       }
       unsigned long long idle_since = global_ns();
       uint32_t idle_spins = 0;
+      bool prefetched = !a.l2_prefetch;
       while (remaining > 0) {
         bool progress = false;
         for (int g = 0; g < G; ++g) {
@@ -168,6 +161,27 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
           next[g] = i + 1;
           --remaining;
           progress = true;
+        }
+        if (!prefetched) {
+          // Once every group's first ring fill is out, pull the rows that do not fit
+          // the ring into L2, so that their refills later hit L2 instead of waiting
+          // behind the next kernel's prefill in the DRAM queues.
+          bool filled = true;
+          for (int g = 0; g < G; ++g) filled = filled && next[g] >= min(SG, gstages(g));
+          if (filled) {
+            for (int g = 0; g < G; ++g) {
+              const int64_t lo = gbeg(g) + SG * kRowsPerStage, hi = gbeg(g + 1);
+              if (lo >= hi) continue;
+              const int64_t s_plane = int64_t(a.n_out) * s_row;
+              prefetch_range_l2(a.W, q_bytes, lo * q_row, hi * q_row);
+              prefetch_range_l2(a.W + q_bytes, s_plane, lo * s_row, hi * s_row);
+              if (EPI == kSwiglu) {
+                prefetch_range_l2(a.W2, q_bytes, lo * q_row, hi * q_row);
+                prefetch_range_l2(a.W2 + q_bytes, s_plane, lo * s_row, hi * s_row);
+              }
+            }
+            prefetched = true;
+          }
         }
         if (progress) {
           idle_spins = 0;
