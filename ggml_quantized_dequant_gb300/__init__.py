@@ -25,7 +25,7 @@ QDQ_ERR_ALIAS = -6
 QDQ_ERR_SCRATCH = -7
 QDQ_NOALLOC_FFN_MAX_MID = 262144
 QDQ_MAX_GEMV_BATCH = 8
-QDQ_MAX_GEMV_N_IN = 49152
+QDQ_MAX_GEMV_N_IN = 32768
 QDQ_OPT_PDL = 1
 QDQ_OPT_L2_PREFETCH = 2
 QDQ_OPT_CTAS_PER_SM = 3

@@ -77,7 +77,7 @@ const char *qdq_version(void);
 #define QDQ_MAX_GEMV_BATCH 8
 /* Largest supported n_in for the GEMV-family calls (activations are staged in
  * shared memory: batch_group * n_in * 4 bytes per CTA). */
-#define QDQ_MAX_GEMV_N_IN 49152
+#define QDQ_MAX_GEMV_N_IN 32768
 
 /* ---- one-time repack (the pages' preload step) ----------------------------
  * "Module cuda_lane", Functions: preload_q4k_soa_weights -- bulk upload once

@@ -77,7 +77,10 @@ def test_q4k_dequant_extreme_scales_bit_exact(cuda_lib):
 # ------------------------------------------------------------------ GEMV
 
 Q8_SHAPES = [(256, 512, 1), (1, 32, 1), (3, 96, 1), (157, 800, 1), (300, 4096, 3), (64, 512, 8),
-             (33, 8192, 8), (1000, 1024, 2)]
+             (33, 8192, 8), (1000, 1024, 2),
+             # the largest row the batch-1 pipeline takes (16 slice warps), rows it hands to the
+             # general kernel (n_in % 256 != 0, n_in > 16384), and the largest n_in accepted
+             (40, 16384, 1), (150, 20000, 1), (24, 32768, 1), (16, 32768, 8)]
 
 
 @pytest.mark.parametrize("n_out,n_in,batch", Q8_SHAPES)
@@ -143,7 +146,7 @@ def test_gemv_zero_x_gives_exact_zero(cuda_lib):
 
 
 Q4_SHAPES = [(1, 256, 1), (5, 512, 1), (157, 2048, 1), (300, 3072, 4), (64, 512, 8), (33, 8192, 8),
-             (1000, 1280, 2)]
+             (1000, 1280, 2), (40, 16384, 1), (24, 32768, 1), (16, 32768, 8)]
 
 
 @pytest.mark.parametrize("n_out,n_in,batch", Q4_SHAPES)
@@ -227,7 +230,7 @@ def _ffn_case(qdq, n_embd, n_ff, batch, seed, in_place=False, layer=None):
     assert np.all(np.abs(_np(mid) - o["mid"]) <= swiglu_eps(o))
 
 
-@pytest.mark.parametrize("n_embd,n_ff,batch", [(256, 512, 1), (512, 1280, 2), (768, 2048, 5)])
+@pytest.mark.parametrize("n_embd,n_ff,batch", [(256, 512, 1), (512, 1280, 2), (768, 2048, 5), (512, 1024, 8)])
 def test_q4k_ffn_residual_parity(cuda_lib, n_embd, n_ff, batch):
     _ffn_case(cuda_lib, n_embd, n_ff, batch, seed=n_embd + n_ff + batch)
 
@@ -260,7 +263,7 @@ def _gemm_case(qdq, n_out, n_in, M, wb=None, X=None, sample_rows=None, seed=0):
     assert qdq.pipeline_timeouts() == 0
 
 
-@pytest.mark.parametrize("M", [1, 16, 20, 64, 100, 200, 257, 512])
+@pytest.mark.parametrize("M", [1, 16, 20, 64, 100, 200, 257, 512, 1000])
 def test_q8_0_gemm_batch_parity_small(cuda_lib, M):
     _gemm_case(cuda_lib, 256, 512, M, seed=M)
 
