@@ -79,7 +79,7 @@ struct XsArgs {
   int n_in;
   int wpr;          // slice warps per row
   int groups;       // consumer groups per CTA
-  int sg;           // ring slots per consumer group (the ring holds groups * sg stages)
+  int slots;        // ring slots in all (the groups share them out as evenly as possible)
   int stage_bytes;  // bytes per ring stage (multiple of 128)
   int l2_prefetch;
 };
@@ -91,7 +91,10 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ncw = a.wpr * a.groups;  // consumer warps; warp ncw is the producer
   const int n_in = a.n_in;
-  const int G = a.groups, SG = a.sg, S = G * SG;  // slots: group g owns g*SG .. g*SG+SG-1
+  const int G = a.groups, S = a.slots;
+  // group g owns the ring slots [sbase(g), sbase(g) + scount(g))
+  auto scount = [&](int g) { return S / G + (g < S % G ? 1 : 0); };
+  auto sbase = [&](int g) { return g * (S / G) + min(g, S % G); };
 
   const int r0 = int(int64_t(blockIdx.x) * a.n_out / gridDim.x);
   const int r1 = int(int64_t(blockIdx.x + 1) * a.n_out / gridDim.x);
@@ -125,7 +128,7 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
   if (warp == ncw) {
     // ---------------- producer: weights only, so no wait on the previous kernel ----------------
     // Round i issues stage i of every group that has one.  Group g consumes its
-    // stages in order from its own slots g*SG + i % SG; a slot is refilled only
+    // stages in order from its own slots sbase(g) + i % scount(g); a slot is refilled only
     // after that group released it, so no wait can ever see a phase that is two
     // fills old.
     if (lane == 0) {
@@ -145,7 +148,8 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
         for (int g = 0; g < G; ++g) {
           const int i = next[g];
           if (i >= gstages(g)) continue;
-          const int s = g * SG + i % SG;
+          const int SG = scount(g);
+          const int s = sbase(g) + i % SG;
           if (i >= SG && !mbar_test(&empty[s], ((i / SG) + 1) & 1)) continue;
           uint8_t *stq = smem + size_t(s) * a.stage_bytes;
           uint8_t *sts = stq + kStageRows * q_row;
@@ -167,10 +171,10 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
           // the ring into L2, so that their refills later hit L2 instead of waiting
           // behind the next kernel's prefill in the DRAM queues.
           bool filled = true;
-          for (int g = 0; g < G; ++g) filled = filled && next[g] >= min(SG, gstages(g));
+          for (int g = 0; g < G; ++g) filled = filled && next[g] >= min(scount(g), gstages(g));
           if (filled) {
             for (int g = 0; g < G; ++g) {
-              const int64_t lo = gbeg(g) + SG * kRowsPerStage, hi = gbeg(g + 1);
+              const int64_t lo = gbeg(g) + scount(g) * kRowsPerStage, hi = gbeg(g + 1);
               if (lo >= hi) continue;
               const int64_t s_plane = int64_t(a.n_out) * s_row;
               prefetch_range_l2(a.W, q_bytes, lo * q_row, hi * q_row);
@@ -196,8 +200,8 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
       }
       // never exit with copies in flight: wait for the last fill of every slot
       for (int g = 0; g < G; ++g)
-        for (int i = next[g] - SG < 0 ? 0 : next[g] - SG; i < next[g]; ++i)
-          mbar_wait(&full[g * SG + i % SG], (i / SG) & 1);
+        for (int i = next[g] - scount(g) < 0 ? 0 : next[g] - scount(g); i < next[g]; ++i)
+          mbar_wait(&full[sbase(g) + i % scount(g)], (i / scount(g)) & 1);
     }
   } else {
     // ---------------- consumers ----------------
@@ -253,7 +257,8 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
     const int rbeg = gbeg(grp) - r0;                 // this group's first local output row
     const int vend = (gbeg(grp + 1) - r0) * kV;      // end of its virtual rows
     const int nst = gstages(grp);
-    int s = grp * SG;      // this group's current slot and the parity of its fill:
+    const int s_lo = sbase(grp), s_hi = s_lo + scount(grp);
+    int s = s_lo;          // this group's current slot and the parity of its fill:
     uint32_t parity = 0;   // tracked incrementally (no division in the loop)
     for (int t = 0; t < nst; ++t) {
       if (!mbar_wait(&full[s], parity)) {
@@ -342,8 +347,8 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
           part[k] = fmaf(DM[k].x, st.x + st.y, -DM[k].y * xsum);  // d sc_j sum(q x) - dmin m_j sum(x)
         }
       }
-      if (++s == (grp + 1) * SG) {
-        s = grp * SG;
+      if (++s == s_hi) {
+        s = s_lo;
         parity ^= 1u;
       }
       butterfly4(part, lane);
@@ -437,12 +442,13 @@ int launch_xs(const uint8_t *W, const uint8_t *W2, const float *x, const float *
     const int g_smem = int(budget / (2L * a.stage_bytes));
     if (a.groups > g_smem) a.groups = g_smem < 1 ? 1 : g_smem;
   }
-  int sg = int(budget / (long(a.stage_bytes) * a.groups));
-  if (sg > 8) sg = 8;
-  if (sg < 2) sg = 2;
-  if (opt_xs_stages() > 0) sg = opt_xs_stages();
-  a.sg = sg;
-  const int stages = a.groups * sg;
+  // every slot the budget holds, at least two and at most eight per group
+  int slots = int(budget / long(a.stage_bytes));
+  if (slots > 8 * a.groups) slots = 8 * a.groups;
+  if (slots < 2 * a.groups) slots = 2 * a.groups;
+  if (opt_xs_stages() > 0) slots = opt_xs_stages() * a.groups;
+  a.slots = slots;
+  const int stages = slots;
   const size_t smem = size_t(stages) * a.stage_bytes + 2 * stages * sizeof(uint64_t) + psum_bytes;
   if (smem > size_t(di.max_smem_optin)) return QDQ_ERR_UNSUPPORTED;
   const cudaError_t e0 = allow_dynamic_smem(reinterpret_cast<const void *>(kern), int(smem));
