@@ -87,6 +87,9 @@ cudaError_t allow_dynamic_smem(const void *func, int bytes) {
     }
   }
   e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  // the largest shared-memory carve-out, so that a CTA of the next kernel fits beside one of this kernel
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess) g_smem.push_back({func, dev, bytes});
   return e;
 }

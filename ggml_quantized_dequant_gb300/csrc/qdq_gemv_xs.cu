@@ -41,7 +41,6 @@ namespace {
 
 constexpr int kStageRows = 4;    // virtual rows per stage = butterfly width
 constexpr int kMaxThreads = 544;  // up to 16 consumer warps + the producer
-constexpr int kMaxGroups = 16;    // consumer groups per CTA (one slice warp per group at least)
 
 enum Fmt { kQ8 = 0, kQ4 = 1 };
 enum Epi { kPlain = 0, kSwiglu = 1, kResidual = 2 };
@@ -79,7 +78,7 @@ struct XsArgs {
   int n_in;
   int wpr;          // slice warps per row
   int groups;       // consumer groups per CTA
-  int slots;        // ring slots in all (the groups share them out as evenly as possible)
+  int sg;           // ring slots per consumer group (the ring holds groups * sg stages)
   int stage_bytes;  // bytes per ring stage (multiple of 128)
   int l2_prefetch;
 };
@@ -91,10 +90,7 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ncw = a.wpr * a.groups;  // consumer warps; warp ncw is the producer
   const int n_in = a.n_in;
-  const int G = a.groups, S = a.slots;
-  // group g owns the ring slots [sbase(g), sbase(g) + scount(g))
-  auto scount = [&](int g) { return S / G + (g < S % G ? 1 : 0); };
-  auto sbase = [&](int g) { return g * (S / G) + min(g, S % G); };
+  const int G = a.groups, SG = a.sg, S = G * SG;  // slots: group g owns g*SG .. g*SG+SG-1
 
   const int r0 = int(int64_t(blockIdx.x) * a.n_out / gridDim.x);
   const int r1 = int(int64_t(blockIdx.x + 1) * a.n_out / gridDim.x);
@@ -128,29 +124,31 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
   if (warp == ncw) {
     // ---------------- producer: weights only, so no wait on the previous kernel ----------------
     // Round i issues stage i of every group that has one.  Group g consumes its
-    // stages in order from its own slots sbase(g) + i % scount(g); a slot is refilled only
+    // stages in order from its own slots g*SG + i % SG; a slot is refilled only
     // after that group released it, so no wait can ever see a phase that is two
     // fills old.
     if (lane == 0) {
-      // Issue each group's stages in order as soon as that group frees a slot, never
-      // blocking on one group while another could be fed.
-      int next[kMaxGroups];  // next stage to issue, per group
-      int remaining = 0;
-      for (int g = 0; g < G; ++g) {
-        next[g] = 0;
-        remaining += gstages(g);
+      if (a.l2_prefetch) {
+        prefetch_range_l2(a.W, q_bytes, r0 * q_row, r1 * q_row);
+        prefetch_range_l2(a.W + q_bytes, int64_t(a.n_out) * s_row, r0 * s_row, r1 * s_row);
+        if (EPI == kSwiglu) {
+          prefetch_range_l2(a.W2, q_bytes, r0 * q_row, r1 * q_row);
+          prefetch_range_l2(a.W2 + q_bytes, int64_t(a.n_out) * s_row, r0 * s_row, r1 * s_row);
+        }
       }
-      unsigned long long idle_since = global_ns();
-      uint32_t idle_spins = 0;
-      bool prefetched = !a.l2_prefetch;
-      while (remaining > 0) {
-        bool progress = false;
+      int rounds = 0;
+      for (int g = 0; g < G; ++g) rounds = max(rounds, gstages(g));
+      int stop_i = rounds, stop_g = 0;  // first stage not issued, if the loop stopped early
+      for (int i = 0; i < rounds && stop_i == rounds; ++i) {
         for (int g = 0; g < G; ++g) {
-          const int i = next[g];
           if (i >= gstages(g)) continue;
-          const int SG = scount(g);
-          const int s = sbase(g) + i % SG;
-          if (i >= SG && !mbar_test(&empty[s], ((i / SG) + 1) & 1)) continue;
+          const int s = g * SG + i % SG;
+          if (i >= SG && !mbar_wait(&empty[s], ((i / SG) + 1) & 1)) {
+            s_abort = 1;
+            stop_i = i;
+            stop_g = g;
+            break;
+          }
           uint8_t *stq = smem + size_t(s) * a.stage_bytes;
           uint8_t *sts = stq + kStageRows * q_row;
           const int rr = gbeg(g) + i * kRowsPerStage;           // first output row of the stage
@@ -162,46 +160,14 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
             bulk_copy_g2s(stq + 2 * q_row, a.W2 + rr * q_row, uint32_t(nr * q_row), &full[s]);
             bulk_copy_g2s(sts + 2 * s_row, a.W2 + q_bytes + rr * s_row, uint32_t(nr * s_row), &full[s]);
           }
-          next[g] = i + 1;
-          --remaining;
-          progress = true;
-        }
-        if (!prefetched) {
-          // Once every group's first ring fill is out, pull the rows that do not fit
-          // the ring into L2, so that their refills later hit L2 instead of waiting
-          // behind the next kernel's prefill in the DRAM queues.
-          bool filled = true;
-          for (int g = 0; g < G; ++g) filled = filled && next[g] >= min(scount(g), gstages(g));
-          if (filled) {
-            for (int g = 0; g < G; ++g) {
-              const int64_t lo = gbeg(g) + scount(g) * kRowsPerStage, hi = gbeg(g + 1);
-              if (lo >= hi) continue;
-              const int64_t s_plane = int64_t(a.n_out) * s_row;
-              prefetch_range_l2(a.W, q_bytes, lo * q_row, hi * q_row);
-              prefetch_range_l2(a.W + q_bytes, s_plane, lo * s_row, hi * s_row);
-              if (EPI == kSwiglu) {
-                prefetch_range_l2(a.W2, q_bytes, lo * q_row, hi * q_row);
-                prefetch_range_l2(a.W2 + q_bytes, s_plane, lo * s_row, hi * s_row);
-              }
-            }
-            prefetched = true;
-          }
-        }
-        if (progress) {
-          idle_spins = 0;
-          idle_since = global_ns();
-        } else {
-          if ((++idle_spins & 255u) == 0 && global_ns() - idle_since > kWaitLimitNs) {
-            s_abort = 1;  // no slot came free within the limit: stop issuing
-            break;
-          }
-          __nanosleep(64);  // leave the issue slots to the consumers while no slot is free
         }
       }
       // never exit with copies in flight: wait for the last fill of every slot
-      for (int g = 0; g < G; ++g)
-        for (int i = next[g] - scount(g) < 0 ? 0 : next[g] - scount(g); i < next[g]; ++i)
-          mbar_wait(&full[sbase(g) + i % scount(g)], (i / scount(g)) & 1);
+      for (int g = 0; g < G; ++g) {
+        const int issued = stop_i == rounds ? gstages(g) : min(gstages(g), stop_i + (g < stop_g ? 1 : 0));
+        for (int i = issued - SG < 0 ? 0 : issued - SG; i < issued; ++i)
+          mbar_wait(&full[g * SG + i % SG], (i / SG) & 1);
+      }
     }
   } else {
     // ---------------- consumers ----------------
@@ -257,8 +223,7 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
     const int rbeg = gbeg(grp) - r0;                 // this group's first local output row
     const int vend = (gbeg(grp + 1) - r0) * kV;      // end of its virtual rows
     const int nst = gstages(grp);
-    const int s_lo = sbase(grp), s_hi = s_lo + scount(grp);
-    int s = s_lo;          // this group's current slot and the parity of its fill:
+    int s = grp * SG;      // this group's current slot and the parity of its fill:
     uint32_t parity = 0;   // tracked incrementally (no division in the loop)
     for (int t = 0; t < nst; ++t) {
       if (!mbar_wait(&full[s], parity)) {
@@ -266,9 +231,12 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
         break;
       }
       const uint8_t *stq = smem + size_t(s) * a.stage_bytes;
-      // The stage's bytes are in registers once the loads below are issued: the
-      // arrive (a release) orders those reads before the slot is refilled, so the
-      // producer can start the next copy while this warp computes.
+      // Q4_K GEMV / down projection: the slot is released as soon as the stage's bytes
+      // are in registers (the arrive is a release, so the reads are ordered before the
+      // refill) and the producer refills it while this warp computes.  Measured on
+      // 3072 <-> 8192 chains, that helps there but slows the SwiGLU and the Q8_0 GEMV,
+      // which release after their arithmetic.
+      constexpr bool kEarlyRelease = FMT == kQ4 && EPI != kSwiglu;
       auto release = [&](int slot) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
@@ -287,7 +255,7 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
           qb[k] = *reinterpret_cast<const uint4 *>(stq + qofs[k] + 16);
           dv[k] = __half2float(*reinterpret_cast<const __half *>(stq + sofs[k]));
         }
-        release(s);
+        if (kEarlyRelease) release(s);
         float2 s0[kStageRows], s1[kStageRows];
 #pragma unroll
         for (int k = 0; k < kStageRows; ++k) s0[k] = s1[k] = f2(0.f, 0.f);
@@ -315,7 +283,7 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
           q[k] = *reinterpret_cast<const uint4 *>(stq + qofs[k]);
           h[k] = *reinterpret_cast<const uint4 *>(stq + sofs[k]);
         }
-        release(s);
+        if (kEarlyRelease) release(s);
         float2 DM[kStageRows];
 #pragma unroll
         for (int k = 0; k < kStageRows; ++k) {
@@ -347,8 +315,9 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
           part[k] = fmaf(DM[k].x, st.x + st.y, -DM[k].y * xsum);  // d sc_j sum(q x) - dmin m_j sum(x)
         }
       }
-      if (++s == s_hi) {
-        s = s_lo;
+      if (!kEarlyRelease) release(s);
+      if (++s == (grp + 1) * SG) {
+        s = grp * SG;
         parity ^= 1u;
       }
       butterfly4(part, lane);
@@ -442,13 +411,12 @@ int launch_xs(const uint8_t *W, const uint8_t *W2, const float *x, const float *
     const int g_smem = int(budget / (2L * a.stage_bytes));
     if (a.groups > g_smem) a.groups = g_smem < 1 ? 1 : g_smem;
   }
-  // every slot the budget holds, at least two and at most eight per group
-  int slots = int(budget / long(a.stage_bytes));
-  if (slots > 8 * a.groups) slots = 8 * a.groups;
-  if (slots < 2 * a.groups) slots = 2 * a.groups;
-  if (opt_xs_stages() > 0) slots = opt_xs_stages() * a.groups;
-  a.slots = slots;
-  const int stages = slots;
+  int sg = int(budget / (long(a.stage_bytes) * a.groups));
+  if (sg > 8) sg = 8;
+  if (sg < 2) sg = 2;
+  if (opt_xs_stages() > 0) sg = opt_xs_stages();
+  a.sg = sg;
+  const int stages = a.groups * sg;
   const size_t smem = size_t(stages) * a.stage_bytes + 2 * stages * sizeof(uint64_t) + psum_bytes;
   if (smem > size_t(di.max_smem_optin)) return QDQ_ERR_UNSUPPORTED;
   const cudaError_t e0 = allow_dynamic_smem(reinterpret_cast<const void *>(kern), int(smem));
