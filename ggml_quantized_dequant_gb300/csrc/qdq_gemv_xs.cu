@@ -19,11 +19,12 @@
 //    with 1-D bulk async copies into a ring of stages in shared memory.  The
 //    weights do not depend on the previous kernel, so the ring is filled
 //    before the previous kernel has finished (programmatic dependent launch);
-//  * the slice warps form G groups; group g consumes stages g, g+G, ...  For
-//    each stage a lane reads its block of the 4 rows, and a recursive-halving
-//    butterfly reduces the 4 per-lane partial sums across the warp (lane 8k
-//    ends with row k's warp total).  The WPR slice totals of a row are added
-//    in fixed order at the end, so results are deterministic.
+//  * the slice warps form G groups; group g owns a contiguous share of the
+//    CTA's rows and consumes its stages, in order, from its own ring slots.
+//    For each stage a lane reads its block of the 4 rows, and a
+//    recursive-halving butterfly reduces the 4 per-lane partial sums across the
+//    warp (lane 8k ends with row k's warp total).  The WPR slice totals of a
+//    row are added in fixed order at the end, so results are deterministic.
 // SwiGLU streams gate and up rows as pairs (a stage = 2 output rows, each
 // with its gate row and its up row) and combines them in the epilogue.
 // Every pipeline wait is bounded; a wait that runs out is counted
