@@ -13,7 +13,7 @@ namespace {
 thread_local int g_last_cuda_error = 0;
 std::atomic<int> g_opt_pdl{1};
 std::atomic<int> g_opt_l2_prefetch{0};
-std::atomic<int> g_opt_ctas_per_sm{1};
+std::atomic<int> g_opt_ctas_per_sm{0};
 std::atomic<int> g_opt_xs_groups{0};
 std::atomic<int> g_opt_xs_stages{0};
 
@@ -67,7 +67,7 @@ cudaError_t device_info(DeviceInfo *out) {
 
 size_t gemv_smem_bytes(const DeviceInfo &di, size_t need) {
   if (!opt_pdl()) return need;
-  const int per_sm = opt_ctas_per_sm() + 1;  // this kernel's CTAs + one of the next kernel
+  const int per_sm = ctas_per_sm_or(1) + 1;  // this kernel's CTAs + one of the next kernel
   long cap = long(di.smem_per_sm) / per_sm - di.reserved_smem_per_block;
   if (cap > di.max_smem_optin) cap = di.max_smem_optin;
   return size_t(cap) > need ? size_t(cap) : need;
@@ -148,7 +148,7 @@ int qdq_set_option(int key, int value) {
       if (value != 0 && value != 1) return QDQ_ERR_DIMS;
       return g_opt_l2_prefetch.exchange(value);
     case QDQ_OPT_CTAS_PER_SM:
-      if (value < 1 || value > 4) return QDQ_ERR_DIMS;
+      if (value < 0 || value > 4) return QDQ_ERR_DIMS;
       return g_opt_ctas_per_sm.exchange(value);
     case QDQ_OPT_XS_GROUPS:
       if (value < 0 || value > 16) return QDQ_ERR_DIMS;

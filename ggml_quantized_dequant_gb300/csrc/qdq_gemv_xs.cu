@@ -401,7 +401,11 @@ int launch_xs(const uint8_t *W, const uint8_t *W2, const float *x, const float *
   const int64_t q_row = FMT == kQ8 ? n_in : n_in / 2;
   const int64_t s_row = FMT == kQ8 ? n_in / 16 : (n_in / 256) * 16;
   a.stage_bytes = int((kStageRows * (q_row + s_row) + 127) / 128 * 128);
-  int grid = di.sm_count * opt_ctas_per_sm();
+  // The FFN kernels (SwiGLU, down + residual) run two CTAs per SM with two ring slots
+  // per group: both CTAs compute at once instead of one computing beside the next
+  // kernel's prefill, which measured ~7 % faster for the block.  The GEMVs keep one.
+  constexpr bool kFfn = EPI != kPlain;
+  int grid = di.sm_count * ctas_per_sm_or(kFfn ? 2 : 1);
   if (grid > n_out) grid = n_out;
   const int max_rows = (n_out + grid - 1) / grid;
   const size_t psum_bytes = size_t(max_rows) * (EPI == kSwiglu ? 2 : 1) * a.wpr * sizeof(float);
@@ -412,7 +416,7 @@ int launch_xs(const uint8_t *W, const uint8_t *W2, const float *x, const float *
     const int g_smem = int(budget / (2L * a.stage_bytes));
     if (a.groups > g_smem) a.groups = g_smem < 1 ? 1 : g_smem;
   }
-  int sg = int(budget / (long(a.stage_bytes) * a.groups));
+  int sg = kFfn ? 2 : int(budget / (long(a.stage_bytes) * a.groups));
   if (sg > 8) sg = 8;
   if (sg < 2) sg = 2;
   if (opt_xs_stages() > 0) sg = opt_xs_stages();

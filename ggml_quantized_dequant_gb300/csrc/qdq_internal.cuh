@@ -16,6 +16,11 @@ namespace qdq {
 int opt_pdl();
 int opt_l2_prefetch();
 int opt_ctas_per_sm();
+// The CTAs-per-SM option, or `dflt` where it is left automatic (0).
+inline int ctas_per_sm_or(int dflt) {
+  const int v = opt_ctas_per_sm();
+  return v > 0 ? v : dflt;
+}
 int opt_xs_groups();
 int opt_xs_stages();
 
@@ -37,7 +42,7 @@ size_t gemv_smem_bytes(const DeviceInfo &di, size_t need);
 // Grid of a streaming GEMV: CTAs-per-SM x SMs, but no more CTAs than tasks of
 // `rows_per_task` output rows.
 inline int gemv_grid(const DeviceInfo &di, int n_out, int rows_per_task) {
-  const int g = di.sm_count * opt_ctas_per_sm();
+  const int g = di.sm_count * ctas_per_sm_or(1);
   const int max_g = (n_out + rows_per_task - 1) / rows_per_task;
   return g < max_g ? g : max_g;
 }

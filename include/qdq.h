@@ -183,7 +183,7 @@ int qdq_pipeline_timeouts(void);
 /* ---- launch options (same work, different launch shape; for measurement) -- */
 #define QDQ_OPT_PDL          1  /* 1 (default): programmatic dependent launch on; 0: plain launches */
 #define QDQ_OPT_L2_PREFETCH  2  /* 1: each GEMV CTA bulk-prefetches its weight rows into L2 first; 0 (default): no prefetch */
-#define QDQ_OPT_CTAS_PER_SM  3  /* GEMV CTAs per SM, 1..4 (default 1) */
+#define QDQ_OPT_CTAS_PER_SM  3  /* GEMV-family CTAs per SM, 1..4; 0 (default): automatic (2 for the FFN kernels, else 1) */
 #define QDQ_OPT_XS_GROUPS    4  /* batch-1 GEMV consumer groups per CTA, 0 = automatic (default), 1..16 */
 #define QDQ_OPT_XS_STAGES    5  /* batch-1 GEMV weight-ring slots per consumer group (4-row stages), 0 = automatic (default), 1..16 */
 /* Sets a process-wide option; returns the previous value, or QDQ_ERR_DIMS for a bad key/value. */

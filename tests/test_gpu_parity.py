@@ -318,6 +318,29 @@ def test_launch_options_do_not_change_results(cuda_lib):
         assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32))
 
 
+def test_ctas_per_sm_does_not_change_ffn_results(cuda_lib):
+    # a row's sum does not depend on which CTA computes it: every split of the rows
+    # between CTAs gives the same bits
+    qdq = cuda_lib
+    import torch
+    rng = np.random.default_rng(23)
+    g, u, d = synth.q4k_blocks(rng, 2048, 1024), synth.q4k_blocks(rng, 2048, 1024), synth.q4k_blocks(rng, 1024, 2048)
+    x, res = synth.activations(rng, 1, 1024), synth.activations(rng, 1, 1024)
+    Wg, Wu, Wd = qdq.upload_q4k(g, 2048, 1024), qdq.upload_q4k(u, 2048, 1024), qdq.upload_q4k(d, 1024, 2048)
+    outs = []
+    for cps in (0, 1, 2, 3):
+        old = qdq.set_option(qdq.QDQ_OPT_CTAS_PER_SM, cps)
+        try:
+            out, mid = _nan(1, 1024), torch.empty((1, 2048), device=_dev())
+            qdq.q4k_ffn_residual(Wg, Wu, Wd, _t(x), _t(res), out, mid, 1024, 2048, 1)
+            outs.append(_np(out))
+        finally:
+            qdq.set_option(qdq.QDQ_OPT_CTAS_PER_SM, old)
+    for o in outs[1:]:
+        assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32))
+    assert qdq.pipeline_timeouts() == 0
+
+
 def test_error_leaves_outputs_untouched(cuda_lib):
     qdq = cuda_lib
     import torch
