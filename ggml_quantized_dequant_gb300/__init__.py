@@ -31,6 +31,7 @@ QDQ_OPT_L2_PREFETCH = 2
 QDQ_OPT_CTAS_PER_SM = 3
 QDQ_OPT_XS_GROUPS = 4
 QDQ_OPT_XS_STAGES = 5
+QDQ_OPT_XS_FLOAT_X = 6
 
 _c_int, _c_size, _c_vp, _c_char_p = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_char_p
 

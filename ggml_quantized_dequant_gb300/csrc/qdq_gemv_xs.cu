@@ -27,6 +27,24 @@
 //    row are added in fixed order at the end, so results are deterministic.
 // SwiGLU streams gate and up rows as pairs (a stage = 2 output rows, each
 // with its gate row and its up row) and combines them in the epilogue.
+//
+// Arithmetic.  Turning int8 / u4 weights into floats costs more issue slots
+// on this GPU than streaming them from HBM, so by default the weights stay
+// integers: a lane turns its 32 activations once into 24-bit block fixed point
+// X_j = rint(x_j 2^e) (e from the block's largest |x|, |X_j| <= 2^22), split
+// into three int8 limbs, and a row's block dot product sum_j q_j X_j is three
+// exact dp4a byte dot products per 4 weights.  The scales are applied to that
+// integer sum in f32 ((d / 2^e) sum q X, and for Q4_K
+// (d sc sum q X - dmin m sum X) / 2^e).  The only approximation beyond f32
+// rounding is |x_j - X_j 2^-e| <= 2^-22 max_block |x|, so
+//   |y - exact| <= 2^-22 sum_b max_{j in b} |x_j| sum_{j in b} |w_j| + f32 rounding,
+// which is within 1e-5 sum |w||x| unless a row's weights concentrate on the
+// small activations of blocks whose largest activation they skip (a ratio
+// above ~40 between the two sums).  QDQ_OPT_XS_FLOAT_X selects the f32 path
+// instead: weights converted exactly to f32 (magic-number LOP3s) and packed
+// f32x2 FMAs against the f32 activations, within 1e-5 sum |w||x| for every
+// finite input.  A block holding an inf or a NaN gives NaN rows on the fixed
+// path (the f32 path propagates them by IEEE rules).
 // Every pipeline wait is bounded; a wait that runs out is counted
 // (qdq_pipeline_timeouts) and the CTA winds down instead of hanging.
 #include <mutex>
@@ -45,6 +63,93 @@ constexpr int kMaxThreads = 544;  // up to 16 consumer warps + the producer
 
 enum Fmt { kQ8 = 0, kQ4 = 1 };
 enum Epi { kPlain = 0, kSwiglu = 1, kResidual = 2 };
+enum Arith { kFixedX = 0, kFloatX = 1 };
+
+// Four-way byte dot products: c + sum_i a.byte[i] * b.byte[i], the bytes of a
+// and b read as signed (s) or unsigned (u).
+__device__ __forceinline__ int dp4a_su(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+// max that returns NaN when either input is NaN
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// One lane's 32 activations in block fixed point (see Arithmetic above):
+// X_j = rint(x_j 2^e), e = 148 - (biased exponent of max_j |x_j|), so
+// 2^21 <= max|X| <= 2^22 for a normal maximum.  X_j = L2 2^16 + L1 2^8 + L0
+// with L0, L1 the unsigned bytes 0, 1 of X_j and L2 = X_j >> 16 in [-64, 64].
+// p[l][w] packs limb l of the four activations that weight word w multiplies:
+// Q8_0 word w holds weights 4w..4w+3; Q4_K word c holds nibbles 8c..8c+7 and is
+// split into its even nibbles (packed word 2c) and odd nibbles (word 2c + 1).
+struct FixedX {
+  uint32_t p[3][8];
+  float inv_s;  // 2^-e (NaN when the block holds an inf or a NaN)
+  float xsum;   // sum_j X_j
+};
+
+template <int FMT>
+__device__ __forceinline__ void to_fixed(const float (&xv)[32], FixedX &f) {
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) m = max_nan(m, fabsf(xv[j]));
+  const int E = __float_as_int(m) >> 23;
+  if (E >= 255) {
+#pragma unroll
+    for (int l = 0; l < 3; ++l)
+#pragma unroll
+      for (int w = 0; w < 8; ++w) f.p[l][w] = 0u;
+    f.inv_s = __int_as_float(0x7fffffff);
+    f.xsum = 0.f;
+    return;
+  }
+  const int e = 148 - (E > 1 ? E : 1);  // -106 .. 147; a zero or subnormal maximum takes E = 1
+  // 2^e as two normal factors; x * 2^(e>>1) is exact wherever the product can round to X != 0
+  const float s1 = __int_as_float(((e >> 1) + 127) << 23);
+  const float s2 = __int_as_float((e - (e >> 1) + 127) << 23);
+  f.inv_s = e <= 126 ? __int_as_float((127 - e) << 23) : __int_as_float(1 << (149 - e));
+  int X[32];
+  int sum = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    // |x 2^e| < 2^22: adding 1.5 * 2^23 rounds it to an integer in the low mantissa bits
+    X[j] = __float_as_int(__fmaf_rn(__fmul_rn(xv[j], s1), s2, 12582912.0f)) - 0x4B400000;
+    sum += X[j];
+  }
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    int i[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) i[b] = FMT == kQ8 ? 4 * w + b : 8 * (w >> 1) + 2 * b + (w & 1);
+    const uint32_t t0 = __byte_perm(X[i[0]], X[i[1]], 0x5140);  // b0 b0' b1 b1' of elements 0, 1
+    const uint32_t t1 = __byte_perm(X[i[2]], X[i[3]], 0x5140);
+    f.p[0][w] = __byte_perm(t0, t1, 0x5410);
+    f.p[1][w] = __byte_perm(t0, t1, 0x7632);
+    const uint32_t u0 = __byte_perm(X[i[0]], X[i[1]], 0x0062);  // b2 b2' of elements 0, 1
+    const uint32_t u1 = __byte_perm(X[i[2]], X[i[3]], 0x0062);
+    f.p[2][w] = __byte_perm(u0, u1, 0x5410);
+  }
+  f.xsum = __int2float_rn(sum);
+}
 
 // Reduce v[0..3] (one partial per row per lane) over the warp; afterwards lane
 // 8k holds the warp total of row k.
@@ -84,7 +189,7 @@ struct XsArgs {
   int l2_prefetch;
 };
 
-template <int FMT, int EPI>
+template <int FMT, int EPI, int AR>
 __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, const Magic mg_param) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int kV = EPI == kSwiglu ? 2 : 1;  // virtual rows per output row
@@ -183,25 +288,37 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
     if (warp == 0) pdl_wait();
     named_bar_sync(1, 32 * ncw);
     pdl_wait();
-    float2 xr[16];  // activation pairs, kept as aligned register pairs for the packed FMAs
+    float2 xr[16];  // f32 path: activation pairs, aligned register pairs for the packed FMAs
     float xsum = 0.f;
-    if (valid) {
-      const float4 *xp = reinterpret_cast<const float4 *>(a.x + blk * 32);
+    FixedX fx;      // fixed path
+    {
+      float xv[32];
+      if (valid) {
+        const float4 *xp = reinterpret_cast<const float4 *>(a.x + blk * 32);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const float4 v = __ldg(xp + c);
-        xr[2 * c] = f2(v.x, v.y);
-        xr[2 * c + 1] = f2(v.z, v.w);
+        for (int c = 0; c < 8; ++c) {
+          const float4 v = ld_after_wait(xp + c);  // x comes from the previous kernel
+          xv[4 * c] = v.x;
+          xv[4 * c + 1] = v.y;
+          xv[4 * c + 2] = v.z;
+          xv[4 * c + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) xv[k] = 0.f;
       }
-      if constexpr (FMT == kQ4) {
-        float2 t = f2(0.f, 0.f);
+      if constexpr (AR == kFixedX) {
+        to_fixed<FMT>(xv, fx);
+      } else {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) t = __fadd2_rn(t, xr[c]);
-        xsum = t.x + t.y;
+        for (int c = 0; c < 16; ++c) xr[c] = f2(xv[2 * c], xv[2 * c + 1]);
+        if constexpr (FMT == kQ4) {
+          float2 t = f2(0.f, 0.f);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) t = __fadd2_rn(t, xr[c]);
+          xsum = t.x + t.y;
+        }
       }
-    } else {
-#pragma unroll
-      for (int k = 0; k < 16; ++k) xr[k] = f2(0.f, 0.f);
     }
     // Q4_K: this lane's 12-bit (sc, m) field lives at bit 12 j of header words 1..3
     const int j = lane & 7;
@@ -257,25 +374,48 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
           dv[k] = __half2float(*reinterpret_cast<const __half *>(stq + sofs[k]));
         }
         if (kEarlyRelease) release(s);
-        float2 s0[kStageRows], s1[kStageRows];
+        if constexpr (AR == kFixedX) {
+          int c0[kStageRows], c1[kStageRows], c2[kStageRows];  // sum_j q_j L_l(X_j), one per limb
 #pragma unroll
-        for (int k = 0; k < kStageRows; ++k) s0[k] = s1[k] = f2(0.f, 0.f);
+          for (int k = 0; k < kStageRows; ++k) c0[k] = c1[k] = c2[k] = 0;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+          for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+            for (int k = 0; k < kStageRows; ++k) {
+              const uint32_t w = kk == 0 ? qa[k].x : kk == 1 ? qa[k].y : kk == 2 ? qa[k].z : kk == 3 ? qa[k].w
+                               : kk == 4 ? qb[k].x : kk == 5 ? qb[k].y : kk == 6 ? qb[k].z : qb[k].w;
+              c0[k] = dp4a_su(w, fx.p[0][kk], c0[k]);
+              c1[k] = dp4a_su(w, fx.p[1][kk], c1[k]);
+              c2[k] = dp4a_ss(w, fx.p[2][kk], c2[k]);
+            }
+          }
 #pragma unroll
           for (int k = 0; k < kStageRows; ++k) {
-            const uint32_t w = kk == 0 ? qa[k].x : kk == 1 ? qa[k].y : kk == 2 ? qa[k].z : kk == 3 ? qa[k].w
-                             : kk == 4 ? qb[k].x : kk == 5 ? qb[k].y : kk == 6 ? qb[k].z : qb[k].w;
-            float2 q01, q23;
-            s8x4_to_f2(w, mg, q01, q23);
-            s0[k] = __ffma2_rn(q01, xr[2 * kk], s0[k]);
-            s1[k] = __ffma2_rn(q23, xr[2 * kk + 1], s1[k]);
+            // sum q X = c2 2^16 + (c1 2^8 + c0); the bracket is exact in int32 (|.| < 2^30)
+            const float qx = fmaf(__int2float_rn(c2[k]), 65536.0f, __int2float_rn(c0[k] + c1[k] * 256));
+            part[k] = (dv[k] * qx) * fx.inv_s;
           }
-        }
+        } else {
+          float2 s0[kStageRows], s1[kStageRows];
 #pragma unroll
-        for (int k = 0; k < kStageRows; ++k) {
-          const float2 st = __fadd2_rn(s0[k], s1[k]);
-          part[k] = dv[k] * (st.x + st.y);
+          for (int k = 0; k < kStageRows; ++k) s0[k] = s1[k] = f2(0.f, 0.f);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+            for (int k = 0; k < kStageRows; ++k) {
+              const uint32_t w = kk == 0 ? qa[k].x : kk == 1 ? qa[k].y : kk == 2 ? qa[k].z : kk == 3 ? qa[k].w
+                               : kk == 4 ? qb[k].x : kk == 5 ? qb[k].y : kk == 6 ? qb[k].z : qb[k].w;
+              float2 q01, q23;
+              s8x4_to_f2(w, mg, q01, q23);
+              s0[k] = __ffma2_rn(q01, xr[2 * kk], s0[k]);
+              s1[k] = __ffma2_rn(q23, xr[2 * kk + 1], s1[k]);
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < kStageRows; ++k) {
+            const float2 st = __fadd2_rn(s0[k], s1[k]);
+            part[k] = dv[k] * (st.x + st.y);
+          }
         }
       } else {
         uint4 q[kStageRows], h[kStageRows];
@@ -294,26 +434,48 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
           const float2 scm = q4k_field_to_f2(f, mg);  // (sc, m)
           DM[k] = __fmul2_rn(__half22float2(*reinterpret_cast<const __half2 *>(&h[k].x)), scm);  // (d sc, dmin m)
         }
-        float2 s0[kStageRows], s1[kStageRows];
+        if constexpr (AR == kFixedX) {
+          int c0[kStageRows], c1[kStageRows], c2[kStageRows];
 #pragma unroll
-        for (int k = 0; k < kStageRows; ++k) s0[k] = s1[k] = f2(0.f, 0.f);
+          for (int k = 0; k < kStageRows; ++k) c0[k] = c1[k] = c2[k] = 0;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
+          for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+            for (int k = 0; k < kStageRows; ++k) {
+              const uint32_t w = kk == 0 ? q[k].x : kk == 1 ? q[k].y : kk == 2 ? q[k].z : q[k].w;
+              const uint32_t ev = w & 0x0F0F0F0Fu, od = (w >> 4) & 0x0F0F0F0Fu;  // even / odd nibbles as bytes
+              c0[k] = dp4a_uu(od, fx.p[0][2 * kk + 1], dp4a_uu(ev, fx.p[0][2 * kk], c0[k]));
+              c1[k] = dp4a_uu(od, fx.p[1][2 * kk + 1], dp4a_uu(ev, fx.p[1][2 * kk], c1[k]));
+              c2[k] = dp4a_us(od, fx.p[2][2 * kk + 1], dp4a_us(ev, fx.p[2][2 * kk], c2[k]));
+            }
+          }
 #pragma unroll
           for (int k = 0; k < kStageRows; ++k) {
-            const uint32_t w = kk == 0 ? q[k].x : kk == 1 ? q[k].y : kk == 2 ? q[k].z : q[k].w;
-            float2 qq[4];
-            u4x8_to_f2(w, mg, qq);
-            s0[k] = __ffma2_rn(qq[0], xr[4 * kk], s0[k]);
-            s1[k] = __ffma2_rn(qq[1], xr[4 * kk + 1], s1[k]);
-            s0[k] = __ffma2_rn(qq[2], xr[4 * kk + 2], s0[k]);
-            s1[k] = __ffma2_rn(qq[3], xr[4 * kk + 3], s1[k]);
+            const float qx = fmaf(__int2float_rn(c2[k]), 65536.0f, __int2float_rn(c0[k] + c1[k] * 256));
+            part[k] = fmaf(DM[k].x, qx, -DM[k].y * fx.xsum) * fx.inv_s;  // (d sc sum qX - dmin m sum X) / 2^e
           }
-        }
+        } else {
+          float2 s0[kStageRows], s1[kStageRows];
 #pragma unroll
-        for (int k = 0; k < kStageRows; ++k) {
-          const float2 st = __fadd2_rn(s0[k], s1[k]);
-          part[k] = fmaf(DM[k].x, st.x + st.y, -DM[k].y * xsum);  // d sc_j sum(q x) - dmin m_j sum(x)
+          for (int k = 0; k < kStageRows; ++k) s0[k] = s1[k] = f2(0.f, 0.f);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+            for (int k = 0; k < kStageRows; ++k) {
+              const uint32_t w = kk == 0 ? q[k].x : kk == 1 ? q[k].y : kk == 2 ? q[k].z : q[k].w;
+              float2 qq[4];
+              u4x8_to_f2(w, mg, qq);
+              s0[k] = __ffma2_rn(qq[0], xr[4 * kk], s0[k]);
+              s1[k] = __ffma2_rn(qq[1], xr[4 * kk + 1], s1[k]);
+              s0[k] = __ffma2_rn(qq[2], xr[4 * kk + 2], s0[k]);
+              s1[k] = __ffma2_rn(qq[3], xr[4 * kk + 3], s1[k]);
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < kStageRows; ++k) {
+            const float2 st = __fadd2_rn(s0[k], s1[k]);
+            part[k] = fmaf(DM[k].x, st.x + st.y, -DM[k].y * xsum);  // d sc_j sum(q x) - dmin m_j sum(x)
+          }
         }
       }
       if (!kEarlyRelease) release(s);
@@ -369,9 +531,9 @@ cudaError_t kernel_regs(const void *func, int *regs) {
   return cudaSuccess;
 }
 
-template <int FMT, int EPI>
-int launch_xs(const uint8_t *W, const uint8_t *W2, const float *x, const float *residual, float *y, int n_out,
-              int n_in, cudaStream_t s, const DeviceInfo &di) {
+template <int FMT, int EPI, int AR>
+int launch_xs_ar(const uint8_t *W, const uint8_t *W2, const float *x, const float *residual, float *y, int n_out,
+                 int n_in, cudaStream_t s, const DeviceInfo &di) {
   XsArgs a;
   a.W = W;
   a.W2 = W2;
@@ -381,7 +543,7 @@ int launch_xs(const uint8_t *W, const uint8_t *W2, const float *x, const float *
   a.n_out = n_out;
   a.n_in = n_in;
   a.wpr = ((n_in >> 5) + 31) / 32;
-  auto kern = gemv_xs_kernel<FMT, EPI>;
+  auto kern = gemv_xs_kernel<FMT, EPI, AR>;
   // About 6 (Q8_0) or 9 (Q4_K, twice the weights per byte) consumer warps:
   // measured best on 3072 <-> 8192 decode chains.  More warps add contention
   // without adding throughput.  The groups must also fit in half an SM's
@@ -428,6 +590,13 @@ int launch_xs(const uint8_t *W, const uint8_t *W2, const float *x, const float *
   if (e0 != cudaSuccess) return fail_cuda(e0);
   const cudaError_t e = launch(kern, dim3(grid), dim3(32 * (a.wpr * a.groups + 1)), smem, s, a, make_magic());
   return e == cudaSuccess ? QDQ_OK : fail_cuda(e);
+}
+
+template <int FMT, int EPI>
+int launch_xs(const uint8_t *W, const uint8_t *W2, const float *x, const float *residual, float *y, int n_out,
+              int n_in, cudaStream_t s, const DeviceInfo &di) {
+  return opt_xs_float_x() ? launch_xs_ar<FMT, EPI, kFloatX>(W, W2, x, residual, y, n_out, n_in, s, di)
+                          : launch_xs_ar<FMT, EPI, kFixedX>(W, W2, x, residual, y, n_out, n_in, s, di);
 }
 
 }  // namespace

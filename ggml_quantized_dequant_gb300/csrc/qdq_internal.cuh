@@ -23,6 +23,7 @@ inline int ctas_per_sm_or(int dflt) {
 }
 int opt_xs_groups();
 int opt_xs_stages();
+int opt_xs_float_x();
 
 // Per-device facts queried once (SM count, opt-in shared memory).
 struct DeviceInfo {
@@ -204,6 +205,18 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
                    smem_u32(dst)),
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
+}
+
+// 128-bit coherent load of data an earlier kernel wrote.  A volatile asm with a
+// memory clobber stays after a preceding griddepcontrol.wait; __ldg (ld.global.nc)
+// is an invariant load the compiler may hoist above that wait.
+__device__ __forceinline__ float4 ld_after_wait(const float4 *p) {
+  float4 v;
+  asm volatile("ld.global.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
 }
 
 // 128-bit read-only load that does not allocate in L1 (streamed weights).

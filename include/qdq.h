@@ -104,8 +104,10 @@ int qdq_q4k_dequant(const void *W, float *out, int n_out, int n_in, cudaStream_t
  * "Module cuda_lane", Functions: try_q8_0_cuda_gemv, q8_0_gemv_oracle_into,
  * try_q4k_soa_gemv.  W: packed (16-byte aligned).  x: batch x n_in f32,
  * 16-byte aligned.  y: batch x n_out f32, 4-byte aligned, must not overlap W
- * or x.  1 <= batch <= QDQ_MAX_GEMV_BATCH.  f32 accumulation; the error
- * against the exact sum stays far below 1e-5 * sum_k |w[r,k]| |x[b,k]|.
+ * or x.  1 <= batch <= QDQ_MAX_GEMV_BATCH.  Batch 2..8: f32 arithmetic; the
+ * error against the exact sum stays far below 1e-5 * sum_k |w[r,k]| |x[b,k]|.
+ * Batch 1: the arithmetic QDQ_OPT_XS_FLOAT_X selects, with the bound stated
+ * there (the same holds for the SwiGLU and FFN calls below at batch 1).
  */
 int qdq_q8_0_gemv(const void *W, const float *x, float *y,
                   int n_out, int n_in, int batch, cudaStream_t stream);
@@ -186,6 +188,18 @@ int qdq_pipeline_timeouts(void);
 #define QDQ_OPT_CTAS_PER_SM  3  /* GEMV-family CTAs per SM, 1..4; 0 (default): automatic (2 for the FFN kernels, else 1) */
 #define QDQ_OPT_XS_GROUPS    4  /* batch-1 GEMV consumer groups per CTA, 0 = automatic (default), 1..16 */
 #define QDQ_OPT_XS_STAGES    5  /* batch-1 GEMV weight-ring slots per consumer group (4-row stages), 0 = automatic (default), 1..16 */
+/* Arithmetic of the batch-1 kernels (qdq_q8_0_gemv and qdq_q4k_gemv at batch 1,
+ * qdq_q4k_swiglu and both FFN calls at batch 1):
+ *   0 (default): each 32-activation block becomes 24-bit block fixed point
+ *     X_j = rint(x_j 2^e), |X_j| <= 2^22, and block dot products are exact
+ *     integer byte dot products, scaled in f32.  Error against the exact sum
+ *     <= 2^-22 sum_blocks max_j |x_j| sum_j |w_j| + f32 rounding: within
+ *     1e-5 sum |w||x| unless a row's weights sit on the small activations of
+ *     blocks whose largest activation they skip.  A block with an inf or NaN
+ *     activation gives NaN outputs.
+ *   1: weights converted to f32 and multiplied with f32 FMAs: within
+ *     1e-5 sum |w||x| for every finite input, about half the ALU throughput. */
+#define QDQ_OPT_XS_FLOAT_X   6
 /* Sets a process-wide option; returns the previous value, or QDQ_ERR_DIMS for a bad key/value. */
 int qdq_set_option(int key, int value);
 

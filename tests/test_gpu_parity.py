@@ -297,6 +297,147 @@ def test_q8_0_gemm_batch_m1_matches_gemv_within_bf16_bound(cuda_lib):
     assert np.all(np.abs(_np(Y) - _np(y)) <= 4e-3 * a)
 
 
+# ------------------------------------------------------------------ batch-1 arithmetic
+# The batch-1 kernels multiply in 24-bit block fixed point by default (the integer
+# byte dot products); QDQ_OPT_XS_FLOAT_X = 1 selects f32 arithmetic.  Their error
+# bounds (include/qdq.h):
+#   fixed:  2^-22 sum_b max_{j in b} |x_j| sum_{j in b} |w_j| + f32 rounding
+#   float:  1e-5 sum |w||x|
+
+class _FloatX:
+    def __init__(self, qdq, value):
+        self.qdq, self.value = qdq, value
+
+    def __enter__(self):
+        self.old = self.qdq.set_option(self.qdq.QDQ_OPT_XS_FLOAT_X, self.value)
+
+    def __exit__(self, *exc):
+        self.qdq.set_option(self.qdq.QDQ_OPT_XS_FLOAT_X, self.old)
+
+
+def _gemv1(qdq, fmt, wb, x, n_out, n_in):
+    W = qdq.upload_q8_0(wb, n_out, n_in) if fmt == "q8_0" else qdq.upload_q4k(wb, n_out, n_in)
+    y = _nan(1, n_out)
+    (qdq.q8_0_gemv if fmt == "q8_0" else qdq.q4k_gemv)(W, _t(x), y, n_out, n_in, 1)
+    return _np(y)
+
+
+def _blocks(fmt, rng, n_out, n_in):
+    return synth.q8_0_blocks(rng, n_out, n_in) if fmt == "q8_0" else synth.q4k_blocks(rng, n_out, n_in)
+
+
+def _deq(fmt, wb, n_out, n_in):
+    return oracle.q8_0_dequant(wb, n_out, n_in) if fmt == "q8_0" else oracle.q4k_dequant(wb, n_out, n_in)
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4k"])
+@pytest.mark.parametrize("n_out,n_in", [(256, 512), (157, 3072), (40, 16384), (8192, 3072)])
+def test_batch1_float_x_parity(cuda_lib, fmt, n_out, n_in):
+    qdq = cuda_lib
+    rng = np.random.default_rng(n_out + n_in + len(fmt))
+    wb, x = _blocks(fmt, rng, n_out, n_in), synth.activations(rng, 1, n_in)
+    with _FloatX(qdq, 1):
+        y = _gemv1(qdq, fmt, wb, x, n_out, n_in)
+    y_ref, a = oracle.gemv(_deq(fmt, wb, n_out, n_in), x)
+    assert gemv_excess(y, y_ref, a) <= 1.0
+
+
+def test_batch1_float_x_ffn_parity(cuda_lib):
+    with _FloatX(cuda_lib, 1):
+        _ffn_case(cuda_lib, 768, 2048, 1, seed=77)
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4k"])
+def test_batch1_outlier_channels(cuda_lib, fmt):
+    # residual-stream-like activations: 1 % of the channels 300x larger than the rest.
+    # Weights that do not single out the outliers keep the fixed-point error far inside
+    # the 1e-5 bar, whichever arithmetic runs.
+    qdq = cuda_lib
+    n_out, n_in = 512, 3072
+    rng = np.random.default_rng(31)
+    wb, x = _blocks(fmt, rng, n_out, n_in), synth.activations(rng, 1, n_in)
+    x[:, rng.choice(n_in, n_in // 100, replace=False)] *= 300.0
+    y_ref, a = oracle.gemv(_deq(fmt, wb, n_out, n_in), x)
+    for fx in (0, 1):
+        with _FloatX(qdq, fx):
+            assert gemv_excess(_gemv1(qdq, fmt, wb, x, n_out, n_in), y_ref, a) <= 1.0
+
+
+def test_batch1_fixed_x_stated_bound(cuda_lib):
+    # Adversarial for fixed point: one activation per 32-block is 1e4 and its weights are
+    # all zero; the rest are ~1e-2.  The fixed path stays within its stated bound, the
+    # f32 path within 1e-5 sum|w||x|.
+    qdq = cuda_lib
+    n_out, n_in = 96, 1024
+    rng = np.random.default_rng(41)
+    wb = synth.q8_0_blocks(rng, n_out, n_in)
+    j0 = rng.integers(0, 32, n_in // 32)
+    blk = wb.reshape(n_out, n_in // 32, 34)
+    blk[:, np.arange(n_in // 32), 2 + j0] = 0
+    x = 1e-2 * synth.activations(rng, 1, n_in)
+    x[0, 32 * np.arange(n_in // 32) + j0] = 1e4
+    w = oracle.q8_0_dequant(wb, n_out, n_in)
+    y_ref, a = oracle.gemv(w, x)
+    m_b = np.abs(x[0]).reshape(-1, 32).max(axis=1)                       # max |x| per block
+    w_b = np.abs(w.astype(np.float64)).reshape(n_out, -1, 32).sum(axis=2)  # sum |w| per row and block
+    fixed_bound = 2.0 ** -22 * (w_b * m_b).sum(axis=1) + 1e-5 * a[0]
+    with _FloatX(qdq, 0):
+        y = _gemv1(qdq, "q8_0", wb, x, n_out, n_in)
+    assert np.all(np.abs(y[0].astype(np.float64) - y_ref[0]) <= fixed_bound)
+    with _FloatX(qdq, 1):
+        assert gemv_excess(_gemv1(qdq, "q8_0", wb, x, n_out, n_in), y_ref, a) <= 1.0
+
+
+@pytest.mark.parametrize("fx", [0, 1])
+def test_batch1_chain_reads_the_previous_output(cuda_lib, fx):
+    # up then down back to back on one stream (the down kernel starts early under
+    # programmatic dependent launch), the intermediate freshly filled with NaN each
+    # time: the down kernel must read h only after the up kernel wrote it
+    qdq = cuda_lib
+    n_embd, n_ff = 3072, 8192
+    up, dn = synth.config1_up(0), synth.config1_down(0)
+    Wu, Wd = qdq.upload_q8_0(up, n_ff, n_embd), qdq.upload_q8_0(dn, n_embd, n_ff)
+    x = synth.config1_x()
+    wd = oracle.q8_0_dequant(dn, n_embd, n_ff)
+    with _FloatX(qdq, fx):
+        for _ in range(4):
+            h, y = _nan(1, n_ff), _nan(1, n_embd)
+            qdq.q8_0_gemv(Wu, _t(x), h, n_ff, n_embd, 1)
+            qdq.q8_0_gemv(Wd, h, y, n_embd, n_ff, 1)
+            hh = _np(h)
+            assert np.all(np.isfinite(hh))
+            y_ref, a = oracle.gemv(wd, hh)
+            assert gemv_excess(_np(y), y_ref, a) <= 1.0
+
+
+@pytest.mark.parametrize("fx", [0, 1])
+def test_batch1_one_hot_x_extracts_column(cuda_lib, fx):
+    # x = e_k: y is column k of W exactly (d q is exact in f32; X_k = 2^21 exactly)
+    qdq = cuda_lib
+    n_out, n_in = 200, 2048
+    wb = synth.q8_0_blocks(np.random.default_rng(51), n_out, n_in)
+    w = oracle.q8_0_dequant(wb, n_out, n_in)
+    for k in (0, 31, 1000, 2047):
+        x = np.zeros((1, n_in), np.float32)
+        x[0, k] = 1.0
+        with _FloatX(qdq, fx):
+            y = _gemv1(qdq, "q8_0", wb, x, n_out, n_in)
+        assert np.array_equal(y[0], w[:, k])
+
+
+@pytest.mark.parametrize("fx", [0, 1])
+@pytest.mark.parametrize("fmt", ["q8_0", "q4k"])
+def test_batch1_nan_activation_gives_nan_rows(cuda_lib, fmt, fx):
+    qdq = cuda_lib
+    n_out, n_in = 64, 512
+    rng = np.random.default_rng(61)
+    wb, x = _blocks(fmt, rng, n_out, n_in), synth.activations(rng, 1, n_in)
+    x[0, 300] = np.nan
+    with _FloatX(qdq, fx):
+        y = _gemv1(qdq, fmt, wb, x, n_out, n_in)
+    assert np.all(np.isnan(y))
+
+
 # ------------------------------------------------------------------ launch options, errors
 
 def test_launch_options_do_not_change_results(cuda_lib):
