@@ -387,7 +387,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                    "timing": "CUDA graph of one step (56 launches, programmatic dependent launch), "
                              "replayed; CUDA events on the replay stream",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "kernel": "gemv_xs_kernel<0, 0> (Q8_0 batch-1 GEMV)", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": "gemv_xs_kernel<0, 0, 0> (Q8_0 batch-1 GEMV, fixed-point activations)", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "traffic": args.traffic if args.traffic is not None else recorded_traffic("q8_0_gemv"),
                      "peak_source": peaks["source"],

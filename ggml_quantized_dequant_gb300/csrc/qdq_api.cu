@@ -147,7 +147,7 @@ int qdq_set_option(int key, int value) {
       if (value != 0 && value != 1) return QDQ_ERR_DIMS;
       return g_opt_pdl.exchange(value);
     case QDQ_OPT_L2_PREFETCH:
-      if (value != 0 && value != 1) return QDQ_ERR_DIMS;
+      if (value < 0 || value > 3) return QDQ_ERR_DIMS;
       return g_opt_l2_prefetch.exchange(value);
     case QDQ_OPT_CTAS_PER_SM:
       if (value < 0 || value > 4) return QDQ_ERR_DIMS;

@@ -269,7 +269,7 @@ int launch_nb(const uint8_t *W, const uint8_t *W2, const float *x, const float *
     if (e != cudaSuccess) return fail_cuda(e);
   }
   const cudaError_t e = launch(kern, dim3(grid), dim3(kThreads), smem, s, W, W2, x, residual, y, n_out,
-                               n_in, opt_l2_prefetch(), make_magic());
+                               n_in, opt_l2_prefetch() == 1, make_magic());
   return e == cudaSuccess ? QDQ_OK : fail_cuda(e);
 }
 

@@ -209,7 +209,7 @@ int launch_nb(const uint8_t *W, const float *x, float *y, int n_out, int n_in, c
     if (e != cudaSuccess) return fail_cuda(e);
   }
   const cudaError_t e = launch(kern, dim3(grid), dim3(kThreads), smem, s, W, x, y, n_out, n_in,
-                               opt_l2_prefetch(), make_magic());
+                               opt_l2_prefetch() == 1, make_magic());
   return e == cudaSuccess ? QDQ_OK : fail_cuda(e);
 }
 

@@ -87,12 +87,6 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
   asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
-// max that returns NaN when either input is NaN
-__device__ __forceinline__ float max_nan(float a, float b) {
-  float d;
-  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
-  return d;
-}
 
 // One lane's 32 activations in block fixed point (see Arithmetic above):
 // X_j = rint(x_j 2^e), e = 148 - (biased exponent of max_j |x_j|), so
@@ -109,10 +103,17 @@ struct FixedX {
 
 template <int FMT>
 __device__ __forceinline__ void to_fixed(const float (&xv)[32], FixedX &f) {
-  float m = 0.f;
+  // max |x| as the largest bit pattern with the sign cleared (inf and NaN patterns
+  // are the largest of all), reduced as a tree
+  uint32_t mb[16];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) m = max_nan(m, fabsf(xv[j]));
-  const int E = __float_as_int(m) >> 23;
+  for (int j = 0; j < 16; ++j)
+    mb[j] = max(__float_as_uint(xv[2 * j]) & 0x7fffffffu, __float_as_uint(xv[2 * j + 1]) & 0x7fffffffu);
+#pragma unroll
+  for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+    for (int j = 0; j < w; ++j) mb[j] = max(mb[j], mb[j + w]);
+  const int E = int(mb[0] >> 23);
   if (E >= 255) {
 #pragma unroll
     for (int l = 0; l < 3; ++l)
@@ -128,13 +129,9 @@ __device__ __forceinline__ void to_fixed(const float (&xv)[32], FixedX &f) {
   const float s2 = __int_as_float((e - (e >> 1) + 127) << 23);
   f.inv_s = e <= 126 ? __int_as_float((127 - e) << 23) : __int_as_float(1 << (149 - e));
   int X[32];
-  int sum = 0;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    // |x 2^e| < 2^22: adding 1.5 * 2^23 rounds it to an integer in the low mantissa bits
+  for (int j = 0; j < 32; ++j)  // |x 2^e| < 2^22: adding 1.5 * 2^23 rounds it to an integer in the low mantissa bits
     X[j] = __float_as_int(__fmaf_rn(__fmul_rn(xv[j], s1), s2, 12582912.0f)) - 0x4B400000;
-    sum += X[j];
-  }
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
     int i[4];
@@ -148,7 +145,18 @@ __device__ __forceinline__ void to_fixed(const float (&xv)[32], FixedX &f) {
     const uint32_t u1 = __byte_perm(X[i[2]], X[i[3]], 0x0062);
     f.p[2][w] = __byte_perm(u0, u1, 0x5410);
   }
-  f.xsum = __int2float_rn(sum);
+  if constexpr (FMT == kQ4) {
+    int t[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) t[j] = X[2 * j] + X[2 * j + 1];
+#pragma unroll
+    for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+      for (int j = 0; j < w; ++j) t[j] += t[j + w];
+    f.xsum = __int2float_rn(t[0]);
+  } else {
+    f.xsum = 0.f;
+  }
 }
 
 // Reduce v[0..3] (one partial per row per lane) over the warp; afterwards lane
@@ -234,7 +242,7 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
     // after that group released it, so no wait can ever see a phase that is two
     // fills old.
     if (lane == 0) {
-      if (a.l2_prefetch) {
+      if (a.l2_prefetch == 1) {
         prefetch_range_l2(a.W, q_bytes, r0 * q_row, r1 * q_row);
         prefetch_range_l2(a.W + q_bytes, int64_t(a.n_out) * s_row, r0 * s_row, r1 * s_row);
         if (EPI == kSwiglu) {
@@ -246,6 +254,20 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
       for (int g = 0; g < G; ++g) rounds = max(rounds, gstages(g));
       int stop_i = rounds, stop_g = 0;  // first stage not issued, if the loop stopped early
       for (int i = 0; i < rounds && stop_i == rounds; ++i) {
+        if (i == SG && a.l2_prefetch == 2) {
+          // after the first fill of every slot: pull the rows that did not fit the ring
+          // into L2, so that their refills do not wait on HBM
+          for (int g = 0; g < G; ++g) {
+            const int lo = min(gbeg(g) + SG * kRowsPerStage, gbeg(g + 1)), hi = gbeg(g + 1);
+            if (lo >= hi) continue;
+            prefetch_range_l2(a.W, q_bytes, lo * q_row, hi * q_row);
+            prefetch_range_l2(a.W + q_bytes, int64_t(a.n_out) * s_row, lo * s_row, hi * s_row);
+            if (EPI == kSwiglu) {
+              prefetch_range_l2(a.W2, q_bytes, lo * q_row, hi * q_row);
+              prefetch_range_l2(a.W2 + q_bytes, int64_t(a.n_out) * s_row, lo * s_row, hi * s_row);
+            }
+          }
+        }
         for (int g = 0; g < G; ++g) {
           if (i >= gstages(g)) continue;
           const int s = g * SG + i % SG;
@@ -544,22 +566,25 @@ int launch_xs_ar(const uint8_t *W, const uint8_t *W2, const float *x, const floa
   a.n_in = n_in;
   a.wpr = ((n_in >> 5) + 31) / 32;
   auto kern = gemv_xs_kernel<FMT, EPI, AR>;
-  // About 6 (Q8_0) or 9 (Q4_K, twice the weights per byte) consumer warps:
-  // measured best on 3072 <-> 8192 decode chains.  More warps add contention
-  // without adding throughput.  The groups must also fit in half an SM's
+  // About 6 consumer warps (9 for the f32 Q4_K arithmetic and the SwiGLU, which
+  // carry twice the weights per byte, or two matrices): measured best on
+  // 3072 <-> 8192 decode chains.  More warps add contention without adding throughput.  The groups must also fit in half an SM's
   // registers together with the producer warp, so that the next kernel's CTA
   // fits beside this one and its weights stream in while this one computes.
   int regs = 0;
   const cudaError_t er = kernel_regs(reinterpret_cast<const void *>(kern), &regs);
   if (er != cudaSuccess) return fail_cuda(er);
   const int warps_half_sm = di.regs_per_sm / 2 / (((regs + 7) / 8) * 8 * 32);
-  a.groups = (FMT == kQ8 ? 6 : 9) / a.wpr;
+  a.groups = (FMT == kQ8 || (AR == kFixedX && EPI != kSwiglu) ? 6 : 9) / a.wpr;
   if (a.groups > (warps_half_sm - 1) / a.wpr) a.groups = (warps_half_sm - 1) / a.wpr;
   if (a.groups > (kMaxThreads / 32 - 1) / a.wpr) a.groups = (kMaxThreads / 32 - 1) / a.wpr;
   if (a.groups < 1) a.groups = 1;
   if (opt_xs_groups() > 0) a.groups = opt_xs_groups();
   if (32 * (a.wpr * a.groups + 1) > kMaxThreads) return QDQ_ERR_UNSUPPORTED;
-  a.l2_prefetch = opt_l2_prefetch();
+  // L2 prefetch of the rows the first ring fill leaves out: measured faster for the
+  // Q8_0 GEMV chains (the 8192-wide down projection most), slower for the FFN
+  const int pf = opt_l2_prefetch();
+  a.l2_prefetch = pf == 0 ? (FMT == kQ8 ? 2 : 0) : pf == 3 ? 0 : pf;
   const int64_t q_row = FMT == kQ8 ? n_in : n_in / 2;
   const int64_t s_row = FMT == kQ8 ? n_in / 16 : (n_in / 256) * 16;
   a.stage_bytes = int((kStageRows * (q_row + s_row) + 127) / 128 * 128);

@@ -184,7 +184,9 @@ int qdq_pipeline_timeouts(void);
 
 /* ---- launch options (same work, different launch shape; for measurement) -- */
 #define QDQ_OPT_PDL          1  /* 1 (default): programmatic dependent launch on; 0: plain launches */
-#define QDQ_OPT_L2_PREFETCH  2  /* 1: each GEMV CTA bulk-prefetches its weight rows into L2 first; 0 (default): no prefetch */
+#define QDQ_OPT_L2_PREFETCH  2  /* L2 prefetch of weight rows.  0 (default): automatic -- the batch-1 Q8_0 GEMV prefetches the rows its first ring fill
+                                   leaves out, nothing else prefetches; 1: every GEMV CTA prefetches all its rows first; 2: every batch-1 CTA
+                                   prefetches the rows its first ring fill leaves out; 3: no prefetch */
 #define QDQ_OPT_CTAS_PER_SM  3  /* GEMV-family CTAs per SM, 1..4; 0 (default): automatic (2 for the FFN kernels, else 1) */
 #define QDQ_OPT_XS_GROUPS    4  /* batch-1 GEMV consumer groups per CTA, 0 = automatic (default), 1..16 */
 #define QDQ_OPT_XS_STAGES    5  /* batch-1 GEMV weight-ring slots per consumer group (4-row stages), 0 = automatic (default), 1..16 */

@@ -447,7 +447,7 @@ def test_launch_options_do_not_change_results(cuda_lib):
     x = synth.activations(rng, 1, 2048)
     W = qdq.upload_q4k(wb, 700, 2048)
     outs = []
-    for pdl, pf in [(1, 1), (0, 0), (1, 0), (0, 1)]:
+    for pdl, pf in [(1, 1), (0, 0), (1, 0), (0, 1), (1, 2), (0, 2), (1, 3)]:
         old_pdl = qdq.set_option(qdq.QDQ_OPT_PDL, pdl)
         old_pf = qdq.set_option(qdq.QDQ_OPT_L2_PREFETCH, pf)
         y = _nan(1, 700)
