@@ -461,6 +461,25 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
                                           "bytes_per_block": b, "launches_per_block": 2}
     del L
 
+    # fused Q4_K QKV projection (GQA 3072 -> 3072 + 1024 + 1024), 28 layers cycled
+    qkv = gen_parallel([lambda t=t: synth.qkv_layer(t) for t in range(N_LAYERS)])
+    LQ = [(qdq.upload_q4k(wq, synth.N_Q, N_EMBD, device=dev), qdq.upload_q4k(wk, synth.N_KV, N_EMBD, device=dev),
+           qdq.upload_q4k(wv, synth.N_KV, N_EMBD, device=dev)) for wq, wk, wv in qkv]
+    del qkv
+    xq = torch.from_numpy(synth.activations(synth.rng_for(5, 3), 1, N_EMBD)).to(dev)
+    oq, ok, ov = (torch.empty((1, n), device=dev) for n in (synth.N_Q, synth.N_KV, synth.N_KV))
+    gq = capture(torch, lambda: [qdq.q4k_qkv(Wq, Wk, Wv, xq, oq, ok, ov, synth.N_Q, synth.N_KV, N_EMBD, 1)
+                                 for Wq, Wk, Wv in LQ])
+    for _ in range(5):
+        gq.replay()
+    dt = timer(gq.replay, iters)
+    us = dt / (iters * N_LAYERS) * 1e6
+    rows_q = synth.N_Q + 2 * synth.N_KV
+    b = rows_q * (N_EMBD // 256) * 144 + N_EMBD * 4 + rows_q * 4
+    rows["q4k_qkv_3072_q3072_kv1024"] = {"us_per_call": us, "gbs": b / us / 1e3, "frac_hbm": b / us / 1e3 / hbm,
+                                         "bytes_per_call": b}
+    del LQ
+
     # config 4: tensor-core batch GEMM, 8 copies of each shape cycled
     ncopy = 8
     for kind, (n_out, n_in) in ((0, (N_FF, N_EMBD)), (1, (N_EMBD, N_FF))):

@@ -49,6 +49,8 @@ SIGNATURES = {
     "qdq_q8_0_gemv": (_c_int, [_c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_vp]),
     "qdq_q4k_gemv": (_c_int, [_c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_vp]),
     "qdq_q4k_swiglu": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_vp]),
+    "qdq_q4k_qkv": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_int,
+                             _c_vp]),
     "qdq_q4k_ffn_residual": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
                                       _c_int, _c_int, _c_int, _c_vp]),
     "qdq_q4k_ffn_residual_noalloc": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
@@ -157,6 +159,11 @@ def q4k_gemv(W, x, y, n_out: int, n_in: int, batch: int = 1, stream=None):
 def q4k_swiglu(Wg, Wu, x, mid, n_ff: int, n_embd: int, batch: int = 1, stream=None):
     _check("qdq_q4k_swiglu", lib().qdq_q4k_swiglu(_ptr(Wg), _ptr(Wu), _ptr(x), _ptr(mid), n_ff, n_embd, batch,
                                                   _stream(stream)))
+
+
+def q4k_qkv(Wq, Wk, Wv, x, q, k, v, n_q: int, n_kv: int, n_embd: int, batch: int = 1, stream=None):
+    _check("qdq_q4k_qkv", lib().qdq_q4k_qkv(_ptr(Wq), _ptr(Wk), _ptr(Wv), _ptr(x), _ptr(q), _ptr(k), _ptr(v),
+                                            n_q, n_kv, n_embd, batch, _stream(stream)))
 
 
 def q4k_ffn_residual(Wg, Wu, Wd, x, residual, out, mid_workspace, n_embd: int, n_ff: int, batch: int = 1,

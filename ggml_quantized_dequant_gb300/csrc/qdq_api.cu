@@ -254,6 +254,36 @@ int qdq_q4k_ffn_residual(const void *Wg, const void *Wu, const void *Wd, const f
   return launch_q4k_gemv(2, Wd, nullptr, mid, residual, out, n_embd, n_ff, batch, stream);
 }
 
+int qdq_q4k_qkv(const void *Wq, const void *Wk, const void *Wv, const float *x, float *q, float *k, float *v,
+                int n_q, int n_kv, int n_embd, int batch, cudaStream_t stream) {
+  if (!Wq || !Wk || !Wv || !x || !q || !k || !v) return QDQ_ERR_NULL;
+  if (!dims_q4k(n_q, n_embd) || !dims_q4k(n_kv, n_embd) || n_kv > n_q) return QDQ_ERR_DIMS;
+  if (batch < 1 || batch > QDQ_MAX_GEMV_BATCH) return QDQ_ERR_DIMS;
+  if (n_embd > QDQ_MAX_GEMV_N_IN) return QDQ_ERR_UNSUPPORTED;
+  if (int64_t(n_q) + 2 * int64_t(n_kv) > int64_t(1 << 30)) return QDQ_ERR_UNSUPPORTED;  // one row range
+  if (!aligned(Wq, 16) || !aligned(Wk, 16) || !aligned(Wv, 16) || !aligned(x, 16) || !aligned(q, 4) ||
+      !aligned(k, 4) || !aligned(v, 4))
+    return QDQ_ERR_ALIGN;
+  const size_t wqb = q4k_bytes(n_q, n_embd), wkb = q4k_bytes(n_kv, n_embd), xb = size_t(batch) * n_embd * 4;
+  const size_t qb = size_t(batch) * n_q * 4, kb = size_t(batch) * n_kv * 4;
+  const void *ins[4] = {Wq, Wk, Wv, x};
+  const size_t inb[4] = {wqb, wkb, wkb, xb};
+  const void *outs[3] = {q, k, v};
+  const size_t outb[3] = {qb, kb, kb};
+  for (int o = 0; o < 3; ++o) {
+    for (int i = 0; i < 4; ++i)
+      if (overlaps(outs[o], outb[o], ins[i], inb[i])) return QDQ_ERR_ALIAS;
+    for (int p = o + 1; p < 3; ++p)
+      if (overlaps(outs[o], outb[o], outs[p], outb[p])) return QDQ_ERR_ALIAS;
+  }
+  if (gemv_xs_supported(n_embd, batch, 1)) return launch_gemv_xs_qkv(Wq, Wk, Wv, x, q, k, v, n_q, n_kv, n_embd, stream);
+  // batch 2..8 (or rows wider than the batch-1 pipeline takes): three GEMV launches
+  int rc = launch_q4k_gemv(0, Wq, nullptr, x, nullptr, q, n_q, n_embd, batch, stream);
+  if (rc == QDQ_OK) rc = launch_q4k_gemv(0, Wk, nullptr, x, nullptr, k, n_kv, n_embd, batch, stream);
+  if (rc == QDQ_OK) rc = launch_q4k_gemv(0, Wv, nullptr, x, nullptr, v, n_kv, n_embd, batch, stream);
+  return rc;
+}
+
 size_t qdq_q8_0_gemm_batch_workspace_bytes(int M, int n_in) {
   if (M < 1 || n_in < 1) return 0;
   return size_t(M) * size_t(n_in) * 2;

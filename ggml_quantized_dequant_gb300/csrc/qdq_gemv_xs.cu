@@ -27,6 +27,10 @@
 //    row are added in fixed order at the end, so results are deterministic.
 // SwiGLU streams gate and up rows as pairs (a stage = 2 output rows, each
 // with its gate row and its up row) and combines them in the epilogue.
+// The fused QKV projection ("Module cuda_lane", try_q4k_soa_qkv) runs the rows
+// of W_q, then W_k, then W_v as one row range against the one x; a stage that
+// crosses from one matrix into the next is copied in pieces, and the epilogue
+// writes each row to q, k or v.
 //
 // Arithmetic.  Turning int8 / u4 weights into floats costs more issue slots
 // on this GPU than streaming them from HBM, so by default the weights stay
@@ -62,7 +66,7 @@ constexpr int kStageRows = 4;    // virtual rows per stage = butterfly width
 constexpr int kMaxThreads = 544;  // up to 16 consumer warps + the producer
 
 enum Fmt { kQ8 = 0, kQ4 = 1 };
-enum Epi { kPlain = 0, kSwiglu = 1, kResidual = 2 };
+enum Epi { kPlain = 0, kSwiglu = 1, kResidual = 2, kQkv = 3 };
 enum Arith { kFixedX = 0, kFloatX = 1 };
 
 // Four-way byte dot products: c + sum_i a.byte[i] * b.byte[i], the bytes of a
@@ -183,11 +187,14 @@ __device__ __forceinline__ void butterfly4(float v[kStageRows], int lane) {
 }
 
 struct XsArgs {
-  const uint8_t *W;   // packed matrix (gate for SwiGLU)
-  const uint8_t *W2;  // up matrix (SwiGLU only)
+  const uint8_t *W;   // packed matrix (gate for SwiGLU, W_q for QKV)
+  const uint8_t *W2;  // up matrix (SwiGLU), W_k (QKV)
+  const uint8_t *W3;  // W_v (QKV)
   const float *x;
   const float *residual;
-  float *y;
+  float *y;           // output (q for QKV)
+  float *y2, *y3;     // k, v (QKV)
+  int seg1, seg2;     // QKV: rows [0, seg1) are W_q's, [seg1, seg2) W_k's, [seg2, n_out) W_v's
   int n_out;        // output rows
   int n_in;
   int wpr;          // slice warps per row
@@ -242,7 +249,7 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
     // after that group released it, so no wait can ever see a phase that is two
     // fills old.
     if (lane == 0) {
-      if (a.l2_prefetch == 1) {
+      if (EPI != kQkv && a.l2_prefetch == 1) {
         prefetch_range_l2(a.W, q_bytes, r0 * q_row, r1 * q_row);
         prefetch_range_l2(a.W + q_bytes, int64_t(a.n_out) * s_row, r0 * s_row, r1 * s_row);
         if (EPI == kSwiglu) {
@@ -254,7 +261,7 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
       for (int g = 0; g < G; ++g) rounds = max(rounds, gstages(g));
       int stop_i = rounds, stop_g = 0;  // first stage not issued, if the loop stopped early
       for (int i = 0; i < rounds && stop_i == rounds; ++i) {
-        if (i == SG && a.l2_prefetch == 2) {
+        if (EPI != kQkv && i == SG && a.l2_prefetch == 2) {
           // after the first fill of every slot: pull the rows that did not fit the ring
           // into L2, so that their refills do not wait on HBM
           for (int g = 0; g < G; ++g) {
@@ -282,8 +289,24 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
           const int rr = gbeg(g) + i * kRowsPerStage;           // first output row of the stage
           const int nr = min(kRowsPerStage, gbeg(g + 1) - rr);  // output rows in the stage
           mbar_arrive_expect_tx(&full[s], uint32_t(kV * nr * (q_row + s_row)));
-          bulk_copy_g2s(stq, a.W + rr * q_row, uint32_t(nr * q_row), &full[s]);
-          bulk_copy_g2s(sts, a.W + q_bytes + rr * s_row, uint32_t(nr * s_row), &full[s]);
+          if constexpr (EPI == kQkv) {
+            // rows [rr, rr + nr) of W_q | W_k | W_v, one piece per matrix they touch
+            const uint8_t *Wm[3] = {a.W, a.W2, a.W3};
+            const int off[4] = {0, a.seg1, a.seg2, a.n_out};
+#pragma unroll
+            for (int m = 0; m < 3; ++m) {
+              const int lo = max(rr, off[m]), hi = min(rr + nr, off[m + 1]);
+              if (lo >= hi) continue;
+              const int64_t qb = int64_t(off[m + 1] - off[m]) * q_row;  // this matrix's quant plane
+              bulk_copy_g2s(stq + (lo - rr) * q_row, Wm[m] + (lo - off[m]) * q_row, uint32_t((hi - lo) * q_row),
+                            &full[s]);
+              bulk_copy_g2s(sts + (lo - rr) * s_row, Wm[m] + qb + (lo - off[m]) * s_row,
+                            uint32_t((hi - lo) * s_row), &full[s]);
+            }
+          } else {
+            bulk_copy_g2s(stq, a.W + rr * q_row, uint32_t(nr * q_row), &full[s]);
+            bulk_copy_g2s(sts, a.W + q_bytes + rr * s_row, uint32_t(nr * s_row), &full[s]);
+          }
           if (EPI == kSwiglu) {  // up rows go to slots 2, 3
             bulk_copy_g2s(stq + 2 * q_row, a.W2 + rr * q_row, uint32_t(nr * q_row), &full[s]);
             bulk_copy_g2s(sts + 2 * s_row, a.W2 + q_bytes + rr * s_row, uint32_t(nr * s_row), &full[s]);
@@ -530,7 +553,14 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
       float v = 0.f;
       const float *ps = psum + r * a.wpr;
       for (int s = 0; s < a.wpr; ++s) v += ps[s];
-      a.y[r0 + r] = EPI == kResidual ? a.residual[r0 + r] + v : v;
+      const int R = r0 + r;
+      if (EPI == kQkv) {
+        if (R < a.seg1) a.y[R] = v;
+        else if (R < a.seg2) a.y2[R - a.seg1] = v;
+        else a.y3[R - a.seg2] = v;
+      } else {
+        a.y[R] = EPI == kResidual ? a.residual[R] + v : v;
+      }
     }
   }
 }
@@ -553,17 +583,10 @@ cudaError_t kernel_regs(const void *func, int *regs) {
   return cudaSuccess;
 }
 
+// `a` arrives with the pointers, n_out and n_in set; this fills in the launch shape.
 template <int FMT, int EPI, int AR>
-int launch_xs_ar(const uint8_t *W, const uint8_t *W2, const float *x, const float *residual, float *y, int n_out,
-                 int n_in, cudaStream_t s, const DeviceInfo &di) {
-  XsArgs a;
-  a.W = W;
-  a.W2 = W2;
-  a.x = x;
-  a.residual = residual;
-  a.y = y;
-  a.n_out = n_out;
-  a.n_in = n_in;
+int launch_xs_ar(XsArgs a, cudaStream_t s, const DeviceInfo &di) {
+  const int n_out = a.n_out, n_in = a.n_in;
   a.wpr = ((n_in >> 5) + 31) / 32;
   auto kern = gemv_xs_kernel<FMT, EPI, AR>;
   // About 6 consumer warps (9 for the f32 Q4_K arithmetic and the SwiGLU, which
@@ -584,14 +607,14 @@ int launch_xs_ar(const uint8_t *W, const uint8_t *W2, const float *x, const floa
   // L2 prefetch of the rows the first ring fill leaves out: measured faster for the
   // Q8_0 GEMV chains (the 8192-wide down projection most), slower for the FFN
   const int pf = opt_l2_prefetch();
-  a.l2_prefetch = pf == 0 ? (FMT == kQ8 ? 2 : 0) : pf == 3 ? 0 : pf;
+  a.l2_prefetch = EPI == kQkv ? 0 : pf == 0 ? (FMT == kQ8 ? 2 : 0) : pf == 3 ? 0 : pf;
   const int64_t q_row = FMT == kQ8 ? n_in : n_in / 2;
   const int64_t s_row = FMT == kQ8 ? n_in / 16 : (n_in / 256) * 16;
   a.stage_bytes = int((kStageRows * (q_row + s_row) + 127) / 128 * 128);
   // The FFN kernels (SwiGLU, down + residual) run two CTAs per SM with two ring slots
   // per group: both CTAs compute at once instead of one computing beside the next
   // kernel's prefill, which measured ~7 % faster for the block.  The GEMVs keep one.
-  constexpr bool kFfn = EPI != kPlain;
+  constexpr bool kFfn = EPI == kSwiglu || EPI == kResidual;
   int grid = di.sm_count * ctas_per_sm_or(kFfn ? 2 : 1);
   if (grid > n_out) grid = n_out;
   const int max_rows = (n_out + grid - 1) / grid;
@@ -618,10 +641,8 @@ int launch_xs_ar(const uint8_t *W, const uint8_t *W2, const float *x, const floa
 }
 
 template <int FMT, int EPI>
-int launch_xs(const uint8_t *W, const uint8_t *W2, const float *x, const float *residual, float *y, int n_out,
-              int n_in, cudaStream_t s, const DeviceInfo &di) {
-  return opt_xs_float_x() ? launch_xs_ar<FMT, EPI, kFloatX>(W, W2, x, residual, y, n_out, n_in, s, di)
-                          : launch_xs_ar<FMT, EPI, kFixedX>(W, W2, x, residual, y, n_out, n_in, s, di);
+int launch_xs(const XsArgs &a, cudaStream_t s, const DeviceInfo &di) {
+  return opt_xs_float_x() ? launch_xs_ar<FMT, EPI, kFloatX>(a, s, di) : launch_xs_ar<FMT, EPI, kFixedX>(a, s, di);
 }
 
 }  // namespace
@@ -637,11 +658,38 @@ int launch_gemv_xs(int fmt_q4k, int mode, const void *W, const void *W2, const f
   DeviceInfo di;
   const cudaError_t e = device_info(&di);
   if (e != cudaSuccess) return fail_cuda(e);
-  const uint8_t *w = static_cast<const uint8_t *>(W), *w2 = static_cast<const uint8_t *>(W2);
-  if (!fmt_q4k) return launch_xs<kQ8, kPlain>(w, w2, x, residual, y, n_out, n_in, s, di);
-  if (mode == 1) return launch_xs<kQ4, kSwiglu>(w, w2, x, residual, y, n_out, n_in, s, di);
-  if (mode == 2) return launch_xs<kQ4, kResidual>(w, w2, x, residual, y, n_out, n_in, s, di);
-  return launch_xs<kQ4, kPlain>(w, w2, x, residual, y, n_out, n_in, s, di);
+  XsArgs a{};
+  a.W = static_cast<const uint8_t *>(W);
+  a.W2 = static_cast<const uint8_t *>(W2);
+  a.x = x;
+  a.residual = residual;
+  a.y = y;
+  a.n_out = n_out;
+  a.n_in = n_in;
+  if (!fmt_q4k) return launch_xs<kQ8, kPlain>(a, s, di);
+  if (mode == 1) return launch_xs<kQ4, kSwiglu>(a, s, di);
+  if (mode == 2) return launch_xs<kQ4, kResidual>(a, s, di);
+  return launch_xs<kQ4, kPlain>(a, s, di);
+}
+
+int launch_gemv_xs_qkv(const void *Wq, const void *Wk, const void *Wv, const float *x, float *q, float *k, float *v,
+                       int n_q, int n_kv, int n_in, cudaStream_t s) {
+  DeviceInfo di;
+  const cudaError_t e = device_info(&di);
+  if (e != cudaSuccess) return fail_cuda(e);
+  XsArgs a{};
+  a.W = static_cast<const uint8_t *>(Wq);
+  a.W2 = static_cast<const uint8_t *>(Wk);
+  a.W3 = static_cast<const uint8_t *>(Wv);
+  a.x = x;
+  a.y = q;
+  a.y2 = k;
+  a.y3 = v;
+  a.seg1 = n_q;
+  a.seg2 = n_q + n_kv;
+  a.n_out = n_q + 2 * n_kv;
+  a.n_in = n_in;
+  return launch_xs<kQ4, kQkv>(a, s, di);
 }
 
 int read_xs_timeouts() {

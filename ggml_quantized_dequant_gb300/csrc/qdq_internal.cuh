@@ -96,6 +96,9 @@ int launch_q4k_gemv(int mode, const void *W, const void *W2, const float *x, con
 // Batch-1 "x-stationary" GEMV fast path (qdq_gemv_xs.cu); fmt_q4k 0 = Q8_0,
 // 1 = Q4_K with mode 0/1/2 as launch_q4k_gemv.
 bool gemv_xs_supported(int n_in, int batch, int fmt_q4k);
+// Fused Q4_K QKV projection at batch 1 (n_in as gemv_xs_supported allows for Q4_K).
+int launch_gemv_xs_qkv(const void *Wq, const void *Wk, const void *Wv, const float *x, float *q, float *k, float *v,
+                       int n_q, int n_kv, int n_in, cudaStream_t s);
 int launch_gemv_xs(int fmt_q4k, int mode, const void *W, const void *W2, const float *x, const float *residual,
                    float *y, int n_out, int n_in, cudaStream_t s);
 // Pipeline-timeout counters of the translation units that run bounded waits:

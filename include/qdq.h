@@ -7,6 +7,7 @@
  *     q8_0_gemv_oracle_into / try_q8_0_cuda_gemv   -> qdq_q8_0_gemv
  *     try_q4k_soa_gemv                              -> qdq_q4k_gemv
  *     try_q4k_soa_fused_swiglu                      -> qdq_q4k_swiglu
+ *     try_q4k_soa_qkv                               -> qdq_q4k_qkv
  *     try_q4k_soa_ffn_block / _ffn_block_residual   -> qdq_q4k_ffn_residual
  *     preload_q4k_soa_weights (one-time upload)     -> qdq_q8_0_pack / qdq_q4k_pack
  *   "Module cuda_lane", Goal (batch prefill-shaped GEMMs on tensor cores) and
@@ -123,6 +124,20 @@ int qdq_q4k_gemv(const void *W, const float *x, float *y,
  */
 int qdq_q4k_swiglu(const void *Wg, const void *Wu, const float *x, float *mid,
                    int n_ff, int n_embd, int batch, cudaStream_t stream);
+
+/* ---- fused QKV projection ---------------------------------------------------
+ * "Module cuda_lane", Functions: try_q4k_soa_qkv (one activation, one fused
+ * kernel; GQA: K and V only for rows below n_kv):
+ *   q[b, r] = Wq_r . x_b (r < n_q),  k[b, r] = Wk_r . x_b,  v[b, r] = Wv_r . x_b (r < n_kv).
+ * Wq: packed Q4_K n_q x n_embd; Wk, Wv: packed Q4_K n_kv x n_embd, 1 <= n_kv <= n_q
+ * (16-byte aligned).  x: batch x n_embd (16-byte aligned).  q: batch x n_q; k, v:
+ * batch x n_kv (4-byte aligned); no output may overlap an input or another output.
+ * Batch 1 is one kernel over the rows of Wq, Wk, Wv; batch 2..8 is three GEMV
+ * launches.  Error bound as qdq_q4k_gemv.
+ */
+int qdq_q4k_qkv(const void *Wq, const void *Wk, const void *Wv, const float *x,
+                float *q, float *k, float *v, int n_q, int n_kv, int n_embd, int batch,
+                cudaStream_t stream);
 
 /* ---- FFN block with on-device residual --------------------------------------
  * "Module cuda_lane", Functions: try_q4k_soa_ffn_block_residual:

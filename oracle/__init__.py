@@ -13,5 +13,6 @@ from .ggml_oracle import (  # noqa: F401
     silu,
     swiglu,
     ffn_residual,
+    qkv,
     gemm_batch,
 )

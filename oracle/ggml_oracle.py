@@ -12,6 +12,9 @@ Sources (the pages are rustdoc for the ``qualia_core_db`` crate):
 * "Module cuda_lane", *Functions: try_q4k_soa_gemv / try_q4k_soa_fused_swiglu /
   try_q4k_soa_ffn_block_residual* -- Q4_K GEMV, the SwiGLU expansion
   ``out[i] = silu(gate_row_i . x) * (up_row_i . x)`` and ``out = residual + FFN(x)``.
+* "Module cuda_lane", *Functions: try_q4k_soa_qkv* -- Q, K and V projected from
+  the same activation; with grouped-query attention K and V exist only for the
+  first n_kv rows.
 * "weight_cache.rs", *try_cuda_batch_gemv* doc comment -- layouts: W is
   row-major ``n_out x n_in`` (rows = outputs, GGML convention); activations are
   packed ``batch x n_in``; outputs are ``batch x n_out``.
@@ -217,6 +220,22 @@ def ffn_residual(w_gate, w_up, w_down, x, residual):
     res = np.atleast_2d(np.asarray(residual, dtype=np.float32)).astype(np.float64)
     s.update(out=res + down, down=down, A_down=a_down)
     return s
+
+
+def qkv(w_q: np.ndarray, w_k: np.ndarray, w_v: np.ndarray, x: np.ndarray):
+    """QKV projection from one activation: ``q = W_q x``, ``k = W_k x``, ``v = W_v x``.
+
+    ``W_q`` is ``n_q x n_in``; ``W_k`` and ``W_v`` are ``n_kv x n_in`` with
+    ``n_kv <= n_q`` (grouped-query attention: K and V rows stop at n_kv).  Returns
+    a dict with ``q``, ``k``, ``v`` and their ``A_q``, ``A_k``, ``A_v``
+    (``sum |w||x|``), all float64.
+    """
+    if w_k.shape != w_v.shape or w_k.shape[1] != w_q.shape[1] or w_k.shape[0] > w_q.shape[0]:
+        raise ValueError("W_k and W_v must be n_kv x n_in with n_kv <= n_q")
+    q, a_q = gemv(w_q, x)
+    k, a_k = gemv(w_k, x)
+    v, a_v = gemv(w_v, x)
+    return dict(q=q, k=k, v=v, A_q=a_q, A_k=a_k, A_v=a_v)
 
 
 def gemm_batch(w: np.ndarray, x: np.ndarray):

@@ -147,6 +147,18 @@ def config3_x_residual():
     return activations(rng_for(3, 3), 1, N_EMBD), activations(rng_for(3, 4), 1, N_EMBD)
 
 
+#: Fused QKV workload: 3B-class grouped-query attention, 24 query heads and 8 KV heads of 128.
+N_Q = 3072
+N_KV = 1024
+
+
+def qkv_layer(t: int):
+    """QKV layer ``t``: ``(W_q, W_k, W_v)`` Q4_K bytes (3072->3072, 3072->1024, 3072->1024)."""
+    return (q4k_blocks(rng_for(5, 0, t), N_Q, N_EMBD),
+            q4k_blocks(rng_for(5, 1, t), N_KV, N_EMBD),
+            q4k_blocks(rng_for(5, 2, t), N_KV, N_EMBD))
+
+
 #: Config 4 token counts.
 C4_M = (16, 64, 512)
 

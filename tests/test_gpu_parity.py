@@ -297,6 +297,60 @@ def test_q8_0_gemm_batch_m1_matches_gemv_within_bf16_bound(cuda_lib):
     assert np.all(np.abs(_np(Y) - _np(y)) <= 4e-3 * a)
 
 
+# ------------------------------------------------------------------ fused QKV
+
+def _qkv_case(qdq, n_q, n_kv, n_embd, batch, seed):
+    rng = np.random.default_rng(seed)
+    bq, bk, bv = (synth.q4k_blocks(rng, n_q, n_embd), synth.q4k_blocks(rng, n_kv, n_embd),
+                  synth.q4k_blocks(rng, n_kv, n_embd))
+    x = synth.activations(rng, batch, n_embd)
+    Wq, Wk, Wv = qdq.upload_q4k(bq, n_q, n_embd), qdq.upload_q4k(bk, n_kv, n_embd), qdq.upload_q4k(bv, n_kv, n_embd)
+    q, k, v = _nan(batch, n_q), _nan(batch, n_kv), _nan(batch, n_kv)
+    qdq.q4k_qkv(Wq, Wk, Wv, _t(x), q, k, v, n_q, n_kv, n_embd, batch)
+    o = oracle.qkv(oracle.q4k_dequant(bq, n_q, n_embd), oracle.q4k_dequant(bk, n_kv, n_embd),
+                   oracle.q4k_dequant(bv, n_kv, n_embd), x)
+    for name, got in (("q", q), ("k", k), ("v", v)):
+        assert gemv_excess(_np(got), o[name], o["A_" + name]) <= 1.0, name
+    assert qdq.pipeline_timeouts() == 0
+
+
+# 3B-class GQA (24 heads / 8 KV heads of 128), Q->K and K->V boundaries inside a 4-row stage,
+# n_kv == n_q, a single K/V row, 16 slice warps per row, batch 3 (three GEMV launches)
+QKV_SHAPES = [(3072, 1024, 3072, 1), (256, 64, 512, 1), (101, 37, 1024, 1), (50, 50, 256, 1), (7, 1, 256, 1),
+              (64, 16, 16384, 1), (40, 8, 768, 3)]
+
+
+@pytest.mark.parametrize("n_q,n_kv,n_embd,batch", QKV_SHAPES)
+def test_q4k_qkv_parity(cuda_lib, n_q, n_kv, n_embd, batch):
+    _qkv_case(cuda_lib, n_q, n_kv, n_embd, batch, seed=n_q + 7 * n_kv + n_embd + batch)
+
+
+def test_q4k_qkv_float_x_parity(cuda_lib):
+    qdq = cuda_lib
+    old = qdq.set_option(qdq.QDQ_OPT_XS_FLOAT_X, 1)
+    try:
+        _qkv_case(qdq, 101, 37, 1024, 1, seed=5)
+    finally:
+        qdq.set_option(qdq.QDQ_OPT_XS_FLOAT_X, old)
+
+
+def test_q4k_qkv_rows_equal_the_separate_gemvs(cuda_lib):
+    # the fused kernel reduces each row exactly as the Q4_K GEMV kernel does
+    qdq = cuda_lib
+    n_q, n_kv, n_embd = 301, 77, 2048
+    rng = np.random.default_rng(8)
+    bq, bk, bv = (synth.q4k_blocks(rng, n_q, n_embd), synth.q4k_blocks(rng, n_kv, n_embd),
+                  synth.q4k_blocks(rng, n_kv, n_embd))
+    x = _t(synth.activations(rng, 1, n_embd))
+    Wq, Wk, Wv = qdq.upload_q4k(bq, n_q, n_embd), qdq.upload_q4k(bk, n_kv, n_embd), qdq.upload_q4k(bv, n_kv, n_embd)
+    q, k, v = _nan(1, n_q), _nan(1, n_kv), _nan(1, n_kv)
+    qdq.q4k_qkv(Wq, Wk, Wv, x, q, k, v, n_q, n_kv, n_embd, 1)
+    for W, got, n in ((Wq, q, n_q), (Wk, k, n_kv), (Wv, v, n_kv)):
+        y = _nan(1, n)
+        qdq.q4k_gemv(W, x, y, n, n_embd, 1)
+        assert np.allclose(_np(got), _np(y), rtol=0, atol=1e-5 * float(np.abs(_np(y)).max()))
+
+
 # ------------------------------------------------------------------ batch-1 arithmetic
 # The batch-1 kernels multiply in 24-bit block fixed point by default (the integer
 # byte dot products); QDQ_OPT_XS_FLOAT_X = 1 selects f32 arithmetic.  Their error

@@ -99,6 +99,27 @@ def test_swiglu_and_ffn_validation(lib):
     assert lib.qdq_q4k_ffn_residual(Wg, Wu, Wd, x, res, out, mid, 256, 512, 9, None) == qdq.QDQ_ERR_DIMS
 
 
+def test_qkv_validation(lib):
+    import ggml_quantized_dequant_gb300 as qdq
+    Wq, Wk, Wv = GOOD, GOOD + (1 << 28), GOOD + (2 << 28)
+    x, q, k, v = GOOD + (3 << 28), GOOD + (4 << 28), GOOD + (5 << 28), GOOD + (6 << 28)
+    f = lambda *p, n_q=512, n_kv=128, n_embd=256, batch=1: lib.qdq_q4k_qkv(  # noqa: E731
+        *p, n_q, n_kv, n_embd, batch, None)
+    assert f(Wq, Wk, None, x, q, k, v) == qdq.QDQ_ERR_NULL
+    assert f(Wq, Wk, Wv, x, q, k, None) == qdq.QDQ_ERR_NULL
+    assert f(Wq, Wk, Wv, x, q, k, v, n_embd=255) == qdq.QDQ_ERR_DIMS
+    assert f(Wq, Wk, Wv, x, q, k, v, n_kv=0) == qdq.QDQ_ERR_DIMS
+    assert f(Wq, Wk, Wv, x, q, k, v, n_kv=513) == qdq.QDQ_ERR_DIMS         # K/V wider than Q
+    assert f(Wq, Wk, Wv, x, q, k, v, batch=9) == qdq.QDQ_ERR_DIMS
+    assert f(Wq, Wk + 8, Wv, x, q, k, v) == qdq.QDQ_ERR_ALIGN
+    assert f(Wq, Wk, Wv, x + 4, q, k, v) == qdq.QDQ_ERR_ALIGN
+    assert f(Wq, Wk, Wv, x, q, k, v + 2) == qdq.QDQ_ERR_ALIGN
+    assert f(Wq, Wk, Wv, x, q, q + 4 * 100, v) == qdq.QDQ_ERR_ALIAS        # k inside q
+    assert f(Wq, Wk, Wv, x, q, k, Wv + 64) == qdq.QDQ_ERR_ALIAS            # v inside W_v
+    assert f(Wq, Wk, Wv, x, x, k, v) == qdq.QDQ_ERR_ALIAS                  # q over x
+    assert f(Wq, Wk, Wv, x, q, k, v, n_embd=1 << 20) == qdq.QDQ_ERR_UNSUPPORTED
+
+
 def test_gemm_validation(lib):
     import ggml_quantized_dequant_gb300 as qdq
     W, X, Y, ws = GOOD, GOOD + (1 << 28), GOOD + (2 << 28), GOOD + (3 << 28)

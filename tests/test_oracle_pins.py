@@ -354,6 +354,43 @@ def test_ffn_identity_down_gives_residual_plus_mid():
     assert np.array_equal(o["out"], res.astype(np.float64) + o["mid"])
 
 
+# ---------------------------------------------------------------- fused QKV
+
+def test_qkv_one_hot_extracts_each_matrix_column():
+    # distinct matrices and a non-square Q: one-hot x gives column j of each, in its own output
+    n_q, n_kv, n_in = 12, 4, 512
+    wq, wk, wv = _small_q4k(n_q, n_in, 61), _small_q4k(n_kv, n_in, 62), _small_q4k(n_kv, n_in, 63)
+    for j in (0, 255, 256, 511):
+        x = np.zeros((1, n_in), np.float32)
+        x[0, j] = 1.0
+        o = oracle.qkv(wq, wk, wv, x)
+        assert o["q"].shape == (1, n_q) and o["k"].shape == (1, n_kv) and o["v"].shape == (1, n_kv)
+        assert np.array_equal(o["q"][0], wq[:, j].astype(np.float64))
+        assert np.array_equal(o["k"][0], wk[:, j].astype(np.float64))
+        assert np.array_equal(o["v"][0], wv[:, j].astype(np.float64))
+
+
+def test_qkv_closed_form_constant_matrices():
+    # W_q = 1, W_k = 2, W_v = -3 everywhere (d = 1, q = 1, 2, -3) and x = 1: q = n_in, k = 2 n_in, v = -3 n_in
+    n_q, n_kv, n_in = 8, 2, 64
+    def const_q8(rows, val):
+        blk = np.zeros((rows, n_in // 32, 34), np.uint8)
+        blk[..., 0:2] = np.frombuffer(np.float16(1.0).tobytes(), np.uint8)
+        blk[..., 2:] = np.uint8(val & 0xFF)
+        return oracle.q8_0_dequant(blk.reshape(rows, -1), rows, n_in)
+    o = oracle.qkv(const_q8(n_q, 1), const_q8(n_kv, 2), const_q8(n_kv, -3), np.ones((1, n_in), np.float32))
+    assert np.all(o["q"] == n_in) and np.all(o["k"] == 2 * n_in) and np.all(o["v"] == -3 * n_in)
+    assert np.all(o["A_v"] == 3 * n_in)
+
+
+def test_qkv_rejects_kv_wider_than_q():
+    w = _small_q8(4, 64, 1)
+    with pytest.raises(ValueError):
+        oracle.qkv(w[:2], w, w, np.ones((1, 64), np.float32))
+    with pytest.raises(ValueError):
+        oracle.qkv(w, w[:2], w[:3], np.ones((1, 64), np.float32))
+
+
 # ---------------------------------------------------------------- batch GEMM
 
 def test_gemm_batch_m1_equals_gemv_and_permutes_rows():
