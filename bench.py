@@ -480,6 +480,25 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
                                          "bytes_per_call": b}
     del LQ
 
+    # output projection 3072 -> 128256 (Q8_0, 418 MB: larger than L2) with the on-device argmax
+    wb, xo = synth.output_projection()
+    WO = qdq.upload_q8_0(wb, synth.N_VOCAB, N_EMBD, device=dev)
+    del wb
+    xo = torch.from_numpy(xo).to(dev)
+    lo = torch.empty((1, synth.N_VOCAB), device=dev)
+    io = torch.empty((1,), dtype=torch.int32, device=dev)
+    vo = torch.empty((1,), device=dev)
+    go = capture(torch, lambda: [qdq.q8_0_logits_argmax(WO, xo, lo, io, vo, synth.N_VOCAB, N_EMBD, 1)
+                                 for _ in range(4)])
+    for _ in range(3):
+        go.replay()
+    dt = timer(go.replay, max(5, iters // 4))
+    us = dt / (max(5, iters // 4) * 4) * 1e6
+    b = synth.N_VOCAB * (N_EMBD // 32) * 34 + N_EMBD * 4 + synth.N_VOCAB * 4 + 8
+    rows["q8_0_logits_argmax_3072x128256"] = {"us_per_call": us, "gbs": b / us / 1e3, "frac_hbm": b / us / 1e3 / hbm,
+                                              "bytes_per_call": b, "launches_per_call": 2}
+    del WO
+
     # config 4: tensor-core batch GEMM, 8 copies of each shape cycled
     ncopy = 8
     for kind, (n_out, n_in) in ((0, (N_FF, N_EMBD)), (1, (N_EMBD, N_FF))):

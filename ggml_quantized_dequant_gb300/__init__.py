@@ -49,6 +49,7 @@ SIGNATURES = {
     "qdq_q8_0_gemv": (_c_int, [_c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_vp]),
     "qdq_q4k_gemv": (_c_int, [_c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_vp]),
     "qdq_q4k_swiglu": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_vp]),
+    "qdq_q8_0_logits_argmax": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_vp]),
     "qdq_q4k_qkv": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_int,
                              _c_vp]),
     "qdq_q4k_ffn_residual": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
@@ -159,6 +160,13 @@ def q4k_gemv(W, x, y, n_out: int, n_in: int, batch: int = 1, stream=None):
 def q4k_swiglu(Wg, Wu, x, mid, n_ff: int, n_embd: int, batch: int = 1, stream=None):
     _check("qdq_q4k_swiglu", lib().qdq_q4k_swiglu(_ptr(Wg), _ptr(Wu), _ptr(x), _ptr(mid), n_ff, n_embd, batch,
                                                   _stream(stream)))
+
+
+def q8_0_logits_argmax(W, x, logits, index, value, n_vocab: int, n_in: int, batch: int = 1, stream=None):
+    """Output projection plus on-device argmax: ``index`` (int32) and ``value`` (f32) per batch row."""
+    _check("qdq_q8_0_logits_argmax",
+           lib().qdq_q8_0_logits_argmax(_ptr(W), _ptr(x), _ptr(logits), _ptr(index), _ptr(value), n_vocab, n_in,
+                                        batch, _stream(stream)))
 
 
 def q4k_qkv(Wq, Wk, Wv, x, q, k, v, n_q: int, n_kv: int, n_embd: int, batch: int = 1, stream=None):

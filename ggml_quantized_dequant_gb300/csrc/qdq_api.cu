@@ -9,6 +9,9 @@
 
 namespace qdq {
 
+// Argmax over each of `batch` rows of n floats (csrc/qdq_argmax.cu).
+int launch_argmax_rows(const float *logits, int n, int batch, int *index, float *value, cudaStream_t s);
+
 namespace {
 thread_local int g_last_cuda_error = 0;
 std::atomic<int> g_opt_pdl{1};
@@ -252,6 +255,24 @@ int qdq_q4k_ffn_residual(const void *Wg, const void *Wu, const void *Wd, const f
   int rc = launch_q4k_gemv(1, Wg, Wu, x, nullptr, mid, n_ff, n_embd, batch, stream);
   if (rc != QDQ_OK) return rc;
   return launch_q4k_gemv(2, Wd, nullptr, mid, residual, out, n_embd, n_ff, batch, stream);
+}
+
+int qdq_q8_0_logits_argmax(const void *W, const float *x, float *logits, int *index, float *value, int n_vocab,
+                           int n_in, int batch, cudaStream_t stream) {
+  if (!W || !x || !logits || !index || !value) return QDQ_ERR_NULL;
+  if (!dims_q8(n_vocab, n_in)) return QDQ_ERR_DIMS;
+  const int rc = check_gemv_common(W, x, logits, n_vocab, n_in, batch, q8_bytes(n_vocab, n_in));
+  if (rc != QDQ_OK) return rc;
+  if (!aligned(index, 4) || !aligned(value, 4)) return QDQ_ERR_ALIGN;
+  const size_t lb = size_t(batch) * n_vocab * 4, rb = size_t(batch) * 4;
+  const void *others[3] = {W, x, logits};
+  const size_t ob[3] = {q8_bytes(n_vocab, n_in), size_t(batch) * n_in * 4, lb};
+  for (int i = 0; i < 3; ++i)
+    if (overlaps(index, rb, others[i], ob[i]) || overlaps(value, rb, others[i], ob[i])) return QDQ_ERR_ALIAS;
+  if (overlaps(index, rb, value, rb)) return QDQ_ERR_ALIAS;
+  const int r = launch_q8_0_gemv(W, x, logits, n_vocab, n_in, batch, stream);
+  if (r != QDQ_OK) return r;
+  return launch_argmax_rows(logits, n_vocab, batch, index, value, stream);
 }
 
 int qdq_q4k_qkv(const void *Wq, const void *Wk, const void *Wv, const float *x, float *q, float *k, float *v,

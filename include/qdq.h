@@ -8,6 +8,7 @@
  *     try_q4k_soa_gemv                              -> qdq_q4k_gemv
  *     try_q4k_soa_fused_swiglu                      -> qdq_q4k_swiglu
  *     try_q4k_soa_qkv                               -> qdq_q4k_qkv
+ *     output projection + argmax epilogue            -> qdq_q8_0_logits_argmax
  *     try_q4k_soa_ffn_block / _ffn_block_residual   -> qdq_q4k_ffn_residual
  *     preload_q4k_soa_weights (one-time upload)     -> qdq_q8_0_pack / qdq_q4k_pack
  *   "Module cuda_lane", Goal (batch prefill-shaped GEMMs on tensor cores) and
@@ -124,6 +125,21 @@ int qdq_q4k_gemv(const void *W, const float *x, float *y,
  */
 int qdq_q4k_swiglu(const void *Wg, const void *Wu, const float *x, float *mid,
                    int n_ff, int n_embd, int batch, cudaStream_t stream);
+
+/* ---- output projection with on-device argmax --------------------------------
+ * "Module cuda_lane": the output projection with an on-device top-k/argmax
+ * epilogue, so a decode step reads back one token instead of the logits.
+ *   logits[b, t] = W_t . x_b (a Q8_0 GEMV, as qdq_q8_0_gemv), then
+ *   index[b] = the first t with the largest logits[b, t], value[b] = that logit
+ *   (a NaN logit counts as the largest: the first NaN wins).
+ * W: packed Q8_0 n_vocab x n_in (16-byte aligned).  x: batch x n_in (16-byte
+ * aligned).  logits: batch x n_vocab f32 scratch the caller owns, overwritten
+ * (4-byte aligned).  index (int32), value (f32): batch entries each, 4-byte
+ * aligned.  No output may overlap an input or another output.  Two kernels on
+ * `stream`; nothing is read back.
+ */
+int qdq_q8_0_logits_argmax(const void *W, const float *x, float *logits, int *index, float *value,
+                           int n_vocab, int n_in, int batch, cudaStream_t stream);
 
 /* ---- fused QKV projection ---------------------------------------------------
  * "Module cuda_lane", Functions: try_q4k_soa_qkv (one activation, one fused

@@ -14,5 +14,6 @@ from .ggml_oracle import (  # noqa: F401
     swiglu,
     ffn_residual,
     qkv,
+    logits_argmax,
     gemm_batch,
 )

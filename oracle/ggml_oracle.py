@@ -15,6 +15,8 @@ Sources (the pages are rustdoc for the ``qualia_core_db`` crate):
 * "Module cuda_lane", *Functions: try_q4k_soa_qkv* -- Q, K and V projected from
   the same activation; with grouped-query attention K and V exist only for the
   first n_kv rows.
+* "Module cuda_lane" -- the output projection with an on-device top-k / argmax
+  epilogue (one token read back instead of the logits).
 * "weight_cache.rs", *try_cuda_batch_gemv* doc comment -- layouts: W is
   row-major ``n_out x n_in`` (rows = outputs, GGML convention); activations are
   packed ``batch x n_in``; outputs are ``batch x n_out``.
@@ -236,6 +238,24 @@ def qkv(w_q: np.ndarray, w_k: np.ndarray, w_v: np.ndarray, x: np.ndarray):
     k, a_k = gemv(w_k, x)
     v, a_v = gemv(w_v, x)
     return dict(q=q, k=k, v=v, A_q=a_q, A_k=a_k, A_v=a_v)
+
+
+def logits_argmax(w: np.ndarray, x: np.ndarray):
+    """Output projection with argmax: ``logits = W x`` and, per activation row, the first
+    index of the largest logit and that logit.
+
+    A NaN logit counts as larger than every number, so the first NaN wins (the
+    numpy.argmax convention).  Returns a dict with ``logits``, ``A`` (``sum |w||x|``),
+    ``index`` (int64) and ``value`` (float64).
+    """
+    logits, a = gemv(w, x)
+    index = np.empty(logits.shape[0], dtype=np.int64)
+    value = np.empty(logits.shape[0], dtype=np.float64)
+    for b, row in enumerate(logits):
+        nan = np.flatnonzero(np.isnan(row))
+        i = int(nan[0]) if nan.size else int(np.flatnonzero(row == row.max())[0])
+        index[b], value[b] = i, row[i]
+    return dict(logits=logits, A=a, index=index, value=value)
 
 
 def gemm_batch(w: np.ndarray, x: np.ndarray):

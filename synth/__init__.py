@@ -159,6 +159,15 @@ def qkv_layer(t: int):
             q4k_blocks(rng_for(5, 2, t), N_KV, N_EMBD))
 
 
+#: Output projection workload: a 3B-class vocabulary.
+N_VOCAB = 128256
+
+
+def output_projection():
+    """Output projection ``(W, x)``: Q8_0 bytes 3072 -> 128256 (config-1 distributions) and x (1, 3072)."""
+    return q8_0_blocks(rng_for(6, 0), N_VOCAB, N_EMBD), activations(rng_for(6, 1), 1, N_EMBD)
+
+
 #: Config 4 token counts.
 C4_M = (16, 64, 512)
 

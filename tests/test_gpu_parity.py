@@ -351,6 +351,58 @@ def test_q4k_qkv_rows_equal_the_separate_gemvs(cuda_lib):
         assert np.allclose(_np(got), _np(y), rtol=0, atol=1e-5 * float(np.abs(_np(y)).max()))
 
 
+# ------------------------------------------------------------------ output projection + argmax
+
+def _check_argmax(qdq, wb, x, n_vocab, n_in, batch):
+    import torch
+    W = qdq.upload_q8_0(wb, n_vocab, n_in)
+    logits = _nan(batch, n_vocab)
+    idx = torch.full((batch,), -1, dtype=torch.int32, device=_dev())
+    val = _nan(batch)
+    qdq.q8_0_logits_argmax(W, _t(x), logits, idx, val, n_vocab, n_in, batch)
+    lg, ix, vl = _np(logits), _np(idx), _np(val)
+    o = oracle.logits_argmax(oracle.q8_0_dequant(wb, n_vocab, n_in), x)
+    return lg, ix, vl, o
+
+
+# a 3B-class vocabulary (128256 x 3072), ragged sizes, batch 3 (general GEMV + argmax)
+@pytest.mark.parametrize("n_vocab,n_in,batch", [(128256, 3072, 1), (1000, 512, 1), (5003, 2048, 3), (1, 32, 1)])
+def test_logits_argmax_parity(cuda_lib, n_vocab, n_in, batch):
+    rng = np.random.default_rng(n_vocab + n_in + batch)
+    wb, x = synth.q8_0_blocks(rng, n_vocab, n_in), synth.activations(rng, batch, n_in)
+    lg, ix, vl, o = _check_argmax(cuda_lib, wb, x, n_vocab, n_in, batch)
+    assert gemv_excess(lg, o["logits"], o["A"]) <= 1.0
+    for b in range(batch):
+        # unique: the first maximum of the logits the GPU computed, and that logit bit for bit
+        assert ix[b] == int(np.argmax(lg[b])) and vl[b].view(np.uint32) == lg[b, ix[b]].view(np.uint32)
+        # valid: within the GEMV bound of the exact maximum
+        assert o["logits"][b, ix[b]] >= o["value"][b] - 2e-5 * o["A"][b].max()
+
+
+def test_logits_argmax_first_of_equal_rows(cuda_lib):
+    # identical rows give identical logits; the first of the maximal pair wins
+    n_vocab, n_in = 4000, 1024
+    rng = np.random.default_rng(81)
+    wb, x = synth.q8_0_blocks(rng, n_vocab, n_in), synth.activations(rng, 1, n_in)
+    y, _ = oracle.gemv(oracle.q8_0_dequant(wb, n_vocab, n_in), x)
+    top = int(np.argmax(y[0]))
+    wb[3001] = wb[top]
+    wb[17] = wb[top]
+    lg, ix, vl, o = _check_argmax(cuda_lib, wb, x, n_vocab, n_in, 1)
+    assert lg[0, 17] == lg[0, top] == lg[0, 3001]
+    assert ix[0] == min(17, top) and o["index"][0] == min(17, top)
+
+
+def test_logits_argmax_nan_activation(cuda_lib):
+    n_vocab, n_in = 700, 512
+    rng = np.random.default_rng(82)
+    wb, x = synth.q8_0_blocks(rng, n_vocab, n_in), synth.activations(rng, 2, n_in)
+    x[1, 7] = np.nan
+    lg, ix, vl, o = _check_argmax(cuda_lib, wb, x, n_vocab, n_in, 2)
+    assert ix[1] == 0 and np.isnan(vl[1]) and np.all(np.isnan(lg[1]))
+    assert ix[0] == o["index"][0] or o["logits"][0, ix[0]] >= o["value"][0] - 2e-5 * o["A"][0].max()
+
+
 # ------------------------------------------------------------------ batch-1 arithmetic
 # The batch-1 kernels multiply in 24-bit block fixed point by default (the integer
 # byte dot products); QDQ_OPT_XS_FLOAT_X = 1 selects f32 arithmetic.  Their error

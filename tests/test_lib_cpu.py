@@ -120,6 +120,19 @@ def test_qkv_validation(lib):
     assert f(Wq, Wk, Wv, x, q, k, v, n_embd=1 << 20) == qdq.QDQ_ERR_UNSUPPORTED
 
 
+def test_logits_argmax_validation(lib):
+    import ggml_quantized_dequant_gb300 as qdq
+    W, x, lg, idx, val = GOOD, GOOD + (1 << 28), GOOD + (2 << 28), GOOD + (3 << 28), GOOD + (4 << 28)
+    f = lib.qdq_q8_0_logits_argmax
+    assert f(W, x, lg, None, val, 1000, 512, 1, None) == qdq.QDQ_ERR_NULL
+    assert f(W, x, lg, idx, val, 1000, 500, 1, None) == qdq.QDQ_ERR_DIMS
+    assert f(W, x, lg, idx, val, 1000, 512, 9, None) == qdq.QDQ_ERR_DIMS
+    assert f(W, x, lg, idx + 2, val, 1000, 512, 1, None) == qdq.QDQ_ERR_ALIGN
+    assert f(W, x, lg, idx, lg + 40, 1000, 512, 1, None) == qdq.QDQ_ERR_ALIAS     # value inside logits
+    assert f(W, x, lg, idx, idx + 2 * 4 - 4, 1000, 512, 2, None) == qdq.QDQ_ERR_ALIAS  # index/value overlap
+    assert f(W, x, x, idx, val, 1000, 512, 1, None) == qdq.QDQ_ERR_ALIAS          # logits over x
+
+
 def test_gemm_validation(lib):
     import ggml_quantized_dequant_gb300 as qdq
     W, X, Y, ws = GOOD, GOOD + (1 << 28), GOOD + (2 << 28), GOOD + (3 << 28)

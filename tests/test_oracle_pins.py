@@ -391,6 +391,37 @@ def test_qkv_rejects_kv_wider_than_q():
         oracle.qkv(w, w[:2], w[:3], np.ones((1, 64), np.float32))
 
 
+# ---------------------------------------------------------------- output projection + argmax
+
+def test_logits_argmax_closed_form_and_first_of_ties():
+    # one-hot x picks column 5; rows 3 and 7 hold the same largest value there (index 3, the
+    # first of the tie); row 9's large weight sits in a column x does not use
+    n_vocab, n_in = 12, 64
+    w = np.zeros((n_vocab, n_in), np.float32)
+    w[:, 5] = np.arange(n_vocab, dtype=np.float32) * 0.25 - 2.0
+    w[3, 5] = w[7, 5] = 9.5
+    w[9, 6] = 100.0
+    x = np.zeros((2, n_in), np.float32)
+    x[0, 5] = 1.0
+    x[1, 5] = -1.0                      # negated: the smallest entry of column 5 wins
+    o = oracle.logits_argmax(w, x)
+    assert o["index"][0] == 3 and o["value"][0] == 9.5
+    assert o["index"][1] == 0 and o["value"][1] == 2.0
+
+
+def test_logits_argmax_nan_wins_and_matches_numpy():
+    rng = np.random.default_rng(71)
+    w = _small_q8(300, 96, 72)
+    x = synth.activations(rng, 3, 96)
+    o = oracle.logits_argmax(w, x)
+    assert np.array_equal(o["index"], np.argmax(o["logits"], axis=1))
+    assert np.array_equal(o["value"], o["logits"].max(axis=1))
+    x[1, 10] = np.nan
+    o = oracle.logits_argmax(w, x)
+    assert o["index"][1] == 0 and np.isnan(o["value"][1])
+    assert np.array_equal(o["index"], np.argmax(o["logits"], axis=1))
+
+
 # ---------------------------------------------------------------- batch GEMM
 
 def test_gemm_batch_m1_equals_gemv_and_permutes_rows():
