@@ -22,9 +22,12 @@
  *     never allocates, frees or keeps a pointer after a call returns.
  *   - Every compute call is asynchronous and stream-ordered on `stream`
  *     (0 = the legacy default stream); nothing synchronises the host.
- *   - Calls return QDQ_OK or a negative status.  On any error nothing has been
- *     launched and every output buffer is untouched.  There is no fallback
- *     path: an unsupported shape is an error, never a silent slower route.
+ *   - Calls return QDQ_OK or a negative status.  On a rejected argument (every
+ *     status but QDQ_ERR_CUDA) nothing has been launched and every output
+ *     buffer is untouched.  QDQ_ERR_CUDA from a call that launches several
+ *     kernels (the FFN block, the batch GEMM, the argmax, QKV at batch > 1) can leave the
+ *     kernels before the failing launch enqueued.  There is no fallback path:
+ *     an unsupported shape is an error, never a silent slower route.
  *   - Kernels are launched with programmatic dependent launch: a kernel may
  *     start streaming its own weights while the previous kernel on the stream
  *     finishes, but it reads activations only after that kernel completed.
