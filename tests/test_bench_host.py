@@ -89,3 +89,20 @@ def test_measured_peaks_shape():
 def test_warmup_floor():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2", "--impl", "reference"])
+
+
+def test_algorithmic_bytes_of_the_headline():
+    # GGML encodings: Q8_0 34 B per 32 weights, Q4_K 144 B per 256; plus x read and y written in f32
+    assert bench.Q8_W_BYTES == 8192 * 3072 // 32 * 34 == 26_738_688
+    assert bench.Q4_W_BYTES == 8192 * 3072 // 256 * 144 == 14_155_776
+    assert bench.Q8_W_BYTES + bench.GEMV_IO_BYTES == 26_783_744
+    assert bench.Q4_W_BYTES + bench.GEMV_IO_BYTES == 14_200_832
+
+
+def test_recorded_traffic_is_keyed_to_the_kernel_sources(monkeypatch):
+    # the recorded ncu bytes are reported only for the kernel sources they were captured on
+    for case in bench.KERNEL_SOURCES:
+        got = bench.recorded_traffic(case)
+        assert got is None or got > 0
+    monkeypatch.setitem(bench.KERNEL_SOURCES, "q8_0_gemv", ["qdq_gemv_xs.cu", "qdq_internal.cuh", "qdq_api.cu"])
+    assert bench.recorded_traffic("q8_0_gemv") is None
