@@ -19,7 +19,7 @@ std::atomic<int> g_opt_l2_prefetch{0};
 std::atomic<int> g_opt_ctas_per_sm{0};
 std::atomic<int> g_opt_xs_groups{0};
 std::atomic<int> g_opt_xs_stages{0};
-std::atomic<int> g_opt_xs_float_x{0};
+std::atomic<int> g_opt_xs_float_x{1};
 
 constexpr int kMaxDevices = 64;
 std::once_flag g_dev_once[kMaxDevices];
@@ -63,6 +63,7 @@ cudaError_t device_info(DeviceInfo *out) {
       err = cudaDeviceGetAttribute(&di.reserved_smem_per_block, cudaDevAttrReservedSharedMemoryPerBlock, dev);
     if (err == cudaSuccess)
       err = cudaDeviceGetAttribute(&di.regs_per_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&di.l2_bytes, cudaDevAttrL2CacheSize, dev);
     g_dev_info[dev] = di;
     g_dev_err[dev] = err;
   });
@@ -97,6 +98,33 @@ cudaError_t allow_dynamic_smem(const void *func, int bytes) {
     e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess) g_smem.push_back({func, dev, bytes});
   return e;
+}
+
+namespace {
+bool dims_q4k_(int n_out, int n_in) { return n_out > 0 && n_in > 0 && (n_in % 256) == 0; }
+size_t q4k_bytes_(int n_out, int n_in) { return size_t(n_out) * size_t(n_in / 256) * 144; }
+}  // namespace
+
+int check_ffn_residual(const void *Wg, const void *Wu, const void *Wd, const float *x, const float *residual,
+                       const float *out, const float *mid, int n_embd, int n_ff, int batch) {
+  if (!Wg || !Wu || !Wd || !x || !residual || !out) return QDQ_ERR_NULL;
+  if (!dims_q4k_(n_ff, n_embd) || !dims_q4k_(n_embd, n_ff)) return QDQ_ERR_DIMS;
+  if (batch < 1 || batch > QDQ_MAX_GEMV_BATCH) return QDQ_ERR_DIMS;
+  if (n_embd > QDQ_MAX_GEMV_N_IN || n_ff > QDQ_MAX_GEMV_N_IN) return QDQ_ERR_UNSUPPORTED;
+  if (!aligned(Wg, 16) || !aligned(Wu, 16) || !aligned(Wd, 16) || !aligned(x, 16) || !aligned(residual, 4) ||
+      !aligned(out, 4) || (mid && !aligned(mid, 16)))
+    return QDQ_ERR_ALIGN;
+  const size_t wgb = q4k_bytes_(n_ff, n_embd), wdb = q4k_bytes_(n_embd, n_ff);
+  const size_t eb = size_t(batch) * n_embd * 4, fb = size_t(batch) * n_ff * 4;
+  // mid may overlap nothing; out may only coincide exactly with residual
+  if (mid && (overlaps(mid, fb, Wg, wgb) || overlaps(mid, fb, Wu, wgb) || overlaps(mid, fb, Wd, wdb) ||
+              overlaps(mid, fb, x, eb) || overlaps(mid, fb, residual, eb) || overlaps(mid, fb, out, eb)))
+    return QDQ_ERR_ALIAS;
+  if (overlaps(out, eb, Wg, wgb) || overlaps(out, eb, Wu, wgb) || overlaps(out, eb, Wd, wdb) ||
+      overlaps(out, eb, x, eb))
+    return QDQ_ERR_ALIAS;
+  if (out != residual && overlaps(out, eb, residual, eb)) return QDQ_ERR_ALIAS;
+  return QDQ_OK;
 }
 
 }  // namespace qdq
@@ -235,24 +263,10 @@ int qdq_q4k_swiglu(const void *Wg, const void *Wu, const float *x, float *mid, i
 int qdq_q4k_ffn_residual(const void *Wg, const void *Wu, const void *Wd, const float *x,
                          const float *residual, float *out, float *mid, int n_embd, int n_ff, int batch,
                          cudaStream_t stream) {
-  if (!Wg || !Wu || !Wd || !x || !residual || !out || !mid) return QDQ_ERR_NULL;
-  if (!dims_q4k(n_ff, n_embd) || !dims_q4k(n_embd, n_ff)) return QDQ_ERR_DIMS;
-  if (batch < 1 || batch > QDQ_MAX_GEMV_BATCH) return QDQ_ERR_DIMS;
-  if (n_embd > QDQ_MAX_GEMV_N_IN || n_ff > QDQ_MAX_GEMV_N_IN) return QDQ_ERR_UNSUPPORTED;
-  if (!aligned(Wg, 16) || !aligned(Wu, 16) || !aligned(Wd, 16) || !aligned(x, 16) ||
-      !aligned(mid, 16) || !aligned(residual, 4) || !aligned(out, 4))
-    return QDQ_ERR_ALIGN;
-  const size_t wgb = q4k_bytes(n_ff, n_embd), wdb = q4k_bytes(n_embd, n_ff);
-  const size_t eb = size_t(batch) * n_embd * 4, fb = size_t(batch) * n_ff * 4;
-  // mid may overlap nothing; out may only coincide exactly with residual
-  if (overlaps(mid, fb, Wg, wgb) || overlaps(mid, fb, Wu, wgb) || overlaps(mid, fb, Wd, wdb) ||
-      overlaps(mid, fb, x, eb) || overlaps(mid, fb, residual, eb) || overlaps(mid, fb, out, eb))
-    return QDQ_ERR_ALIAS;
-  if (overlaps(out, eb, Wg, wgb) || overlaps(out, eb, Wu, wgb) || overlaps(out, eb, Wd, wdb) ||
-      overlaps(out, eb, x, eb))
-    return QDQ_ERR_ALIAS;
-  if (out != residual && overlaps(out, eb, residual, eb)) return QDQ_ERR_ALIAS;
-  int rc = launch_q4k_gemv(1, Wg, Wu, x, nullptr, mid, n_ff, n_embd, batch, stream);
+  if (!mid) return QDQ_ERR_NULL;
+  int rc = check_ffn_residual(Wg, Wu, Wd, x, residual, out, mid, n_embd, n_ff, batch);
+  if (rc != QDQ_OK) return rc;
+  rc = launch_q4k_gemv(1, Wg, Wu, x, nullptr, mid, n_ff, n_embd, batch, stream);
   if (rc != QDQ_OK) return rc;
   return launch_q4k_gemv(2, Wd, nullptr, mid, residual, out, n_embd, n_ff, batch, stream);
 }

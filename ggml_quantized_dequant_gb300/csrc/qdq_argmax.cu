@@ -2,8 +2,8 @@
 // projection, so that a decode step reads back one index and one value per token
 // instead of the whole vocabulary of logits.
 //
-// "Module cuda_lane" (the output projection and the on-device top-k/argmax
-// epilogue that saves the logits readback).  One CTA per batch row: the logits
+// "QTensorEngine", dispatch_output_top1_chunked (the output projection plus a
+// GPU block argmax, k = 1, that saves the logits readback).  One CTA per batch row: the logits
 // of one row (a few hundred KB) come from L2, where the projection just wrote
 // them.  The first maximal index wins; a NaN counts as larger than every
 // number (the first NaN wins), the numpy.argmax convention.

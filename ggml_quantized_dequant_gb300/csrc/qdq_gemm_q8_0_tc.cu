@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int issued = 0;  // TMA stages the producer issued (drained before the CTA exits)
   const int tile_n = blockIdx.x, tile_m = blockIdx.y;
   const int nkb = n_in / BK;
   const int kb0 = blockIdx.z * kb_per_split;
@@ -181,10 +182,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < npre; ++i)
         tma_load_2d(smem + i * C::kStageBytes + kQTileBytes + kATileBytes, &tm_x, (kb0 + i) * BK, tile_m * N,
                     &full[i]);
-      int issued = npre;
+      issued = npre;
       for (int i = npre; i < nk; ++i) {
         const int s = i % S;
-        if (!mbar_wait(&empty[s], ((i / S) + 1) & 1)) {
+        // after any timed-out wait in this CTA, issue nothing more
+        if (*reinterpret_cast<volatile int *>(&s_abort) || !mbar_wait(&empty[s], ((i / S) + 1) & 1)) {
           s_abort = 1;
           break;
         }
@@ -194,8 +196,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(st + kQTileBytes + kATileBytes, &tm_x, (kb0 + i) * BK, tile_m * N, &full[s]);
         issued = i + 1;
       }
-      // never leave with copies in flight: wait (bounded) for the last loads issued
-      for (int i = issued - S < 0 ? 0 : issued - S; i < issued; ++i) mbar_wait(&full[i % S], (i / S) & 1);
     } else {
       pdl_wait();
     }
@@ -304,8 +304,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // The last waits of the CTA: every MMA the issuer started has completed (the
+  // accumulator commit is issued after the MMA loop even when it stopped early)
+  // before the TMEM is freed, and every TMA load the producer issued has landed
+  // before the CTA's shared memory is released.
+  bool drained = true;
+  if (warp == kDequantWarps + 1 && lane == 0) drained = mbar_wait(accum, 0);
+  if (warp == kDequantWarps && lane == 0)
+    for (int i = issued - S < 0 ? 0 : issued - S; i < issued; ++i) drained = mbar_wait(&full[i % S], (i / S) & 1) && drained;
+  if (!drained) atomicAdd(&g_pipeline_timeouts, 1u);
   if (threadIdx.x == 0 && s_abort) atomicAdd(&g_pipeline_timeouts, 1u);
   if (warp == kDequantWarps + 1) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }

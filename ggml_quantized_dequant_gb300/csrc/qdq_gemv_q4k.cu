@@ -7,10 +7,13 @@
 //                                      one kernel, one read of x for both weights;
 //   try_q4k_soa_ffn_block_residual  -- out = residual + FFN(x), mid kept on device.
 //
-// Per 32-weight sub-block j of a superblock, weight = d*sc_j*q - dmin*m_j, so a
-// row's dot product is  sum_j ( d*sc_j * S_j - dmin*m_j * X_j )  with
-// S_j = sum_k q_k x_k over the sub-block and X_j = sum_k x_k.  X_j depends only
-// on x and is computed once per CTA; S_j is the per-weight work.
+// Per 32-weight sub-block j of a superblock, weight = d*sc_j*q - dmin*m_j
+// = d*sc_j*(q - mu_j) - R_j with an integer shift mu_j and R_j = dmin*m_j -
+// d*sc_j*mu_j (q4k_mu), so a row's dot product is
+// sum_j ( d*sc_j * S_j - R_j * X_j )  with S_j = sum_k (q_k - mu_j) x_k over the
+// sub-block and X_j = sum_k x_k.  X_j depends only on x and is computed once per
+// CTA; S_j is the per-weight work.  The shift keeps the rounding error a small
+// multiple of sum |w||x| even where d*sc_j*q and dmin*m_j nearly cancel.
 //
 // Design (HBM-bound, like the Q8_0 kernel): one CTA per SM over a contiguous
 // row range, L2 bulk prefetch of that range before the programmatic-launch
@@ -170,9 +173,17 @@ __global__ void __launch_bounds__(kThreads) q4k_gemv_kernel(const uint8_t *__res
         if (k < k1) {
           const int J = lane + 32 * ci;
           if (J < nsb) {
-            float2 DM[2];
+            // (d sc_j, R) with R = dmin m_j - d sc_j mu: the quants are summed as q - mu
+            // (q4k_mu), which keeps near-cancelling weights' error proportional to sum |w||x|
+            float2 DM[2], b01[2], b23[2];
 #pragma unroll
-            for (int r = 0; r < 2; ++r) DM[r] = q4k_scale_pair(hb[p][r], g0, g1, sh, mg);
+            for (int r = 0; r < 2; ++r) {
+              DM[r] = q4k_scale_pair(hb[p][r], g0, g1, sh, mg);
+              const float mu = q4k_mu(DM[r]);
+              DM[r].y = fmaf(-DM[r].x, mu, DM[r].y);
+              b01[r] = __fadd2_rn(mg.b_u4_01, f2(-mu, -mu));
+              b23[r] = __fadd2_rn(mg.b_u4_23, f2(-mu, -mu));
+            }
             float2 S[2][NB], T[2][NB];  // two independent chains per row
 #pragma unroll
             for (int r = 0; r < 2; ++r)
@@ -185,7 +196,7 @@ __global__ void __launch_bounds__(kThreads) q4k_gemv_kernel(const uint8_t *__res
 #pragma unroll
               for (int r = 0; r < 2; ++r) {
                 const uint32_t w = wd == 0 ? qb[p][r].x : wd == 1 ? qb[p][r].y : wd == 2 ? qb[p][r].z : qb[p][r].w;
-                u4x8_to_f2(w, mg, q[r]);
+                u4x8_to_f2_shifted(w, mg, b01[r], b23[r], q[r]);
               }
 #pragma unroll
               for (int b = 0; b < NB; ++b) {
@@ -205,7 +216,7 @@ __global__ void __launch_bounds__(kThreads) q4k_gemv_kernel(const uint8_t *__res
               const float xsum = xj[b * nsb * kXStride + 32];
 #pragma unroll
               for (int r = 0; r < 2; ++r) {
-                // (acc.x, acc.y) += (D * S.x, D * S.y - M * X_J)
+                // (acc.x, acc.y) += (D * S.x, D * S.y - R * X_J)
                 const float2 t = __ffma2_rn(f2(DM[r].x, DM[r].x), __fadd2_rn(S[r][b], T[r][b]), acc[r][b]);
                 acc[r][b] = f2(t.x, fmaf(-DM[r].y, xsum, t.y));
               }

@@ -32,23 +32,27 @@
 // crosses from one matrix into the next is copied in pieces, and the epilogue
 // writes each row to q, k or v.
 //
-// Arithmetic.  Turning int8 / u4 weights into floats costs more issue slots
-// on this GPU than streaming them from HBM, so by default the weights stay
-// integers: a lane turns its 32 activations once into 24-bit block fixed point
+// Arithmetic (QDQ_OPT_XS_FLOAT_X).  By default the weights are converted
+// exactly to f32 (magic-number LOP3s, one packed subtraction per pair) and
+// multiplied with packed f32x2 FMAs against the f32 activations: every
+// product's error is relative to |w_j x_j| itself, so a row is within
+// 1e-5 sum |w||x| for every finite input.  Q4_K sums its quants shifted by the
+// sub-block's integer offset mu (q4k_mu) and applies d sc and the remainder R
+// once per sub-block: d sc sum (q - mu) x - R sum x.
+// The opt-in fixed-point arithmetic keeps the weights integers instead: a lane
+// turns its 32 activations once into 24-bit block fixed point
 // X_j = rint(x_j 2^e) (e from the block's largest |x|, |X_j| <= 2^22), split
 // into three int8 limbs, and a row's block dot product sum_j q_j X_j is three
-// exact dp4a byte dot products per 4 weights.  The scales are applied to that
-// integer sum in f32 ((d / 2^e) sum q X, and for Q4_K
-// (d sc sum q X - dmin m sum X) / 2^e).  The only approximation beyond f32
-// rounding is |x_j - X_j 2^-e| <= 2^-22 max_block |x|, so
+// exact dp4a byte dot products per 4 weights, scaled in f32 ((d / 2^e) sum q X,
+// and for Q4_K (d sc sum (q - mu) X - R sum X) / 2^e, the shift applied to the
+// exact integer sums).  Its approximation beyond f32 rounding is
+// |x_j - X_j 2^-e| <= 2^-22 max_block |x|, so
 //   |y - exact| <= 2^-22 sum_b max_{j in b} |x_j| sum_{j in b} |w_j| + f32 rounding,
 // which is within 1e-5 sum |w||x| unless a row's weights concentrate on the
-// small activations of blocks whose largest activation they skip (a ratio
-// above ~40 between the two sums).  QDQ_OPT_XS_FLOAT_X selects the f32 path
-// instead: weights converted exactly to f32 (magic-number LOP3s) and packed
-// f32x2 FMAs against the f32 activations, within 1e-5 sum |w||x| for every
-// finite input.  A block holding an inf or a NaN gives NaN rows on the fixed
-// path (the f32 path propagates them by IEEE rules).
+// small activations of blocks whose largest activation they skip: a bound
+// relative to each block's largest activation, not to each product, so it is
+// not the default.  A block holding an inf or a NaN gives NaN rows on the
+// fixed path (the f32 path propagates them by IEEE rules).
 // Every pipeline wait is bounded; a wait that runs out is counted
 // (qdq_pipeline_timeouts) and the CTA winds down instead of hanging.
 #include <mutex>
@@ -102,7 +106,9 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
 struct FixedX {
   uint32_t p[3][8];
   float inv_s;  // 2^-e (NaN when the block holds an inf or a NaN)
-  float xsum;   // sum_j X_j
+  float xsum;   // sum_j X_j (Q4_K)
+  int s01;      // sum_j (L1_j 2^8 + L0_j) = sum_j (X_j & 0xFFFF) (Q4_K)
+  int s2;       // sum_j L2_j (Q4_K)
 };
 
 template <int FMT>
@@ -125,6 +131,7 @@ __device__ __forceinline__ void to_fixed(const float (&xv)[32], FixedX &f) {
       for (int w = 0; w < 8; ++w) f.p[l][w] = 0u;
     f.inv_s = __int_as_float(0x7fffffff);
     f.xsum = 0.f;
+    f.s01 = f.s2 = 0;
     return;
   }
   const int e = 148 - (E > 1 ? E : 1);  // -106 .. 147; a zero or subnormal maximum takes E = 1
@@ -150,16 +157,27 @@ __device__ __forceinline__ void to_fixed(const float (&xv)[32], FixedX &f) {
     f.p[2][w] = __byte_perm(u0, u1, 0x5410);
   }
   if constexpr (FMT == kQ4) {
-    int t[16];
+    int t[16], lo[16], hi[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) t[j] = X[2 * j] + X[2 * j + 1];
+    for (int j = 0; j < 16; ++j) {
+      t[j] = X[2 * j] + X[2 * j + 1];
+      lo[j] = (X[2 * j] & 0xFFFF) + (X[2 * j + 1] & 0xFFFF);
+      hi[j] = (X[2 * j] >> 16) + (X[2 * j + 1] >> 16);
+    }
 #pragma unroll
     for (int w = 8; w > 0; w >>= 1)
 #pragma unroll
-      for (int j = 0; j < w; ++j) t[j] += t[j + w];
+      for (int j = 0; j < w; ++j) {
+        t[j] += t[j + w];
+        lo[j] += lo[j + w];
+        hi[j] += hi[j + w];
+      }
     f.xsum = __int2float_rn(t[0]);
+    f.s01 = lo[0];
+    f.s2 = hi[0];
   } else {
     f.xsum = 0.f;
+    f.s01 = f.s2 = 0;
   }
 }
 
@@ -242,6 +260,8 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
   __syncthreads();
   pdl_launch_dependents();
 
+  // producer bookkeeping for the final drain: stages issued so far
+  int rounds = 0, stop_i = 0, stop_g = 0;
   if (warp == ncw) {
     // ---------------- producer: weights only, so no wait on the previous kernel ----------------
     // Round i issues stage i of every group that has one.  Group g consumes its
@@ -257,9 +277,8 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
           prefetch_range_l2(a.W2 + q_bytes, int64_t(a.n_out) * s_row, r0 * s_row, r1 * s_row);
         }
       }
-      int rounds = 0;
       for (int g = 0; g < G; ++g) rounds = max(rounds, gstages(g));
-      int stop_i = rounds, stop_g = 0;  // first stage not issued, if the loop stopped early
+      stop_i = rounds;  // first stage not issued (stop_i, stop_g), if the loop stopped early
       for (int i = 0; i < rounds && stop_i == rounds; ++i) {
         if (EPI != kQkv && i == SG && a.l2_prefetch == 2) {
           // after the first fill of every slot: pull the rows that did not fit the ring
@@ -278,7 +297,9 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
         for (int g = 0; g < G; ++g) {
           if (i >= gstages(g)) continue;
           const int s = g * SG + i % SG;
-          if (i >= SG && !mbar_wait(&empty[s], ((i / SG) + 1) & 1)) {
+          // after any timed-out wait in this CTA, issue nothing more
+          if (*reinterpret_cast<volatile int *>(&s_abort) ||
+              (i >= SG && !mbar_wait(&empty[s], ((i / SG) + 1) & 1))) {
             s_abort = 1;
             stop_i = i;
             stop_g = g;
@@ -312,12 +333,6 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
             bulk_copy_g2s(sts + 2 * s_row, a.W2 + q_bytes + rr * s_row, uint32_t(nr * s_row), &full[s]);
           }
         }
-      }
-      // never exit with copies in flight: wait for the last fill of every slot
-      for (int g = 0; g < G; ++g) {
-        const int issued = stop_i == rounds ? gstages(g) : min(gstages(g), stop_i + (g < stop_g ? 1 : 0));
-        for (int i = issued - SG < 0 ? 0 : issued - SG; i < issued; ++i)
-          mbar_wait(&full[g * SG + i % SG], (i / SG) & 1);
       }
     }
   } else {
@@ -471,6 +486,7 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
         }
         if (kEarlyRelease) release(s);
         float2 DM[kStageRows];
+        float mu[kStageRows], R[kStageRows];
 #pragma unroll
         for (int k = 0; k < kStageRows; ++k) {
           const uint32_t lo = g0 ? h[k].y : (g1 ? h[k].z : h[k].w);
@@ -478,6 +494,11 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
           const uint32_t f = __funnelshift_r(lo, hi, sh);
           const float2 scm = q4k_field_to_f2(f, mg);  // (sc, m)
           DM[k] = __fmul2_rn(__half22float2(*reinterpret_cast<const __half2 *>(&h[k].x)), scm);  // (d sc, dmin m)
+          // each weight is d sc (q - mu) - R with the shift mu of q4k_mu: the quants are
+          // shifted before they are summed, so near-cancelling weights keep the error
+          // proportional to sum |w||x|
+          mu[k] = q4k_mu(DM[k]);
+          R[k] = fmaf(-DM[k].x, mu[k], DM[k].y);
         }
         if constexpr (AR == kFixedX) {
           int c0[kStageRows], c1[kStageRows], c2[kStageRows];
@@ -496,20 +517,28 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
           }
 #pragma unroll
           for (int k = 0; k < kStageRows; ++k) {
-            const float qx = fmaf(__int2float_rn(c2[k]), 65536.0f, __int2float_rn(c0[k] + c1[k] * 256));
-            part[k] = fmaf(DM[k].x, qx, -DM[k].y * fx.xsum) * fx.inv_s;  // (d sc sum qX - dmin m sum X) / 2^e
+            // sum (q - mu) X = hi 2^16 + lo, both exact in int32 (|hi| < 2^17, |lo| < 2^26)
+            const int m = int(mu[k]);
+            const int hi = c2[k] - m * fx.s2;
+            const int lo = c0[k] + c1[k] * 256 - m * fx.s01;
+            const float qx = fmaf(__int2float_rn(hi), 65536.0f, __int2float_rn(lo));
+            part[k] = fmaf(DM[k].x, qx, -R[k] * fx.xsum) * fx.inv_s;  // (d sc sum (q - mu) X - R sum X) / 2^e
           }
         } else {
-          float2 s0[kStageRows], s1[kStageRows];
+          float2 s0[kStageRows], s1[kStageRows], b01[kStageRows], b23[kStageRows];
 #pragma unroll
-          for (int k = 0; k < kStageRows; ++k) s0[k] = s1[k] = f2(0.f, 0.f);
+          for (int k = 0; k < kStageRows; ++k) {
+            s0[k] = s1[k] = f2(0.f, 0.f);
+            b01[k] = __fadd2_rn(mg.b_u4_01, f2(-mu[k], -mu[k]));  // -(2^23 + mu), -(2^19 + mu): exact
+            b23[k] = __fadd2_rn(mg.b_u4_23, f2(-mu[k], -mu[k]));
+          }
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
             for (int k = 0; k < kStageRows; ++k) {
               const uint32_t w = kk == 0 ? q[k].x : kk == 1 ? q[k].y : kk == 2 ? q[k].z : q[k].w;
-              float2 qq[4];
-              u4x8_to_f2(w, mg, qq);
+              float2 qq[4];  // q - mu, exactly
+              u4x8_to_f2_shifted(w, mg, b01[k], b23[k], qq);
               s0[k] = __ffma2_rn(qq[0], xr[4 * kk], s0[k]);
               s1[k] = __ffma2_rn(qq[1], xr[4 * kk + 1], s1[k]);
               s0[k] = __ffma2_rn(qq[2], xr[4 * kk + 2], s0[k]);
@@ -519,7 +548,7 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
 #pragma unroll
           for (int k = 0; k < kStageRows; ++k) {
             const float2 st = __fadd2_rn(s0[k], s1[k]);
-            part[k] = fmaf(DM[k].x, st.x + st.y, -DM[k].y * xsum);  // d sc_j sum(q x) - dmin m_j sum(x)
+            part[k] = fmaf(DM[k].x, st.x + st.y, -R[k] * xsum);  // d sc_j sum((q - mu) x) - R sum(x)
           }
         }
       }
@@ -563,6 +592,18 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
       }
     }
   }
+  // The last thing the CTA waits for: the completion of every copy the producer
+  // issued (the last fill of each slot), so that no bulk copy can still be writing
+  // into this CTA's shared memory when it exits, also after a timed-out wait.
+  if (warp == ncw && lane == 0) {
+    bool drained = true;
+    for (int g = 0; g < G; ++g) {
+      const int issued = stop_i == rounds ? gstages(g) : min(gstages(g), stop_i + (g < stop_g ? 1 : 0));
+      for (int i = issued - SG < 0 ? 0 : issued - SG; i < issued; ++i)
+        drained = mbar_wait(&full[g * SG + i % SG], (i / SG) & 1) && drained;
+    }
+    if (!drained) atomicAdd(&g_xs_timeouts, 1u);
+  }
 }
 
 // Registers per thread of a kernel (queried once per kernel).
@@ -604,10 +645,8 @@ int launch_xs_ar(XsArgs a, cudaStream_t s, const DeviceInfo &di) {
   if (a.groups < 1) a.groups = 1;
   if (opt_xs_groups() > 0) a.groups = opt_xs_groups();
   if (32 * (a.wpr * a.groups + 1) > kMaxThreads) return QDQ_ERR_UNSUPPORTED;
-  // L2 prefetch of the rows the first ring fill leaves out: measured faster for the
-  // Q8_0 GEMV chains (the 8192-wide down projection most), slower for the FFN
   const int pf = opt_l2_prefetch();
-  a.l2_prefetch = EPI == kQkv ? 0 : pf == 0 ? (FMT == kQ8 ? 2 : 0) : pf == 3 ? 0 : pf;
+  a.l2_prefetch = EPI == kQkv ? 0 : pf == 3 ? 0 : pf;
   const int64_t q_row = FMT == kQ8 ? n_in : n_in / 2;
   const int64_t s_row = FMT == kQ8 ? n_in / 16 : (n_in / 256) * 16;
   a.stage_bytes = int((kStageRows * (q_row + s_row) + 127) / 128 * 128);
@@ -632,6 +671,15 @@ int launch_xs_ar(XsArgs a, cudaStream_t s, const DeviceInfo &di) {
   if (opt_xs_stages() > 0) sg = opt_xs_stages();
   a.sg = sg;
   const int stages = a.groups * sg;
+  // Automatic L2 prefetch (option 0) of the rows the first ring fill leaves out:
+  // measured faster for the Q8_0 GEMV chains (the 8192-wide down projection most),
+  // slower for the FFN.  Only when those rows fit in half the L2: on a matrix
+  // several times larger than L2 (a vocabulary projection) the prefetched lines
+  // evict one another before they are read, and the prefetch costs time.
+  if (pf == 0 && FMT == kQ8 && EPI != kQkv) {
+    const int64_t rest = int64_t(n_out) * (q_row + s_row) - int64_t(grid) * stages * kStageRows * (q_row + s_row);
+    a.l2_prefetch = rest <= int64_t(di.l2_bytes) / 2 ? 2 : 0;
+  }
   const size_t smem = size_t(stages) * a.stage_bytes + 2 * stages * sizeof(uint64_t) + psum_bytes;
   if (smem > size_t(di.max_smem_optin)) return QDQ_ERR_UNSUPPORTED;
   const cudaError_t e0 = allow_dynamic_smem(reinterpret_cast<const void *>(kern), int(smem));

@@ -32,6 +32,7 @@ struct DeviceInfo {
   int smem_per_sm;
   int reserved_smem_per_block;
   int regs_per_sm;
+  int l2_bytes;
 };
 
 // Dynamic shared memory for a streaming GEMV CTA: at least `need`, and when
@@ -81,6 +82,11 @@ inline bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   return na && nb && pa < pb + nb && pb < pa + na;
 }
 inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Argument checks of the FFN block (qdq_q4k_ffn_residual); `mid` NULL skips the
+// checks of the intermediate buffer (the allocation-free entry point owns it).
+int check_ffn_residual(const void *Wg, const void *Wu, const void *Wd, const float *x, const float *residual,
+                       const float *out, const float *mid, int n_embd, int n_ff, int batch);
 
 // Kernel launchers (defined in the per-kernel translation units).
 int launch_q8_0_pack(const void *ggml, void *packed, int n_out, int n_in, cudaStream_t s);
@@ -315,9 +321,33 @@ __device__ __forceinline__ void u4x8_to_f2(uint32_t w, const Magic &k, float2 q[
   q[3] = __fadd2_rn(f2_bits(lop3_and_or<0x0F00u>(h, k.u4_2), lop3_and_or<0xF000u>(h, k.u4_3)), k.b_u4_23);
 }
 
+// As u4x8_to_f2 with the subtraction constants given: with b01 = b_u4_01 - (mu, mu)
+// and b23 = b_u4_23 - (mu, mu) for an integer mu in [0, 15] the pairs hold q - mu, exactly.
+__device__ __forceinline__ void u4x8_to_f2_shifted(uint32_t w, const Magic &k, float2 b01, float2 b23,
+                                                   float2 q[4]) {
+  const uint32_t h = w >> 16;
+  q[0] = __fadd2_rn(f2_bits(lop3_and_or<0x000Fu>(w, k.u4_0), lop3_and_or<0x00F0u>(w, k.u4_1)), b01);
+  q[1] = __fadd2_rn(f2_bits(lop3_and_or<0x0F00u>(w, k.u4_2), lop3_and_or<0xF000u>(w, k.u4_3)), b23);
+  q[2] = __fadd2_rn(f2_bits(lop3_and_or<0x000Fu>(h, k.u4_0), lop3_and_or<0x00F0u>(h, k.u4_1)), b01);
+  q[3] = __fadd2_rn(f2_bits(lop3_and_or<0x0F00u>(h, k.u4_2), lop3_and_or<0xF000u>(h, k.u4_3)), b23);
+}
+
 // Q4_K header field (sc in bits 0..5, m in bits 6..11) -> (sc, m) as floats.
 __device__ __forceinline__ float2 q4k_field_to_f2(uint32_t f, const Magic &k) {
   return __fadd2_rn(f2_bits(lop3_and_or<0x3Fu>(f, k.sc), lop3_and_or<0xFC0u>(f, k.m)), k.b_scm);
+}
+
+// Shift of a Q4_K sub-block with D = d*sc_j, Dm = dmin*m_j: mu is the integer in
+// [0, 15] nearest Dm / D (0 when D is 0 or of the other sign), and R = Dm - D*mu
+// (one rounding).  Each weight is then w = D*(q - mu) - R, where either |R| <= D/2
+// (up to the quotient's approximation) or every term has the sign of w, so that
+// |D*(q - mu)| <= 2|w| and |R| <= |w| for every weight of the sub-block.  A dot
+// product formed as D*sum((q - mu) x) - R*sum(x) therefore has an f32 error that is
+// a small multiple of sum |w||x| -- also where D*q and Dm cancel (w near 0), which
+// the plain regrouping D*sum(q x) - Dm*sum(x) does not give.
+__device__ __forceinline__ float q4k_mu(float2 DDm) {
+  const float mu = rintf(__fdividef(DDm.y, DDm.x));
+  return fminf(fmaxf(mu, 0.f), 15.f);  // a NaN quotient (0 / 0) gives 0
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -53,8 +53,11 @@ extern "C" int qdq_q4k_ffn_residual_noalloc(const void *Wg, const void *Wu, cons
                                             cudaStream_t stream) {
   // the intermediate vector is batch x n_ff floats; it must fit the fixed array
   if (batch > 0 && n_ff > 0 && int64_t(batch) * n_ff > int64_t(QDQ_NOALLOC_FFN_MAX_MID)) return QDQ_ERR_SCRATCH;
+  // then the same argument checks as the workspace entry point, all before any CUDA call
+  int rc = qdq::check_ffn_residual(Wg, Wu, Wd, x, residual, out, nullptr, n_embd, n_ff, batch);
+  if (rc != QDQ_OK) return rc;
   float *mid = nullptr;
-  const int rc = scratch_on_current_device(&mid);
+  rc = scratch_on_current_device(&mid);
   if (rc != QDQ_OK) return rc;
   // Every element of mid is written by the SwiGLU kernel before the down
   // projection reads it, so nothing left from an earlier call needs clearing.

@@ -8,11 +8,11 @@
  *     try_q4k_soa_gemv                              -> qdq_q4k_gemv
  *     try_q4k_soa_fused_swiglu                      -> qdq_q4k_swiglu
  *     try_q4k_soa_qkv                               -> qdq_q4k_qkv
- *     output projection + argmax epilogue            -> qdq_q8_0_logits_argmax
  *     try_q4k_soa_ffn_block / _ffn_block_residual   -> qdq_q4k_ffn_residual
  *     preload_q4k_soa_weights (one-time upload)     -> qdq_q8_0_pack / qdq_q4k_pack
  *   "Module cuda_lane", Goal (batch prefill-shaped GEMMs on tensor cores) and
  *   "weight_cache.rs", try_cuda_batch_gemv          -> qdq_q8_0_gemm_batch
+ *   "QTensorEngine", dispatch_output_top1_chunked   -> qdq_q8_0_logits_argmax
  *
  * Conventions for every call
  *   - W is row-major n_out x n_in (rows = outputs, the GGML convention).
@@ -109,10 +109,11 @@ int qdq_q4k_dequant(const void *W, float *out, int n_out, int n_in, cudaStream_t
  * "Module cuda_lane", Functions: try_q8_0_cuda_gemv, q8_0_gemv_oracle_into,
  * try_q4k_soa_gemv.  W: packed (16-byte aligned).  x: batch x n_in f32,
  * 16-byte aligned.  y: batch x n_out f32, 4-byte aligned, must not overlap W
- * or x.  1 <= batch <= QDQ_MAX_GEMV_BATCH.  Batch 2..8: f32 arithmetic; the
- * error against the exact sum stays far below 1e-5 * sum_k |w[r,k]| |x[b,k]|.
- * Batch 1: the arithmetic QDQ_OPT_XS_FLOAT_X selects, with the bound stated
- * there (the same holds for the SwiGLU and FFN calls below at batch 1).
+ * or x.  1 <= batch <= QDQ_MAX_GEMV_BATCH.  Error against the exact sum:
+ * <= 1e-5 * sum_k |w[r,k]| |x[b,k]| for every finite input (f32 arithmetic; for
+ * Q4_K also where d*sc_j*q and dmin*m_j cancel).  Batch 1 can opt into the
+ * faster fixed-point arithmetic of QDQ_OPT_XS_FLOAT_X = 0, with the bound
+ * stated there (the same holds for the SwiGLU, QKV and FFN calls below).
  */
 int qdq_q8_0_gemv(const void *W, const float *x, float *y,
                   int n_out, int n_in, int batch, cudaStream_t stream);
@@ -130,8 +131,9 @@ int qdq_q4k_swiglu(const void *Wg, const void *Wu, const float *x, float *mid,
                    int n_ff, int n_embd, int batch, cudaStream_t stream);
 
 /* ---- output projection with on-device argmax --------------------------------
- * "Module cuda_lane": the output projection with an on-device top-k/argmax
- * epilogue, so a decode step reads back one token instead of the logits.
+ * "QTensorEngine", dispatch_output_top1_chunked (GPU block argmax, k = 1): the
+ * output projection with an on-device argmax epilogue, so a decode step reads
+ * back one token instead of the logits.
  *   logits[b, t] = W_t . x_b (a Q8_0 GEMV, as qdq_q8_0_gemv), then
  *   index[b] = the first t with the largest logits[b, t], value[b] = that logit
  *   (a NaN logit counts as the largest: the first NaN wins).
@@ -225,16 +227,18 @@ int qdq_pipeline_timeouts(void);
 #define QDQ_OPT_XS_GROUPS    4  /* batch-1 GEMV consumer groups per CTA, 0 = automatic (default), 1..16 */
 #define QDQ_OPT_XS_STAGES    5  /* batch-1 GEMV weight-ring slots per consumer group (4-row stages), 0 = automatic (default), 1..16 */
 /* Arithmetic of the batch-1 kernels (qdq_q8_0_gemv and qdq_q4k_gemv at batch 1,
- * qdq_q4k_swiglu and both FFN calls at batch 1):
- *   0 (default): each 32-activation block becomes 24-bit block fixed point
- *     X_j = rint(x_j 2^e), |X_j| <= 2^22, and block dot products are exact
- *     integer byte dot products, scaled in f32.  Error against the exact sum
- *     <= 2^-22 sum_blocks max_j |x_j| sum_j |w_j| + f32 rounding: within
- *     1e-5 sum |w||x| unless a row's weights sit on the small activations of
+ * qdq_q4k_swiglu, qdq_q4k_qkv, the output projections and both FFN calls at batch 1):
+ *   1 (default): weights converted exactly to f32 and multiplied with f32 FMAs
+ *     (Q4_K: quants shifted by the sub-block's integer offset before they are
+ *     summed): within 1e-5 sum |w||x| of the exact sum for every finite input.
+ *   0 (opt-in, faster): each 32-activation block becomes 24-bit block fixed
+ *     point X_j = rint(x_j 2^e), |X_j| <= 2^22, and block dot products are
+ *     exact integer byte dot products, scaled in f32.  Error against the exact
+ *     sum <= 2^-22 sum_blocks max_j |x_j| sum_j |w_j| + f32 rounding: a bound
+ *     relative to each block's largest activation, so it exceeds
+ *     1e-5 sum |w||x| where a row's weights sit on the small activations of
  *     blocks whose largest activation they skip.  A block with an inf or NaN
- *     activation gives NaN outputs.
- *   1: weights converted to f32 and multiplied with f32 FMAs: within
- *     1e-5 sum |w||x| for every finite input, about half the ALU throughput. */
+ *     activation gives NaN outputs. */
 #define QDQ_OPT_XS_FLOAT_X   6
 /* Sets a process-wide option; returns the previous value, or QDQ_ERR_DIMS for a bad key/value. */
 int qdq_set_option(int key, int value);

@@ -15,8 +15,9 @@ Sources (the pages are rustdoc for the ``qualia_core_db`` crate):
 * "Module cuda_lane", *Functions: try_q4k_soa_qkv* -- Q, K and V projected from
   the same activation; with grouped-query attention K and V exist only for the
   first n_kv rows.
-* "Module cuda_lane" -- the output projection with an on-device top-k / argmax
-  epilogue (one token read back instead of the logits).
+* "QTensorEngine", *dispatch_output_top1_chunked* / *dispatch_output_topk_chunked*
+  -- the output projection with an on-device argmax (k = 1) or top-k epilogue:
+  only the winning (id, logit) candidates are read back instead of the logits.
 * "weight_cache.rs", *try_cuda_batch_gemv* doc comment -- layouts: W is
   row-major ``n_out x n_in`` (rows = outputs, GGML convention); activations are
   packed ``batch x n_in``; outputs are ``batch x n_out``.

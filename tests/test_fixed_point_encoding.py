@@ -1,5 +1,6 @@
-"""The block fixed-point activation encoding the batch-1 kernels use by default,
-restated in numpy, checked against the claims its error bound rests on:
+"""Kernel-claims test (not an oracle pin): the block fixed-point activation
+encoding of the batch-1 kernels' opt-in arithmetic (QDQ_OPT_XS_FLOAT_X = 0),
+restated in numpy and checked against the claims its stated error bound rests on:
 
 * e = 148 - max(E, 1), E the biased exponent of the block's largest |x|, puts
   every X_j = rint(x_j 2^e) in [-2^22, 2^22];
@@ -8,7 +9,10 @@ restated in numpy, checked against the claims its error bound rests on:
 * X_j = L2 2^16 + L1 2^8 + L0 with L0, L1 unsigned bytes and L2 in [-64, 64],
   so each limb fits the byte lanes of a dp4a;
 * q_j int8 or u4 against those limbs: every per-limb dot product over 32 weights
-  fits int32, and so does c0 + 256 c1.
+  fits int32, and so does c0 + 256 c1;
+* the Q4_K sub-block shift applied to the exact sums, hi = c2 - mu S2 and
+  lo = c0 + 256 c1 - mu (S0 + 256 S1) with S_l = sum_j L_l, stays within int32 and
+  reassembles sum (q - mu) X exactly.
 
 This is a statement of the arithmetic, not a copy of the kernel: the GPU tests
 compare the kernel itself with the oracle.
@@ -97,3 +101,17 @@ def test_limb_dot_products_reassemble_the_exact_sum():
         q = rng.integers(-128, 128, 32)
         c0, c1, c2 = int((q * L0).sum()), int((q * L1).sum()), int((q * L2).sum())
         assert c2 * 65536 + (c0 + 256 * c1) == int((q * X).sum())
+
+
+@pytest.mark.parametrize("mu", [0, 7, 15])
+def test_q4k_shifted_limb_sums_fit_int32_and_reassemble(mu):
+    rng = np.random.default_rng(7 + mu)
+    for xb in _blocks(rng):
+        X, _ = encode(xb)
+        L0, L1, L2 = limbs(X)
+        for q in (np.full(32, 15), np.zeros(32, np.int64), rng.integers(0, 16, 32)):
+            c0, c1, c2 = (int((q * L).sum()) for L in (L0, L1, L2))
+            hi = c2 - mu * int(L2.sum())
+            lo = c0 + 256 * c1 - mu * int((X & 0xFFFF).sum())
+            assert abs(hi) < 2 ** 17 and abs(lo) < 2 ** 26
+            assert hi * 65536 + lo == int(((q - mu) * X).sum())

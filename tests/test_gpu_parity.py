@@ -278,7 +278,10 @@ def test_q8_0_gemm_batch_parity_shapes(cuda_lib, n_out, n_in, M):
 @pytest.mark.parametrize("M", [16, 64, 512])
 def test_q8_0_gemm_batch_full_size_config4(cuda_lib, kind, M):
     n_out, n_in = (8192, 3072) if kind == 0 else (3072, 8192)
-    sample = None if M <= 64 else np.random.default_rng(M).choice(M, 12, replace=False)
+    # M = 512: 32 rows from each 256-token tile (every output column, so every weight
+    # tile and K split, enters each sampled row)
+    sample = None if M <= 64 else np.sort(np.concatenate(
+        [t * 256 + np.random.default_rng(M + t).choice(256, 32, replace=False) for t in range(M // 256)]))
     _gemm_case(cuda_lib, n_out, n_in, M, wb=synth.config4_w(kind), X=synth.config4_x(kind, M),
                sample_rows=sample)
 
@@ -470,9 +473,10 @@ def test_batch1_outlier_channels(cuda_lib, fmt):
 
 
 def test_batch1_fixed_x_stated_bound(cuda_lib):
-    # Adversarial for fixed point: one activation per 32-block is 1e4 and its weights are
-    # all zero; the rest are ~1e-2.  The fixed path stays within its stated bound, the
-    # f32 path within 1e-5 sum|w||x|.
+    # Adversarial for block fixed point: one activation per 32-block is 1e4 and its
+    # weights are all zero; the rest are ~1e-2.  The default (f32) arithmetic meets the
+    # 1e-5 sum|w||x| bound here as everywhere; the opt-in fixed-point path stays within
+    # its own stated bound, which is relative to each block's largest activation.
     qdq = cuda_lib
     n_out, n_in = 96, 1024
     rng = np.random.default_rng(41)
@@ -484,14 +488,77 @@ def test_batch1_fixed_x_stated_bound(cuda_lib):
     x[0, 32 * np.arange(n_in // 32) + j0] = 1e4
     w = oracle.q8_0_dequant(wb, n_out, n_in)
     y_ref, a = oracle.gemv(w, x)
+    assert gemv_excess(_gemv1(qdq, "q8_0", wb, x, n_out, n_in), y_ref, a) <= 1.0   # the default path
     m_b = np.abs(x[0]).reshape(-1, 32).max(axis=1)                       # max |x| per block
     w_b = np.abs(w.astype(np.float64)).reshape(n_out, -1, 32).sum(axis=2)  # sum |w| per row and block
     fixed_bound = 2.0 ** -22 * (w_b * m_b).sum(axis=1) + 1e-5 * a[0]
     with _FloatX(qdq, 0):
         y = _gemv1(qdq, "q8_0", wb, x, n_out, n_in)
     assert np.all(np.abs(y[0].astype(np.float64) - y_ref[0]) <= fixed_bound)
-    with _FloatX(qdq, 1):
-        assert gemv_excess(_gemv1(qdq, "q8_0", wb, x, n_out, n_in), y_ref, a) <= 1.0
+
+
+def _cancelling_q4k(rng, n_out, n_in, frac_zero, d=1e-2, dmin=1e-2):
+    """Q4_K rows whose sub-blocks have sc_j = 4, m_j = 32 everywhere: with d == dmin a
+    quant of 8 dequantises to exactly 0, and `frac_zero` of the quant bytes are 0x88."""
+    wb = synth.q4k_blocks(rng, n_out, n_in, d_range=(d, d), dmin_range=(dmin, dmin))
+    sb = wb.reshape(n_out, n_in // 256, 144)
+    # bytes 0..3: sc_0..3 = 4; 4..7: m_0..3 = 32 with the top bits (2) of m_4..7; 8..11:
+    # low nibbles sc_4..7 = 4 and m_4..7 = 0 (m_4..7 = 0 | 2 << 4 = 32)
+    sb[..., 4:16] = np.array([4, 4, 4, 4, 160, 160, 160, 160, 4, 4, 4, 4], dtype=np.uint8)
+    keep = rng.random(sb[..., 16:].shape) >= frac_zero
+    sb[..., 16:] = np.where(keep, sb[..., 16:], 0x88).astype(np.uint8)
+    return wb
+
+
+@pytest.mark.parametrize("batch", [1, 4])
+@pytest.mark.parametrize("frac_zero", [1.0, 0.99])
+def test_q4k_gemv_cancelling_rows(cuda_lib, batch, frac_zero):
+    # d*sc_j*q == dmin*m_j for 100 % / 99 % of the weights: sum|w||x| is a tiny part of
+    # the two regrouped terms; a row of zero weights must give exactly 0
+    qdq = cuda_lib
+    n_out, n_in = 200, 2048
+    rng = np.random.default_rng(int(frac_zero * 100) + batch)
+    wb = _cancelling_q4k(rng, n_out, n_in, frac_zero)
+    x = synth.activations(rng, batch, n_in)
+    W = qdq.upload_q4k(wb, n_out, n_in)
+    y = _nan(batch, n_out)
+    qdq.q4k_gemv(W, _t(x), y, n_out, n_in, batch)
+    w = oracle.q4k_dequant(wb, n_out, n_in)
+    y_ref, a = oracle.gemv(w, x)
+    if frac_zero == 1.0:
+        assert np.all(w == 0) and np.all(_np(y) == 0.0)
+    assert gemv_excess(_np(y), y_ref, a) <= 1.0
+
+
+def test_q4k_gemv_near_cancelling_adjacent_scales(cuda_lib):
+    # dmin one fp16 step above d: every weight of a quant-8 sub-block is the same tiny
+    # value 32 (d - dmin); the regrouped terms are ~10^3 times larger than the weights
+    qdq = cuda_lib
+    n_out, n_in = 64, 1024
+    d = 1e-2
+    dmin = float(np.nextafter(np.float16(d), np.float16(1)))
+    rng = np.random.default_rng(12)
+    wb = _cancelling_q4k(rng, n_out, n_in, 1.0, d=d, dmin=dmin)
+    x = synth.activations(rng, 1, n_in)
+    W = qdq.upload_q4k(wb, n_out, n_in)
+    y = _nan(1, n_out)
+    qdq.q4k_gemv(W, _t(x), y, n_out, n_in, 1)
+    w = oracle.q4k_dequant(wb, n_out, n_in)
+    assert np.all(w != 0) and np.abs(w).max() < 1e-3 * d
+    y_ref, a = oracle.gemv(w, x)
+    assert gemv_excess(_np(y), y_ref, a) <= 1.0
+
+
+def test_q4k_fixed_x_zero_rows_stay_zero(cuda_lib):
+    # the opt-in fixed-point path applies the sub-block shift to exact integer sums:
+    # weights that are all exactly zero still give exactly zero
+    qdq = cuda_lib
+    rng = np.random.default_rng(13)
+    wb = _cancelling_q4k(rng, 64, 1024, 1.0)
+    x = synth.activations(rng, 1, 1024)
+    with _FloatX(qdq, 0):
+        y = _gemv1(qdq, "q4k", wb, x, 64, 1024)
+    assert np.all(y == 0.0)
 
 
 @pytest.mark.parametrize("fx", [0, 1])

@@ -157,8 +157,8 @@ def test_options_and_strings(lib):
     assert lib.qdq_set_option(99, 1) == qdq.QDQ_ERR_DIMS
     assert lib.qdq_set_option(qdq.QDQ_OPT_CTAS_PER_SM, 9) == qdq.QDQ_ERR_DIMS
     assert lib.qdq_set_option(qdq.QDQ_OPT_XS_FLOAT_X, 2) == qdq.QDQ_ERR_DIMS
-    assert lib.qdq_set_option(qdq.QDQ_OPT_XS_FLOAT_X, 1) == 0  # fixed-point x is the default
-    assert lib.qdq_set_option(qdq.QDQ_OPT_XS_FLOAT_X, 0) == 1
+    assert lib.qdq_set_option(qdq.QDQ_OPT_XS_FLOAT_X, 0) == 1  # the f32 arithmetic is the default
+    assert lib.qdq_set_option(qdq.QDQ_OPT_XS_FLOAT_X, 1) == 0
     prev = lib.qdq_set_option(qdq.QDQ_OPT_PDL, 0)
     assert prev in (0, 1)
     assert lib.qdq_set_option(qdq.QDQ_OPT_PDL, prev) == 0

@@ -31,6 +31,24 @@ def test_oversize_request_is_refused_before_any_cuda_call():
     assert "scratch" in qdq.status_string(qdq.QDQ_ERR_SCRATCH)
 
 
+def test_bad_arguments_are_refused_before_the_scratch_lookup():
+    # NULL, misaligned and overlapping arguments get the same status as from the
+    # workspace entry point, before the call looks up its device array (so also
+    # on a machine without a GPU, where that lookup would fail)
+    from ggml_quantized_dequant_gb300 import _build
+    import ggml_quantized_dequant_gb300 as qdq
+    _build.build()
+    lib = qdq.load()
+    base = 0x10000000
+    wg, wu, wd, x, r, o = (base + i * (1 << 24) for i in range(6))  # distinct, 16-byte aligned
+    f = lib.qdq_q4k_ffn_residual_noalloc
+    assert f(wg, None, wd, x, r, o, 256, 512, 1, None) == qdq.QDQ_ERR_NULL
+    assert f(wg, wu, wd, x + 4, r, o, 256, 512, 1, None) == qdq.QDQ_ERR_ALIGN
+    assert f(wg, wu, wd, x, r, o, 300, 512, 1, None) == qdq.QDQ_ERR_DIMS
+    assert f(wg, wu, wd, x, r, x, 256, 512, 1, None) == qdq.QDQ_ERR_ALIAS
+    assert f(wg, wu, wd, x, r, o, 256, 512, 0, None) == qdq.QDQ_ERR_DIMS
+
+
 def _layer(rng, n_embd, n_ff):
     return (synth.q4k_blocks(rng, n_ff, n_embd), synth.q4k_blocks(rng, n_ff, n_embd),
             synth.q4k_blocks(rng, n_embd, n_ff))
