@@ -25,6 +25,7 @@ QDQ_ERR_ALIAS = -6
 QDQ_ERR_SCRATCH = -7
 QDQ_NOALLOC_FFN_MAX_MID = 262144
 QDQ_MAX_GEMV_BATCH = 8
+QDQ_MAX_TOPK = 64
 QDQ_MAX_GEMV_N_IN = 32768
 QDQ_OPT_PDL = 1
 QDQ_OPT_L2_PREFETCH = 2
@@ -56,6 +57,15 @@ SIGNATURES = {
                                       _c_int, _c_int, _c_int, _c_vp]),
     "qdq_q4k_ffn_residual_noalloc": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
                                               _c_int, _c_int, _c_int, _c_vp]),
+    "qdq_q6k_packed_bytes": (_c_size, [_c_int, _c_int]),
+    "qdq_q6k_pack": (_c_int, [_c_vp, _c_vp, _c_int, _c_int, _c_vp]),
+    "qdq_q6k_dequant": (_c_int, [_c_vp, _c_vp, _c_int, _c_int, _c_vp]),
+    "qdq_q6k_gemv": (_c_int, [_c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_vp]),
+    "qdq_q6k_get_rows": (_c_int, [_c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_vp]),
+    "qdq_topk_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int]),
+    "qdq_topk_rows": (_c_int, [_c_vp, _c_int, _c_int, _c_int, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "qdq_q8_0_logits_topk": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_int,
+                                      _c_vp]),
     "qdq_q8_0_gemm_batch_workspace_bytes": (_c_size, [_c_int, _c_int]),
     "qdq_q8_0_gemm_batch": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_vp]),
     "qdq_pipeline_timeouts": (_c_int, []),
@@ -192,6 +202,45 @@ def q4k_ffn_residual_noalloc(Wg, Wu, Wd, x, residual, out, n_embd: int, n_ff: in
                                               n_embd, n_ff, batch, _stream(stream)))
 
 
+def q6k_packed_bytes(n_out: int, n_in: int) -> int:
+    return int(lib().qdq_q6k_packed_bytes(n_out, n_in))
+
+
+def q6k_pack(ggml, packed, n_out: int, n_in: int, stream=None):
+    _check("qdq_q6k_pack", lib().qdq_q6k_pack(_ptr(ggml), _ptr(packed), n_out, n_in, _stream(stream)))
+
+
+def q6k_dequant(W, out, n_out: int, n_in: int, stream=None):
+    _check("qdq_q6k_dequant", lib().qdq_q6k_dequant(_ptr(W), _ptr(out), n_out, n_in, _stream(stream)))
+
+
+def q6k_gemv(W, x, y, n_out: int, n_in: int, batch: int = 1, stream=None):
+    _check("qdq_q6k_gemv", lib().qdq_q6k_gemv(_ptr(W), _ptr(x), _ptr(y), n_out, n_in, batch, _stream(stream)))
+
+
+def q6k_get_rows(W, ids, out, n_ids: int, n_rows: int, n_in: int, stream=None):
+    """Embedding lookup: ``out[i] = dequantised row ids[i]`` (int32 ids on the device)."""
+    _check("qdq_q6k_get_rows", lib().qdq_q6k_get_rows(_ptr(W), _ptr(ids), _ptr(out), n_ids, n_rows, n_in,
+                                                      _stream(stream)))
+
+
+def topk_workspace_bytes(n: int, batch: int, k: int) -> int:
+    return int(lib().qdq_topk_workspace_bytes(n, batch, k))
+
+
+def topk_rows(logits, n: int, batch: int, k: int, workspace, index, value, stream=None):
+    """Per row of ``logits``: the k best (index, value) pairs, NaN first, larger first, smaller index on ties."""
+    _check("qdq_topk_rows", lib().qdq_topk_rows(_ptr(logits), n, batch, k, _ptr(workspace), _ptr(index), _ptr(value),
+                                                _stream(stream)))
+
+
+def q8_0_logits_topk(W, x, logits, workspace, index, value, n_vocab: int, n_in: int, batch: int, k: int,
+                     stream=None):
+    _check("qdq_q8_0_logits_topk",
+           lib().qdq_q8_0_logits_topk(_ptr(W), _ptr(x), _ptr(logits), _ptr(workspace), _ptr(index), _ptr(value),
+                                      n_vocab, n_in, batch, k, _stream(stream)))
+
+
 def q8_0_gemm_batch_workspace_bytes(M: int, n_in: int) -> int:
     return int(lib().qdq_q8_0_gemm_batch_workspace_bytes(M, n_in))
 
@@ -221,6 +270,15 @@ def upload_q8_0(ggml_bytes, n_out: int, n_in: int, device="cuda", stream=None):
     raw = torch.as_tensor(ggml_bytes, dtype=torch.uint8).reshape(-1).to(device)
     packed = torch.empty(q8_0_packed_bytes(n_out, n_in), dtype=torch.uint8, device=device)
     q8_0_pack(raw, packed, n_out, n_in, stream)
+    return packed
+
+
+def upload_q6k(ggml_bytes, n_out: int, n_in: int, device="cuda", stream=None):
+    """Copy raw GGML Q6_K bytes (numpy uint8 or torch) to the device and repack them; returns the packed tensor."""
+    import torch
+    raw = torch.as_tensor(ggml_bytes, dtype=torch.uint8).reshape(-1).to(device)
+    packed = torch.empty(q6k_packed_bytes(n_out, n_in), dtype=torch.uint8, device=device)
+    q6k_pack(raw, packed, n_out, n_in, stream)
     return packed
 
 

@@ -138,6 +138,21 @@ bool dims_q4k(int n_out, int n_in) { return n_out > 0 && n_in > 0 && (n_in % 256
 
 size_t q8_bytes(int n_out, int n_in) { return size_t(n_out) * size_t(n_in / 32) * 34; }
 size_t q4k_bytes(int n_out, int n_in) { return size_t(n_out) * size_t(n_in / 256) * 144; }
+size_t q6k_ggml_bytes(int n_out, int n_in) { return size_t(n_out) * size_t(n_in / 256) * 210; }
+size_t q6k_bytes(int n_out, int n_in) { return size_t(n_out) * size_t(q6k_row_bytes(n_in)); }
+
+// Arguments of a top-k over `batch` rows of n logits (qdq_topk_rows).
+int check_topk(const float *logits, int n, int batch, int k, const void *ws, const int *index, const float *value) {
+  if (!logits || !ws || !index || !value) return QDQ_ERR_NULL;
+  if (n < 1 || batch < 1 || k < 1 || k > n) return QDQ_ERR_DIMS;
+  if (k > QDQ_MAX_TOPK) return QDQ_ERR_UNSUPPORTED;
+  if (!aligned(logits, 4) || !aligned(ws, 16) || !aligned(index, 4) || !aligned(value, 4)) return QDQ_ERR_ALIGN;
+  const size_t lb = size_t(batch) * n * 4, wb = topk_workspace_bytes(n, batch, k), rb = size_t(batch) * k * 4;
+  if (overlaps(ws, wb, logits, lb) || overlaps(index, rb, logits, lb) || overlaps(value, rb, logits, lb) ||
+      overlaps(index, rb, ws, wb) || overlaps(value, rb, ws, wb) || overlaps(index, rb, value, rb))
+    return QDQ_ERR_ALIAS;
+  return QDQ_OK;
+}
 
 int check_gemv_common(const void *W, const float *x, const float *y, int n_out, int n_in, int batch,
                       size_t w_bytes) {
@@ -287,6 +302,71 @@ int qdq_q8_0_logits_argmax(const void *W, const float *x, float *logits, int *in
   const int r = launch_q8_0_gemv(W, x, logits, n_vocab, n_in, batch, stream);
   if (r != QDQ_OK) return r;
   return launch_argmax_rows(logits, n_vocab, batch, index, value, stream);
+}
+
+size_t qdq_q6k_packed_bytes(int n_out, int n_in) { return dims_q4k(n_out, n_in) ? q6k_bytes(n_out, n_in) : 0; }
+
+int qdq_q6k_pack(const void *ggml, void *packed, int n_out, int n_in, cudaStream_t stream) {
+  if (!ggml || !packed) return QDQ_ERR_NULL;
+  if (!dims_q4k(n_out, n_in)) return QDQ_ERR_DIMS;
+  if (!aligned(packed, 16)) return QDQ_ERR_ALIGN;
+  if (overlaps(ggml, q6k_ggml_bytes(n_out, n_in), packed, q6k_bytes(n_out, n_in))) return QDQ_ERR_ALIAS;
+  return launch_q6k_pack(ggml, packed, n_out, n_in, stream);
+}
+
+int qdq_q6k_dequant(const void *W, float *out, int n_out, int n_in, cudaStream_t stream) {
+  if (!W || !out) return QDQ_ERR_NULL;
+  if (!dims_q4k(n_out, n_in)) return QDQ_ERR_DIMS;
+  if (!aligned(W, 16) || !aligned(out, 4)) return QDQ_ERR_ALIGN;
+  if (overlaps(out, size_t(n_out) * n_in * 4, W, q6k_bytes(n_out, n_in))) return QDQ_ERR_ALIAS;
+  return launch_q6k_dequant(W, out, n_out, n_in, stream);
+}
+
+int qdq_q6k_gemv(const void *W, const float *x, float *y, int n_out, int n_in, int batch, cudaStream_t stream) {
+  if (!dims_q4k(n_out, n_in)) return (!W || !x || !y) ? QDQ_ERR_NULL : QDQ_ERR_DIMS;
+  const int rc = check_gemv_common(W, x, y, n_out, n_in, batch, q6k_bytes(n_out, n_in));
+  if (rc != QDQ_OK) return rc;
+  return launch_q6k_gemv(W, x, y, n_out, n_in, batch, stream);
+}
+
+int qdq_q6k_get_rows(const void *W, const int *ids, float *out, int n_ids, int n_rows, int n_in, cudaStream_t stream) {
+  if (!W || !ids || !out) return QDQ_ERR_NULL;
+  if (n_ids < 0 || !dims_q4k(n_rows, n_in)) return QDQ_ERR_DIMS;
+  if (!aligned(W, 16) || !aligned(ids, 4) || !aligned(out, 4)) return QDQ_ERR_ALIGN;
+  const size_t ob = size_t(n_ids) * n_in * 4;
+  if (overlaps(out, ob, W, q6k_bytes(n_rows, n_in)) || overlaps(out, ob, ids, size_t(n_ids) * 4)) return QDQ_ERR_ALIAS;
+  if (n_ids == 0) return QDQ_OK;  // nothing to look up
+  return launch_q6k_get_rows(W, ids, out, n_ids, n_rows, n_in, stream);
+}
+
+size_t qdq_topk_workspace_bytes(int n, int batch, int k) {
+  if (n < 1 || batch < 1 || k < 1 || k > n || k > QDQ_MAX_TOPK) return 0;
+  return topk_workspace_bytes(n, batch, k);
+}
+
+int qdq_topk_rows(const float *logits, int n, int batch, int k, void *workspace, int *index, float *value,
+                  cudaStream_t stream) {
+  const int rc = check_topk(logits, n, batch, k, workspace, index, value);
+  if (rc != QDQ_OK) return rc;
+  return launch_topk_rows(logits, n, batch, k, workspace, index, value, stream);
+}
+
+int qdq_q8_0_logits_topk(const void *W, const float *x, float *logits, void *workspace, int *index, float *value,
+                         int n_vocab, int n_in, int batch, int k, cudaStream_t stream) {
+  if (!W || !x || !logits || !workspace || !index || !value) return QDQ_ERR_NULL;
+  if (!dims_q8(n_vocab, n_in)) return QDQ_ERR_DIMS;
+  int rc = check_gemv_common(W, x, logits, n_vocab, n_in, batch, q8_bytes(n_vocab, n_in));
+  if (rc != QDQ_OK) return rc;
+  rc = check_topk(logits, n_vocab, batch, k, workspace, index, value);
+  if (rc != QDQ_OK) return rc;
+  const size_t wb = q8_bytes(n_vocab, n_in), xb = size_t(batch) * n_in * 4, rb = size_t(batch) * k * 4;
+  const size_t sb = topk_workspace_bytes(n_vocab, batch, k);
+  if (overlaps(workspace, sb, W, wb) || overlaps(workspace, sb, x, xb) || overlaps(index, rb, W, wb) ||
+      overlaps(index, rb, x, xb) || overlaps(value, rb, W, wb) || overlaps(value, rb, x, xb))
+    return QDQ_ERR_ALIAS;
+  rc = launch_q8_0_gemv(W, x, logits, n_vocab, n_in, batch, stream);
+  if (rc != QDQ_OK) return rc;
+  return launch_topk_rows(logits, n_vocab, batch, k, workspace, index, value, stream);
 }
 
 int qdq_q4k_qkv(const void *Wq, const void *Wk, const void *Wv, const float *x, float *q, float *k, float *v,

@@ -69,7 +69,7 @@ namespace {
 constexpr int kStageRows = 4;    // virtual rows per stage = butterfly width
 constexpr int kMaxThreads = 544;  // up to 16 consumer warps + the producer
 
-enum Fmt { kQ8 = 0, kQ4 = 1 };
+enum Fmt { kQ8 = 0, kQ4 = 1, kQ6 = 2 };
 enum Epi { kPlain = 0, kSwiglu = 1, kResidual = 2, kQkv = 3 };
 enum Arith { kFixedX = 0, kFloatX = 1 };
 
@@ -240,8 +240,9 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
   auto gstages = [&](int g) { return ((gbeg(g + 1) - gbeg(g)) * kV + kStageRows - 1) / kStageRows; };
   constexpr int kRowsPerStage = kStageRows / kV;
 
-  const int64_t q_row = FMT == kQ8 ? int64_t(n_in) : int64_t(n_in >> 1);                  // quant bytes per row
-  const int64_t s_row = FMT == kQ8 ? int64_t(n_in >> 4) : int64_t(n_in >> 8) * 16;      // scale/header bytes per row
+  // quant bytes and scale/header bytes per row (Q6_K: the whole padded row, one plane)
+  const int64_t q_row = FMT == kQ8 ? int64_t(n_in) : FMT == kQ4 ? int64_t(n_in >> 1) : q6k_row_bytes(n_in);
+  const int64_t s_row = FMT == kQ8 ? int64_t(n_in >> 4) : FMT == kQ4 ? int64_t(n_in >> 8) * 16 : 0;
   const int64_t q_bytes = int64_t(a.n_out) * q_row;
 
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + size_t(S) * a.stage_bytes);
@@ -326,7 +327,7 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
             }
           } else {
             bulk_copy_g2s(stq, a.W + rr * q_row, uint32_t(nr * q_row), &full[s]);
-            bulk_copy_g2s(sts, a.W + q_bytes + rr * s_row, uint32_t(nr * s_row), &full[s]);
+            if (FMT != kQ6) bulk_copy_g2s(sts, a.W + q_bytes + rr * s_row, uint32_t(nr * s_row), &full[s]);
           }
           if (EPI == kSwiglu) {  // up rows go to slots 2, 3
             bulk_copy_g2s(stq + 2 * q_row, a.W2 + rr * q_row, uint32_t(nr * q_row), &full[s]);
@@ -387,7 +388,10 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
     // a lane past the end of the row reads block 0 (finite data) against x = 0
     const int bq = valid ? blk : 0;
     const int qoff = FMT == kQ8 ? bq * 32 : bq * 16;
-    const int soff = FMT == kQ8 ? bq * 2 : (bq >> 3) * 16;
+    const int soff = FMT == kQ8 ? bq * 2 : FMT == kQ4 ? (bq >> 3) * 16 : 0;
+    // Q6_K: this lane's high-bit, scale and d bytes within the packed row
+    const int q6_hi = (n_in >> 1) + 8 * bq, q6_sc = (n_in >> 1) + (n_in >> 2) + 2 * bq;
+    const int q6_d = (n_in >> 1) + (n_in >> 2) + (n_in >> 4) + 2 * (bq >> 3);
     // byte offsets of this lane's data for the 4 rows of a stage (the same in every stage);
     // SwiGLU: virtual rows gate r, up r, gate r+1, up r+1 sit in slots 0, 2, 1, 3
     int qofs[kStageRows], sofs[kStageRows];
@@ -414,7 +418,7 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
       // refill) and the producer refills it while this warp computes.  Measured on
       // 3072 <-> 8192 chains, that helps there but slows the SwiGLU and the Q8_0 GEMV,
       // which release after their arithmetic.
-      constexpr bool kEarlyRelease = FMT == kQ4 && EPI != kSwiglu;
+      constexpr bool kEarlyRelease = (FMT == kQ4 || FMT == kQ6) && EPI != kSwiglu;
       auto release = [&](int slot) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
@@ -477,6 +481,37 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
             part[k] = dv[k] * (st.x + st.y);
           }
         }
+      } else if constexpr (FMT == kQ6) {
+        // f32 only: each block is two 16-weight sub-blocks, scaled once each by the
+        // exact d * scale (no offset term, so the error is relative to sum |w||x|)
+        uint4 ql[kStageRows];
+        uint2 qh[kStageRows];
+        float ds0[kStageRows], ds1[kStageRows];
+#pragma unroll
+        for (int k = 0; k < kStageRows; ++k) {
+          const uint8_t *rw = stq + qofs[k] - qoff;  // the row's first byte in the stage
+          ql[k] = *reinterpret_cast<const uint4 *>(rw + qoff);
+          qh[k] = *reinterpret_cast<const uint2 *>(rw + q6_hi);
+          const uint32_t sc2 = *reinterpret_cast<const uint16_t *>(rw + q6_sc);
+          const float d = __half2float(*reinterpret_cast<const __half *>(rw + q6_d));
+          ds0[k] = __fmul_rn(d, float(int8_t(sc2 & 0xFFu)));
+          ds1[k] = __fmul_rn(d, float(int8_t(sc2 >> 8)));
+        }
+        if (kEarlyRelease) release(s);
+        float2 a0[kStageRows], a1[kStageRows];
+#pragma unroll
+        for (int k = 0; k < kStageRows; ++k) a0[k] = a1[k] = f2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < kStageRows; ++k) {
+          float2 v[16];
+          q6k_block_to_f2(ql[k], qh[k], mg, v);
+#pragma unroll
+          for (int p = 0; p < 8; ++p) a0[k] = __ffma2_rn(v[p], xr[p], a0[k]);
+#pragma unroll
+          for (int p = 8; p < 16; ++p) a1[k] = __ffma2_rn(v[p], xr[p], a1[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < kStageRows; ++k) part[k] = fmaf(ds1[k], a1[k].x + a1[k].y, ds0[k] * (a0[k].x + a0[k].y));
       } else {
         uint4 q[kStageRows], h[kStageRows];
 #pragma unroll
@@ -647,8 +682,8 @@ int launch_xs_ar(XsArgs a, cudaStream_t s, const DeviceInfo &di) {
   if (32 * (a.wpr * a.groups + 1) > kMaxThreads) return QDQ_ERR_UNSUPPORTED;
   const int pf = opt_l2_prefetch();
   a.l2_prefetch = EPI == kQkv ? 0 : pf == 3 ? 0 : pf;
-  const int64_t q_row = FMT == kQ8 ? n_in : n_in / 2;
-  const int64_t s_row = FMT == kQ8 ? n_in / 16 : (n_in / 256) * 16;
+  const int64_t q_row = FMT == kQ8 ? n_in : FMT == kQ4 ? n_in / 2 : q6k_row_bytes(n_in);
+  const int64_t s_row = FMT == kQ8 ? n_in / 16 : FMT == kQ4 ? (n_in / 256) * 16 : 0;
   a.stage_bytes = int((kStageRows * (q_row + s_row) + 127) / 128 * 128);
   // The FFN kernels (SwiGLU, down + residual) run two CTAs per SM with two ring slots
   // per group: both CTAs compute at once instead of one computing beside the next
@@ -690,18 +725,20 @@ int launch_xs_ar(XsArgs a, cudaStream_t s, const DeviceInfo &di) {
 
 template <int FMT, int EPI>
 int launch_xs(const XsArgs &a, cudaStream_t s, const DeviceInfo &di) {
-  return opt_xs_float_x() ? launch_xs_ar<FMT, EPI, kFloatX>(a, s, di) : launch_xs_ar<FMT, EPI, kFixedX>(a, s, di);
+  if constexpr (FMT == kQ6) return launch_xs_ar<FMT, EPI, kFloatX>(a, s, di);  // Q6_K: f32 arithmetic only
+  else
+    return opt_xs_float_x() ? launch_xs_ar<FMT, EPI, kFloatX>(a, s, di) : launch_xs_ar<FMT, EPI, kFixedX>(a, s, di);
 }
 
 }  // namespace
 
-bool gemv_xs_supported(int n_in, int batch, int fmt_q4k) {
+bool gemv_xs_supported(int n_in, int batch, int fmt) {
   // one 32-weight block per lane and at most 16 slice warps per row; stage copies of
   // the Q8_0 scale plane start on 16-byte boundaries only when n_in % 256 == 0
-  return batch == 1 && (n_in >> 5) <= 32 * 16 && (fmt_q4k || n_in % 256 == 0);
+  return batch == 1 && (n_in >> 5) <= 32 * 16 && (fmt != 0 || n_in % 256 == 0);
 }
 
-int launch_gemv_xs(int fmt_q4k, int mode, const void *W, const void *W2, const float *x, const float *residual,
+int launch_gemv_xs(int fmt, int mode, const void *W, const void *W2, const float *x, const float *residual,
                    float *y, int n_out, int n_in, cudaStream_t s) {
   DeviceInfo di;
   const cudaError_t e = device_info(&di);
@@ -714,7 +751,8 @@ int launch_gemv_xs(int fmt_q4k, int mode, const void *W, const void *W2, const f
   a.y = y;
   a.n_out = n_out;
   a.n_in = n_in;
-  if (!fmt_q4k) return launch_xs<kQ8, kPlain>(a, s, di);
+  if (fmt == 0) return launch_xs<kQ8, kPlain>(a, s, di);
+  if (fmt == 2) return launch_xs<kQ6, kPlain>(a, s, di);
   if (mode == 1) return launch_xs<kQ4, kSwiglu>(a, s, di);
   if (mode == 2) return launch_xs<kQ4, kResidual>(a, s, di);
   return launch_xs<kQ4, kPlain>(a, s, di);

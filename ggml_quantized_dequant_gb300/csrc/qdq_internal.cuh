@@ -99,14 +99,24 @@ int launch_q8_0_gemv(const void *W, const float *x, float *y, int n_out, int n_i
 // mode 2: y = residual + W x.
 int launch_q4k_gemv(int mode, const void *W, const void *W2, const float *x, const float *residual,
                     float *y, int n_out, int n_in, int batch, cudaStream_t s);
-// Batch-1 "x-stationary" GEMV fast path (qdq_gemv_xs.cu); fmt_q4k 0 = Q8_0,
-// 1 = Q4_K with mode 0/1/2 as launch_q4k_gemv.
-bool gemv_xs_supported(int n_in, int batch, int fmt_q4k);
+// Batch-1 "x-stationary" GEMV fast path (qdq_gemv_xs.cu); fmt 0 = Q8_0,
+// 1 = Q4_K with mode 0/1/2 as launch_q4k_gemv, 2 = Q6_K (mode 0).
+bool gemv_xs_supported(int n_in, int batch, int fmt);
 // Fused Q4_K QKV projection at batch 1 (n_in as gemv_xs_supported allows for Q4_K).
 int launch_gemv_xs_qkv(const void *Wq, const void *Wk, const void *Wv, const float *x, float *q, float *k, float *v,
                        int n_q, int n_kv, int n_in, cudaStream_t s);
-int launch_gemv_xs(int fmt_q4k, int mode, const void *W, const void *W2, const float *x, const float *residual,
+int launch_gemv_xs(int fmt, int mode, const void *W, const void *W2, const float *x, const float *residual,
                    float *y, int n_out, int n_in, cudaStream_t s);
+// Top-k of each row of a logits matrix (qdq_topk.cu); the workspace holds the
+// candidate keys of two merge rounds.
+size_t topk_workspace_bytes(int n, int batch, int k);
+int launch_topk_rows(const float *logits, int n, int batch, int k, void *workspace, int *index, float *value,
+                     cudaStream_t s);
+// Q6_K (qdq_q6k.cu): repack, dequantisation, embedding-row lookup, GEMV (batch 1..8).
+int launch_q6k_pack(const void *ggml, void *packed, int n_out, int n_in, cudaStream_t s);
+int launch_q6k_dequant(const void *W, float *out, int n_out, int n_in, cudaStream_t s);
+int launch_q6k_get_rows(const void *W, const int *ids, float *out, int n_ids, int n_rows, int n_in, cudaStream_t s);
+int launch_q6k_gemv(const void *W, const float *x, float *y, int n_out, int n_in, int batch, cudaStream_t s);
 // Pipeline-timeout counters of the translation units that run bounded waits:
 // each returns its count since the last call and resets it (-1 on CUDA error).
 int read_gemm_timeouts();
@@ -228,6 +238,13 @@ __device__ __forceinline__ float4 ld_after_wait(const float4 *p) {
   return v;
 }
 
+// 32-bit coherent load of data an earlier kernel wrote (see ld_after_wait).
+__device__ __forceinline__ int ld_s32_after_wait(const int *p) {
+  int v;
+  asm volatile("ld.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // 128-bit read-only load that does not allocate in L1 (streamed weights).
 __device__ __forceinline__ uint4 ldg_stream(const void *p) {
   uint4 v;
@@ -269,6 +286,7 @@ struct Magic {
   uint32_t u4_0, u4_1, u4_2, u4_3;    // Q4_K: nibble 0..3 of a half: 2^23, 2^19, 2^15, 2^11
   uint32_t sc, m;                     // Q4_K header: 6-bit scale at bit 0 (2^23), 6-bit min at bit 6 (2^17)
   float2 b_s8, b_u4_01, b_u4_23, b_scm;  // subtraction constants
+  float2 b_q6;                        // Q6_K: unsigned byte 0 / byte 1 at 2^23, 2^15, minus the offset 32
 };
 inline Magic make_magic() {
   Magic k;
@@ -284,6 +302,7 @@ inline Magic make_magic() {
   k.b_u4_01 = make_float2(-8388608.0f, -524288.0f);  // -2^23, -2^19
   k.b_u4_23 = make_float2(-32768.0f, -2048.0f);      // -2^15, -2^11
   k.b_scm = make_float2(-8388608.0f, -131072.0f);    // -2^23, -2^17
+  k.b_q6 = make_float2(-8388640.0f, -32800.0f);      // -(2^23 + 32), -(2^15 + 32)
   return k;
 }
 __device__ __forceinline__ uint32_t lane_reg(uint32_t v) { return __shfl_sync(0xffffffffu, v, threadIdx.x & 31); }
@@ -302,6 +321,7 @@ __device__ __forceinline__ Magic lane_magic(const Magic &k) {
   r.b_u4_01 = f2(lane_regf(k.b_u4_01.x), lane_regf(k.b_u4_01.y));
   r.b_u4_23 = f2(lane_regf(k.b_u4_23.x), lane_regf(k.b_u4_23.y));
   r.b_scm = f2(lane_regf(k.b_scm.x), lane_regf(k.b_scm.y));
+  r.b_q6 = f2(lane_regf(k.b_q6.x), lane_regf(k.b_q6.y));
   return r;
 }
 
@@ -330,6 +350,35 @@ __device__ __forceinline__ void u4x8_to_f2_shifted(uint32_t w, const Magic &k, f
   q[1] = __fadd2_rn(f2_bits(lop3_and_or<0x0F00u>(w, k.u4_2), lop3_and_or<0xF000u>(w, k.u4_3)), b23);
   q[2] = __fadd2_rn(f2_bits(lop3_and_or<0x000Fu>(h, k.u4_0), lop3_and_or<0x00F0u>(h, k.u4_1)), b01);
   q[3] = __fadd2_rn(f2_bits(lop3_and_or<0x0F00u>(h, k.u4_2), lop3_and_or<0xF000u>(h, k.u4_3)), b23);
+}
+
+// Q6_K packed block of 32 weights (the layout qdq_q6k_pack writes): `ql` holds
+// the low 4 bits -- byte b of word c has weight 8c+b in its low nibble and
+// weight 8c+4+b in its high nibble -- and `qh` the high 2 bits -- byte b of word
+// h has those of weights 16h+b, 16h+4+b, 16h+8+b, 16h+12+b at bits 0-1, 2-3,
+// 4-5, 6-7.  Returns the exact floats q - 32 of weights (2p, 2p+1) in v[p].
+__device__ __forceinline__ void q6k_block_to_f2(uint4 ql, uint2 qh, const Magic &k, float2 v[16]) {
+  const uint32_t lw[4] = {ql.x, ql.y, ql.z, ql.w};
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t H = (c >> 1) ? qh.y : qh.x;
+    const uint32_t hlo = (c & 1) ? H : (H << 4);        // high bits of weights 8c..8c+3 at bits 4-5
+    const uint32_t hhi = (c & 1) ? (H >> 2) : (H << 2);  // of weights 8c+4..8c+7
+    const uint32_t ev = (lw[c] & 0x0F0F0F0Fu) | (hlo & 0x30303030u);         // bytes = q of 8c..8c+3
+    const uint32_t od = ((lw[c] >> 4) & 0x0F0F0F0Fu) | (hhi & 0x30303030u);  // bytes = q of 8c+4..8c+7
+    const uint32_t e2 = ev >> 16, o2 = od >> 16;
+    v[4 * c + 0] = __fadd2_rn(f2_bits(lop3_and_or<0x00FFu>(ev, k.u4_0), lop3_and_or<0xFF00u>(ev, k.u4_2)), k.b_q6);
+    v[4 * c + 1] = __fadd2_rn(f2_bits(lop3_and_or<0x00FFu>(e2, k.u4_0), lop3_and_or<0xFF00u>(e2, k.u4_2)), k.b_q6);
+    v[4 * c + 2] = __fadd2_rn(f2_bits(lop3_and_or<0x00FFu>(od, k.u4_0), lop3_and_or<0xFF00u>(od, k.u4_2)), k.b_q6);
+    v[4 * c + 3] = __fadd2_rn(f2_bits(lop3_and_or<0x00FFu>(o2, k.u4_0), lop3_and_or<0xFF00u>(o2, k.u4_2)), k.b_q6);
+  }
+}
+
+// Bytes of one packed Q6_K row of n_in weights: the low-bit plane (n_in/2), the
+// high-bit plane (n_in/4), the int8 scales (n_in/16) and the fp16 d (n_in/128),
+// padded to a multiple of 16 bytes.
+__host__ __device__ __forceinline__ int64_t q6k_row_bytes(int n_in) {
+  return (int64_t(n_in) / 256 * 210 + 15) / 16 * 16;
 }
 
 // Q4_K header field (sc in bits 0..5, m in bits 6..11) -> (sc, m) as floats.

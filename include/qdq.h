@@ -13,6 +13,10 @@
  *   "Module cuda_lane", Goal (batch prefill-shaped GEMMs on tensor cores) and
  *   "weight_cache.rs", try_cuda_batch_gemv          -> qdq_q8_0_gemm_batch
  *   "QTensorEngine", dispatch_output_top1_chunked   -> qdq_q8_0_logits_argmax
+ *   "QTensorEngine", dispatch_output_topk_chunked   -> qdq_topk_rows / qdq_q8_0_logits_topk
+ *   "QTensorEngine", embedding_pipeline (Q6_K dequant + matmul on the GPU),
+ *     dispatch_quantized_token_embedding, dispatch_gemm_into (Q6_K)
+ *                                                   -> qdq_q6k_pack / _gemv / _get_rows
  *
  * Conventions for every call
  *   - W is row-major n_out x n_in (rows = outputs, the GGML convention).
@@ -25,7 +29,7 @@
  *   - Calls return QDQ_OK or a negative status.  On a rejected argument (every
  *     status but QDQ_ERR_CUDA) nothing has been launched and every output
  *     buffer is untouched.  QDQ_ERR_CUDA from a call that launches several
- *     kernels (the FFN block, the batch GEMM, the argmax, QKV at batch > 1) can leave the
+ *     kernels (the FFN block, the batch GEMM, the argmax and top-k, QKV at batch > 1) can leave the
  *     kernels before the failing launch enqueued.  There is no fallback path:
  *     an unsupported shape is an error, never a silent slower route.
  *   - Kernels are launched with programmatic dependent launch: a kernel may
@@ -37,6 +41,12 @@
  *   Q4_K: 144-byte superblock per 256 weights: fp16 d, fp16 dmin, 12 bytes of
  *         eight 6-bit scales sc_j and eight 6-bit mins m_j, 128 bytes of 4-bit
  *         quants; sub-block j = weights 32j..32j+31; w = d*sc_j*q - dmin*m_j.
+ *   Q6_K: 210-byte superblock per 256 weights: ql[128] (low 4 bits of each
+ *         quant), qh[64] (high 2 bits), sixteen int8 scales, fp16 d (at byte
+ *         208); weight e = d*scale[e/16]*(q_e - 32), q_e in 0..63, where weight
+ *         128h + 32t + l (h < 2, t < 4, l < 32) takes its low 4 bits from the low
+ *         (t < 2) or high (t >= 2) nibble of ql[64h + 32(t & 1) + l] and its high
+ *         2 bits from bits 2t..2t+1 of qh[32h + l].
  *
  * Packed (device) formats -- produced once by qdq_*_pack, same byte count as
  * the GGML input, laid out as planes so that every kernel load is a 16-byte
@@ -49,6 +59,14 @@
  *                  word0 = d | dmin << 16 (fp16 bits); words 1..3 form a
  *                  96-bit little-endian field with sc_j at bits 12j..12j+5
  *                  and m_j at bits 12j+6..12j+11 ]
+ *   Q6_K packed: rows of qdq_q6k_packed_bytes(1, n_in) bytes (the 210/256
+ *                bytes per weight padded to a multiple of 16; no padding when
+ *                n_in % 2048 == 0): [ low-bit plane n_in/2 | high-bit plane
+ *                n_in/4 | int8 scales n_in/16 | fp16 d n_in/128 | zeros ];
+ *                32-weight block b: low bits at 16b (byte i of word c: weight
+ *                8c+i in the low nibble, 8c+4+i in the high nibble), high bits
+ *                at n_in/2 + 8b (byte i of word h: weights 16h+i, 16h+4+i,
+ *                16h+8+i, 16h+12+i at bits 0-1, 2-3, 4-5, 6-7).
  */
 #ifndef QDQ_H
 #define QDQ_H
@@ -130,6 +148,29 @@ int qdq_q4k_gemv(const void *W, const float *x, float *y,
 int qdq_q4k_swiglu(const void *Wg, const void *Wu, const float *x, float *mid,
                    int n_ff, int n_embd, int batch, cudaStream_t stream);
 
+/* ---- Q6_K: repack, dequantisation, GEMV, embedding lookup -------------------
+ * "QTensorEngine": embedding_pipeline (Q6_K embedding dequant + matmul on the
+ * GPU, no CPU dequant), dispatch_quantized_token_embedding (raw quantised
+ * embedding bytes uploaded, used without CPU dequant) and dispatch_gemm_into
+ * (quantised GEMM into the caller's buffer, Q6_K).
+ * qdq_q6k_packed_bytes: bytes of the packed matrix (0 on bad dims: n_in % 256).
+ * qdq_q6k_pack: as qdq_q4k_pack, for GGML Q6_K input (n_out*n_in/256*210 bytes).
+ * qdq_q6k_dequant: w = d*scale*(q - 32), exact in f32, into `out` (n_out x n_in).
+ * qdq_q6k_gemv: as qdq_q8_0_gemv (same pointer, alignment, aliasing and batch
+ *   rules); error <= 1e-5 * sum_k |w[r,k]| |x[b,k]| for every finite input.
+ * qdq_q6k_get_rows: embedding lookup, out[i, :] = the dequantised row ids[i] of
+ *   the packed n_rows x n_in matrix W, for i < n_ids (0 = nothing to do).  ids:
+ *   int32 device array (4-byte aligned), read after the previous kernel on the
+ *   stream; an id outside [0, n_rows) gives a row of NaN.  out: n_ids x n_in
+ *   f32 (4-byte aligned), must not overlap W or ids.
+ */
+size_t qdq_q6k_packed_bytes(int n_out, int n_in);
+int qdq_q6k_pack(const void *ggml, void *packed, int n_out, int n_in, cudaStream_t stream);
+int qdq_q6k_dequant(const void *W, float *out, int n_out, int n_in, cudaStream_t stream);
+int qdq_q6k_gemv(const void *W, const float *x, float *y, int n_out, int n_in, int batch, cudaStream_t stream);
+int qdq_q6k_get_rows(const void *W, const int *ids, float *out, int n_ids, int n_rows, int n_in,
+                     cudaStream_t stream);
+
 /* ---- output projection with on-device argmax --------------------------------
  * "QTensorEngine", dispatch_output_top1_chunked (GPU block argmax, k = 1): the
  * output projection with an on-device argmax epilogue, so a decode step reads
@@ -145,6 +186,26 @@ int qdq_q4k_swiglu(const void *Wg, const void *Wu, const float *x, float *mid,
  */
 int qdq_q8_0_logits_argmax(const void *W, const float *x, float *logits, int *index, float *value,
                            int n_vocab, int n_in, int batch, cudaStream_t stream);
+
+/* ---- on-device top-k of the logits --------------------------------------------
+ * "QTensorEngine", dispatch_output_topk_chunked (the logits stay on the GPU, a
+ * top-k kernel reduces them per chunk, only K (id, logit) candidates are read
+ * back).  For each of `batch` rows of n logits (row-major, 4-byte aligned):
+ * index[b, j], value[b, j] (j < k, int32 / f32, 4-byte aligned) = the j-th entry
+ * of the order NaN first (the first NaN first), then larger logits first, equal
+ * logits (+0 == -0) by smaller index; value holds the logit's exact bits.
+ * 1 <= k <= min(n, QDQ_MAX_TOPK).  workspace: qdq_topk_workspace_bytes(n, batch,
+ * k) bytes of caller scratch (16-byte aligned, overwritten).  Outputs and
+ * workspace may overlap nothing.  Several kernels on `stream`.
+ * qdq_q8_0_logits_topk: the Q8_0 output projection (as qdq_q8_0_logits_argmax)
+ * followed by the top-k; logits: batch x n_vocab scratch the caller owns.
+ */
+#define QDQ_MAX_TOPK 64
+size_t qdq_topk_workspace_bytes(int n, int batch, int k);   /* 0 on bad arguments */
+int qdq_topk_rows(const float *logits, int n, int batch, int k, void *workspace, int *index, float *value,
+                  cudaStream_t stream);
+int qdq_q8_0_logits_topk(const void *W, const float *x, float *logits, void *workspace, int *index, float *value,
+                         int n_vocab, int n_in, int batch, int k, cudaStream_t stream);
 
 /* ---- fused QKV projection ---------------------------------------------------
  * "Module cuda_lane", Functions: try_q4k_soa_qkv (one activation, one fused

@@ -9,11 +9,15 @@ from .ggml_oracle import (  # noqa: F401
     q8_0_dequant,
     q4k_scales_mins,
     q4k_dequant,
+    q6k_quants,
+    q6k_dequant,
+    get_rows,
     gemv,
     silu,
     swiglu,
     ffn_residual,
     qkv,
     logits_argmax,
+    logits_topk,
     gemm_batch,
 )

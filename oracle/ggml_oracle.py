@@ -166,6 +166,73 @@ def q4k_dequant(raw, n_out: int, n_in: int) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
+# Q6_K
+# ---------------------------------------------------------------------------
+
+
+def q6k_quants(ql: np.ndarray, qh: np.ndarray) -> np.ndarray:
+    """The 6-bit quants ``q`` (0..63) of Q6_K superblocks, ``(..., 256)`` int64.
+
+    ``ql``: ``(..., 128)`` bytes of low 4-bit parts, ``qh``: ``(..., 64)`` bytes of
+    high 2-bit parts.  The superblock is two halves h = 0, 1 of 128 weights, each
+    using ``ql[64h .. 64h+63]`` and ``qh[32h .. 32h+31]``; inside a half, weight
+    ``32t + l`` (t = 0..3, l = 0..31) takes
+      low 4 bits:  t = 0: low nibble of ql[64h + l],   t = 1: low nibble of ql[64h + 32 + l],
+                   t = 2: high nibble of ql[64h + l],  t = 3: high nibble of ql[64h + 32 + l];
+      high 2 bits: bits 2t, 2t+1 of qh[32h + l].
+    """
+    ql = np.asarray(ql, dtype=np.uint8).astype(np.int64)
+    qh = np.asarray(qh, dtype=np.uint8).astype(np.int64)
+    q = np.empty(ql.shape[:-1] + (256,), dtype=np.int64)
+    for h in range(2):
+        for t in range(4):
+            lo_src = ql[..., 64 * h + 32 * (t & 1): 64 * h + 32 * (t & 1) + 32]
+            lo = (lo_src & 0x0F) if t < 2 else (lo_src >> 4)
+            hi = (qh[..., 32 * h: 32 * h + 32] >> (2 * t)) & 3
+            q[..., 128 * h + 32 * t: 128 * h + 32 * t + 32] = lo | (hi << 4)
+    return q
+
+
+def q6k_dequant(raw, n_out: int, n_in: int) -> np.ndarray:
+    """Dequantise a row-major GGML Q6_K matrix to f32, shape ``(n_out, n_in)``.
+
+    Superblock of 210 bytes for 256 weights: ``ql`` (128 bytes of low 4-bit
+    parts) @0, ``qh`` (64 bytes of high 2-bit parts) @128, sixteen int8 scales
+    @192, fp16 ``d`` @208.  Weight ``e`` of the superblock has the 6-bit quant
+    ``q_e`` of :func:`q6k_quants` and belongs to the 16-weight sub-block
+    ``e // 16``: its value is ``d * scales[e // 16] * (q_e - 32)``.
+
+    Exactness: ``d`` has at most 11 significant bits, ``|scale| <= 128`` and
+    ``|q - 32| <= 32``, so the product has at most 23 significant bits and is
+    exact in f32 (formed here in float64 and stored without rounding).
+    """
+    if n_in % 256:
+        raise ValueError("Q6_K rows are whole 256-element superblocks")
+    nb = n_in // 256
+    blk = np.asarray(raw, dtype=np.uint8).reshape(n_out, nb, 210)
+    q = q6k_quants(blk[..., 0:128], blk[..., 128:192])                    # (n_out, nb, 256)
+    sc = blk[..., 192:208].view(np.int8).astype(np.float64)                # (n_out, nb, 16)
+    d = fp16_bits_to_f64(_le_u16(blk[..., 208], blk[..., 209]))           # (n_out, nb)
+    sub = np.arange(256) // 16
+    w = d[..., None] * sc[..., sub] * (q - 32).astype(np.float64)
+    return w.reshape(n_out, n_in).astype(np.float32)
+
+
+def get_rows(w: np.ndarray, ids) -> np.ndarray:
+    """Embedding lookup: rows ``ids`` of the dequantised matrix ``w``, shape ``(len(ids), n_in)``.
+
+    An id outside ``[0, n_rows)`` has no row; its output row is NaN.
+    """
+    w = np.asarray(w, dtype=np.float32)
+    ids = np.asarray(ids, dtype=np.int64).reshape(-1)
+    out = np.full((ids.size, w.shape[1]), np.nan, dtype=np.float32)
+    for i, t in enumerate(ids):
+        if 0 <= t < w.shape[0]:
+            out[i] = w[t]
+    return out
+
+
+# ---------------------------------------------------------------------------
 # GEMV / GEMM / SwiGLU / FFN (float64 accumulation)
 # ---------------------------------------------------------------------------
 
@@ -256,6 +323,37 @@ def logits_argmax(w: np.ndarray, x: np.ndarray):
         nan = np.flatnonzero(np.isnan(row))
         i = int(nan[0]) if nan.size else int(np.flatnonzero(row == row.max())[0])
         index[b], value[b] = i, row[i]
+    return dict(logits=logits, A=a, index=index, value=value)
+
+
+def logits_topk(w: np.ndarray, x: np.ndarray, k: int):
+    """Output projection with top-k: ``logits = W x``; per activation row, the ``k``
+    first (index, logit) pairs of the order NaN first, then larger logit first, then
+    smaller index first -- the k = 1 case is :func:`logits_argmax`.
+
+    Selection by k passes: each pass takes, among the logits not yet taken, the first
+    NaN if there is one, else the first index holding the largest value.  Returns a
+    dict with ``logits``, ``A``, ``index`` (int64, ``(batch, k)``) and ``value``
+    (float64, ``(batch, k)``).
+    """
+    logits, a = gemv(w, x)
+    n = logits.shape[1]
+    if not 1 <= k <= n:
+        raise ValueError("k must be in 1..n_vocab")
+    index = np.empty((logits.shape[0], k), dtype=np.int64)
+    value = np.empty((logits.shape[0], k), dtype=np.float64)
+    for b, row in enumerate(logits):
+        free = np.ones(n, dtype=bool)
+        nan = np.isnan(row)
+        for j in range(k):
+            cand_nan = np.flatnonzero(free & nan)
+            if cand_nan.size:
+                i = int(cand_nan[0])
+            else:
+                top = row[free].max()
+                i = int(np.flatnonzero(free & (row == top))[0])
+            free[i] = False
+            index[b, j], value[b, j] = i, row[i]
     return dict(logits=logits, A=a, index=index, value=value)
 
 

@@ -13,11 +13,15 @@ Block encodings (GGML, little-endian), as the workload descriptions state them:
 * Q4_K superblock, 144 bytes for 256 weights: fp16 ``d`` at byte 0, fp16
   ``dmin`` at byte 2, 12 bytes packing eight 6-bit scales and eight 6-bit mins
   at bytes 4..15, 128 bytes of 4-bit quants at bytes 16..143.
+* Q6_K superblock, 210 bytes for 256 weights: 128 bytes of low 4-bit quant parts
+  at bytes 0..127, 64 bytes of high 2-bit parts at bytes 128..191, sixteen int8
+  scales at bytes 192..207, fp16 ``d`` at bytes 208..209.
 
 Drawing the 12 scale bytes and the 128 quant bytes as independent uniform
 bytes makes every 6-bit scale, 6-bit min and 4-bit quant uniform over its whole
 range, because each of those fields is a fixed set of distinct bits; the
-generator therefore never has to pack a field.
+generator therefore never has to pack a field.  The same holds for the Q6_K
+quant bytes (every 6-bit quant uniform over 0..63).
 
 Seeds: every array is drawn from ``numpy.random.default_rng([config, *path])``
 (``rng_for``), so each workload matrix has its own reproducible stream.
@@ -31,6 +35,8 @@ Q8_0_BLOCK_ELEMS = 32
 Q8_0_BLOCK_BYTES = 34
 Q4K_BLOCK_ELEMS = 256
 Q4K_BLOCK_BYTES = 144
+Q6K_BLOCK_ELEMS = 256
+Q6K_BLOCK_BYTES = 210
 
 
 def rng_for(config: int, *path: int) -> np.random.Generator:
@@ -82,6 +88,27 @@ def q4k_blocks(rng: np.random.Generator, n_out: int, n_in: int,
     out[..., 4:16] = scales
     out[..., 16:] = qs
     return out.reshape(n_out, nb * Q4K_BLOCK_BYTES)
+
+
+def q6k_blocks(rng: np.random.Generator, n_out: int, n_in: int,
+               d_range=(1e-3, 1e-2), scale_range=(-128, 127)) -> np.ndarray:
+    """Random GGML Q6_K matrix as raw bytes, shape ``(n_out, n_in//256*210)`` uint8.
+
+    ``d`` ~ U[d_range] cast to fp16; the sixteen int8 scales ~ U{scale_range}; the
+    192 quant bytes are uniform random bytes (every 6-bit quant uniform over 0..63).
+    Draw order: d, scales, quant bytes.
+    """
+    if n_in % Q6K_BLOCK_ELEMS:
+        raise ValueError("n_in must be a multiple of 256 for Q6_K")
+    nb = n_in // Q6K_BLOCK_ELEMS
+    d = rng.uniform(d_range[0], d_range[1], size=(n_out, nb))
+    sc = rng.integers(scale_range[0], scale_range[1] + 1, size=(n_out, nb, 16), dtype=np.int8)
+    qs = rng.integers(0, 256, size=(n_out, nb, 192), dtype=np.uint8)
+    out = np.empty((n_out, nb, Q6K_BLOCK_BYTES), dtype=np.uint8)
+    out[..., 0:192] = qs
+    out[..., 192:208] = sc.view(np.uint8)
+    out[..., 208:210] = _fp16_le_bytes(d)
+    return out.reshape(n_out, nb * Q6K_BLOCK_BYTES)
 
 
 def activations(rng: np.random.Generator, rows: int, n: int) -> np.ndarray:
@@ -183,3 +210,14 @@ def config4_x(kind: int, m: int) -> np.ndarray:
     """Config 4 activations ``(m, n_in)`` for weight ``kind``."""
     n_in = N_EMBD if kind == 0 else N_FF
     return activations(rng_for(4, 2 + kind, m), m, n_in)
+
+
+def q6k_output_projection():
+    """Q6_K output projection ``(W, x)``: 3072 -> 128256 (a 3B-class vocabulary, Q6_K
+    as quantised files keep the output and embedding tables) and x (1, 3072)."""
+    return q6k_blocks(rng_for(7, 0), N_VOCAB, N_EMBD), activations(rng_for(7, 1), 1, N_EMBD)
+
+
+def token_ids(rng: np.random.Generator, n: int, n_vocab: int = N_VOCAB) -> np.ndarray:
+    """``n`` token ids uniform over the vocabulary (int32), for embedding lookups."""
+    return rng.integers(0, n_vocab, size=n).astype(np.int32)

@@ -1,0 +1,219 @@
+"""GPU parity of the Q6_K path and the on-device top-k (through the C ABI).
+
+Bars:
+* Q6_K dequantised weights and embedding rows: bit-exact (d*scale*(q-32) is
+  exact in f32);
+* Q6_K GEMV: |y - y_ref| <= 1e-5 * sum|w||x| against the float64 oracle;
+* top-k: the indices and values are unique given the logits, so they are
+  compared with the stable top-k of the logits the GPU computed (value bits
+  included), and every returned logit must be within the GEMV bound of the
+  oracle's k-th best logit.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from _bounds import gemv_excess
+
+pytestmark = pytest.mark.gpu
+
+
+def _dev():
+    import torch
+    return torch.device("cuda")
+
+
+def _t(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).to(_dev())
+
+
+def _nan(*shape):
+    import torch
+    return torch.full(shape, float("nan"), dtype=torch.float32, device=_dev())
+
+
+def _np(t):
+    import torch
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+# ------------------------------------------------------------------ Q6_K
+
+@pytest.mark.parametrize("n_out,n_in", [(1, 256), (37, 768), (5, 3072), (300, 2048), (1000, 8192)])
+def test_q6k_dequant_bit_exact(cuda_lib, n_out, n_in):
+    qdq = cuda_lib
+    wb = synth.q6k_blocks(np.random.default_rng(n_out + n_in), n_out, n_in)
+    W = qdq.upload_q6k(wb, n_out, n_in)
+    out = _nan(n_out, n_in)
+    qdq.q6k_dequant(W, out, n_out, n_in)
+    assert np.array_equal(_np(out).view(np.uint32), oracle.q6k_dequant(wb, n_out, n_in).view(np.uint32))
+
+
+def test_q6k_dequant_extreme_scales_bit_exact(cuda_lib):
+    # largest fp16 d, scales -128 / 127, every quant 0 or 63
+    qdq = cuda_lib
+    rng = np.random.default_rng(4)
+    wb = synth.q6k_blocks(rng, 16, 512, d_range=(65504.0, 65504.0))
+    sb = wb.reshape(16, 2, 210)
+    sb[..., 192:208] = np.where(rng.random((16, 2, 16)) < 0.5, 0x80, 0x7F).astype(np.uint8)
+    sb[..., 0:192] = np.where(rng.random((16, 2, 192)) < 0.5, 0x00, 0xFF).astype(np.uint8)
+    W = qdq.upload_q6k(wb, 16, 512)
+    out = _nan(16, 512)
+    qdq.q6k_dequant(W, out, 16, 512)
+    assert np.array_equal(_np(out).view(np.uint32), oracle.q6k_dequant(wb, 16, 512).view(np.uint32))
+
+
+Q6_SHAPES = [(1, 256, 1), (5, 512, 1), (157, 3072, 1), (64, 512, 8), (33, 8192, 3), (1000, 1280, 2),
+             (40, 16384, 1), (24, 32768, 1), (16, 32768, 8), (3001, 4096, 1)]
+
+
+@pytest.mark.parametrize("n_out,n_in,batch", Q6_SHAPES)
+def test_q6k_gemv_parity(cuda_lib, n_out, n_in, batch):
+    qdq = cuda_lib
+    rng = np.random.default_rng(n_out + 7 * n_in + batch)
+    wb = synth.q6k_blocks(rng, n_out, n_in)
+    x = synth.activations(rng, batch, n_in)
+    W = qdq.upload_q6k(wb, n_out, n_in)
+    y = _nan(batch, n_out)
+    qdq.q6k_gemv(W, _t(x), y, n_out, n_in, batch)
+    y_ref, a = oracle.gemv(oracle.q6k_dequant(wb, n_out, n_in), x)
+    assert gemv_excess(_np(y), y_ref, a) <= 1.0
+
+
+def test_q6k_gemv_output_projection_full_size(cuda_lib):
+    # the 3B-class vocabulary projection (128256 x 3072), checked on every row
+    qdq = cuda_lib
+    wb, x = synth.q6k_output_projection()
+    W = qdq.upload_q6k(wb, synth.N_VOCAB, synth.N_EMBD)
+    y = _nan(1, synth.N_VOCAB)
+    qdq.q6k_gemv(W, _t(x), y, synth.N_VOCAB, synth.N_EMBD, 1)
+    yh = _np(y)
+    rows = wb.reshape(synth.N_VOCAB, -1)
+    for r0 in range(0, synth.N_VOCAB, 16032):   # the oracle in row blocks (bounded host memory)
+        r1 = min(r0 + 16032, synth.N_VOCAB)
+        y_ref, a = oracle.gemv(oracle.q6k_dequant(rows[r0:r1], r1 - r0, synth.N_EMBD), x)
+        assert gemv_excess(yh[:, r0:r1], y_ref, a) <= 1.0
+
+
+def test_q6k_gemv_one_hot_extracts_column(cuda_lib):
+    qdq = cuda_lib
+    wb = synth.q6k_blocks(np.random.default_rng(17), 200, 2048)
+    W = qdq.upload_q6k(wb, 200, 2048)
+    w = oracle.q6k_dequant(wb, 200, 2048)
+    for k in (0, 15, 16, 1000, 2047):
+        x = np.zeros((1, 2048), np.float32)
+        x[0, k] = 1.0
+        y = _nan(1, 200)
+        qdq.q6k_gemv(W, _t(x), y, 200, 2048, 1)
+        assert np.array_equal(_np(y)[0], w[:, k])
+
+
+def test_q6k_get_rows_bit_exact(cuda_lib):
+    # embedding lookup on the vocabulary table: repeated, first and last ids, and ids
+    # outside the table (a NaN row each)
+    import torch
+    qdq = cuda_lib
+    n_rows, n_in = 4096, 3072
+    wb = synth.q6k_blocks(np.random.default_rng(18), n_rows, n_in)
+    W = qdq.upload_q6k(wb, n_rows, n_in)
+    ids = np.concatenate([synth.token_ids(np.random.default_rng(19), 29, n_rows), [0, n_rows - 1, 7, 7, -1, n_rows]])
+    ids = ids.astype(np.int32)
+    out = _nan(len(ids), n_in)
+    qdq.q6k_get_rows(W, torch.from_numpy(ids).to(_dev()), out, len(ids), n_rows, n_in)
+    ref = oracle.get_rows(oracle.q6k_dequant(wb, n_rows, n_in), ids)
+    got = _np(out)
+    ok = ~np.isnan(ref[:, 0])
+    assert np.array_equal(got[ok].view(np.uint32), ref[ok].view(np.uint32))
+    assert np.all(np.isnan(got[~ok]))
+
+
+# ------------------------------------------------------------------ top-k
+
+def _stable_topk(row, k):
+    """Top-k of one logits row in the stated order (NaN first, larger, smaller index)."""
+    nan = np.isnan(row)
+    key = np.where(nan, np.inf, row.astype(np.float64))
+    order = np.lexsort((np.arange(row.size), ~nan, -key))   # NaN group first, then value desc, index asc
+    return order[:k]
+
+
+def _topk_case(qdq, wb, x, n_vocab, n_in, batch, k, fused=True):
+    """`wb`: raw Q8_0 bytes, or a matrix already uploaded (a torch tensor)."""
+    import torch
+    W = wb if isinstance(wb, torch.Tensor) else qdq.upload_q8_0(wb, n_vocab, n_in)
+    logits = _nan(batch, n_vocab)
+    ws = torch.empty(qdq.topk_workspace_bytes(n_vocab, batch, k), dtype=torch.uint8, device=_dev())
+    idx = torch.full((batch, k), -1, dtype=torch.int32, device=_dev())
+    val = _nan(batch, k)
+    if fused:
+        qdq.q8_0_logits_topk(W, _t(x), logits, ws, idx, val, n_vocab, n_in, batch, k)
+    else:
+        qdq.q8_0_gemv(W, _t(x), logits, n_vocab, n_in, batch)
+        qdq.topk_rows(logits, n_vocab, batch, k, ws, idx, val)
+    return _np(logits), _np(idx), _np(val)
+
+
+def test_topk_full_vocabulary(cuda_lib):
+    # the 3B-class vocabulary (128256 x 3072 Q8_0), k = 1, 8, 40 and the largest k
+    qdq = cuda_lib
+    wb, x = synth.output_projection()
+    n_vocab, n_in = synth.N_VOCAB, synth.N_EMBD
+    rows = wb.reshape(n_vocab, -1)
+    ref, a = np.empty((1, n_vocab)), np.empty((1, n_vocab))
+    for r0 in range(0, n_vocab, 16032):        # oracle logits in row blocks (bounded host memory)
+        r1 = min(r0 + 16032, n_vocab)
+        ref[:, r0:r1], a[:, r0:r1] = oracle.gemv(oracle.q8_0_dequant(rows[r0:r1], r1 - r0, n_in), x)
+    kmax = qdq.QDQ_MAX_TOPK
+    W = qdq.upload_q8_0(wb, n_vocab, n_in)
+    exact_order = np.lexsort((np.arange(n_vocab), -ref[0]))[:kmax]            # exact top-k of the oracle logits
+    for k in (1, 8, 40, kmax):
+        lg, ix, vl = _topk_case(qdq, W, x, n_vocab, n_in, 1, k)
+        order = _stable_topk(lg[0], k)
+        assert np.array_equal(ix[0], order)                                # unique given the logits
+        assert np.array_equal(vl[0].view(np.uint32), lg[0, order].view(np.uint32))
+        tol = 2e-5 * a[0].max()
+        assert np.all(ref[0, ix[0]] >= ref[0, exact_order[k - 1]] - tol)   # valid: near the exact top-k
+        assert np.all(np.abs(vl[0] - ref[0, ix[0]]) <= 1e-5 * a[0, ix[0]])
+
+
+@pytest.mark.parametrize("n_vocab,n_in,batch,k", [(1000, 512, 1, 8), (5003, 2048, 3, 40), (64, 32, 2, 64),
+                                                  (1, 32, 1, 1), (9000, 256, 8, 17)])
+def test_topk_shapes(cuda_lib, n_vocab, n_in, batch, k):
+    qdq = cuda_lib
+    rng = np.random.default_rng(n_vocab + k)
+    wb, x = synth.q8_0_blocks(rng, n_vocab, n_in), synth.activations(rng, batch, n_in)
+    lg, ix, vl = _topk_case(qdq, wb, x, n_vocab, n_in, batch, k, fused=(batch % 2 == 1))
+    for b in range(batch):
+        order = _stable_topk(lg[b], k)
+        assert np.array_equal(ix[b], order)
+        assert np.array_equal(vl[b].view(np.uint32), lg[b, order].view(np.uint32))
+
+
+def test_topk_ties_nans_and_signed_zeros(cuda_lib):
+    # logits written directly: runs of equal values across chunk borders, NaNs, +0 / -0
+    import torch
+    qdq = cuda_lib
+    n, k = 5000, 40
+    rng = np.random.default_rng(23)
+    lg = rng.integers(-5, 6, size=(2, n)).astype(np.float32)   # many ties
+    lg[0, [17, 1023, 1024, 4999]] = 5.0
+    lg[1, [3000, 12]] = np.nan
+    lg[1, 100:200] = -0.0
+    lg[1, 200:300] = 0.0
+    logits = _t(lg)
+    ws = torch.empty(qdq.topk_workspace_bytes(n, 2, k), dtype=torch.uint8, device=_dev())
+    idx = torch.full((2, k), -1, dtype=torch.int32, device=_dev())
+    val = _nan(2, k)
+    qdq.topk_rows(logits, n, 2, k, ws, idx, val)
+    ix, vl = _np(idx), _np(val)
+    for b in range(2):
+        order = _stable_topk(lg[b], k)
+        assert np.array_equal(ix[b], order)
+        assert np.array_equal(vl[b].view(np.uint32), lg[b, order].view(np.uint32))
+    assert list(ix[1, :2]) == [12, 3000]
+    # the oracle's selection on the same logits (row 0: an identity projection reproduces them)
+    o = oracle.logits_topk(np.eye(n, dtype=np.float32), lg[:1], k)
+    assert np.array_equal(o["index"][0], ix[0].astype(np.int64))

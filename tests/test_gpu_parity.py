@@ -544,7 +544,7 @@ def test_q4k_gemv_near_cancelling_adjacent_scales(cuda_lib):
     y = _nan(1, n_out)
     qdq.q4k_gemv(W, _t(x), y, n_out, n_in, 1)
     w = oracle.q4k_dequant(wb, n_out, n_in)
-    assert np.all(w != 0) and np.abs(w).max() < 1e-3 * d
+    assert np.all(w != 0) and np.abs(w).max() < 1e-3 * (4 * d * 8)   # 1000x below d*sc*q
     y_ref, a = oracle.gemv(w, x)
     assert gemv_excess(_np(y), y_ref, a) <= 1.0
 

@@ -165,3 +165,51 @@ def test_options_and_strings(lib):
     assert b"QDQ_ERR_ALIAS" in lib.qdq_status_string(qdq.QDQ_ERR_ALIAS)
     assert lib.qdq_last_cuda_error() == 0
     assert b"sm_103a" in lib.qdq_version()
+
+
+def test_q6k_validation_and_sizes(lib):
+    import ggml_quantized_dequant_gb300 as qdq
+    # packed rows: 210 bytes per 256 weights padded to 16 bytes (none at n_in % 2048 == 0)
+    assert lib.qdq_q6k_packed_bytes(5, 3072) == 5 * 2528
+    assert lib.qdq_q6k_packed_bytes(5, 8192) == 5 * 8192 // 256 * 210
+    assert lib.qdq_q6k_packed_bytes(5, 300) == 0
+    W, x, y, ids = GOOD, GOOD + (1 << 28), GOOD + (2 << 28), GOOD + (3 << 28)
+    assert lib.qdq_q6k_pack(GOOD, None, 4, 256, None) == qdq.QDQ_ERR_NULL
+    assert lib.qdq_q6k_pack(GOOD, GOOD + 16 * 1024, 4, 255, None) == qdq.QDQ_ERR_DIMS
+    assert lib.qdq_q6k_pack(GOOD, GOOD + 8, 4, 256, None) == qdq.QDQ_ERR_ALIGN
+    assert lib.qdq_q6k_pack(GOOD, GOOD + 16, 4, 256, None) == qdq.QDQ_ERR_ALIAS
+    assert lib.qdq_q6k_gemv(W, x, y, 64, 300, 1, None) == qdq.QDQ_ERR_DIMS
+    assert lib.qdq_q6k_gemv(W, x, y, 64, 256, 9, None) == qdq.QDQ_ERR_DIMS
+    assert lib.qdq_q6k_gemv(W, x + 4, y, 64, 256, 1, None) == qdq.QDQ_ERR_ALIGN
+    assert lib.qdq_q6k_gemv(W, x, W + 16, 64, 256, 1, None) == qdq.QDQ_ERR_ALIAS
+    assert lib.qdq_q6k_dequant(W, None, 64, 256, None) == qdq.QDQ_ERR_NULL
+    assert lib.qdq_q6k_get_rows(W, None, y, 4, 64, 256, None) == qdq.QDQ_ERR_NULL
+    assert lib.qdq_q6k_get_rows(W, ids, y, -1, 64, 256, None) == qdq.QDQ_ERR_DIMS
+    assert lib.qdq_q6k_get_rows(W, ids + 2, y, 4, 64, 256, None) == qdq.QDQ_ERR_ALIGN
+    assert lib.qdq_q6k_get_rows(W, ids, ids, 4, 64, 256, None) == qdq.QDQ_ERR_ALIAS
+    assert lib.qdq_q6k_get_rows(W, ids, y, 0, 64, 256, None) == qdq.QDQ_OK   # empty: nothing launched
+
+
+def test_topk_validation_and_sizes(lib):
+    import ggml_quantized_dequant_gb300 as qdq
+    # two rounds of candidate keys: batch * ceil(n / 1024) * k 8-byte keys each
+    assert lib.qdq_topk_workspace_bytes(128256, 2, 40) == 2 * 2 * 126 * 40 * 8
+    assert lib.qdq_topk_workspace_bytes(100, 1, 101) == 0
+    assert lib.qdq_topk_workspace_bytes(1000, 1, qdq.QDQ_MAX_TOPK + 1) == 0
+    lg, ws, idx, val = GOOD, GOOD + (1 << 28), GOOD + (2 << 28), GOOD + (3 << 28)
+    f = lib.qdq_topk_rows
+    assert f(lg, 1000, 1, 8, None, idx, val, None) == qdq.QDQ_ERR_NULL
+    assert f(lg, 1000, 1, 0, ws, idx, val, None) == qdq.QDQ_ERR_DIMS
+    assert f(lg, 5, 1, 6, ws, idx, val, None) == qdq.QDQ_ERR_DIMS             # k > n
+    assert f(lg, 1000, 0, 8, ws, idx, val, None) == qdq.QDQ_ERR_DIMS
+    assert f(lg, 1000, 1, 65, ws, idx, val, None) == qdq.QDQ_ERR_UNSUPPORTED
+    assert f(lg, 1000, 1, 8, ws + 8, idx, val, None) == qdq.QDQ_ERR_ALIGN
+    assert f(lg, 1000, 1, 8, ws, idx, lg + 64, None) == qdq.QDQ_ERR_ALIAS    # value inside the logits
+    assert f(lg, 1000, 1, 8, ws, idx, idx + 16, None) == qdq.QDQ_ERR_ALIAS   # value over index
+    assert f(lg, 1000, 1, 8, lg + 16, idx, val, None) == qdq.QDQ_ERR_ALIAS   # workspace over the logits
+    W, x = GOOD + (4 << 28), GOOD + (5 << 28)
+    g = lib.qdq_q8_0_logits_topk
+    assert g(W, x, lg, ws, idx, val, 1000, 500, 1, 8, None) == qdq.QDQ_ERR_DIMS
+    assert g(W, x, lg, ws, idx, val, 1000, 512, 1, 0, None) == qdq.QDQ_ERR_DIMS
+    assert g(W, x, lg, ws, idx, x, 1000, 512, 1, 8, None) == qdq.QDQ_ERR_ALIAS   # value over x
+    assert g(W, x, lg, W + 16, idx, val, 1000, 512, 1, 8, None) == qdq.QDQ_ERR_ALIAS

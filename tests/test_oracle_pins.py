@@ -433,3 +433,145 @@ def test_gemm_batch_m1_equals_gemv_and_permutes_rows():
     perm = np.random.default_rng(53).permutation(9)
     yp, ap = oracle.gemm_batch(w, x[perm])
     assert np.array_equal(yp, y[perm]) and np.array_equal(ap, a[perm])
+
+
+# ---------------------------------------------------------------- Q6_K
+
+def _q6k_block(ql=None, qh=None, scales=None, d_bits=0x3C00):
+    """One 210-byte Q6_K superblock: ql (128), qh (64), int8 scales (16), fp16 d."""
+    b = np.zeros(210, dtype=np.uint8)
+    if ql is not None:
+        b[0:128] = ql
+    if qh is not None:
+        b[128:192] = qh
+    if scales is not None:
+        b[192:208] = np.asarray(scales, dtype=np.int64).astype(np.int8).view(np.uint8)
+    b[208], b[209] = d_bits & 0xFF, d_bits >> 8
+    return b
+
+
+def _golden_q6k():
+    rows = []
+    with open(os.path.join(GOLDEN, "q6k_quants.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            lhs, rhs = line.split("|")
+            ql, qh = np.zeros(128, np.uint8), np.zeros(64, np.uint8)
+            for tok in lhs.split():
+                name, val = tok.split("=")
+                plane, idx = name.rstrip("]").split("[")
+                (ql if plane == "ql" else qh)[int(idx)] = int(val, 16)
+            want = np.zeros(256, np.int64)
+            for tok in rhs.split():
+                e, q = tok.split("=")
+                want[int(e)] = int(q)
+            rows.append((ql, qh, want))
+    return rows
+
+
+@pytest.mark.parametrize("row", range(6))
+def test_q6k_quants_golden(row):
+    ql, qh, want = _golden_q6k()[row]
+    assert np.array_equal(oracle.q6k_quants(ql[None], qh[None])[0], want)
+
+
+def _q6k_encode(q):
+    """Field-wise encoder written from the placement text, one weight at a time."""
+    ql, qh = np.zeros(128, np.uint8), np.zeros(64, np.uint8)
+    for e in range(256):
+        h, p = divmod(e, 128)
+        t, l = divmod(p, 32)
+        i = 64 * h + 32 * (t & 1) + l
+        ql[i] |= (int(q[e]) & 0xF) << (4 * (t >> 1))
+        qh[32 * h + l] |= (int(q[e]) >> 4) << (2 * t)
+    return ql, qh
+
+
+def test_q6k_quants_roundtrip_random():
+    rng = np.random.default_rng(91)
+    for _ in range(20):
+        q = rng.integers(0, 64, 256)
+        ql, qh = _q6k_encode(q)
+        assert np.array_equal(oracle.q6k_quants(ql[None], qh[None])[0], q)
+
+
+@pytest.mark.parametrize("j", range(16))
+def test_q6k_one_hot_scale_lights_one_subblock(j):
+    # every q = 33 (q - 32 = 1), d = 1, only scale j non-zero: weights 16j..16j+15 equal it
+    ql, qh = _q6k_encode(np.full(256, 33))
+    sc = np.zeros(16, np.int64)
+    sc[j] = -77
+    w = oracle.q6k_dequant(_q6k_block(ql, qh, sc), 1, 256)[0]
+    want = np.zeros(256, np.float32)
+    want[16 * j: 16 * j + 16] = -77.0
+    assert np.array_equal(w, want)
+
+
+def test_q6k_extremes_exact_and_two_rows():
+    # q = 0 and 63 against scale -128 and the largest fp16 d: d*sc*(q-32) exact in f32
+    q = np.where(np.arange(256) % 2 == 0, 0, 63)
+    ql, qh = _q6k_encode(q)
+    d_max = 0x7BFF  # 65504
+    b0 = _q6k_block(ql, qh, np.full(16, -128), d_max)
+    b1 = _q6k_block(ql, qh, np.arange(16) - 8, 0x0001)  # smallest subnormal d = 2^-24
+    w = oracle.q6k_dequant(np.stack([np.concatenate([b0, b1]), np.concatenate([b1, b0])]), 2, 512)
+    for r, (first, second) in enumerate(((b0, b1), (b1, b0))):
+        for half, blk in enumerate((first, second)):
+            d = Fraction(65504) if blk is b0 else Fraction(1, 2 ** 24)
+            for e in (0, 1, 17, 254, 255):
+                sc = -128 if blk is b0 else (e // 16) - 8
+                exact = d * sc * (int(q[e]) - 32)
+                assert Fraction(float(w[r, 256 * half + e])) == exact
+
+
+def test_q6k_gemv_one_hot_extracts_column():
+    wb = synth.q6k_blocks(np.random.default_rng(92), 7, 512)
+    w = oracle.q6k_dequant(wb, 7, 512)
+    for k in (0, 15, 16, 255, 256, 511):
+        x = np.zeros((1, 512), np.float32)
+        x[0, k] = 1.0
+        y, a = oracle.gemv(w, x)
+        assert np.array_equal(y[0], w[:, k].astype(np.float64))
+
+
+def test_get_rows_picks_rows_and_nans_bad_ids():
+    w = _small_q8(10, 64, 93)
+    out = oracle.get_rows(w, [3, 0, 9, 3, 10, -1])
+    assert np.array_equal(out[0], w[3]) and np.array_equal(out[1], w[0]) and np.array_equal(out[2], w[9])
+    assert np.array_equal(out[3], w[3]) and np.all(np.isnan(out[4])) and np.all(np.isnan(out[5]))
+
+
+# ---------------------------------------------------------------- top-k
+
+def test_logits_topk_closed_form_with_ties():
+    # one-hot rows: logit r = x[col(r)]; rows 1 and 3 tie at 7, rows 0 and 5 tie at 9
+    w = np.eye(6, dtype=np.float32)[[3, 1, 4, 1, 0, 3]]
+    x = np.array([[5, 7, 2, 9, 1, 0]], np.float32)
+    o = oracle.logits_topk(w, x, 6)
+    assert list(o["index"][0]) == [0, 5, 1, 3, 4, 2]
+    assert list(o["value"][0]) == [9, 9, 7, 7, 5, 1]
+
+
+def test_logits_topk_matches_lexsort_and_argmax():
+    rng = np.random.default_rng(94)
+    w = _small_q8(500, 96, 95)
+    x = synth.activations(rng, 3, 96)
+    for k in (1, 8, 40):
+        o = oracle.logits_topk(w, x, k)
+        for b in range(3):
+            order = np.lexsort((np.arange(500), -o["logits"][b]))   # value desc, then index asc
+            assert np.array_equal(o["index"][b], order[:k])
+            assert np.array_equal(o["value"][b], o["logits"][b][order[:k]])
+        if k == 1:
+            assert np.array_equal(o["index"][:, 0], oracle.logits_argmax(w, x)["index"])
+
+
+def test_logits_topk_nan_first():
+    w = _small_q8(50, 64, 96)
+    x = synth.activations(np.random.default_rng(97), 2, 64)
+    x[1, 3] = np.nan
+    o = oracle.logits_topk(w, x, 5)
+    assert list(o["index"][1]) == [0, 1, 2, 3, 4] and np.all(np.isnan(o["value"][1]))
+    assert np.all(np.isfinite(o["value"][0]))
