@@ -515,7 +515,38 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
     b = synth.N_VOCAB * (N_EMBD // 32) * 34 + N_EMBD * 4 + synth.N_VOCAB * 4 + 8
     rows["q8_0_logits_argmax_3072x128256"] = {"us_per_call": us, "gbs": b / us / 1e3, "frac_hbm": b / us / 1e3 / hbm,
                                               "bytes_per_call": b, "launches_per_call": 2}
+
+    # the same projection with the on-device top-40 (k candidates read back instead of the logits)
+    K = 40
+    wsk = torch.empty(qdq.topk_workspace_bytes(synth.N_VOCAB, 1, K), dtype=torch.uint8, device=dev)
+    ik = torch.empty((1, K), dtype=torch.int32, device=dev)
+    vk = torch.empty((1, K), device=dev)
+    gk = capture(torch, lambda: [qdq.q8_0_logits_topk(WO, xo, lo, wsk, ik, vk, synth.N_VOCAB, N_EMBD, 1, K)
+                                 for _ in range(4)])
+    for _ in range(3):
+        gk.replay()
+    dt = timer(gk.replay, max(5, iters // 4))
+    us = dt / (max(5, iters // 4) * 4) * 1e6
+    b = synth.N_VOCAB * (N_EMBD // 32) * 34 + N_EMBD * 4 + synth.N_VOCAB * 4 + 8 * K
+    rows["q8_0_logits_top40_3072x128256"] = {"us_per_call": us, "gbs": b / us / 1e3, "frac_hbm": b / us / 1e3 / hbm,
+                                             "bytes_per_call": b, "launches_per_call": 4}
     del WO
+
+    # Q6_K output projection 3072 -> 128256 (323 MB, larger than L2)
+    wb, xq6 = synth.q6k_output_projection()
+    W6 = qdq.upload_q6k(wb, synth.N_VOCAB, N_EMBD, device=dev)
+    del wb
+    xq6 = torch.from_numpy(xq6).to(dev)
+    y6 = torch.empty((1, synth.N_VOCAB), device=dev)
+    g6 = capture(torch, lambda: [qdq.q6k_gemv(W6, xq6, y6, synth.N_VOCAB, N_EMBD, 1) for _ in range(4)])
+    for _ in range(3):
+        g6.replay()
+    dt = timer(g6.replay, max(5, iters // 4))
+    us = dt / (max(5, iters // 4) * 4) * 1e6
+    b = synth.N_VOCAB * (N_EMBD // 256) * 210 + N_EMBD * 4 + synth.N_VOCAB * 4
+    rows["q6k_gemv_3072x128256"] = {"us_per_call": us, "gbs": b / us / 1e3, "frac_hbm": b / us / 1e3 / hbm,
+                                    "bytes_per_call": b}
+    del W6
 
     # config 4: tensor-core batch GEMM, 8 copies of each shape cycled
     ncopy = 8
