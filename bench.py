@@ -557,7 +557,7 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
         for M in synth.C4_M:
             X = torch.from_numpy(synth.config4_x(kind, M)).to(dev)
             Y = torch.empty((M, n_out), device=dev)
-            wsp = torch.empty(qdq.q8_0_gemm_batch_workspace_bytes(M, n_in), dtype=torch.uint8, device=dev)
+            wsp = torch.empty(qdq.gemm_batch_workspace_bytes(M, n_out, n_in), dtype=torch.uint8, device=dev)
             gq = capture(torch, lambda: [qdq.q8_0_gemm_batch(w, X, Y, wsp, n_out, n_in, M) for w in Wq])
             for _ in range(3):
                 gq.replay()
@@ -571,6 +571,50 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
                  "frac_bf16": flops / us / 1e6 / peaks["bf16_tflops"]}
             r["bound"] = "tensor" if M >= 256 else "hbm"
             rows["q8_0_gemm_%s_M%d" % ("3072x8192" if kind == 0 else "8192x3072", M)] = r
+        del Wq
+
+    # Q4_K batch GEMM on tensor cores (config-2/3 shapes, 8 copies cycled) and the M-token SwiGLU
+    for kind, (n_out, n_in) in ((0, (N_FF, N_EMBD)), (1, (N_EMBD, N_FF))):
+        wsq = gen_parallel([lambda t=t: synth.q4k_blocks(synth.rng_for(8, kind, t), n_out, n_in)
+                            for t in range(ncopy)])
+        Wq = [qdq.upload_q4k(w, n_out, n_in, device=dev) for w in wsq]
+        del wsq
+        for M in synth.C4_M:
+            X = torch.from_numpy(synth.activations(synth.rng_for(8, 2 + kind, M), M, n_in)).to(dev)
+            Y = torch.empty((M, n_out), device=dev)
+            wsp = torch.empty(qdq.gemm_batch_workspace_bytes(M, n_out, n_in), dtype=torch.uint8, device=dev)
+            gq = capture(torch, lambda: [qdq.q4k_gemm_batch(w, X, Y, wsp, n_out, n_in, M) for w in Wq])
+            for _ in range(3):
+                gq.replay()
+            it = max(10, iters // 2)
+            dt = timer(gq.replay, it)
+            us = dt / (it * ncopy) * 1e6
+            b = Q4_W_BYTES + M * n_in * 4 + M * n_out * 4
+            flops = 2.0 * M * n_out * n_in
+            rows["q4k_gemm_%s_M%d" % ("3072x8192" if kind == 0 else "8192x3072", M)] = {
+                "us_per_call": us, "gbs": b / us / 1e3, "tflops": flops / us / 1e6, "bytes_per_call": b,
+                "flop_per_call": flops, "frac_hbm": b / us / 1e3 / hbm,
+                "frac_bf16": flops / us / 1e6 / peaks["bf16_tflops"], "bound": "tensor" if M >= 256 else "hbm"}
+        if kind == 0:  # gate and up share the 3072 -> 8192 shape: pairs of the copies
+            for M in synth.C4_M:
+                X = torch.from_numpy(synth.activations(synth.rng_for(8, 4, M), M, n_in)).to(dev)
+                mid = torch.empty((M, n_out), device=dev)
+                wsp = torch.empty(qdq.q4k_swiglu_batch_workspace_bytes(M, n_out, n_in), dtype=torch.uint8,
+                                  device=dev)
+                pairs = [(Wq[2 * t], Wq[2 * t + 1]) for t in range(ncopy // 2)]
+                gq = capture(torch, lambda: [qdq.q4k_swiglu_batch(a, c, X, mid, wsp, n_out, n_in, M)
+                                             for a, c in pairs])
+                for _ in range(3):
+                    gq.replay()
+                it = max(10, iters // 2)
+                dt = timer(gq.replay, it)
+                us = dt / (it * len(pairs)) * 1e6
+                b = 2 * Q4_W_BYTES + M * n_in * 4 + M * n_out * 4
+                flops = 4.0 * M * n_out * n_in
+                rows["q4k_swiglu_batch_3072x8192_M%d" % M] = {
+                    "us_per_call": us, "gbs": b / us / 1e3, "tflops": flops / us / 1e6, "bytes_per_call": b,
+                    "flop_per_call": flops, "frac_hbm": b / us / 1e3 / hbm,
+                    "frac_bf16": flops / us / 1e6 / peaks["bf16_tflops"], "bound": "tensor" if M >= 256 else "hbm"}
         del Wq
     rows["timeouts"] = qdq.pipeline_timeouts()
     return rows
@@ -617,7 +661,7 @@ def run_profile_case(case: str):
         W = qdq.upload_q8_0(synth.config4_w(0, 0), N_FF, N_EMBD, device=dev)
         X = torch.from_numpy(synth.config4_x(0, M)).to(dev)
         Y = torch.empty((M, N_FF), device=dev)
-        ws = torch.empty(qdq.q8_0_gemm_batch_workspace_bytes(M, N_EMBD), dtype=torch.uint8, device=dev)
+        ws = torch.empty(qdq.gemm_batch_workspace_bytes(M, N_FF, N_EMBD), dtype=torch.uint8, device=dev)
         fn = lambda: qdq.q8_0_gemm_batch(W, X, Y, ws, N_FF, N_EMBD, M)
     else:
         raise SystemExit("unknown --profile case %r" % case)

@@ -66,8 +66,11 @@ SIGNATURES = {
     "qdq_topk_rows": (_c_int, [_c_vp, _c_int, _c_int, _c_int, _c_vp, _c_vp, _c_vp, _c_vp]),
     "qdq_q8_0_logits_topk": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_int,
                                       _c_vp]),
-    "qdq_q8_0_gemm_batch_workspace_bytes": (_c_size, [_c_int, _c_int]),
+    "qdq_gemm_batch_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int]),
     "qdq_q8_0_gemm_batch": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_vp]),
+    "qdq_q4k_gemm_batch": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_vp]),
+    "qdq_q4k_swiglu_batch_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int]),
+    "qdq_q4k_swiglu_batch": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_vp]),
     "qdq_pipeline_timeouts": (_c_int, []),
     "qdq_set_option": (_c_int, [_c_int, _c_int]),
 }
@@ -241,13 +244,28 @@ def q8_0_logits_topk(W, x, logits, workspace, index, value, n_vocab: int, n_in: 
                                       n_vocab, n_in, batch, k, _stream(stream)))
 
 
-def q8_0_gemm_batch_workspace_bytes(M: int, n_in: int) -> int:
-    return int(lib().qdq_q8_0_gemm_batch_workspace_bytes(M, n_in))
+def gemm_batch_workspace_bytes(M: int, n_out: int, n_in: int) -> int:
+    """Workspace bytes of the tensor-core batch GEMMs on the current device."""
+    return int(lib().qdq_gemm_batch_workspace_bytes(M, n_out, n_in))
 
 
 def q8_0_gemm_batch(W, X, Y, workspace, n_out: int, n_in: int, M: int, stream=None):
     _check("qdq_q8_0_gemm_batch", lib().qdq_q8_0_gemm_batch(_ptr(W), _ptr(X), _ptr(Y), _ptr(workspace), n_out,
                                                             n_in, M, _stream(stream)))
+
+
+def q4k_gemm_batch(W, X, Y, workspace, n_out: int, n_in: int, M: int, stream=None):
+    _check("qdq_q4k_gemm_batch", lib().qdq_q4k_gemm_batch(_ptr(W), _ptr(X), _ptr(Y), _ptr(workspace), n_out,
+                                                          n_in, M, _stream(stream)))
+
+
+def q4k_swiglu_batch_workspace_bytes(M: int, n_ff: int, n_embd: int) -> int:
+    return int(lib().qdq_q4k_swiglu_batch_workspace_bytes(M, n_ff, n_embd))
+
+
+def q4k_swiglu_batch(Wg, Wu, X, mid, workspace, n_ff: int, n_embd: int, M: int, stream=None):
+    _check("qdq_q4k_swiglu_batch", lib().qdq_q4k_swiglu_batch(_ptr(Wg), _ptr(Wu), _ptr(X), _ptr(mid),
+                                                              _ptr(workspace), n_ff, n_embd, M, _stream(stream)))
 
 
 def pipeline_timeouts() -> int:

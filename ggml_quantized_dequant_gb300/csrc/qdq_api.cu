@@ -399,24 +399,60 @@ int qdq_q4k_qkv(const void *Wq, const void *Wk, const void *Wv, const float *x, 
   return rc;
 }
 
-size_t qdq_q8_0_gemm_batch_workspace_bytes(int M, int n_in) {
-  if (M < 1 || n_in < 1) return 0;
-  return size_t(M) * size_t(n_in) * 2;
+size_t qdq_gemm_batch_workspace_bytes(int M, int n_out, int n_in) {
+  if (M < 1 || n_out < 1 || n_in < 1) return 0;
+  return gemm_workspace_bytes(M, n_out, n_in, 1);
 }
+
+size_t qdq_q4k_swiglu_batch_workspace_bytes(int M, int n_ff, int n_embd) {
+  if (M < 1 || n_ff < 1 || n_embd < 1) return 0;
+  return gemm_workspace_bytes(M, n_ff, n_embd, 2);
+}
+
+namespace {
+// Shared checks of the tensor-core batch GEMMs: W (and W2 when non-NULL) packed
+// n_out x n_in of w_bytes each, X M x n_in, Y M x n_out, workspace of ws_bytes.
+int check_gemm_batch(const void *W, const void *W2, const float *X, const float *Y, const void *ws, int n_out,
+                     int n_in, int M, size_t w_bytes) {
+  if (!W || !X || !Y || !ws) return QDQ_ERR_NULL;
+  if ((n_in % 64) != 0 || (n_out % 128) != 0) return QDQ_ERR_UNSUPPORTED;
+  if (!aligned(W, 16) || (W2 && !aligned(W2, 16)) || !aligned(X, 16) || !aligned(Y, 16) || !aligned(ws, 256))
+    return QDQ_ERR_ALIGN;
+  const size_t xb = size_t(M) * n_in * 4, yb = size_t(M) * n_out * 4;
+  const size_t wsb = size_t(M) * n_in * 2;  // at least the bf16 activations (the exact size needs the device)
+  if (overlaps(Y, yb, W, w_bytes) || (W2 && overlaps(Y, yb, W2, w_bytes)) || overlaps(Y, yb, X, xb) ||
+      overlaps(Y, yb, ws, wsb) || overlaps(ws, wsb, W, w_bytes) || (W2 && overlaps(ws, wsb, W2, w_bytes)) ||
+      overlaps(ws, wsb, X, xb))
+    return QDQ_ERR_ALIAS;
+  return QDQ_OK;
+}
+}  // namespace
 
 int qdq_q8_0_gemm_batch(const void *W, const float *X, float *Y, void *workspace, int n_out, int n_in,
                         int M, cudaStream_t stream) {
   if (!W || !X || !Y || !workspace) return QDQ_ERR_NULL;
   if (!dims_q8(n_out, n_in) || M < 1) return QDQ_ERR_DIMS;
-  if ((n_in % 64) != 0 || (n_out % 128) != 0) return QDQ_ERR_UNSUPPORTED;
-  if (!aligned(W, 16) || !aligned(X, 16) || !aligned(Y, 16) || !aligned(workspace, 128))
-    return QDQ_ERR_ALIGN;
-  const size_t wb = q8_bytes(n_out, n_in), xb = size_t(M) * n_in * 4, yb = size_t(M) * n_out * 4;
-  const size_t ws = qdq_q8_0_gemm_batch_workspace_bytes(M, n_in);
-  if (overlaps(Y, yb, W, wb) || overlaps(Y, yb, X, xb) || overlaps(Y, yb, workspace, ws) ||
-      overlaps(workspace, ws, W, wb) || overlaps(workspace, ws, X, xb))
-    return QDQ_ERR_ALIAS;
+  const int rc = check_gemm_batch(W, nullptr, X, Y, workspace, n_out, n_in, M, q8_bytes(n_out, n_in));
+  if (rc != QDQ_OK) return rc;
   return launch_q8_0_gemm_batch(W, X, Y, workspace, n_out, n_in, M, stream);
+}
+
+int qdq_q4k_gemm_batch(const void *W, const float *X, float *Y, void *workspace, int n_out, int n_in,
+                       int M, cudaStream_t stream) {
+  if (!W || !X || !Y || !workspace) return QDQ_ERR_NULL;
+  if (!dims_q4k(n_out, n_in) || M < 1) return QDQ_ERR_DIMS;
+  const int rc = check_gemm_batch(W, nullptr, X, Y, workspace, n_out, n_in, M, q4k_bytes(n_out, n_in));
+  if (rc != QDQ_OK) return rc;
+  return launch_q4k_gemm_batch(W, X, Y, workspace, n_out, n_in, M, stream);
+}
+
+int qdq_q4k_swiglu_batch(const void *Wg, const void *Wu, const float *X, float *mid, void *workspace, int n_ff,
+                         int n_embd, int M, cudaStream_t stream) {
+  if (!Wg || !Wu || !X || !mid || !workspace) return QDQ_ERR_NULL;
+  if (!dims_q4k(n_ff, n_embd) || M < 1) return QDQ_ERR_DIMS;
+  const int rc = check_gemm_batch(Wg, Wu, X, mid, workspace, n_ff, n_embd, M, q4k_bytes(n_ff, n_embd));
+  if (rc != QDQ_OK) return rc;
+  return launch_q4k_swiglu_batch(Wg, Wu, X, mid, workspace, n_ff, n_embd, M, stream);
 }
 
 }  // extern "C"

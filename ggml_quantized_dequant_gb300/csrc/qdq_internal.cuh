@@ -121,8 +121,16 @@ int launch_q6k_gemv(const void *W, const float *x, float *y, int n_out, int n_in
 // each returns its count since the last call and resets it (-1 on CUDA error).
 int read_gemm_timeouts();
 int read_xs_timeouts();
+// Tensor-core batch GEMMs (qdq_gemm_tc.cu).  The workspace holds X in bf16, the
+// split-K partial tiles and one ticket per output tile; gemm_workspace_bytes is its
+// size for `na` weight matrices on the current device (0 on a CUDA error).
+size_t gemm_workspace_bytes(int M, int n_out, int n_in, int na);
 int launch_q8_0_gemm_batch(const void *W, const float *X, float *Y, void *workspace, int n_out,
                            int n_in, int M, cudaStream_t s);
+int launch_q4k_gemm_batch(const void *W, const float *X, float *Y, void *workspace, int n_out,
+                          int n_in, int M, cudaStream_t s);
+int launch_q4k_swiglu_batch(const void *Wg, const void *Wu, const float *X, float *mid, void *workspace, int n_ff,
+                            int n_embd, int M, cudaStream_t s);
 
 // ---------------------------------------------------------------- device side
 

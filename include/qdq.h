@@ -11,7 +11,8 @@
  *     try_q4k_soa_ffn_block / _ffn_block_residual   -> qdq_q4k_ffn_residual
  *     preload_q4k_soa_weights (one-time upload)     -> qdq_q8_0_pack / qdq_q4k_pack
  *   "Module cuda_lane", Goal (batch prefill-shaped GEMMs on tensor cores) and
- *   "weight_cache.rs", try_cuda_batch_gemv          -> qdq_q8_0_gemm_batch
+ *   "weight_cache.rs", try_cuda_batch_gemv          -> qdq_q8_0_gemm_batch / qdq_q4k_gemm_batch /
+ *                                                      qdq_q4k_swiglu_batch
  *   "QTensorEngine", dispatch_output_top1_chunked   -> qdq_q8_0_logits_argmax
  *   "QTensorEngine", dispatch_output_topk_chunked   -> qdq_topk_rows / qdq_q8_0_logits_topk
  *   "QTensorEngine", embedding_pipeline (Q6_K dequant + matmul on the GPU),
@@ -254,22 +255,36 @@ int qdq_q4k_ffn_residual_noalloc(const void *Wg, const void *Wu, const void *Wd,
                                  const float *x, const float *residual, float *out,
                                  int n_embd, int n_ff, int batch, cudaStream_t stream);
 
-/* ---- batch-prefill GEMM on tensor cores -----------------------------------
+/* ---- batch-prefill GEMMs on tensor cores -----------------------------------
  * "Module cuda_lane", Goal (tensor-core GEMM for batch prefill-shaped work)
  * and "weight_cache.rs", try_cuda_batch_gemv (hidden packed batch x n_in,
  * W row-major n_out x n_in, out batch x n_out; the reference pads to 16 and
  * trims, this call masks instead):
  *   Y[m, r] = sum_k bf16(X[m, k]) * bf16(w[r, k])   (f32 accumulation)
- * W: packed Q8_0 (16-byte aligned).  X: M x n_in f32 (16-byte aligned).
+ * with w the exact f32 dequantised weight (Q8_0 d*q; Q4_K RN(d*sc*q - dmin*m)).
+ * W: packed Q8_0 / Q4_K (16-byte aligned).  X: M x n_in f32 (16-byte aligned).
  * Y: M x n_out f32 (16-byte aligned), must not overlap W, X or workspace.
- * workspace: caller-owned scratch of qdq_q8_0_gemm_batch_workspace_bytes(M,
- * n_in) bytes, 128-byte aligned, overwritten (X rounded to bf16).
- * Requires n_in % 64 == 0 and n_out % 128 == 0; M >= 1 (tail masked).
+ * workspace: caller-owned scratch of qdq_gemm_batch_workspace_bytes(M, n_out,
+ * n_in) bytes (the size depends on the current device's SM count, 0 when it
+ * cannot be queried), 256-byte aligned, overwritten: X rounded to bf16, the
+ * split-K partial tiles, one counter per output tile.
+ * Requires n_in % 64 == 0 (Q4_K: % 256) and n_out % 128 == 0; M >= 1 (tail
+ * masked).  Results do not depend on the order in which CTAs run (split-K
+ * partials are added in a fixed order).
  * Error against the exact sum: <= 4e-3 * sum_k |w[r,k]| |X[m,k]|.
+ * qdq_q4k_swiglu_batch: the SwiGLU expansion for M tokens ("Module cuda_lane",
+ * try_q4k_soa_fused_swiglu, prefill-shaped): mid[m, i] = silu(g[m, i]) * u[m, i]
+ * with g, u the two GEMMs above against Wg, Wu (packed Q4_K n_ff x n_embd), in
+ * one kernel; workspace of qdq_q4k_swiglu_batch_workspace_bytes(M, n_ff, n_embd).
  */
-size_t qdq_q8_0_gemm_batch_workspace_bytes(int M, int n_in);
+size_t qdq_gemm_batch_workspace_bytes(int M, int n_out, int n_in);
 int qdq_q8_0_gemm_batch(const void *W, const float *X, float *Y, void *workspace,
                         int n_out, int n_in, int M, cudaStream_t stream);
+int qdq_q4k_gemm_batch(const void *W, const float *X, float *Y, void *workspace,
+                       int n_out, int n_in, int M, cudaStream_t stream);
+size_t qdq_q4k_swiglu_batch_workspace_bytes(int M, int n_ff, int n_embd);
+int qdq_q4k_swiglu_batch(const void *Wg, const void *Wu, const float *X, float *mid, void *workspace,
+                         int n_ff, int n_embd, int M, cudaStream_t stream);
 
 /* ---- pipeline health -------------------------------------------------------
  * Every wait inside the tensor-core pipeline is bounded (2 s wall clock); a

@@ -217,3 +217,106 @@ def test_topk_ties_nans_and_signed_zeros(cuda_lib):
     # the oracle's selection on the same logits (row 0: an identity projection reproduces them)
     o = oracle.logits_topk(np.eye(n, dtype=np.float32), lg[:1], k)
     assert np.array_equal(o["index"][0], ix[0].astype(np.int64))
+
+
+# ------------------------------------------------------------------ Q4_K batch GEMM / SwiGLU on tensor cores
+
+def _gemm_q4k(qdq, wb, X, n_out, n_in, M):
+    import torch
+    W = qdq.upload_q4k(wb, n_out, n_in)
+    Y = _nan(M, n_out)
+    ws = torch.empty(qdq.gemm_batch_workspace_bytes(M, n_out, n_in), dtype=torch.uint8, device=_dev())
+    qdq.q4k_gemm_batch(W, _t(X), Y, ws, n_out, n_in, M)
+    return _np(Y)
+
+
+def _tile_sample(M, seed):
+    """All rows for small M, else 32 rows from each 256-token tile."""
+    if M <= 64:
+        return np.arange(M)
+    return np.sort(np.concatenate([t * 256 + np.random.default_rng(seed + t).choice(min(256, M - t * 256),
+                                                                                   min(32, M - t * 256), replace=False)
+                                   for t in range((M + 255) // 256)]))
+
+
+@pytest.mark.parametrize("n_out,n_in,M", [(256, 512, 1), (256, 512, 16), (256, 512, 20), (256, 512, 64),
+                                          (256, 512, 100), (256, 512, 257), (384, 1024, 33), (128, 256, 16),
+                                          (1024, 2048, 130), (512, 768, 300)])
+def test_q4k_gemm_batch_parity(cuda_lib, n_out, n_in, M):
+    rng = np.random.default_rng(n_out + n_in + M)
+    wb, X = synth.q4k_blocks(rng, n_out, n_in), synth.activations(rng, M, n_in)
+    Y = _gemm_q4k(cuda_lib, wb, X, n_out, n_in, M)
+    Y_ref, A = oracle.gemm_batch(oracle.q4k_dequant(wb, n_out, n_in), X)
+    assert gemv_excess(Y, Y_ref, A, rel=4e-3) <= 1.0
+    assert cuda_lib.pipeline_timeouts() == 0
+
+
+@pytest.mark.parametrize("kind", [0, 1])
+@pytest.mark.parametrize("M", [16, 64, 512])
+def test_q4k_gemm_batch_full_size(cuda_lib, kind, M):
+    # the config-2/3 shapes: 3072 -> 8192 (gate / up) and 8192 -> 3072 (down)
+    n_out, n_in = (8192, 3072) if kind == 0 else (3072, 8192)
+    rng = np.random.default_rng(70 + kind)
+    wb, X = synth.q4k_blocks(rng, n_out, n_in), synth.activations(rng, M, n_in)
+    Y = _gemm_q4k(cuda_lib, wb, X, n_out, n_in, M)
+    rows = _tile_sample(M, M)
+    Y_ref, A = oracle.gemm_batch(oracle.q4k_dequant(wb, n_out, n_in), X[rows])
+    assert gemv_excess(Y[rows], Y_ref, A, rel=4e-3) <= 1.0
+
+
+def test_q4k_gemm_batch_m1_matches_gemv_within_bf16_bound(cuda_lib):
+    qdq = cuda_lib
+    rng = np.random.default_rng(72)
+    wb, x = synth.q4k_blocks(rng, 512, 1024), synth.activations(rng, 1, 1024)
+    Y = _gemm_q4k(qdq, wb, x, 512, 1024, 1)
+    W = qdq.upload_q4k(wb, 512, 1024)
+    y = _nan(1, 512)
+    qdq.q4k_gemv(W, _t(x), y, 512, 1024, 1)
+    _, a = oracle.gemv(oracle.q4k_dequant(wb, 512, 1024), x)
+    assert np.all(np.abs(Y - _np(y)) <= 4e-3 * a)
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4k"])
+def test_gemm_batch_split_k_is_deterministic(cuda_lib, fmt):
+    # small M on a 3072-row matrix splits K across CTAs; the partials are added in a
+    # fixed order, so two calls give the same bits
+    import torch
+    qdq = cuda_lib
+    n_out, n_in, M = 3072, 8192, 16
+    rng = np.random.default_rng(73)
+    X = _t(synth.activations(rng, M, n_in))
+    if fmt == "q8_0":
+        W, f = qdq.upload_q8_0(synth.q8_0_blocks(rng, n_out, n_in), n_out, n_in), qdq.q8_0_gemm_batch
+    else:
+        W, f = qdq.upload_q4k(synth.q4k_blocks(rng, n_out, n_in), n_out, n_in), qdq.q4k_gemm_batch
+    ws = torch.empty(qdq.gemm_batch_workspace_bytes(M, n_out, n_in), dtype=torch.uint8, device=_dev())
+    outs = []
+    for _ in range(3):
+        Y = _nan(M, n_out)
+        f(W, X, Y, ws, n_out, n_in, M)
+        outs.append(_np(Y))
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+    assert np.array_equal(outs[0].view(np.uint32), outs[2].view(np.uint32))
+
+
+def _swiglu_batch_bound(s, rel=4e-3):
+    # the batch bound through silu (|silu'| <= 1.1) and the product, plus expf's ulp
+    return (1.1 * np.abs(s["u"]) * rel * s["A_g"] + np.abs(oracle.silu(s["g"])) * rel * s["A_u"]
+            + 1e-6 * np.abs(s["mid"]))
+
+
+@pytest.mark.parametrize("n_ff,n_embd,M", [(512, 256, 20), (1024, 512, 130), (256, 1024, 1), (8192, 3072, 64)])
+def test_q4k_swiglu_batch_parity(cuda_lib, n_ff, n_embd, M):
+    import torch
+    qdq = cuda_lib
+    rng = np.random.default_rng(n_ff + n_embd + M)
+    g, u = synth.q4k_blocks(rng, n_ff, n_embd), synth.q4k_blocks(rng, n_ff, n_embd)
+    X = synth.activations(rng, M, n_embd)
+    Wg, Wu = qdq.upload_q4k(g, n_ff, n_embd), qdq.upload_q4k(u, n_ff, n_embd)
+    mid = _nan(M, n_ff)
+    ws = torch.empty(qdq.q4k_swiglu_batch_workspace_bytes(M, n_ff, n_embd), dtype=torch.uint8, device=_dev())
+    qdq.q4k_swiglu_batch(Wg, Wu, _t(X), mid, ws, n_ff, n_embd, M)
+    rows = _tile_sample(M, 5)[:16]
+    s = oracle.swiglu(oracle.q4k_dequant(g, n_ff, n_embd), oracle.q4k_dequant(u, n_ff, n_embd), X[rows])
+    assert np.all(np.abs(_np(mid)[rows] - s["mid"]) <= _swiglu_batch_bound(s))
+    assert qdq.pipeline_timeouts() == 0

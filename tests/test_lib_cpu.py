@@ -59,7 +59,10 @@ def test_packed_sizes(lib):
     assert lib.qdq_q8_0_packed_bytes(4, 33) == 0
     assert lib.qdq_q4k_packed_bytes(4, 300) == 0
     assert lib.qdq_q8_0_packed_bytes(0, 32) == 0
-    assert lib.qdq_q8_0_gemm_batch_workspace_bytes(16, 3072) == 16 * 3072 * 2
+    # the GEMM workspace size needs the device (its SM count): 0 without one, else at least X in bf16
+    ws = lib.qdq_gemm_batch_workspace_bytes(16, 8192, 3072)
+    assert ws == 0 or ws >= 16 * 3072 * 2
+    assert lib.qdq_gemm_batch_workspace_bytes(0, 8192, 3072) == 0
 
 
 def test_gemv_argument_validation(lib):
@@ -213,3 +216,17 @@ def test_topk_validation_and_sizes(lib):
     assert g(W, x, lg, ws, idx, val, 1000, 512, 1, 0, None) == qdq.QDQ_ERR_DIMS
     assert g(W, x, lg, ws, idx, x, 1000, 512, 1, 8, None) == qdq.QDQ_ERR_ALIAS   # value over x
     assert g(W, x, lg, W + 16, idx, val, 1000, 512, 1, 8, None) == qdq.QDQ_ERR_ALIAS
+
+
+def test_q4k_gemm_and_swiglu_batch_validation(lib):
+    import ggml_quantized_dequant_gb300 as qdq
+    W, X, Y, ws, W2 = GOOD, GOOD + (1 << 28), GOOD + (2 << 28), GOOD + (3 << 28), GOOD + (4 << 28)
+    assert lib.qdq_q4k_gemm_batch(W, X, Y, None, 256, 512, 16, None) == qdq.QDQ_ERR_NULL
+    assert lib.qdq_q4k_gemm_batch(W, X, Y, ws, 256, 320, 16, None) == qdq.QDQ_ERR_DIMS       # n_in % 256
+    assert lib.qdq_q4k_gemm_batch(W, X, Y, ws, 200, 512, 16, None) == qdq.QDQ_ERR_UNSUPPORTED  # n_out % 128
+    assert lib.qdq_q4k_gemm_batch(W, X, Y, ws + 128, 256, 512, 16, None) == qdq.QDQ_ERR_ALIGN
+    assert lib.qdq_q4k_gemm_batch(W, X, W + 16, ws, 256, 512, 16, None) == qdq.QDQ_ERR_ALIAS
+    assert lib.qdq_q4k_swiglu_batch(W, None, X, Y, ws, 512, 256, 16, None) == qdq.QDQ_ERR_NULL
+    assert lib.qdq_q4k_swiglu_batch(W, W2 + 8, X, Y, ws, 512, 256, 16, None) == qdq.QDQ_ERR_ALIGN
+    assert lib.qdq_q4k_swiglu_batch(W, W2, X, W2 + 64, ws, 512, 256, 16, None) == qdq.QDQ_ERR_ALIAS
+    assert lib.qdq_q4k_swiglu_batch(W, W2, X, Y, ws, 512, 256, 0, None) == qdq.QDQ_ERR_DIMS
