@@ -33,6 +33,7 @@ QDQ_OPT_CTAS_PER_SM = 3
 QDQ_OPT_XS_GROUPS = 4
 QDQ_OPT_XS_STAGES = 5
 QDQ_OPT_XS_FLOAT_X = 6
+QDQ_OPT_BATCH1_KERNEL = 7
 
 _c_int, _c_size, _c_vp, _c_char_p = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_char_p
 

@@ -20,6 +20,7 @@ std::atomic<int> g_opt_ctas_per_sm{0};
 std::atomic<int> g_opt_xs_groups{0};
 std::atomic<int> g_opt_xs_stages{0};
 std::atomic<int> g_opt_xs_float_x{1};
+std::atomic<int> g_opt_batch1_kernel{0};
 
 constexpr int kMaxDevices = 64;
 std::once_flag g_dev_once[kMaxDevices];
@@ -41,6 +42,7 @@ int opt_ctas_per_sm() { return g_opt_ctas_per_sm.load(std::memory_order_relaxed)
 int opt_xs_groups() { return g_opt_xs_groups.load(std::memory_order_relaxed); }
 int opt_xs_stages() { return g_opt_xs_stages.load(std::memory_order_relaxed); }
 int opt_xs_float_x() { return g_opt_xs_float_x.load(std::memory_order_relaxed); }
+int opt_batch1_kernel() { return g_opt_batch1_kernel.load(std::memory_order_relaxed); }
 
 int fail_cuda(cudaError_t e) {
   g_last_cuda_error = int(e);
@@ -207,6 +209,9 @@ int qdq_set_option(int key, int value) {
     case QDQ_OPT_XS_FLOAT_X:
       if (value != 0 && value != 1) return QDQ_ERR_DIMS;
       return g_opt_xs_float_x.exchange(value);
+    case QDQ_OPT_BATCH1_KERNEL:
+      if (value != 0 && value != 1) return QDQ_ERR_DIMS;
+      return g_opt_batch1_kernel.exchange(value);
     default: return QDQ_ERR_DIMS;
   }
 }

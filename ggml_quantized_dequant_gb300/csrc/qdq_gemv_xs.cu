@@ -740,6 +740,9 @@ bool gemv_xs_supported(int n_in, int batch, int fmt) {
 
 int launch_gemv_xs(int fmt, int mode, const void *W, const void *W2, const float *x, const float *residual,
                    float *y, int n_out, int n_in, cudaStream_t s) {
+  // the f32 arithmetic runs in the direct-load kernel unless the ring kernel is selected
+  if (opt_batch1_kernel() == 0 && (opt_xs_float_x() || fmt == 2))
+    return launch_gemv_dl(fmt, mode, W, W2, x, residual, y, n_out, n_in, s);
   DeviceInfo di;
   const cudaError_t e = device_info(&di);
   if (e != cudaSuccess) return fail_cuda(e);
@@ -760,6 +763,8 @@ int launch_gemv_xs(int fmt, int mode, const void *W, const void *W2, const float
 
 int launch_gemv_xs_qkv(const void *Wq, const void *Wk, const void *Wv, const float *x, float *q, float *k, float *v,
                        int n_q, int n_kv, int n_in, cudaStream_t s) {
+  if (opt_batch1_kernel() == 0 && opt_xs_float_x())
+    return launch_gemv_dl_qkv(Wq, Wk, Wv, x, q, k, v, n_q, n_kv, n_in, s);
   DeviceInfo di;
   const cudaError_t e = device_info(&di);
   if (e != cudaSuccess) return fail_cuda(e);

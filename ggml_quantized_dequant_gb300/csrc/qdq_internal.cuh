@@ -24,6 +24,7 @@ inline int ctas_per_sm_or(int dflt) {
 int opt_xs_groups();
 int opt_xs_stages();
 int opt_xs_float_x();
+int opt_batch1_kernel();
 
 // Per-device facts queried once (SM count, opt-in shared memory).
 struct DeviceInfo {
@@ -112,6 +113,11 @@ int launch_gemv_xs(int fmt, int mode, const void *W, const void *W2, const float
 size_t topk_workspace_bytes(int n, int batch, int k);
 int launch_topk_rows(const float *logits, int n, int batch, int k, void *workspace, int *index, float *value,
                      cudaStream_t s);
+// Batch-1 direct-load GEMV (qdq_gemv_dl.cu), f32 arithmetic; same fmt / mode as launch_gemv_xs.
+int launch_gemv_dl(int fmt, int mode, const void *W, const void *W2, const float *x, const float *residual, float *y,
+                   int n_out, int n_in, cudaStream_t s);
+int launch_gemv_dl_qkv(const void *Wq, const void *Wk, const void *Wv, const float *x, float *q, float *k, float *v,
+                       int n_q, int n_kv, int n_in, cudaStream_t s);
 // Q6_K (qdq_q6k.cu): repack, dequantisation, embedding-row lookup, GEMV (batch 1..8).
 int launch_q6k_pack(const void *ggml, void *packed, int n_out, int n_in, cudaStream_t s);
 int launch_q6k_dequant(const void *W, float *out, int n_out, int n_in, cudaStream_t s);
@@ -405,6 +411,29 @@ __device__ __forceinline__ float2 q4k_field_to_f2(uint32_t f, const Magic &k) {
 __device__ __forceinline__ float q4k_mu(float2 DDm) {
   const float mu = rintf(__fdividef(DDm.y, DDm.x));
   return fminf(fmaxf(mu, 0.f), 15.f);  // a NaN quotient (0 / 0) gives 0
+}
+
+// Reduce v[0..3] (one partial per row per lane) over the warp by recursive
+// halving; afterwards lane 8k holds the warp total of row k.
+__device__ __forceinline__ void butterfly4_rows(float v[4], int lane) {
+  {
+    const bool up = lane & 16;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float send = up ? v[i] : v[i + 2];
+      const float keep = up ? v[i + 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+  }
+  {
+    const bool up = lane & 8;
+    const float send = up ? v[0] : v[1];
+    const float keep = up ? v[1] : v[0];
+    v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 4);
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -316,6 +316,12 @@ int qdq_pipeline_timeouts(void);
  *     blocks whose largest activation they skip.  A block with an inf or NaN
  *     activation gives NaN outputs. */
 #define QDQ_OPT_XS_FLOAT_X   6
+/* Batch-1 kernel of the f32 arithmetic: 0 (default) the direct-load kernel (weights straight into
+ * registers after an L2 prefetch of each CTA's rows, every warp of the SM computing); 1 the
+ * shared-memory ring kernel (a producer warp streams weights into a ring sized to half an SM, so
+ * that the next kernel's CTA can start streaming beside it).  Same results within the stated
+ * bound; the fixed-point arithmetic always runs in the ring kernel. */
+#define QDQ_OPT_BATCH1_KERNEL 7
 /* Sets a process-wide option; returns the previous value, or QDQ_ERR_DIMS for a bad key/value. */
 int qdq_set_option(int key, int value);
 
