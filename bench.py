@@ -54,9 +54,12 @@ def measured_peaks():
 
 
 # CUDA sources that define each profiled kernel (a recorded counter is stale once any of them changes)
+_DL = ["qdq_gemv_dl.cu", "qdq_internal.cuh"]
+_TC = ["qdq_gemm_tc.cu", "qdq_internal.cuh"]
 KERNEL_SOURCES = {
-    "q8_0_gemv": ["qdq_gemv_xs.cu", "qdq_internal.cuh"],
-    "q4k_ffn": ["qdq_gemv_xs.cu", "qdq_internal.cuh"],
+    "q8_0_gemv": _DL, "q4k_gemv": _DL, "q4k_ffn": _DL, "q4k_qkv": _DL, "q8_0_vocab": _DL, "q6k_gemv": _DL,
+    "q8_0_gemm_M16": _TC, "q8_0_gemm_M64": _TC, "q8_0_gemm_M512": _TC,
+    "q4k_gemm_M16": _TC, "q4k_gemm_M64": _TC, "q4k_gemm_M512": _TC,
 }
 
 
@@ -173,76 +176,131 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU oracle legs
 
-def oracle_rate(n_rows: int, seconds_budget: float):
-    """Time the CPU oracle (dequant + float64 GEMV) on row samples of config-1 matrices.
+_ORACLE_DATA = None
 
-    Returns (bytes_per_s, rows_done, seconds, matrices_rows).  The sample is the
-    first `n_rows` rows of layer 0's up and down matrices, repeated until the
-    budget is spent; bytes are the sampled rows' GGML weight bytes plus x and y.
-    """
-    import oracle
+
+def _oracle_init():
+    """Pool-worker set-up: the config-1 layer-0 up and down matrices and their activations."""
+    global _ORACLE_DATA
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
     import synth
-    up, down = synth.config1_up(0), synth.config1_down(0)
-    x_up = synth.config1_x()
-    x_dn = synth.activations(synth.rng_for(1, 3), 1, N_FF)
-    done_bytes, done_rows, t_used = 0, 0, 0.0
-    while t_used < seconds_budget:
-        for w, n_in, x in ((up, N_EMBD, x_up), (down, N_FF, x_dn)):
-            t0 = time.perf_counter()
-            wd = oracle.q8_0_dequant(w[:n_rows], n_rows, n_in)
-            oracle.gemv(wd, x)
-            t_used += time.perf_counter() - t0
-            done_bytes += n_rows * (n_in // 32 * 34) + n_in * 4 + n_rows * 4
-            done_rows += n_rows
-    return done_bytes / t_used, done_rows, t_used
+    _ORACLE_DATA = (synth.config1_up(0), synth.config1_down(0), synth.config1_x(),
+                    synth.activations(synth.rng_for(1, 3), 1, N_FF))
+
+
+def _oracle_unit(job):
+    """One unit of CPU-oracle work: dequantise + float64 GEMV of `rows` rows (from row r0) of the
+    up and of the down matrix.  Returns the algorithmic bytes of the unit and its seconds."""
+    import oracle
+    r0, rows = job
+    if _ORACLE_DATA is None:
+        _oracle_init()
+    up, down, x_up, x_dn = _ORACLE_DATA
+    t0 = time.perf_counter()
+    for w, n_in, x in ((up, N_EMBD, x_up), (down, N_FF, x_dn)):
+        a = r0 % (w.shape[0] - rows + 1)
+        oracle.gemv(oracle.q8_0_dequant(w[a:a + rows], rows, n_in), x)
+    dt = time.perf_counter() - t0
+    nbytes = rows * (N_EMBD // 32 * 34 + N_FF // 32 * 34) + (N_EMBD + N_FF) * 4 + 2 * rows * 4
+    return nbytes, dt
+
+
+def host_facts():
+    """(logical CPUs this process may use, CPU model string) of the machine."""
+    n = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        import platform
+        model = platform.processor() or platform.machine()
+    return n, model
+
+
+class OraclePool:
+    """The CPU oracle on all host cores: a spawn-started process pool (safe beside CUDA)."""
+
+    def __init__(self, cores: int):
+        import multiprocessing as mp
+        self.cores = cores
+        self.pool = mp.get_context("spawn").Pool(cores, initializer=_oracle_init)
+        self.pool.map(_oracle_unit, [(0, 8)] * cores)  # warm every worker (imports, matrices)
+
+    def run(self, rows: int, first: int = 0):
+        """One unit of `rows` rows on every core at once: (bytes, wall seconds)."""
+        t0 = time.perf_counter()
+        res = self.pool.map(_oracle_unit, [((first + i) * rows, rows) for i in range(self.cores)])
+        return sum(b for b, _ in res), time.perf_counter() - t0
+
+    def close(self):
+        self.pool.terminate()
+        self.pool.join()
 
 
 def cpu_baseline(budget_s: float = 12.0):
-    rate, rows, secs = oracle_rate(512, budget_s)
-    return {"value": rate / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": "CPU oracle (numpy: own fp16 decode, f32 dequant, float64 GEMV, one thread) on the first "
-                      "512 rows of config-1 layer-0 up (3072->8192) and down (8192->3072) Q8_0 matrices, "
-                      "%d rows in %.1f s" % (rows, secs)}
+    """The CPU oracle timed on one thread and on all host cores (GB/s of algorithmic bytes)."""
+    cores, model = host_facts()
+    _oracle_init()
+    rows = 256
+    # one thread: repeat the unit until about a third of the budget is spent
+    nb1, t1, i = 0, 0.0, 0
+    while t1 < budget_s / 3:
+        b, dt = _oracle_unit((i * rows, rows))
+        nb1, t1, i = nb1 + b, t1 + dt, i + 1
+    one = nb1 / t1 / 1e9
+    # all cores: one unit per core at once, repeated for the rest of the budget
+    pool = OraclePool(cores)
+    try:
+        nbp, tp, j = 0, 0.0, 0
+        while tp < budget_s / 2:
+            b, dt = pool.run(rows, first=j * cores)
+            nbp, tp, j = nbp + b, tp + dt, j + 1
+    finally:
+        pool.close()
+    allc = nbp / tp / 1e9
+    return {"value": allc, "unit": "GB/s", "cores": cores, "kind": "oracle", "cpu_model": model,
+            "value_1_thread": one, "threads_1": 1,
+            "sample": "CPU oracle (numpy: own fp16 decode, f32 dequant, float64 GEMV) on row samples of the "
+                      "config-1 layer-0 up (3072->8192) and down (8192->3072) Q8_0 matrices: %d rows of each per "
+                      "unit; one thread: %d units in %.1f s; all %d cores (%s, one process each): %d rounds of "
+                      "%d units in %.1f s" % (rows, i, t1, cores, model, j, cores, tp)}
 
 
 def run_reference(args, rank: int, world: int):
     if rank != 0:
         return 0
-    # size each step so the whole --warmup + --steps run takes about a minute
-    per_step_s = max(0.01, 60.0 / max(1, args.steps + args.warmup))
-    import oracle
-    import synth
-    up, down = synth.config1_up(0), synth.config1_down(0)
-    x_up = synth.config1_x()
-    x_dn = synth.activations(synth.rng_for(1, 3), 1, N_FF)
-    # calibrate rows per step from a 64-row probe
-    t0 = time.perf_counter()
-    oracle.gemv(oracle.q8_0_dequant(up[:64], 64, N_EMBD), x_up)
-    oracle.gemv(oracle.q8_0_dequant(down[:64], 64, N_FF), x_dn)
-    per_row = (time.perf_counter() - t0) / 128
-    rows = int(max(2, min(N_EMBD, per_step_s / per_row / 2)))
-
-    def step(i):
-        r0 = (i * rows) % (N_EMBD - rows + 1)
-        oracle.gemv(oracle.q8_0_dequant(up[r0:r0 + rows], rows, N_EMBD), x_up)
-        oracle.gemv(oracle.q8_0_dequant(down[r0:r0 + rows], rows, N_FF), x_dn)
-        return rows * (N_EMBD // 32 * 34 + N_FF // 32 * 34) + (N_EMBD + N_FF) * 4 + 2 * rows * 4
-
-    for i in range(args.warmup):
-        step(i)
-    t0 = time.perf_counter()
-    nbytes = sum(step(args.warmup + i) for i in range(args.steps))
-    dt = time.perf_counter() - t0
-    gbs = nbytes / dt / 1e9
+    cores, model = host_facts()
+    pool = OraclePool(cores)
+    try:
+        # size each step so the whole --warmup + --steps run takes about a minute
+        per_step_s = max(0.05, 60.0 / max(1, args.steps + args.warmup))
+        b, dt = pool.run(16)
+        rows = int(max(2, min(N_EMBD, 16 * per_step_s / max(dt, 1e-6))))
+        for i in range(args.warmup):
+            pool.run(rows, first=i * cores)
+        nbytes, t_all = 0, 0.0
+        for i in range(args.steps):
+            b, dt = pool.run(rows, first=(args.warmup + i) * cores)
+            nbytes, t_all = nbytes + b, t_all + dt
+    finally:
+        pool.close()
+    gbs = nbytes / t_all / 1e9
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": t_all / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-        "config": {"workload": WORKLOAD, "sample_rows_per_matrix_per_step": rows, "batch": 1,
+        "config": {"workload": WORKLOAD, "sample_rows_per_matrix_per_core_per_step": rows, "batch": 1,
                    "l2": "n/a (CPU)"},
-        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": "%d rows of the config-1 up and down matrices per step (CPU oracle, one thread)"
-                                   % rows},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "cpu_model": model,
+                         "sample": "%d rows of the config-1 up and down matrices per core per step (CPU oracle, "
+                                   "one process per core)" % rows},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -258,6 +316,7 @@ class Timer:
         self.torch = torch
 
     def __call__(self, fn, iters: int) -> float:
+        """Seconds for `iters` back-to-back calls of fn."""
         torch = self.torch
         torch.cuda.synchronize()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -267,6 +326,34 @@ class Timer:
         e.record()
         torch.cuda.synchronize()
         return s.elapsed_time(e) / 1e3
+
+    def each(self, fn, iters: int):
+        """Seconds of each of `iters` back-to-back calls of fn (an event pair around each)."""
+        torch = self.torch
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(iters + 1)]
+        torch.cuda.synchronize()
+        ev[0].record()
+        for i in range(iters):
+            fn()
+            ev[i + 1].record()
+        torch.cuda.synchronize()
+        return [ev[i].elapsed_time(ev[i + 1]) / 1e3 for i in range(iters)]
+
+
+def pct(samples_us):
+    """Median and 10th / 90th percentiles of a list of per-call microseconds."""
+    a = np.asarray(samples_us, dtype=np.float64)
+    return {"median": float(np.median(a)), "p10": float(np.percentile(a, 10)), "p90": float(np.percentile(a, 90)),
+            "samples": int(a.size)}
+
+
+def roofline(bound, units_per_launch, launch_s, peak, unit, traffic, kernel, peak_source):
+    """The roofline object of one kernel: algorithmic bytes (or FLOPs) per launch / its time, against the peak."""
+    scale = 1e9 if unit == "GB/s" else 1e12
+    achieved = units_per_launch / launch_s / scale
+    return {"bound": bound, "kernel": kernel, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": traffic, "peak_source": peak_source,
+            ("bytes_per_launch" if unit == "GB/s" else "flop_per_launch"): units_per_launch}
 
 
 def capture(torch, fn):
@@ -287,6 +374,17 @@ def gen_parallel(fns):
     from concurrent.futures import ThreadPoolExecutor
     with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
         return list(ex.map(lambda f: f(), fns))
+
+
+def time_calls(torch, timer, fn_one, calls, iters, warm=3):
+    """A CUDA graph of `calls` back-to-back calls of fn_one, replayed: mean seconds per call over
+    `iters` replays, and the per-call distribution (each replay's time / calls) in microseconds."""
+    g = capture(torch, lambda: [fn_one(i) for i in range(calls)])
+    for _ in range(warm):
+        g.replay()
+    dt = timer(g.replay, iters)
+    each = timer.each(g.replay, max(10, min(iters, 100)))
+    return dt / (iters * calls), pct([t / calls * 1e6 for t in each])
 
 
 def run_ours(args, rank: int, world: int, local_rank: int):
@@ -346,7 +444,23 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     value_gbs = job_value(bytes_per_step * args.steps, world, t_max) / 1e9
     us_per_matrix = t_max / (args.steps * launches_per_step) * 1e6
     launch_s = t_max / (args.steps * launches_per_step)
-    achieved = bytes_per_launch / launch_s / 1e9
+    # the same graph, each replay timed alone: the per-matrix distribution
+    dist = pct([t / launches_per_step * 1e6 for t in timer.each(g.replay, min(200, max(20, args.steps // 10)))])
+    # the same chain as plain stream launches (no graph)
+    plain_it = max(10, min(100, args.steps // 20))
+    step()
+    plain_us = timer(step, plain_it) / (plain_it * launches_per_step) * 1e6
+    # the launch round trip: an empty kernel, then a host synchronisation, n times
+    stream = torch.cuda.current_stream()
+    for _ in range(20):
+        qdq.noop()
+        stream.synchronize()
+    n_rt = 500
+    t0 = time.perf_counter()
+    for _ in range(n_rt):
+        qdq.noop()
+        stream.synchronize()
+    rt_us = (time.perf_counter() - t0) / n_rt * 1e6
 
     # ---------------- e2e: public API calls, pinned host x in, host y out, every step ----------------
     x_pin = torch.from_numpy(x_host).pin_memory()
@@ -385,10 +499,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             dtf = timer(gf.replay, it)
         finally:
             qdq.set_option(qdq.QDQ_OPT_XS_FLOAT_X, old)
-        usf = dtf / (it * launches_per_step) * 1e6
+        lsf = dtf / (it * launches_per_step)
         rows["q8_0_decode_28L_fixed_point_optin"] = {
-            "us_per_matrix": usf, "gbs": bytes_per_launch / usf / 1e3,
-            "frac_hbm": bytes_per_launch / usf / 1e3 / peaks["hbm_gbs"],
+            "us_per_matrix": lsf * 1e6,
+            "roofline": roofline("hbm", bytes_per_launch, lsf, peaks["hbm_gbs"], "GB/s", None,
+                                 "gemv_xs_kernel<0, 0, 0> (ring kernel, block fixed point)", peaks["source"]),
             "arithmetic": "opt-in block fixed point (bound relative to each block's max |x|, not 1e-5 sum|w||x|)"}
         del gf
         rows.update(measure_rows(torch, qdq, synth, dev, timer, peaks, args))
@@ -399,17 +514,17 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "batch": 1, "layers": N_LAYERS, "shapes": "up 3072->8192, down 8192->3072",
-                   "format": "GGML Q8_0", "us_per_matrix": us_per_matrix,
+                   "format": "GGML Q8_0", "us_per_matrix": us_per_matrix, "us_per_matrix_dist": dist,
+                   "plain_launch_us_per_matrix": plain_us, "launch_roundtrip_us": rt_us,
                    "frac_of_hbm_peak": value_gbs / world / peaks["hbm_gbs"],
                    "l2": "inputs larger than L2: 56 distinct matrices, 1.50 GB, cycled every step",
                    "timing": "CUDA graph of one step (56 launches, programmatic dependent launch), "
-                             "replayed; CUDA events on the replay stream",
+                             "replayed; CUDA events on the replay stream; plain stream launches and one "
+                             "event pair per replay measured beside it",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "kernel": "gemv_xs_kernel<0, 0, 1> (Q8_0 batch-1 GEMV, f32 arithmetic)", "achieved": achieved,
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": args.traffic if args.traffic is not None else recorded_traffic("q8_0_gemv"),
-                     "peak_source": peaks["source"],
-                     "bytes_per_launch": bytes_per_launch},
+        "roofline": roofline("hbm", bytes_per_launch, launch_s, peaks["hbm_gbs"], "GB/s",
+                             args.traffic if args.traffic is not None else recorded_traffic("q8_0_gemv"),
+                             "gemv_dl_kernel<0, 0> (Q8_0 batch-1 GEMV, f32 arithmetic)", peaks["source"]),
         "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": N_EMBD * 4, "d2h_bytes_per_step": N_EMBD * 4,
                 "steps": e2e_steps, "ms_per_step": e2e_dt / e2e_steps * 1e3,
                 "path": "Python binding -> C ABI per GEMV (no graph), pinned H2D of x and D2H of y each step"},
@@ -424,21 +539,26 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     return 0
 
 
+def _row(us_mean_s, dist, rl, **extra):
+    r = {"us_per_call": us_mean_s * 1e6, "us_dist": dist, "roofline": rl}
+    r.update(extra)
+    return r
+
+
 def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
-    """Every hot-path row on its own workload; each returns microseconds per call and its roofline fraction."""
+    """Every hot-path row on its own workload: microseconds per call (mean and the distribution
+    over replays) and a roofline object for its dominant kernel."""
     rows = {}
     iters = max(20, args.row_steps)
-    hbm = peaks["hbm_gbs"]
+    hbm, src = peaks["hbm_gbs"], peaks["source"]
 
     # config 0: 256 x 512 Q8_0 (L2-resident; microseconds only)
     wb, x0 = synth.config0()
     W0 = qdq.upload_q8_0(wb, 256, 512, device=dev)
     x0d = torch.from_numpy(x0).to(dev)
     y0 = torch.empty((1, 256), device=dev)
-    g0 = capture(torch, lambda: [qdq.q8_0_gemv(W0, x0d, y0, 256, 512, 1) for _ in range(100)])
-    g0.replay()
-    dt = timer(g0.replay, iters)
-    rows["q8_0_gemv_256x512"] = {"us_per_call": dt / (iters * 100) * 1e6, "roofline": "n/a (L2-resident)"}
+    ls, dist = time_calls(torch, timer, lambda i: qdq.q8_0_gemv(W0, x0d, y0, 256, 512, 1), 100, iters)
+    rows["q8_0_gemv_256x512"] = {"us_per_call": ls * 1e6, "us_dist": dist, "roofline": "n/a (L2-resident)"}
 
     # config 2: Q4_K 3072 -> 8192, 28 copies cycled
     ws = gen_parallel([lambda t=t: synth.config2_w(t) for t in range(N_LAYERS)])
@@ -446,14 +566,10 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
     del ws
     x2 = torch.from_numpy(synth.config2_x()).to(dev)
     y2 = torch.empty((1, N_FF), device=dev)
-    g2 = capture(torch, lambda: [qdq.q4k_gemv(W2[t], x2, y2, N_FF, N_EMBD, 1) for t in range(N_LAYERS)])
-    for _ in range(5):
-        g2.replay()
-    dt = timer(g2.replay, iters)
-    us = dt / (iters * N_LAYERS) * 1e6
+    ls, dist = time_calls(torch, timer, lambda t: qdq.q4k_gemv(W2[t], x2, y2, N_FF, N_EMBD, 1), N_LAYERS, iters)
     b = Q4_W_BYTES + (N_EMBD + N_FF) * 4
-    rows["q4k_gemv_3072x8192"] = {"us_per_call": us, "gbs": b / us / 1e3, "frac_hbm": b / us / 1e3 / hbm,
-                                  "bytes_per_call": b}
+    rows["q4k_gemv_3072x8192"] = _row(ls, dist, roofline("hbm", b, ls, hbm, "GB/s", recorded_traffic("q4k_gemv"),
+                                                         "gemv_dl_kernel<1, 0>", src))
     del W2
 
     # config 3: fused Q4_K FFN block with residual, 28 layers
@@ -464,19 +580,37 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
     xh, rh = synth.config3_x_residual()
     x3, r3 = torch.from_numpy(xh).to(dev), torch.from_numpy(rh).to(dev)
     mid = torch.empty((1, N_FF), device=dev)
-
-    def ffn_step():
-        for Wg, Wu, Wd in L:
-            qdq.q4k_ffn_residual(Wg, Wu, Wd, x3, r3, r3, mid, N_EMBD, N_FF, 1)
-
-    g3 = capture(torch, ffn_step)
-    for _ in range(5):
-        g3.replay()
-    dt = timer(g3.replay, iters)
-    us = dt / (iters * N_LAYERS) * 1e6
+    ls, dist = time_calls(torch, timer,
+                          lambda t: qdq.q4k_ffn_residual(L[t][0], L[t][1], L[t][2], x3, r3, r3, mid, N_EMBD, N_FF, 1),
+                          N_LAYERS, iters)
     b = 3 * Q4_W_BYTES + N_EMBD * 4 + N_FF * 4 * 2 + N_EMBD * 4 * 2
-    rows["q4k_ffn_residual_3072x8192"] = {"us_per_block": us, "gbs": b / us / 1e3, "frac_hbm": b / us / 1e3 / hbm,
-                                          "bytes_per_block": b, "launches_per_block": 2}
+    rows["q4k_ffn_residual_3072x8192"] = _row(
+        ls, dist, roofline("hbm", b, ls, hbm, "GB/s", recorded_traffic("q4k_ffn"),
+                           "gemv_dl_kernel<1, 1> + gemv_dl_kernel<1, 2> (2 launches per block)", src),
+        launches_per_block=2)
+    # FFN e2e: per block, one pinned H2D of x and one D2H of out, through the public call
+    xp = torch.from_numpy(xh).pin_memory()
+    op = torch.empty((1, N_EMBD), dtype=torch.float32).pin_memory()
+    xe, oe = torch.empty_like(x3), torch.empty_like(r3)
+    stream = torch.cuda.current_stream()
+
+    def ffn_e2e(t):
+        xe.copy_(xp, non_blocking=True)
+        qdq.q4k_ffn_residual(L[t][0], L[t][1], L[t][2], xe, r3, oe, mid, N_EMBD, N_FF, 1)
+        op.copy_(oe, non_blocking=True)
+        stream.synchronize()
+
+    for t in range(5):
+        ffn_e2e(t)
+    n_e = max(56, min(280, iters))
+    t0 = time.perf_counter()
+    for i in range(n_e):
+        ffn_e2e(i % N_LAYERS)
+    dte = (time.perf_counter() - t0) / n_e
+    rows["q4k_ffn_residual_3072x8192"]["e2e"] = {
+        "value": b / dte / 1e9, "unit": "GB/s", "us_per_block": dte * 1e6, "h2d_bytes_per_block": N_EMBD * 4,
+        "d2h_bytes_per_block": N_EMBD * 4, "blocks": n_e,
+        "path": "Python binding -> C ABI per block (no graph), pinned H2D of x and D2H of out, synchronised"}
     del L
 
     # fused Q4_K QKV projection (GQA 3072 -> 3072 + 1024 + 1024), 28 layers cycled
@@ -486,19 +620,15 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
     del qkv
     xq = torch.from_numpy(synth.activations(synth.rng_for(5, 3), 1, N_EMBD)).to(dev)
     oq, ok, ov = (torch.empty((1, n), device=dev) for n in (synth.N_Q, synth.N_KV, synth.N_KV))
-    gq = capture(torch, lambda: [qdq.q4k_qkv(Wq, Wk, Wv, xq, oq, ok, ov, synth.N_Q, synth.N_KV, N_EMBD, 1)
-                                 for Wq, Wk, Wv in LQ])
-    for _ in range(5):
-        gq.replay()
-    dt = timer(gq.replay, iters)
-    us = dt / (iters * N_LAYERS) * 1e6
+    ls, dist = time_calls(torch, timer, lambda t: qdq.q4k_qkv(LQ[t][0], LQ[t][1], LQ[t][2], xq, oq, ok, ov, synth.N_Q,
+                                                               synth.N_KV, N_EMBD, 1), N_LAYERS, iters)
     rows_q = synth.N_Q + 2 * synth.N_KV
     b = rows_q * (N_EMBD // 256) * 144 + N_EMBD * 4 + rows_q * 4
-    rows["q4k_qkv_3072_q3072_kv1024"] = {"us_per_call": us, "gbs": b / us / 1e3, "frac_hbm": b / us / 1e3 / hbm,
-                                         "bytes_per_call": b}
+    rows["q4k_qkv_3072_q3072_kv1024"] = _row(ls, dist, roofline("hbm", b, ls, hbm, "GB/s", recorded_traffic("q4k_qkv"),
+                                                                "gemv_dl_kernel<1, 3>", src))
     del LQ
 
-    # output projection 3072 -> 128256 (Q8_0, 418 MB: larger than L2) with the on-device argmax
+    # output projection 3072 -> 128256 (Q8_0, 418 MB: larger than L2) with the on-device argmax / top-40
     wb, xo = synth.output_projection()
     WO = qdq.upload_q8_0(wb, synth.N_VOCAB, N_EMBD, device=dev)
     del wb
@@ -506,30 +636,27 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
     lo = torch.empty((1, synth.N_VOCAB), device=dev)
     io = torch.empty((1,), dtype=torch.int32, device=dev)
     vo = torch.empty((1,), device=dev)
-    go = capture(torch, lambda: [qdq.q8_0_logits_argmax(WO, xo, lo, io, vo, synth.N_VOCAB, N_EMBD, 1)
-                                 for _ in range(4)])
-    for _ in range(3):
-        go.replay()
-    dt = timer(go.replay, max(5, iters // 4))
-    us = dt / (max(5, iters // 4) * 4) * 1e6
-    b = synth.N_VOCAB * (N_EMBD // 32) * 34 + N_EMBD * 4 + synth.N_VOCAB * 4 + 8
-    rows["q8_0_logits_argmax_3072x128256"] = {"us_per_call": us, "gbs": b / us / 1e3, "frac_hbm": b / us / 1e3 / hbm,
-                                              "bytes_per_call": b, "launches_per_call": 2}
-
-    # the same projection with the on-device top-40 (k candidates read back instead of the logits)
+    it4 = max(5, iters // 4)
+    bw = synth.N_VOCAB * (N_EMBD // 32) * 34 + N_EMBD * 4 + synth.N_VOCAB * 4
+    ls, dist = time_calls(torch, timer, lambda i: qdq.q8_0_gemv(WO, xo, lo, synth.N_VOCAB, N_EMBD, 1), 4, it4)
+    rows["q8_0_gemv_3072x128256"] = _row(ls, dist, roofline("hbm", bw, ls, hbm, "GB/s",
+                                                            recorded_traffic("q8_0_vocab"), "gemv_dl_kernel<0, 0>", src))
+    ls, dist = time_calls(torch, timer, lambda i: qdq.q8_0_logits_argmax(WO, xo, lo, io, vo, synth.N_VOCAB, N_EMBD, 1),
+                          4, it4)
+    rows["q8_0_logits_argmax_3072x128256"] = _row(
+        ls, dist, roofline("hbm", bw + 8, ls, hbm, "GB/s", None, "gemv_dl_kernel<0, 0> + argmax", src),
+        launches_per_call=2)
     K = 40
     wsk = torch.empty(qdq.topk_workspace_bytes(synth.N_VOCAB, 1, K), dtype=torch.uint8, device=dev)
     ik = torch.empty((1, K), dtype=torch.int32, device=dev)
     vk = torch.empty((1, K), device=dev)
-    gk = capture(torch, lambda: [qdq.q8_0_logits_topk(WO, xo, lo, wsk, ik, vk, synth.N_VOCAB, N_EMBD, 1, K)
-                                 for _ in range(4)])
-    for _ in range(3):
-        gk.replay()
-    dt = timer(gk.replay, max(5, iters // 4))
-    us = dt / (max(5, iters // 4) * 4) * 1e6
-    b = synth.N_VOCAB * (N_EMBD // 32) * 34 + N_EMBD * 4 + synth.N_VOCAB * 4 + 8 * K
-    rows["q8_0_logits_top40_3072x128256"] = {"us_per_call": us, "gbs": b / us / 1e3, "frac_hbm": b / us / 1e3 / hbm,
-                                             "bytes_per_call": b, "launches_per_call": 4}
+    ls, dist = time_calls(torch, timer, lambda i: qdq.q8_0_logits_topk(WO, xo, lo, wsk, ik, vk, synth.N_VOCAB, N_EMBD,
+                                                                        1, K), 4, it4)
+    rows["q8_0_logits_top40_3072x128256"] = _row(
+        ls, dist, roofline("hbm", bw + 8 * K, ls, hbm, "GB/s", None, "gemv_dl_kernel<0, 0> + top-k", src))
+    ls, dist = time_calls(torch, timer, lambda i: qdq.topk_rows(lo, synth.N_VOCAB, 1, K, wsk, ik, vk), 4, it4)
+    rows["top40_128256"] = {"us_per_call": ls * 1e6, "us_dist": dist,
+                            "roofline": "n/a (L2-resident logits, latency-bound sort)"}
     del WO
 
     # Q6_K output projection 3072 -> 128256 (323 MB, larger than L2)
@@ -538,84 +665,62 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
     del wb
     xq6 = torch.from_numpy(xq6).to(dev)
     y6 = torch.empty((1, synth.N_VOCAB), device=dev)
-    g6 = capture(torch, lambda: [qdq.q6k_gemv(W6, xq6, y6, synth.N_VOCAB, N_EMBD, 1) for _ in range(4)])
-    for _ in range(3):
-        g6.replay()
-    dt = timer(g6.replay, max(5, iters // 4))
-    us = dt / (max(5, iters // 4) * 4) * 1e6
+    ls, dist = time_calls(torch, timer, lambda i: qdq.q6k_gemv(W6, xq6, y6, synth.N_VOCAB, N_EMBD, 1), 4, it4)
     b = synth.N_VOCAB * (N_EMBD // 256) * 210 + N_EMBD * 4 + synth.N_VOCAB * 4
-    rows["q6k_gemv_3072x128256"] = {"us_per_call": us, "gbs": b / us / 1e3, "frac_hbm": b / us / 1e3 / hbm,
-                                    "bytes_per_call": b}
+    rows["q6k_gemv_3072x128256"] = _row(ls, dist, roofline("hbm", b, ls, hbm, "GB/s", recorded_traffic("q6k_gemv"),
+                                                           "gemv_dl_kernel<2, 0>", src))
     del W6
 
-    # config 4: tensor-core batch GEMM, 8 copies of each shape cycled
+    # config 4 and the Q4_K prefill shapes: tensor-core batch GEMMs, 8 copies of each shape cycled
     ncopy = 8
-    for kind, (n_out, n_in) in ((0, (N_FF, N_EMBD)), (1, (N_EMBD, N_FF))):
-        wsq = gen_parallel([lambda t=t: synth.config4_w(kind, t) for t in range(ncopy)])
-        Wq = [qdq.upload_q8_0(w, n_out, n_in, device=dev) for w in wsq]
-        del wsq
-        for M in synth.C4_M:
-            X = torch.from_numpy(synth.config4_x(kind, M)).to(dev)
-            Y = torch.empty((M, n_out), device=dev)
-            wsp = torch.empty(qdq.gemm_batch_workspace_bytes(M, n_out, n_in), dtype=torch.uint8, device=dev)
-            gq = capture(torch, lambda: [qdq.q8_0_gemm_batch(w, X, Y, wsp, n_out, n_in, M) for w in Wq])
-            for _ in range(3):
-                gq.replay()
-            it = max(10, iters // 2)
-            dt = timer(gq.replay, it)
-            us = dt / (it * ncopy) * 1e6
-            b = Q8_W_BYTES + M * n_in * 4 + M * n_out * 4
-            flops = 2.0 * M * n_out * n_in
-            r = {"us_per_call": us, "gbs": b / us / 1e3, "tflops": flops / us / 1e6, "bytes_per_call": b,
-                 "flop_per_call": flops, "frac_hbm": b / us / 1e3 / hbm,
-                 "frac_bf16": flops / us / 1e6 / peaks["bf16_tflops"]}
-            r["bound"] = "tensor" if M >= 256 else "hbm"
-            rows["q8_0_gemm_%s_M%d" % ("3072x8192" if kind == 0 else "8192x3072", M)] = r
-        del Wq
-
-    # Q4_K batch GEMM on tensor cores (config-2/3 shapes, 8 copies cycled) and the M-token SwiGLU
-    for kind, (n_out, n_in) in ((0, (N_FF, N_EMBD)), (1, (N_EMBD, N_FF))):
-        wsq = gen_parallel([lambda t=t: synth.q4k_blocks(synth.rng_for(8, kind, t), n_out, n_in)
-                            for t in range(ncopy)])
-        Wq = [qdq.upload_q4k(w, n_out, n_in, device=dev) for w in wsq]
-        del wsq
-        for M in synth.C4_M:
-            X = torch.from_numpy(synth.activations(synth.rng_for(8, 2 + kind, M), M, n_in)).to(dev)
-            Y = torch.empty((M, n_out), device=dev)
-            wsp = torch.empty(qdq.gemm_batch_workspace_bytes(M, n_out, n_in), dtype=torch.uint8, device=dev)
-            gq = capture(torch, lambda: [qdq.q4k_gemm_batch(w, X, Y, wsp, n_out, n_in, M) for w in Wq])
-            for _ in range(3):
-                gq.replay()
-            it = max(10, iters // 2)
-            dt = timer(gq.replay, it)
-            us = dt / (it * ncopy) * 1e6
-            b = Q4_W_BYTES + M * n_in * 4 + M * n_out * 4
-            flops = 2.0 * M * n_out * n_in
-            rows["q4k_gemm_%s_M%d" % ("3072x8192" if kind == 0 else "8192x3072", M)] = {
-                "us_per_call": us, "gbs": b / us / 1e3, "tflops": flops / us / 1e6, "bytes_per_call": b,
-                "flop_per_call": flops, "frac_hbm": b / us / 1e3 / hbm,
-                "frac_bf16": flops / us / 1e6 / peaks["bf16_tflops"], "bound": "tensor" if M >= 256 else "hbm"}
-        if kind == 0:  # gate and up share the 3072 -> 8192 shape: pairs of the copies
+    for fmt in ("q8_0", "q4k"):
+        for kind, (n_out, n_in) in ((0, (N_FF, N_EMBD)), (1, (N_EMBD, N_FF))):
+            if fmt == "q8_0":
+                wsq = gen_parallel([lambda t=t: synth.config4_w(kind, t) for t in range(ncopy)])
+                Wq = [qdq.upload_q8_0(w, n_out, n_in, device=dev) for w in wsq]
+                wbytes, f = Q8_W_BYTES, qdq.q8_0_gemm_batch
+            else:
+                wsq = gen_parallel([lambda t=t: synth.q4k_blocks(synth.rng_for(8, kind, t), n_out, n_in)
+                                    for t in range(ncopy)])
+                Wq = [qdq.upload_q4k(w, n_out, n_in, device=dev) for w in wsq]
+                wbytes, f = Q4_W_BYTES, qdq.q4k_gemm_batch
+            del wsq
             for M in synth.C4_M:
-                X = torch.from_numpy(synth.activations(synth.rng_for(8, 4, M), M, n_in)).to(dev)
-                mid = torch.empty((M, n_out), device=dev)
-                wsp = torch.empty(qdq.q4k_swiglu_batch_workspace_bytes(M, n_out, n_in), dtype=torch.uint8,
-                                  device=dev)
+                X = torch.from_numpy(synth.config4_x(kind, M)).to(dev)
+                Y = torch.empty((M, n_out), device=dev)
+                wsp = torch.empty(qdq.gemm_batch_workspace_bytes(M, n_out, n_in), dtype=torch.uint8, device=dev)
+                ls, dist = time_calls(torch, timer, lambda t: f(Wq[t], X, Y, wsp, n_out, n_in, M), ncopy,
+                                      max(10, iters // 2))
+                b = wbytes + M * n_in * 4 + M * n_out * 4
+                flops = 2.0 * M * n_out * n_in
+                shape = "3072x8192" if kind == 0 else "8192x3072"
+                kern = "gemm_tc_kernel<%d, %d, 1>" % (0 if fmt == "q8_0" else 1, min(256, max(16, 1 << (M - 1).bit_length())))
+                if M >= 256:
+                    rl = roofline("tensor", flops, ls, peaks["bf16_tflops"], "TFLOP/s",
+                                  recorded_traffic("%s_gemm_M%d" % (fmt, M)), kern, src)
+                else:
+                    rl = roofline("hbm", b, ls, hbm, "GB/s", recorded_traffic("%s_gemm_M%d" % (fmt, M)), kern, src)
+                rows["%s_gemm_%s_M%d" % (fmt, shape, M)] = _row(ls, dist, rl, gbs=b / ls / 1e9,
+                                                               tflops=flops / ls / 1e12, bytes_per_call=b,
+                                                               flop_per_call=flops)
+            if fmt == "q4k" and kind == 0:  # the M-token SwiGLU: gate / up pairs of the copies
                 pairs = [(Wq[2 * t], Wq[2 * t + 1]) for t in range(ncopy // 2)]
-                gq = capture(torch, lambda: [qdq.q4k_swiglu_batch(a, c, X, mid, wsp, n_out, n_in, M)
-                                             for a, c in pairs])
-                for _ in range(3):
-                    gq.replay()
-                it = max(10, iters // 2)
-                dt = timer(gq.replay, it)
-                us = dt / (it * len(pairs)) * 1e6
-                b = 2 * Q4_W_BYTES + M * n_in * 4 + M * n_out * 4
-                flops = 4.0 * M * n_out * n_in
-                rows["q4k_swiglu_batch_3072x8192_M%d" % M] = {
-                    "us_per_call": us, "gbs": b / us / 1e3, "tflops": flops / us / 1e6, "bytes_per_call": b,
-                    "flop_per_call": flops, "frac_hbm": b / us / 1e3 / hbm,
-                    "frac_bf16": flops / us / 1e6 / peaks["bf16_tflops"], "bound": "tensor" if M >= 256 else "hbm"}
-        del Wq
+                for M in synth.C4_M:
+                    X = torch.from_numpy(synth.activations(synth.rng_for(8, 4, M), M, n_in)).to(dev)
+                    midb = torch.empty((M, n_out), device=dev)
+                    wsp = torch.empty(qdq.q4k_swiglu_batch_workspace_bytes(M, n_out, n_in), dtype=torch.uint8,
+                                      device=dev)
+                    ls, dist = time_calls(torch, timer, lambda t: qdq.q4k_swiglu_batch(
+                        pairs[t][0], pairs[t][1], X, midb, wsp, n_out, n_in, M), len(pairs), max(10, iters // 2))
+                    b = 2 * Q4_W_BYTES + M * n_in * 4 + M * n_out * 4
+                    flops = 4.0 * M * n_out * n_in
+                    kern = "gemm_tc_kernel<1, %d, 2>" % min(256, max(16, 1 << (M - 1).bit_length()))
+                    rl = (roofline("tensor", flops, ls, peaks["bf16_tflops"], "TFLOP/s", None, kern, src) if M >= 256
+                          else roofline("hbm", b, ls, hbm, "GB/s", None, kern, src))
+                    rows["q4k_swiglu_batch_3072x8192_M%d" % M] = _row(ls, dist, rl, gbs=b / ls / 1e9,
+                                                                     tflops=flops / ls / 1e12, bytes_per_call=b,
+                                                                     flop_per_call=flops)
+            del Wq
     rows["timeouts"] = qdq.pipeline_timeouts()
     return rows
 
@@ -656,13 +761,37 @@ def run_profile_case(case: str):
         out = torch.empty_like(r)
         mid = torch.empty((1, N_FF), device=dev)
         fn = lambda: qdq.q4k_ffn_residual(Wg, Wu, Wd, x, r, out, mid, N_EMBD, N_FF, 1)
-    elif case.startswith("q8_0_gemm_M"):
-        M = int(case[len("q8_0_gemm_M"):])
-        W = qdq.upload_q8_0(synth.config4_w(0, 0), N_FF, N_EMBD, device=dev)
+    elif case == "q4k_qkv":
+        wq, wk, wv = synth.qkv_layer(0)
+        Wq, Wk = qdq.upload_q4k(wq, synth.N_Q, N_EMBD, device=dev), qdq.upload_q4k(wk, synth.N_KV, N_EMBD, device=dev)
+        Wv = qdq.upload_q4k(wv, synth.N_KV, N_EMBD, device=dev)
+        x = torch.from_numpy(synth.activations(synth.rng_for(5, 3), 1, N_EMBD)).to(dev)
+        oq, ok, ov = (torch.empty((1, n), device=dev) for n in (synth.N_Q, synth.N_KV, synth.N_KV))
+        fn = lambda: qdq.q4k_qkv(Wq, Wk, Wv, x, oq, ok, ov, synth.N_Q, synth.N_KV, N_EMBD, 1)
+    elif case in ("q8_0_vocab", "q6k_gemv"):
+        # a 40000-row slice of the vocabulary projection (130 MB of Q8_0 / 98 MB of Q6_K): larger than
+        # L2 or near it, a few hundred MB on the device at most; traffic scales with the rows
+        n = 40000
+        x = torch.from_numpy(synth.activations(synth.rng_for(6, 1), 1, N_EMBD)).to(dev)
+        y = torch.empty((1, n), device=dev)
+        if case == "q8_0_vocab":
+            W = qdq.upload_q8_0(synth.q8_0_blocks(synth.rng_for(6, 0), n, N_EMBD), n, N_EMBD, device=dev)
+            fn = lambda: qdq.q8_0_gemv(W, x, y, n, N_EMBD, 1)
+        else:
+            W = qdq.upload_q6k(synth.q6k_blocks(synth.rng_for(7, 0), n, N_EMBD), n, N_EMBD, device=dev)
+            fn = lambda: qdq.q6k_gemv(W, x, y, n, N_EMBD, 1)
+    elif case.startswith("q8_0_gemm_M") or case.startswith("q4k_gemm_M"):
+        M = int(case.split("_M")[1])
+        if case.startswith("q8_0"):
+            W = qdq.upload_q8_0(synth.config4_w(0, 0), N_FF, N_EMBD, device=dev)
+            f = qdq.q8_0_gemm_batch
+        else:
+            W = qdq.upload_q4k(synth.q4k_blocks(synth.rng_for(8, 0, 0), N_FF, N_EMBD), N_FF, N_EMBD, device=dev)
+            f = qdq.q4k_gemm_batch
         X = torch.from_numpy(synth.config4_x(0, M)).to(dev)
         Y = torch.empty((M, N_FF), device=dev)
         ws = torch.empty(qdq.gemm_batch_workspace_bytes(M, N_FF, N_EMBD), dtype=torch.uint8, device=dev)
-        fn = lambda: qdq.q8_0_gemm_batch(W, X, Y, ws, N_FF, N_EMBD, M)
+        fn = lambda: f(W, X, Y, ws, N_FF, N_EMBD, M)
     else:
         raise SystemExit("unknown --profile case %r" % case)
     for _ in range(calls):
@@ -688,7 +817,7 @@ def main(argv=None):
                     help="ncu dram bytes per launch of the dominant kernel, if captured for this build")
     ap.add_argument("--profile", default=None, metavar="CASE",
                     help="run a few calls of one op for a profiler and exit: q8_0_gemv, q4k_gemv, q4k_ffn, "
-                         "q8_0_gemm_M<M>")
+                         "q4k_qkv, q8_0_vocab, q6k_gemv, q8_0_gemm_M<M>, q4k_gemm_M<M>")
     args = ap.parse_args(argv)
     if args.profile:
         return run_profile_case(args.profile)

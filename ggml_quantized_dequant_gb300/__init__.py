@@ -73,6 +73,7 @@ SIGNATURES = {
     "qdq_q4k_swiglu_batch_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int]),
     "qdq_q4k_swiglu_batch": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_vp]),
     "qdq_pipeline_timeouts": (_c_int, []),
+    "qdq_noop": (_c_int, [_c_vp]),
     "qdq_set_option": (_c_int, [_c_int, _c_int]),
 }
 
@@ -267,6 +268,11 @@ def q4k_swiglu_batch_workspace_bytes(M: int, n_ff: int, n_embd: int) -> int:
 def q4k_swiglu_batch(Wg, Wu, X, mid, workspace, n_ff: int, n_embd: int, M: int, stream=None):
     _check("qdq_q4k_swiglu_batch", lib().qdq_q4k_swiglu_batch(_ptr(Wg), _ptr(Wu), _ptr(X), _ptr(mid),
                                                               _ptr(workspace), n_ff, n_embd, M, _stream(stream)))
+
+
+def noop(stream=None):
+    """One empty kernel on the stream (for the launch round-trip measurement)."""
+    _check("qdq_noop", lib().qdq_noop(_stream(stream)))
 
 
 def pipeline_timeouts() -> int:

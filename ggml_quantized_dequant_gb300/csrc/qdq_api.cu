@@ -13,6 +13,8 @@ namespace qdq {
 int launch_argmax_rows(const float *logits, int n, int batch, int *index, float *value, cudaStream_t s);
 
 namespace {
+__global__ void noop_kernel() {}
+
 thread_local int g_last_cuda_error = 0;
 std::atomic<int> g_opt_pdl{1};
 std::atomic<int> g_opt_l2_prefetch{0};
@@ -458,6 +460,12 @@ int qdq_q4k_swiglu_batch(const void *Wg, const void *Wu, const float *X, float *
   const int rc = check_gemm_batch(Wg, Wu, X, mid, workspace, n_ff, n_embd, M, q4k_bytes(n_ff, n_embd));
   if (rc != QDQ_OK) return rc;
   return launch_q4k_swiglu_batch(Wg, Wu, X, mid, workspace, n_ff, n_embd, M, stream);
+}
+
+int qdq_noop(cudaStream_t stream) {
+  noop_kernel<<<1, 1, 0, stream>>>();
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? QDQ_OK : fail_cuda(e);
 }
 
 }  // extern "C"

@@ -444,22 +444,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(1, 32 * kDequantWarps);
         if (s_last) {
           __threadfence();
+          // the tile's partials, added in split order: every load of a 16-column chunk is
+          // issued before any is used, so the reads overlap instead of queueing
 #pragma unroll 1
           for (int c0 = (warp >> 2) * 16; c0 < N; c0 += 16 * (kDequantWarps / 4)) {
 #pragma unroll 1
-            for (int jj = 0; jj < 16; ++jj) {
-              const int m = m0 + c0 + jj;
-              if (m >= M) break;
-              float acc[NA];
+            for (int h = 0; h < 16; h += 8) {  // 8 columns at a time
+              float acc[NA][8];
 #pragma unroll
-              for (int a = 0; a < NA; ++a) {
-                acc[a] = 0.f;
-                for (int zz = 0; zz < g.split; ++zz)
-                  acc[a] += __ldcg(&g.partials[((int64_t(zz) * NA + a) * M + m) * n_out + erow]);
+              for (int a = 0; a < NA; ++a)
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) acc[a][jj] = 0.f;
+              for (int zz = 0; zz < g.split; ++zz) {
+#pragma unroll
+                for (int a = 0; a < NA; ++a)
+#pragma unroll
+                  for (int jj = 0; jj < 8; ++jj) {
+                    const int m = m0 + c0 + h + jj;
+                    if (m < M) acc[a][jj] += __ldcg(&g.partials[((int64_t(zz) * NA + a) * M + m) * n_out + erow]);
+                  }
               }
-              float v = acc[0];
-              if (NA == 2) v = v / (1.0f + expf(-v)) * acc[NA - 1];
-              g.Y[int64_t(m) * n_out + erow] = v;
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) {
+                const int m = m0 + c0 + h + jj;
+                if (m < M) {
+                  float v = acc[0][jj];
+                  if (NA == 2) v = v / (1.0f + expf(-v)) * acc[NA - 1][jj];
+                  g.Y[int64_t(m) * n_out + erow] = v;
+                }
+              }
             }
           }
           if (threadIdx.x == 0) g.tickets[tile_id] = 0;  // ready for the next call
@@ -660,6 +673,6 @@ int read_gemm_timeouts() {
 }  // namespace qdq
 
 extern "C" int qdq_pipeline_timeouts(void) {
-  const int a = qdq::read_gemm_timeouts(), b = qdq::read_xs_timeouts();
-  return (a < 0 || b < 0) ? -1 : a + b;
+  const int a = qdq::read_gemm_timeouts(), b = qdq::read_xs_timeouts(), c = qdq::read_dl_timeouts();
+  return (a < 0 || b < 0 || c < 0) ? -1 : a + b + c;
 }

@@ -127,6 +127,7 @@ int launch_q6k_gemv(const void *W, const float *x, float *y, int n_out, int n_in
 // each returns its count since the last call and resets it (-1 on CUDA error).
 int read_gemm_timeouts();
 int read_xs_timeouts();
+int read_dl_timeouts();
 // Tensor-core batch GEMMs (qdq_gemm_tc.cu).  The workspace holds X in bf16, the
 // split-K partial tiles and one ticket per output tile; gemm_workspace_bytes is its
 // size for `na` weight matrices on the current device (0 on a CUDA error).

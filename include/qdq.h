@@ -294,6 +294,13 @@ int qdq_q4k_swiglu_batch(const void *Wg, const void *Wu, const float *X, float *
  */
 int qdq_pipeline_timeouts(void);
 
+/* ---- launch round trip -------------------------------------------------------
+ * "QTensorEngine", bench_empty_submit_roundtrip (the fixed submit-to-completion
+ * latency, measured with no compute): launches one empty kernel (one thread) on
+ * `stream`; a caller times n of these each followed by a synchronisation.
+ */
+int qdq_noop(cudaStream_t stream);
+
 /* ---- launch options (same work, different launch shape; for measurement) -- */
 #define QDQ_OPT_PDL          1  /* 1 (default): programmatic dependent launch on; 0: plain launches */
 #define QDQ_OPT_L2_PREFETCH  2  /* L2 prefetch of weight rows.  0 (default): automatic -- the batch-1 Q8_0 GEMV prefetches the rows its first ring fill
