@@ -5,8 +5,8 @@
 // "QTensorEngine", dispatch_output_topk_chunked: the logits stay on the GPU, a
 // top-k kernel reduces them per chunk, and only the merged K candidates are read
 // back.  The same here: the row is cut into chunks of 1024 logits, each chunk is
-// sorted in shared memory and keeps its k best; the candidates are then merged by
-// the same sort, 4096 at a time, until one chunk holds them all.
+// sorted on chip and keeps its k best; the candidates are then merged by the
+// same sort, 2048 at a time, until one chunk holds them all.
 //
 // Order (the k = 1 case is the argmax epilogue): a NaN comes before every number
 // (the first NaN first), then larger values first, equal values (+0 and -0 are
@@ -14,15 +14,19 @@
 // is that order: the high word maps the float to an order-preserving integer
 // (every NaN to the largest), the low word is the complement of the index.  A
 // chunk past the row's end is padded with key 0, below every real key.
+//
+// The sort is a bitonic network over N keys held two per thread (warp w holds
+// keys 64w .. 64w+63: lane l has 64w + l and 64w + 32 + l).  Exchanges between
+// keys less than 32 apart are warp shuffles, the 32-apart exchange is between a
+// thread's two registers, and only the longer strides go through shared memory
+// with a block barrier: for N = 1024 that is 10 of the network's 55 steps.
 #include "qdq_internal.cuh"
 
 namespace qdq {
 namespace {
 
 constexpr int kChunk1 = 1024;  // logits per first-round chunk
-constexpr int kThreads1 = 512;
-constexpr int kChunk2 = 4096;  // candidate keys per merge chunk
-constexpr int kThreads2 = 1024;
+constexpr int kChunk2 = 2048;  // candidate keys per merge chunk
 
 __device__ __forceinline__ uint64_t topk_key(float v, uint32_t index) {
   uint32_t o;
@@ -36,72 +40,116 @@ __device__ __forceinline__ uint64_t topk_key(float v, uint32_t index) {
   return (uint64_t(o) << 32) | uint64_t(~index);
 }
 
-// Sorts keys[0..N) (N a power of two) into descending order; every thread of the
-// CTA calls it.
-template <int N, int THREADS>
-__device__ __forceinline__ void bitonic_sort_desc(uint64_t *keys) {
+__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
+  const uint32_t lo = __shfl_xor_sync(0xffffffffu, uint32_t(v), m);
+  const uint32_t hi = __shfl_xor_sync(0xffffffffu, uint32_t(v >> 32), m);
+  return (uint64_t(hi) << 32) | lo;
+}
+
+// Compare-exchange of the key at position p with its partner p ^ j in a stage whose
+// direction is descending where (p & k) == 0: the lower position keeps the larger
+// key in a descending run (the smaller in an ascending one).
+__device__ __forceinline__ uint64_t cmpx(uint64_t mine, uint64_t other, int p, int j, int k) {
+  const bool lower = (p & j) == 0, desc = (p & k) == 0;
+  const bool take_max = lower == desc;
+  return take_max ? (mine > other ? mine : other) : (mine < other ? mine : other);
+}
+
+// Sorts the N keys held in (a, b) by the CTA's N / 2 threads into descending
+// order; `sm` is N keys of shared memory.  Every thread of the CTA calls it.
+template <int N>
+__device__ __forceinline__ void sort_desc(uint64_t &a, uint64_t &b, uint64_t *sm) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pa = 64 * warp + lane, pb = pa + 32;  // positions of a and b
   for (int k = 2; k <= N; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < N / 2; i += THREADS) {
-        const int a = 2 * i - (i & (j - 1));  // i with a zero bit inserted at bit log2(j)
-        const int b = a + j;
-        const bool desc = (a & k) == 0;
-        const uint64_t ka = keys[a], kb = keys[b];
-        if ((ka < kb) == desc) {
-          keys[a] = kb;
-          keys[b] = ka;
-        }
-      }
+    int j = k >> 1;
+    if (j >= 64) {  // strides across warps: through shared memory
+      sm[pa] = a;
+      sm[pb] = b;
       __syncthreads();
+      for (; j >= 64; j >>= 1) {
+        for (int i = threadIdx.x; i < N / 2; i += N / 2) {
+          const int x = 2 * i - (i & (j - 1));  // i with a zero bit inserted at bit log2(j)
+          const int y = x + j;
+          const uint64_t kx = sm[x], ky = sm[y];
+          const bool desc = (x & k) == 0;
+          if ((kx < ky) == desc) {
+            sm[x] = ky;
+            sm[y] = kx;
+          }
+        }
+        __syncthreads();
+      }
+      a = sm[pa];
+      b = sm[pb];
+      __syncthreads();  // the buffer is free again
+    }
+    if (j == 32) {  // between the two registers of a thread
+      const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+      const bool desc = (pa & k) == 0;
+      a = desc ? hi : lo;
+      b = desc ? lo : hi;
+      j = 16;
+    }
+    for (; j > 0; j >>= 1) {  // within a warp
+      const uint64_t oa = shfl_xor_u64(a, j), ob = shfl_xor_u64(b, j);
+      a = cmpx(a, oa, pa, j, k);
+      b = cmpx(b, ob, pb, j, k);
     }
   }
 }
 
 // Round 1: chunk blockIdx.x of batch row blockIdx.y -> its k best keys at
 // out[(row * gridDim.x + chunk) * k ...].
-__global__ void __launch_bounds__(kThreads1) topk_chunk_kernel(const float *logits, int n, int k, uint64_t *out) {
-  __shared__ uint64_t keys[kChunk1];
+__global__ void __launch_bounds__(kChunk1 / 2) topk_chunk_kernel(const float *logits, int n, int k, uint64_t *out) {
+  __shared__ uint64_t sm[kChunk1];
   pdl_launch_dependents();
   pdl_wait();  // the logits come from the previous kernel
   const int row = blockIdx.y;
   const int64_t base = int64_t(blockIdx.x) * kChunk1;
   const float *lr = logits + int64_t(row) * n;
-  for (int i = threadIdx.x; i < kChunk1; i += kThreads1) {
-    const int64_t idx = base + i;
-    float v = 0.f;
-    if (idx < n) asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(lr + idx) : "memory");
-    keys[i] = idx < n ? topk_key(v, uint32_t(idx)) : 0ull;
-  }
-  __syncthreads();
-  bitonic_sort_desc<kChunk1, kThreads1>(keys);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t ia = base + 64 * warp + lane, ib = ia + 32;
+  float va = 0.f, vb = 0.f;
+  if (ia < n) asm volatile("ld.global.f32 %0, [%1];" : "=f"(va) : "l"(lr + ia) : "memory");
+  if (ib < n) asm volatile("ld.global.f32 %0, [%1];" : "=f"(vb) : "l"(lr + ib) : "memory");
+  uint64_t a = ia < n ? topk_key(va, uint32_t(ia)) : 0ull;
+  uint64_t b = ib < n ? topk_key(vb, uint32_t(ib)) : 0ull;
+  sort_desc<kChunk1>(a, b, sm);
+  // the k best are positions 0..k-1: warp 0 holds 0..63
   uint64_t *o = out + (int64_t(row) * gridDim.x + blockIdx.x) * k;
-  for (int j = threadIdx.x; j < k; j += kThreads1) o[j] = keys[j];
+  if (warp == 0) {
+    if (lane < k) o[lane] = a;
+    if (lane + 32 < k) o[lane + 32] = b;
+  }
 }
 
 // Merge rounds: chunk blockIdx.x of the `count` candidate keys of batch row
-// blockIdx.y -> its k best.  With one chunk left (gridDim.x == 1) and `index`
-// non-NULL, writes the final (index, value) pairs instead, the value read back
-// from the logits so that its bits are exactly the logit's.
-__global__ void __launch_bounds__(kThreads2) topk_merge_kernel(const uint64_t *in, int count, int k, uint64_t *out,
-                                                               const float *logits, int n, int *index,
-                                                               float *value) {
-  __shared__ uint64_t keys[kChunk2];
+// blockIdx.y -> its k best.  With `index` non-NULL (one chunk left) writes the
+// final (index, value) pairs instead, the value read back from the logits so that
+// its bits are exactly the logit's.
+template <int N>
+__global__ void __launch_bounds__(N / 2) topk_merge_kernel(const uint64_t *in, int count, int k, uint64_t *out,
+                                                           const float *logits, int n, int *index, float *value) {
+  __shared__ uint64_t sm[N];
   pdl_launch_dependents();
   pdl_wait();
   const int row = blockIdx.y;
-  const int64_t base = int64_t(blockIdx.x) * kChunk2;
+  const int64_t base = int64_t(blockIdx.x) * N;
   const uint64_t *ir = in + int64_t(row) * count;
-  for (int i = threadIdx.x; i < kChunk2; i += kThreads2) {
-    const int64_t idx = base + i;
-    uint64_t v = 0;
-    if (idx < count) asm volatile("ld.global.u64 %0, [%1];" : "=l"(v) : "l"(ir + idx) : "memory");
-    keys[i] = v;
-  }
-  __syncthreads();
-  bitonic_sort_desc<kChunk2, kThreads2>(keys);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t ia = base + 64 * warp + lane, ib = ia + 32;
+  uint64_t a = 0, b = 0;
+  if (ia < count) asm volatile("ld.global.u64 %0, [%1];" : "=l"(a) : "l"(ir + ia) : "memory");
+  if (ib < count) asm volatile("ld.global.u64 %0, [%1];" : "=l"(b) : "l"(ir + ib) : "memory");
+  sort_desc<N>(a, b, sm);
+  if (warp != 0) return;
   if (index != nullptr) {
-    for (int j = threadIdx.x; j < k; j += kThreads2) {
-      const uint32_t id = ~uint32_t(keys[j] & 0xFFFFFFFFull);
+    for (int h = 0; h < 2; ++h) {
+      const int j = lane + 32 * h;
+      if (j >= k) break;
+      const uint64_t key = h ? b : a;
+      const uint32_t id = ~uint32_t(key & 0xFFFFFFFFull);
       float v;
       asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(logits + int64_t(row) * n + id) : "memory");
       index[int64_t(row) * k + j] = int(id);
@@ -109,11 +157,18 @@ __global__ void __launch_bounds__(kThreads2) topk_merge_kernel(const uint64_t *i
     }
   } else {
     uint64_t *o = out + (int64_t(row) * gridDim.x + blockIdx.x) * k;
-    for (int j = threadIdx.x; j < k; j += kThreads2) o[j] = keys[j];
+    if (lane < k) o[lane] = a;
+    if (lane + 32 < k) o[lane + 32] = b;
   }
 }
 
 int64_t chunks1(int n) { return (int64_t(n) + kChunk1 - 1) / kChunk1; }
+
+template <int N>
+cudaError_t launch_merge(int m, int batch, cudaStream_t s, const uint64_t *in, int count, int k, uint64_t *out,
+                         const float *logits, int n, int *index, float *value) {
+  return launch(topk_merge_kernel<N>, dim3(m, batch), dim3(N / 2), 0, s, in, count, k, out, logits, n, index, value);
+}
 
 }  // namespace
 
@@ -127,20 +182,24 @@ int launch_topk_rows(const float *logits, int n, int batch, int k, void *workspa
   buf[0] = static_cast<uint64_t *>(workspace);
   buf[1] = buf[0] + size_t(batch) * size_t(chunks1(n)) * size_t(k);
   const int nch = int(chunks1(n));
-  cudaError_t e = launch(topk_chunk_kernel, dim3(nch, batch), dim3(kThreads1), 0, s, logits, n, k, buf[0]);
+  cudaError_t e = launch(topk_chunk_kernel, dim3(nch, batch), dim3(kChunk1 / 2), 0, s, logits, n, k, buf[0]);
   if (e != cudaSuccess) return fail_cuda(e);
   int count = nch * k, cur = 0;  // candidate keys per batch row in buf[cur]
   while (count > kChunk2) {
     const int m = (count + kChunk2 - 1) / kChunk2;
-    e = launch(topk_merge_kernel, dim3(m, batch), dim3(kThreads2), 0, s, static_cast<const uint64_t *>(buf[cur]),
-               count, k, buf[cur ^ 1], static_cast<const float *>(nullptr), 0, static_cast<int *>(nullptr),
-               static_cast<float *>(nullptr));
+    e = launch_merge<kChunk2>(m, batch, s, buf[cur], count, k, buf[cur ^ 1], nullptr, 0, nullptr, nullptr);
     if (e != cudaSuccess) return fail_cuda(e);
     count = m * k;
     cur ^= 1;
   }
-  e = launch(topk_merge_kernel, dim3(1, batch), dim3(kThreads2), 0, s, static_cast<const uint64_t *>(buf[cur]), count,
-             k, static_cast<uint64_t *>(nullptr), logits, n, index, value);
+  // the last merge, sized to the candidates left (at least 64 keys: one warp)
+  const uint64_t *in = buf[cur];
+  if (count <= 64) e = launch_merge<64>(1, batch, s, in, count, k, nullptr, logits, n, index, value);
+  else if (count <= 128) e = launch_merge<128>(1, batch, s, in, count, k, nullptr, logits, n, index, value);
+  else if (count <= 256) e = launch_merge<256>(1, batch, s, in, count, k, nullptr, logits, n, index, value);
+  else if (count <= 512) e = launch_merge<512>(1, batch, s, in, count, k, nullptr, logits, n, index, value);
+  else if (count <= 1024) e = launch_merge<1024>(1, batch, s, in, count, k, nullptr, logits, n, index, value);
+  else e = launch_merge<2048>(1, batch, s, in, count, k, nullptr, logits, n, index, value);
   return e == cudaSuccess ? QDQ_OK : fail_cuda(e);
 }
 
