@@ -376,7 +376,10 @@ int launch_dl(DlArgs a, cudaStream_t s) {
   // (QDQ_OPT_XS_STAGES = 1 or 2 picks the depth)
   int depth = a.wpr <= kMaxWarpsDepth2 ? 2 : 1;
   if (opt_xs_stages() == 1 || opt_xs_stages() == 2) depth = opt_xs_stages();
-  if (depth == 2 && a.wpr > kMaxWarpsDepth2) return QDQ_ERR_UNSUPPORTED;
+  // more warps than two stages of registers allow (a wide row, or a forced group
+  // count) run one stage deep
+  const int warps = a.wpr * (opt_xs_groups() > 0 ? opt_xs_groups() : 1);
+  if (warps > kMaxWarpsDepth2) depth = 1;
   return depth == 2 ? launch_dl_depth<FMT, EPI, 2>(a, s, di) : launch_dl_depth<FMT, EPI, 1>(a, s, di);
 }
 

@@ -674,11 +674,14 @@ def test_error_leaves_outputs_untouched(cuda_lib):
 
 # ------------------------------------------------------------------ batch-1 pipeline shapes
 
+@pytest.mark.parametrize("kernel", [0, 1])
 @pytest.mark.parametrize("n_out,groups", [(2053, 0), (2053, 3), (1001, 2), (1001, 5), (152 * 9 + 151, 0)])
-def test_batch1_uneven_group_rows(cuda_lib, n_out, groups):
+def test_batch1_uneven_group_rows(cuda_lib, n_out, groups, kernel):
     # rows of a CTA are split between its consumer groups; uneven splits end each
-    # group with a partial stage, which must neither be lost nor spill into the next group
+    # group with a partial stage, which must neither be lost nor spill into the next
+    # group (both batch-1 kernels: 0 direct load, 1 shared-memory ring)
     qdq = cuda_lib
+    old_k = qdq.set_option(qdq.QDQ_OPT_BATCH1_KERNEL, kernel)
     rng = np.random.default_rng(n_out + 7 * groups)
     wq = synth.q8_0_blocks(rng, n_out, 3072)
     g, u, d = synth.q4k_blocks(rng, n_out, 3072), synth.q4k_blocks(rng, n_out, 3072), synth.q4k_blocks(rng, n_out, 3072)
@@ -693,6 +696,7 @@ def test_batch1_uneven_group_rows(cuda_lib, n_out, groups):
         qdq.q4k_gemv(Wd, _t(x), y4, n_out, 3072, 1)
         yh, mh, y4h = _np(y), _np(mid), _np(y4)
     finally:
+        qdq.set_option(qdq.QDQ_OPT_BATCH1_KERNEL, old_k)
         qdq.set_option(qdq.QDQ_OPT_XS_GROUPS, old_g)
     y_ref, a = oracle.gemv(oracle.q8_0_dequant(wq, n_out, 3072), x)
     assert gemv_excess(yh, y_ref, a) <= 1.0
@@ -703,11 +707,15 @@ def test_batch1_uneven_group_rows(cuda_lib, n_out, groups):
     assert qdq.pipeline_timeouts() == 0
 
 
-@pytest.mark.parametrize("groups,slots", [(1, 1), (1, 2), (2, 1), (3, 4), (5, 2), (4, 3)])
-def test_batch1_pipeline_shapes(cuda_lib, groups, slots):
-    # the batch-1 kernels stream weights through per-group shared-memory rings;
-    # every (consumer groups, slots per group) shape must give the same sums
+@pytest.mark.parametrize("kernel,groups,slots", [(1, 1, 1), (1, 1, 2), (1, 2, 1), (1, 3, 4), (1, 5, 2), (1, 4, 3),
+                                                (0, 1, 1), (0, 1, 2), (0, 2, 1), (0, 3, 2), (0, 5, 1), (0, 4, 2)])
+def test_batch1_pipeline_shapes(cuda_lib, kernel, groups, slots):
+    # the ring kernel (kernel 1) streams weights through per-group shared-memory rings
+    # (slots = ring slots per group); the direct-load kernel (kernel 0) holds one or two
+    # stages of registers per warp (slots = that depth): every shape must give the
+    # same sums within the bound
     qdq = cuda_lib
+    old_k = qdq.set_option(qdq.QDQ_OPT_BATCH1_KERNEL, kernel)
     rng = np.random.default_rng(100 + 10 * groups + slots)
     wq = synth.q8_0_blocks(rng, 600, 3072)
     g, u = synth.q4k_blocks(rng, 600, 3072), synth.q4k_blocks(rng, 600, 3072)
@@ -723,6 +731,7 @@ def test_batch1_pipeline_shapes(cuda_lib, groups, slots):
     finally:
         qdq.set_option(qdq.QDQ_OPT_XS_GROUPS, old_g)
         qdq.set_option(qdq.QDQ_OPT_XS_STAGES, old_s)
+        qdq.set_option(qdq.QDQ_OPT_BATCH1_KERNEL, old_k)
     y_ref, a = oracle.gemv(oracle.q8_0_dequant(wq, 600, 3072), x)
     assert gemv_excess(yh, y_ref, a) <= 1.0
     s = oracle.swiglu(oracle.q4k_dequant(g, 600, 3072), oracle.q4k_dequant(u, 600, 3072), x)
