@@ -74,6 +74,8 @@ SIGNATURES = {
     "qdq_q4k_swiglu_batch": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_int, _c_vp]),
     "qdq_pipeline_timeouts": (_c_int, []),
     "qdq_noop": (_c_int, [_c_vp]),
+    "qdq_check_status": (_c_int, []),
+    "qdq_checks_enabled": (_c_int, []),
     "qdq_set_option": (_c_int, [_c_int, _c_int]),
 }
 

@@ -34,28 +34,39 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def _stale(objs) -> bool:
-    if not os.path.exists(LIB):
+LIB_CHECKED = os.path.join(PKG, "libqdq_checked.so")
+BUILD_CHECKED = os.path.join(PKG, "_build_checks")
+
+
+def _stale(lib) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = sources() + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")]
     deps.append(os.path.join(INCLUDE, "qdq.h"))
     deps.append(os.path.abspath(__file__))
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -> str:
-    """Compile every kernel source and link libqdq.so; returns the library path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, jobs: int | None = None, checks: bool = False) -> str:
+    """Compile every kernel source and link libqdq.so; returns the library path.
+
+    checks=True builds the debug variant libqdq_checked.so instead: the same sources with
+    -DQDQ_CHECKS, whose kernels record out-of-bounds indices in a device status word
+    (qdq_check_status) instead of accessing them.
+    """
+    bdir, lib = (BUILD_CHECKED, LIB_CHECKED) if checks else (BUILD, LIB)
+    os.makedirs(bdir, exist_ok=True)
     srcs = sources()
-    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
-    if not force and not _stale(objs):
-        return LIB
+    objs = [os.path.join(bdir, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    if not force and not _stale(lib):
+        return lib
     nvcc = _nvcc()
+    flags = NVCC_FLAGS + (["-DQDQ_CHECKS"] if checks else [])
 
     def compile_one(src_obj):
         src, obj = src_obj
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+        cmd = [nvcc, *ARCH, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("nvcc failed for %s:\n%s\n%s" % (src, " ".join(cmd), r.stderr))
@@ -65,13 +76,13 @@ def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -
         for err in ex.map(compile_one, zip(srcs, objs)):
             if verbose and err.strip():
                 print(err)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

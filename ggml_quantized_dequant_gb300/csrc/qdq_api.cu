@@ -462,6 +462,25 @@ int qdq_q4k_swiglu_batch(const void *Wg, const void *Wu, const float *X, float *
   return launch_q4k_swiglu_batch(Wg, Wu, X, mid, workspace, n_ff, n_embd, M, stream);
 }
 
+int qdq_checks_enabled(void) {
+#ifdef QDQ_CHECKS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+int qdq_check_status(void) {
+  if (qdq_checks_enabled() && cudaDeviceSynchronize() != cudaSuccess) return -1;
+  const int r[5] = {read_checks_dl(), read_checks_xs(), read_checks_gemm(), read_checks_topk(), read_checks_q6k()};
+  int v = 0;
+  for (int x : r) {
+    if (x < 0) return -1;
+    v |= x;
+  }
+  return v;
+}
+
 int qdq_noop(cudaStream_t stream) {
   noop_kernel<<<1, 1, 0, stream>>>();
   const cudaError_t e = cudaGetLastError();

@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float u = __uint_as_float(r[NA - 1][jj]);
                 v = v / (1.0f + expf(-v)) * u;
               }
-              g.Y[int64_t(m) * n_out + erow] = v;
+              if (QDQ_GUARD(erow < n_out, QDQ_CHECK_OUT)) g.Y[int64_t(m) * n_out + erow] = v;
             }
           }
         }
@@ -435,7 +435,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
               const int m = m0 + c0 + jj;
-              if (m < M) g.partials[((int64_t(z) * NA + a) * M + m) * n_out + erow] = __uint_as_float(r[a][jj]);
+              if (m < M && QDQ_GUARD(erow < n_out, QDQ_CHECK_OUT))
+                g.partials[((int64_t(z) * NA + a) * M + m) * n_out + erow] = __uint_as_float(r[a][jj]);
             }
         }
         __threadfence();
@@ -662,6 +663,8 @@ int launch_q4k_swiglu_batch(const void *Wg, const void *Wu, const float *X, floa
   const uint8_t *w[2] = {static_cast<const uint8_t *>(Wg), static_cast<const uint8_t *>(Wu)};
   return launch_gemm<kWQ4, 2>(w, X, mid, ws, n_ff, n_embd, M, s);
 }
+
+QDQ_CHECK_READER(read_checks_gemm)
 
 int read_gemm_timeouts() {
   unsigned int v = 0, zero = 0;

@@ -49,6 +49,7 @@ struct DlArgs {
   float *y, *y2, *y3;          // output (q), k, v
   int seg1, seg2;              // QKV: rows [0, seg1) W_q, [seg1, seg2) W_k, [seg2, n_out) W_v
   int n_out, n_in, wpr, groups, prefetch;
+  int psum_cap;  // floats of the row-total buffer in shared memory
 };
 
 // One lane's data of one row (its 32-weight block).
@@ -97,7 +98,8 @@ __device__ __forceinline__ RowData load_row(const DlArgs &a, int R, int up, int 
   const uint8_t *base = row_matrix<EPI>(a, R, up, lr, nm);
   const int n_in = a.n_in;
   const int64_t qr = q_row_bytes<FMT>(n_in), sr = s_row_bytes<FMT>(n_in);
-  RowData d;
+  RowData d{};
+  if (!QDQ_GUARD(lr >= 0 && lr < nm && bq >= 0 && bq < (n_in >> 5), QDQ_CHECK_ROW)) return d;
   if constexpr (FMT == kQ8) {
     const uint8_t *q = base + int64_t(lr) * qr + 32 * bq;
     d.a = ldg_stream(q);
@@ -284,7 +286,8 @@ __global__ void __launch_bounds__(32 * (DEPTH == 2 ? kMaxWarpsDepth2 : kMaxWarps
     butterfly4_rows(part, lane);
     if ((lane & 7) == 0) {
       const int v = (gb - r0) * kV + 4 * t + (lane >> 3);  // local virtual row
-      if (v < (ge - r0) * kV) psum[v * a.wpr + slice] = part[0];
+      if (v < (ge - r0) * kV && QDQ_GUARD(v * a.wpr + slice < a.psum_cap, QDQ_CHECK_SMEM))
+        psum[v * a.wpr + slice] = part[0];
     }
   };
   if (DEPTH == 2) {
@@ -349,6 +352,7 @@ int launch_dl_depth(DlArgs a, cudaStream_t s, const DeviceInfo &di) {
   if (grid > a.n_out) grid = a.n_out;
   const int max_rows = (a.n_out + grid - 1) / grid;
   const size_t smem = size_t(max_rows) * kV * a.wpr * sizeof(float);
+  a.psum_cap = int(smem / sizeof(float));
   // L2 prefetch of the CTA's rows: on by default when this call's weights fit in half the L2
   const int64_t w_bytes = int64_t(a.n_out) * (FMT == kQ8 ? int64_t(a.n_in) / 32 * 34
                                               : FMT == kQ4 ? int64_t(a.n_in) / 256 * 144
@@ -403,6 +407,7 @@ int launch_gemv_dl(int fmt, int mode, const void *W, const void *W2, const float
 }
 
 int read_dl_timeouts() { return 0; }  // the direct-load kernel has no waits
+QDQ_CHECK_READER(read_checks_dl)
 
 int launch_gemv_dl_qkv(const void *Wq, const void *Wk, const void *Wv, const float *x, float *q, float *k, float *v,
                        int n_q, int n_kv, int n_in, cudaStream_t s) {

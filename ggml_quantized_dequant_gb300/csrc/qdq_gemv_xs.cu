@@ -220,6 +220,7 @@ struct XsArgs {
   int sg;           // ring slots per consumer group (the ring holds groups * sg stages)
   int stage_bytes;  // bytes per ring stage (multiple of 128)
   int l2_prefetch;
+  int psum_cap;     // floats of the row-total buffer in shared memory
 };
 
 template <int FMT, int EPI, int AR>
@@ -595,7 +596,7 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_xs_kernel(const XsArgs a, co
       butterfly4(part, lane);
       if ((lane & 7) == 0) {
         const int v = rbeg * kV + t * kStageRows + (lane >> 3);  // local virtual row
-        if (v < vend) psum[v * a.wpr + slice] = part[0];
+        if (v < vend && QDQ_GUARD(v * a.wpr + slice < a.psum_cap, QDQ_CHECK_SMEM)) psum[v * a.wpr + slice] = part[0];
       }
     }
   }
@@ -716,6 +717,7 @@ int launch_xs_ar(XsArgs a, cudaStream_t s, const DeviceInfo &di) {
     a.l2_prefetch = rest <= int64_t(di.l2_bytes) / 2 ? 2 : 0;
   }
   const size_t smem = size_t(stages) * a.stage_bytes + 2 * stages * sizeof(uint64_t) + psum_bytes;
+  a.psum_cap = int(psum_bytes / sizeof(float));
   if (smem > size_t(di.max_smem_optin)) return QDQ_ERR_UNSUPPORTED;
   const cudaError_t e0 = allow_dynamic_smem(reinterpret_cast<const void *>(kern), int(smem));
   if (e0 != cudaSuccess) return fail_cuda(e0);
@@ -782,6 +784,8 @@ int launch_gemv_xs_qkv(const void *Wq, const void *Wk, const void *Wv, const flo
   a.n_in = n_in;
   return launch_xs<kQ4, kQkv>(a, s, di);
 }
+
+QDQ_CHECK_READER(read_checks_xs)
 
 int read_xs_timeouts() {
   unsigned int v = 0, zero = 0;

@@ -141,6 +141,36 @@ int launch_q4k_swiglu_batch(const void *Wg, const void *Wu, const float *X, floa
 
 // ---------------------------------------------------------------- device side
 
+// Debug-build guards (compiled with -DQDQ_CHECKS): a guarded access whose index
+// is out of bounds is skipped and its check bit is or-ed into this translation
+// unit's status word (qdq_check_status reads and clears them all); nothing traps.
+// In the normal build QDQ_GUARD is `true` and costs nothing.
+#define QDQ_CHECK_SMEM 1u     // a shared-memory index past its buffer
+#define QDQ_CHECK_ROW 2u      // a weight row or activation index past its matrix
+#define QDQ_CHECK_OUT 4u      // an output index past its buffer
+#define QDQ_CHECK_ALIGN 8u    // a bulk copy not 16-byte aligned or sized
+#ifdef QDQ_CHECKS
+static __device__ unsigned int g_check_status = 0;
+#define QDQ_GUARD(cond, bit) ((cond) ? true : (atomicOr(&g_check_status, (bit)), false))
+// Defines this translation unit's reader of its status word (read and clear).
+#define QDQ_CHECK_READER(name)                                                           \
+  int name() {                                                                           \
+    unsigned int v = 0, zero = 0;                                                        \
+    if (cudaMemcpyFromSymbol(&v, g_check_status, sizeof(v)) != cudaSuccess) return -1; \
+    if (cudaMemcpyToSymbol(g_check_status, &zero, sizeof(zero)) != cudaSuccess) return -1; \
+    return int(v);                                                                       \
+  }
+#else
+#define QDQ_GUARD(cond, bit) true
+#define QDQ_CHECK_READER(name) \
+  int name() { return 0; }
+#endif
+int read_checks_dl();
+int read_checks_xs();
+int read_checks_gemm();
+int read_checks_topk();
+int read_checks_q6k();
+
 // Programmatic dependent launch: let the next grid on the stream start early.
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -235,6 +265,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
 // 1-D bulk async copy global -> shared, completing on an mbarrier (16-byte
 // aligned addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  if (!QDQ_GUARD(((smem_u32(dst) | uint32_t(reinterpret_cast<uintptr_t>(src)) | bytes) & 15u) == 0, QDQ_CHECK_ALIGN))
+    return;
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                    smem_u32(dst)),
                "l"(src), "r"(bytes), "r"(smem_u32(bar))

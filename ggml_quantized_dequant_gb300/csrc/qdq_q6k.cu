@@ -126,6 +126,7 @@ __global__ void q6k_get_rows_kernel(const uint8_t *__restrict__ W, const int *id
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < int64_t(n_ids) * nblk;
        i += int64_t(gridDim.x) * blockDim.x) {
     const int r = int(i / nblk), blk = int(i - int64_t(r) * nblk);
+    if (!QDQ_GUARD(r < n_ids, QDQ_CHECK_OUT)) continue;
     const int id = ld_s32_after_wait(ids + r);
     float *o = out + int64_t(r) * n_in + 32 * blk;
     if (id < 0 || id >= n_rows) {
@@ -211,6 +212,8 @@ int launch_nb(const uint8_t *W, const float *x, float *y, int n_out, int n_in, c
 }
 
 }  // namespace
+
+QDQ_CHECK_READER(read_checks_q6k)
 
 int launch_q6k_pack(const void *ggml, void *packed, int n_out, int n_in, cudaStream_t s) {
   const int64_t nsb = int64_t(n_out) * (n_in / 256);

@@ -150,8 +150,9 @@ __global__ void __launch_bounds__(N / 2) topk_merge_kernel(const uint64_t *in, i
       if (j >= k) break;
       const uint64_t key = h ? b : a;
       const uint32_t id = ~uint32_t(key & 0xFFFFFFFFull);
-      float v;
-      asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(logits + int64_t(row) * n + id) : "memory");
+      float v = __int_as_float(0x7fffffff);
+      if (QDQ_GUARD(id < uint32_t(n), QDQ_CHECK_ROW))
+        asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(logits + int64_t(row) * n + id) : "memory");
       index[int64_t(row) * k + j] = int(id);
       value[int64_t(row) * k + j] = v;
     }
@@ -171,6 +172,8 @@ cudaError_t launch_merge(int m, int batch, cudaStream_t s, const uint64_t *in, i
 }
 
 }  // namespace
+
+QDQ_CHECK_READER(read_checks_topk)
 
 size_t topk_workspace_bytes(int n, int batch, int k) {
   return 2 * size_t(batch) * size_t(chunks1(n)) * size_t(k) * sizeof(uint64_t);

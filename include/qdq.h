@@ -294,6 +294,20 @@ int qdq_q4k_swiglu_batch(const void *Wg, const void *Wu, const float *X, float *
  */
 int qdq_pipeline_timeouts(void);
 
+/* ---- debug build: device-side guards ----------------------------------------
+ * A library built with -DQDQ_CHECKS (ggml_quantized_dequant_gb300._build.build(checks=True),
+ * libqdq_checked.so) guards its shared-memory row buffers, weight-row and
+ * activation indices, output indices and bulk-copy alignment inside the kernels:
+ * an index out of bounds skips that access and sets a bit of a device status word
+ * (QDQ_CHECK_* in the library's internal header: 1 shared memory, 2 weight row,
+ * 4 output, 8 copy alignment) instead of trapping.  qdq_check_status waits for the
+ * device, returns the or of the bits since its previous call and clears them (-1
+ * on a CUDA error); in the normal build it returns 0.  qdq_checks_enabled: 1 in
+ * the debug build, else 0.
+ */
+int qdq_check_status(void);
+int qdq_checks_enabled(void);
+
 /* ---- launch round trip -------------------------------------------------------
  * "QTensorEngine", bench_empty_submit_roundtrip (the fixed submit-to-completion
  * latency, measured with no compute): launches one empty kernel (one thread) on

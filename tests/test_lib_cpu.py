@@ -230,3 +230,21 @@ def test_q4k_gemm_and_swiglu_batch_validation(lib):
     assert lib.qdq_q4k_swiglu_batch(W, W2 + 8, X, Y, ws, 512, 256, 16, None) == qdq.QDQ_ERR_ALIGN
     assert lib.qdq_q4k_swiglu_batch(W, W2, X, W2 + 64, ws, 512, 256, 16, None) == qdq.QDQ_ERR_ALIAS
     assert lib.qdq_q4k_swiglu_batch(W, W2, X, Y, ws, 512, 256, 0, None) == qdq.QDQ_ERR_DIMS
+
+
+def test_normal_build_has_no_checks(lib):
+    # the guards compile to nothing in the normal build: no status word, nothing to read
+    assert lib.qdq_checks_enabled() == 0
+    assert lib.qdq_check_status() == 0
+
+
+def test_checked_build_links_and_exports_the_same_symbols():
+    import ctypes
+    from ggml_quantized_dequant_gb300 import _build
+    path = _build.build(checks=True)
+    assert path != _build.LIB
+    dbg = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(dbg, name), name
+    dbg.qdq_checks_enabled.restype = ctypes.c_int
+    assert dbg.qdq_checks_enabled() == 1
