@@ -6,9 +6,14 @@
 // try_q4k_soa_ffn_block_residual (out = residual + W_down . mid), try_q4k_soa_qkv
 // (Q, K, V from one activation); "QTensorEngine", dispatch_gemm_into (Q6_K).
 //
-// Layout of the work is the x-stationary one of the ring kernel: lane l of
-// slice warp s owns the 32-weight column block 32 s + l for the whole kernel
-// and keeps its 32 activations in registers; WPR = ceil(n_in / 1024) slice warps
+// Layout of the work is x-stationary: slice warp s owns the 1024 columns
+// 1024 s .. 1024 s + 1023 for the whole kernel and each lane keeps its 32
+// activations in registers.  Q4_K and Q6_K: lane l owns column block 32 s + l
+// (its 16 bytes of low bits are contiguous with its neighbours').  Q8_0: lane l
+// owns half l & 1 of blocks 32 s + (l >> 1) and 32 s + 16 + (l >> 1), so that
+// each of its two 16-byte loads is one contiguous 512-byte span for the warp
+// (a whole 32-byte block per lane would touch every sector twice).  WPR =
+// ceil(n_in / 1024) slice warps
 // cover a row; G groups of slice warps take contiguous shares of the CTA's rows
 // (one CTA per SM).  A warp handles 4 (virtual) rows per stage: each lane loads
 // its block of the 4 rows with 128-bit loads into registers, multiplies, and a
@@ -52,10 +57,17 @@ struct DlArgs {
   int psum_cap;  // floats of the row-total buffer in shared memory
 };
 
-// One lane's data of one row (its 32-weight block).
+// The columns one lane owns: Q4_K / Q6_K block `bq`; Q8_0 half `h` of blocks qa and qb.
+struct LaneCols {
+  int bq;            // Q4_K / Q6_K: the column block
+  int qa, qb, h;     // Q8_0: the two blocks and the half (16 quants) of each
+};
+
+// One lane's data of one row.
 struct RowData {
-  uint4 a, b;  // Q8_0: the 32 quants; Q4_K: a = 16 bytes of nibbles, b = the superblock header; Q6_K: a = low bits
-  uint32_t c;  // Q8_0: d (fp16 bits); Q6_K: the two int8 scales
+  uint4 a, b;  // Q8_0: the 16 quants of each half; Q4_K: a = 16 bytes of nibbles, b = the superblock header;
+               // Q6_K: a = low bits
+  uint32_t c;  // Q8_0: d of block qa (low half) and of block qb (high half), fp16 bits; Q6_K: the two int8 scales
   uint2 h;     // Q6_K: high bits
   uint32_t d;  // Q6_K: d (fp16 bits)
 };
@@ -69,51 +81,56 @@ __device__ __forceinline__ int64_t s_row_bytes(int n_in) {
   return FMT == kQ8 ? int64_t(n_in >> 4) : FMT == kQ4 ? int64_t(n_in >> 8) * 16 : 0;
 }
 
-// Matrix base, its row count and the local row of global (virtual) row R.
-template <int EPI>
-__device__ __forceinline__ const uint8_t *row_matrix(const DlArgs &a, int R, int up, int &lr, int &nm) {
-  if (EPI == kQkv) {
-    if (R < a.seg1) {
-      lr = R;
-      nm = a.seg1;
-      return a.W;
-    }
-    if (R < a.seg2) {
-      lr = R - a.seg1;
-      nm = a.seg2 - a.seg1;
-      return a.W2;
-    }
-    lr = R - a.seg2;
-    nm = a.n_out - a.seg2;
-    return a.W3;
+// Per-lane pointers into one matrix, set once per kernel: the row-0 address of
+// each piece of this lane's data, so that a row's address is one multiply-add
+// (pointer + row * stride).  Q8_0: quants of half-blocks qa and qb, their two
+// scales.  Q4_K: nibbles, superblock header.  Q6_K: low bits, high bits, scales, d.
+struct LanePtrs {
+  const uint8_t *p[4];
+};
+
+template <int FMT>
+__device__ __forceinline__ LanePtrs lane_ptrs(const uint8_t *W, int nm, int n_in, const LaneCols &lc) {
+  LanePtrs l;
+  const int64_t qr = q_row_bytes<FMT>(n_in);
+  if constexpr (FMT == kQ8) {
+    const uint8_t *S = W + int64_t(nm) * qr;
+    l.p[0] = W + 16 * lc.h + 32 * lc.qa;
+    l.p[1] = W + 16 * lc.h + 32 * lc.qb;
+    l.p[2] = S + 2 * lc.qa;
+    l.p[3] = S + 2 * lc.qb;
+  } else if constexpr (FMT == kQ4) {
+    l.p[0] = W + 16 * lc.bq;
+    l.p[1] = W + int64_t(nm) * qr + 16 * (lc.bq >> 3);
+    l.p[2] = l.p[3] = nullptr;
+  } else {
+    l.p[0] = W + 16 * lc.bq;
+    l.p[1] = W + (n_in >> 1) + 8 * lc.bq;
+    l.p[2] = W + (n_in >> 1) + (n_in >> 2) + 2 * lc.bq;
+    l.p[3] = W + (n_in >> 1) + (n_in >> 2) + (n_in >> 4) + 2 * (lc.bq >> 3);
   }
-  lr = R;
-  nm = a.n_out;
-  return (EPI == kSwiglu && up) ? a.W2 : a.W;
+  return l;
 }
 
-template <int FMT, int EPI>
-__device__ __forceinline__ RowData load_row(const DlArgs &a, int R, int up, int bq) {
-  int lr, nm;
-  const uint8_t *base = row_matrix<EPI>(a, R, up, lr, nm);
-  const int n_in = a.n_in;
+// Loads this lane's data of local row lr of the matrix whose pointers are lp.
+template <int FMT>
+__device__ __forceinline__ RowData load_row(const LanePtrs &lp, int lr, int nm, int n_in) {
   const int64_t qr = q_row_bytes<FMT>(n_in), sr = s_row_bytes<FMT>(n_in);
   RowData d{};
-  if (!QDQ_GUARD(lr >= 0 && lr < nm && bq >= 0 && bq < (n_in >> 5), QDQ_CHECK_ROW)) return d;
+  if (!QDQ_GUARD(lr >= 0 && lr < nm, QDQ_CHECK_ROW)) return d;
   if constexpr (FMT == kQ8) {
-    const uint8_t *q = base + int64_t(lr) * qr + 32 * bq;
-    d.a = ldg_stream(q);
-    d.b = ldg_stream(q + 16);
-    d.c = __ldg(reinterpret_cast<const unsigned short *>(base + int64_t(nm) * qr + int64_t(lr) * sr) + bq);
+    d.a = ldg_stream(lp.p[0] + lr * qr);
+    d.b = ldg_stream(lp.p[1] + lr * qr);
+    d.c = uint32_t(__ldg(reinterpret_cast<const unsigned short *>(lp.p[2] + lr * sr))) |
+          (uint32_t(__ldg(reinterpret_cast<const unsigned short *>(lp.p[3] + lr * sr))) << 16);
   } else if constexpr (FMT == kQ4) {
-    d.a = ldg_stream(base + int64_t(lr) * qr + 16 * bq);
-    d.b = __ldg(reinterpret_cast<const uint4 *>(base + int64_t(nm) * qr + int64_t(lr) * sr) + (bq >> 3));
+    d.a = ldg_stream(lp.p[0] + lr * qr);
+    d.b = __ldg(reinterpret_cast<const uint4 *>(lp.p[1] + lr * sr));
   } else {
-    const uint8_t *row = base + int64_t(lr) * qr;
-    d.a = ldg_stream(row + 16 * bq);
-    d.h = __ldg(reinterpret_cast<const uint2 *>(row + (n_in >> 1)) + bq);
-    d.c = __ldg(reinterpret_cast<const unsigned short *>(row + (n_in >> 1) + (n_in >> 2)) + bq);
-    d.d = __ldg(reinterpret_cast<const unsigned short *>(row + (n_in >> 1) + (n_in >> 2) + (n_in >> 4)) + (bq >> 3));
+    d.a = ldg_stream(lp.p[0] + lr * qr);
+    d.h = __ldg(reinterpret_cast<const uint2 *>(lp.p[1] + lr * qr));
+    d.c = __ldg(reinterpret_cast<const unsigned short *>(lp.p[2] + lr * qr));
+    d.d = __ldg(reinterpret_cast<const unsigned short *>(lp.p[3] + lr * qr));
   }
   return d;
 }
@@ -123,25 +140,30 @@ template <int FMT>
 __device__ __forceinline__ void stage_math(const RowData (&rd)[4], const float2 (&xr)[16], float xsum, bool g0, bool g1,
                                            int sh, const Magic &mg, float (&part)[4]) {
     if constexpr (FMT == kQ8) {
-      float2 s0[4], s1[4];
+      float2 sa[4], sb[4];  // the two half blocks: xr[0..7] and xr[8..15]
 #pragma unroll
-      for (int k = 0; k < 4; ++k) s0[k] = s1[k] = f2(0.f, 0.f);
+      for (int k = 0; k < 4; ++k) sa[k] = sb[k] = f2(0.f, 0.f);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
+      for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const uint4 &u = kk < 4 ? rd[k].a : rd[k].b;
-          const uint32_t w = (kk & 3) == 0 ? u.x : (kk & 3) == 1 ? u.y : (kk & 3) == 2 ? u.z : u.w;
+          const uint4 &u = rd[k].a, &v = rd[k].b;
+          const uint32_t wa = kk == 0 ? u.x : kk == 1 ? u.y : kk == 2 ? u.z : u.w;
+          const uint32_t wb = kk == 0 ? v.x : kk == 1 ? v.y : kk == 2 ? v.z : v.w;
           float2 q01, q23;
-          s8x4_to_f2(w, mg, q01, q23);
-          s0[k] = __ffma2_rn(q01, xr[2 * kk], s0[k]);
-          s1[k] = __ffma2_rn(q23, xr[2 * kk + 1], s1[k]);
+          s8x4_to_f2(wa, mg, q01, q23);
+          sa[k] = __ffma2_rn(q01, xr[2 * kk], sa[k]);
+          sa[k] = __ffma2_rn(q23, xr[2 * kk + 1], sa[k]);
+          s8x4_to_f2(wb, mg, q01, q23);
+          sb[k] = __ffma2_rn(q01, xr[8 + 2 * kk], sb[k]);
+          sb[k] = __ffma2_rn(q23, xr[8 + 2 * kk + 1], sb[k]);
         }
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float2 st = __fadd2_rn(s0[k], s1[k]);
-        part[k] = __half2float(__ushort_as_half(uint16_t(rd[k].c))) * (st.x + st.y);
+        const float da = __half2float(__ushort_as_half(uint16_t(rd[k].c & 0xFFFFu)));
+        const float db = __half2float(__ushort_as_half(uint16_t(rd[k].c >> 16)));
+        part[k] = fmaf(db, sb[k].x + sb[k].y, da * (sa[k].x + sa[k].y));
       }
     } else if constexpr (FMT == kQ4) {
       float2 s0[4], s1[4], b01[4], b23[4];
@@ -206,10 +228,15 @@ __global__ void __launch_bounds__(32 * (DEPTH == 2 ? kMaxWarpsDepth2 : kMaxWarps
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_in = a.n_in, G = a.groups;
   const int slice = warp % a.wpr, grp = warp / a.wpr;
-  const int r0 = int(int64_t(blockIdx.x) * a.n_out / gridDim.x);
-  const int r1 = int(int64_t(blockIdx.x + 1) * a.n_out / gridDim.x);
+  // rows are dealt out in units of one stage (kRowsPerStage output rows), so that
+  // only the matrix's last stage can be partial: units [u0, u1) to this CTA, and
+  // a contiguous share of them to each group
+  const int units = (a.n_out + kRowsPerStage - 1) / kRowsPerStage;
+  const int u0 = int(int64_t(blockIdx.x) * units / gridDim.x), u1 = int(int64_t(blockIdx.x + 1) * units / gridDim.x);
+  const int r0 = u0 * kRowsPerStage, r1 = min(u1 * kRowsPerStage, a.n_out);
   const int nreal = r1 - r0;
-  const int gb = r0 + grp * nreal / G, ge = r0 + (grp + 1) * nreal / G;  // this group's output rows
+  const int gu0 = u0 + grp * (u1 - u0) / G, gu1 = u0 + (grp + 1) * (u1 - u0) / G;
+  const int gb = gu0 * kRowsPerStage, ge = min(gu1 * kRowsPerStage, a.n_out);  // this group's output rows
 
   // HBM starts streaming this CTA's rows at once: the weights do not depend on the previous kernel
   if (a.prefetch && threadIdx.x == 0) {
@@ -234,24 +261,67 @@ __global__ void __launch_bounds__(32 * (DEPTH == 2 ? kMaxWarpsDepth2 : kMaxWarps
   pdl_launch_dependents();
 
   const int nblk = n_in >> 5;
-  const int blk = slice * 32 + lane;
-  const bool valid = blk < nblk;
-  const int bq = valid ? blk : 0;  // a lane past the end of the row reads block 0 against x = 0
+  // this lane's columns; a block past the end of the row reads block 0 against x = 0
+  LaneCols lc;
+  int xo0, xo1;        // the lane's two runs of 16 activations
+  bool valid0, valid1;
+  if (FMT == kQ8) {
+    const int qa = 32 * slice + (lane >> 1), qb = qa + 16;
+    valid0 = qa < nblk;
+    valid1 = qb < nblk;
+    lc.h = lane & 1;
+    lc.qa = valid0 ? qa : 0;
+    lc.qb = valid1 ? qb : 0;
+    lc.bq = 0;
+    xo0 = 32 * lc.qa + 16 * lc.h;
+    xo1 = 32 * lc.qb + 16 * lc.h;
+  } else {
+    const int blk = slice * 32 + lane;
+    valid0 = valid1 = blk < nblk;
+    lc.bq = valid0 ? blk : 0;
+    lc.qa = lc.qb = lc.h = 0;
+    xo0 = 32 * lc.bq;
+    xo1 = xo0 + 16;
+  }
   const Magic mg = lane_magic(mg_param);
-  // virtual row k of the stage starting at output row rr; rows past the group's end
-  // repeat its last row (in bounds) and are dropped
-  auto vrow = [&](int rr, int k, int &up) {
-    up = kV == 2 ? (k & 1) : 0;
-    const int R = rr + (kV == 2 ? (k >> 1) : k);
-    return R < ge ? R : ge - 1;
-  };
-  const int nst = ((ge - gb) * kV + 3) / 4;  // this group's stages of 4 virtual rows
+  // the lane's pointers into each matrix (QKV: W_q, W_k, W_v; SwiGLU: gate, up)
+  constexpr int kM = EPI == kQkv ? 3 : kV;
+  LanePtrs lp[kM];
+  int nmat[kM];
+  if (EPI == kQkv) {
+    nmat[0] = a.seg1;
+    nmat[1 % kM] = a.seg2 - a.seg1;
+    nmat[2 % kM] = a.n_out - a.seg2;
+    lp[0] = lane_ptrs<FMT>(a.W, nmat[0], n_in, lc);
+    lp[1 % kM] = lane_ptrs<FMT>(a.W2, nmat[1 % kM], n_in, lc);
+    lp[2 % kM] = lane_ptrs<FMT>(a.W3, nmat[2 % kM], n_in, lc);
+  } else {
+#pragma unroll
+    for (int m = 0; m < kM; ++m) {
+      nmat[m] = a.n_out;
+      lp[m] = lane_ptrs<FMT>(m ? a.W2 : a.W, a.n_out, n_in, lc);
+    }
+  }
+  const int nst = gu1 - gu0;  // this group's stages
+  // stage t: output rows gb + kRowsPerStage t + i; a row past the group's end (only
+  // in the matrix's last stage) repeats the group's last row and is dropped
   auto load_stage = [&](int t, RowData (&rd)[4]) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      int up;
-      const int R = vrow(gb + t * kRowsPerStage, k, up);
-      rd[k] = load_row<FMT, EPI>(a, R, up, bq);
+      const int up = kV == 2 ? (k & 1) : 0;
+      int R = gb + t * kRowsPerStage + (kV == 2 ? (k >> 1) : k);
+      R = R < ge ? R : ge - 1;
+      if (EPI == kQkv) {
+        const bool m0 = R < a.seg1, m1 = !m0 && R < a.seg2;
+        const int lr = m0 ? R : m1 ? R - a.seg1 : R - a.seg2;
+        const int nm = m0 ? nmat[0] : m1 ? nmat[1 % kM] : nmat[2 % kM];
+        LanePtrs l;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) l.p[i] = m0 ? lp[0].p[i] : m1 ? lp[1 % kM].p[i] : lp[2 % kM].p[i];
+        rd[k] = load_row<FMT>(l, lr, nm, n_in);
+      } else {
+        rd[k] = load_row<FMT>(lp[up], R, nmat[up], n_in);
+      }
     }
   };
   RowData b0[4], b1[4];
@@ -262,10 +332,12 @@ __global__ void __launch_bounds__(32 * (DEPTH == 2 ? kMaxWarpsDepth2 : kMaxWarps
   float2 xr[16];
   float xsum = 0.f;
   {
-    const float4 *xp = reinterpret_cast<const float4 *>(a.x + bq * 32);
+    const float4 *xp0 = reinterpret_cast<const float4 *>(a.x + xo0);
+    const float4 *xp1 = reinterpret_cast<const float4 *>(a.x + xo1);
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      const float4 v = valid ? ld_after_wait(xp + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const bool ok = c < 4 ? valid0 : valid1;
+      const float4 v = ok ? ld_after_wait(c < 4 ? xp0 + c : xp1 + (c - 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
       xr[2 * c] = f2(v.x, v.y);
       xr[2 * c + 1] = f2(v.z, v.w);
     }
@@ -348,9 +420,11 @@ int launch_dl_depth(DlArgs a, cudaStream_t s, const DeviceInfo &di) {
   a.groups = opt_xs_groups() > 0 ? opt_xs_groups() : kCap / a.wpr;
   if (a.groups < 1) a.groups = 1;
   if (a.wpr * a.groups > kCap) return QDQ_ERR_UNSUPPORTED;
+  constexpr int kRowsPerStage = 4 / kV;
+  const int units = (a.n_out + kRowsPerStage - 1) / kRowsPerStage;
   int grid = di.sm_count * ctas_per_sm_or(1);
-  if (grid > a.n_out) grid = a.n_out;
-  const int max_rows = (a.n_out + grid - 1) / grid;
+  if (grid > units) grid = units;
+  const int max_rows = (units + grid - 1) / grid * kRowsPerStage;
   const size_t smem = size_t(max_rows) * kV * a.wpr * sizeof(float);
   a.psum_cap = int(smem / sizeof(float));
   // L2 prefetch of the CTA's rows: on by default when this call's weights fit in half the L2
