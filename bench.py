@@ -688,7 +688,7 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
             for M in synth.C4_M:
                 X = torch.from_numpy(synth.config4_x(kind, M)).to(dev)
                 Y = torch.empty((M, n_out), device=dev)
-                wsp = torch.empty(qdq.gemm_batch_workspace_bytes(M, n_out, n_in), dtype=torch.uint8, device=dev)
+                wsp = torch.zeros(qdq.gemm_batch_workspace_bytes(M, n_out, n_in), dtype=torch.uint8, device=dev)
                 ls, dist = time_calls(torch, timer, lambda t: f(Wq[t], X, Y, wsp, n_out, n_in, M), ncopy,
                                       max(10, iters // 2))
                 b = wbytes + M * n_in * 4 + M * n_out * 4
@@ -708,7 +708,7 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
                 for M in synth.C4_M:
                     X = torch.from_numpy(synth.activations(synth.rng_for(8, 4, M), M, n_in)).to(dev)
                     midb = torch.empty((M, n_out), device=dev)
-                    wsp = torch.empty(qdq.q4k_swiglu_batch_workspace_bytes(M, n_out, n_in), dtype=torch.uint8,
+                    wsp = torch.zeros(qdq.q4k_swiglu_batch_workspace_bytes(M, n_out, n_in), dtype=torch.uint8,
                                       device=dev)
                     ls, dist = time_calls(torch, timer, lambda t: qdq.q4k_swiglu_batch(
                         pairs[t][0], pairs[t][1], X, midb, wsp, n_out, n_in, M), len(pairs), max(10, iters // 2))
@@ -790,7 +790,7 @@ def run_profile_case(case: str):
             f = qdq.q4k_gemm_batch
         X = torch.from_numpy(synth.config4_x(0, M)).to(dev)
         Y = torch.empty((M, N_FF), device=dev)
-        ws = torch.empty(qdq.gemm_batch_workspace_bytes(M, N_FF, N_EMBD), dtype=torch.uint8, device=dev)
+        ws = torch.zeros(qdq.gemm_batch_workspace_bytes(M, N_FF, N_EMBD), dtype=torch.uint8, device=dev)
         fn = lambda: f(W, X, Y, ws, N_FF, N_EMBD, M)
     else:
         raise SystemExit("unknown --profile case %r" % case)

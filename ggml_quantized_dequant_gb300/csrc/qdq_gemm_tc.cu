@@ -73,6 +73,16 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, in
       : "memory");
 }
 
+// L2 prefetch of one TMA tile (no shared memory, no completion): issued well ahead
+// of the tile's load, so that many more weight rows are in flight from HBM than
+// the shared-memory ring alone could hold.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *tm, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tm)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+constexpr int kPrefetchStages = 16;  // how far ahead of the loads the weight tiles are prefetched into L2
+
 // ---- tcgen05 --------------------------------------------------------------------
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -124,20 +134,34 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
 }
 
-// Stage layout: [ NA weight tiles as loaded | NA bf16 A tiles | bf16 B tile ]; every
-// tile starts on a 1024-byte boundary (the 128-byte swizzle atom).
+constexpr uint32_t round1k(uint32_t v) { return (v + 1023u) & ~1023u; }
+
+// Two rings in shared memory, every tile on a 1024-byte boundary (the 128-byte
+// swizzle atom):
+//   load ring, kSL slots, filled by TMA:  [ NA weight tiles as stored | X tile ]
+//     (X tile: the f32 activations, N x 64, when kXF; else the bf16 B tile);
+//   A ring, kSA slots, filled by the dequantising warps:  [ NA bf16 A tiles |
+//     the bf16 B tile when kXF ].
+// The load ring is as deep as shared memory allows (up to 16 slots), so that
+// many weight tiles are in flight per SM; the A ring only needs to keep the
+// tensor core fed.  kXF (token tiles of 64 or fewer): X arrives as f32 and is
+// rounded to bf16 in the kernel, so no conversion kernel runs before it.
 template <int FMT, int N, int NA>
 struct GemmCfg {
+  static constexpr bool kXF = N <= 64;
   static constexpr uint32_t kQTileBytes = FMT == kWQ8 ? BM * BK : BM * BK / 2;
   static constexpr uint32_t kBTileBytes = uint32_t(N) * 128;
-  static constexpr uint32_t kStageBytes = NA * (kQTileBytes + kATileBytes) + kBTileBytes;
-  static constexpr int kFit = int((227u * 1024u - 2048u) / kStageBytes);
-  // as many stages as fit in 227 KB, at most 8: more weight bytes in flight per SM
-  static constexpr int kStages = kFit > 8 ? 8 : kFit;
+  static constexpr uint32_t kXTileBytes = kXF ? uint32_t(N) * BK * 4 : kBTileBytes;
+  static constexpr uint32_t kLoadSlot = round1k(NA * kQTileBytes + kXTileBytes);
+  static constexpr uint32_t kASlot = round1k(NA * kATileBytes + (kXF ? kBTileBytes : 0u));
+  static constexpr int kSA = (NA == 1 && N <= 32) ? 3 : 2;
+  static constexpr int kFit = int((227u * 1024u - 2048u - uint32_t(kSA) * kASlot) / kLoadSlot);
+  static constexpr int kSL = kFit > 16 ? 16 : kFit;
   static constexpr uint32_t kCols = uint32_t(NA * N);
   static constexpr uint32_t kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
-  static constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + 256;
-  static_assert(kStages >= 2, "pipeline needs two stages");
+  static constexpr size_t kSmemBytes = 1024 + size_t(kSL) * kLoadSlot + size_t(kSA) * kASlot + 512;
+  static_assert(kSL >= 2, "the load ring needs two slots");
+  static_assert(kSmemBytes <= 227u * 1024u, "shared memory");
 };
 
 struct GemmArgs {
@@ -173,13 +197,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tm_x, const GemmArgs g, const Magic mg_param) {
   using C = GemmCfg<FMT, N, NA>;
   const Magic mg = lane_magic(mg_param);
-  constexpr int S = C::kStages;
+  constexpr int SL = C::kSL, SA = C::kSA;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + S * C::kStageBytes);
-  uint64_t *aready = full + S;
-  uint64_t *empty = aready + S;
-  uint64_t *accum = empty + S;
+  uint8_t *aring = smem + SL * C::kLoadSlot;
+  uint64_t *lfull = reinterpret_cast<uint64_t *>(aring + SA * C::kASlot);
+  uint64_t *lempty = lfull + SL;
+  uint64_t *aready = lempty + SL;
+  uint64_t *aempty = aready + SA;
+  uint64_t *accum = aempty + SA;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
   __shared__ int s_abort, s_last;
 
@@ -191,16 +217,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb0 = blockIdx.z * g.kb_per_split;
   const int kb1 = min(kb0 + g.kb_per_split, nkb);
   const int nk = kb1 - kb0;
-  auto qtile = [&](int s, int a) { return smem + s * C::kStageBytes + a * C::kQTileBytes; };
-  auto atile = [&](int s, int a) { return smem + s * C::kStageBytes + NA * C::kQTileBytes + a * kATileBytes; };
-  auto btile = [&](int s) { return smem + s * C::kStageBytes + NA * (C::kQTileBytes + kATileBytes); };
+  auto qtile = [&](int s, int a) { return smem + s * C::kLoadSlot + a * C::kQTileBytes; };
+  auto xtile = [&](int s) { return smem + s * C::kLoadSlot + NA * C::kQTileBytes; };
+  auto atile = [&](int j, int a) { return aring + j * C::kASlot + a * kATileBytes; };
+  // the MMA's B operand of stage i: in the A slot (converted here) or the load slot (TMA)
+  auto btile = [&](int i) { return C::kXF ? aring + (i % SA) * C::kASlot + NA * kATileBytes : xtile(i % SL); };
   constexpr int kQBox = FMT == kWQ8 ? BK : BK / 2;  // inner TMA coordinate step of a weight tile per stage
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&aready[s], kDequantWarps * 32);
-      mbar_init(&empty[s], 1);
+    for (int i = 0; i < SL; ++i) {
+      mbar_init(&lfull[i], 1);
+      mbar_init(&lempty[i], 1);
+    }
+    for (int j = 0; j < SA; ++j) {
+      mbar_init(&aready[j], kDequantWarps * 32);
+      mbar_init(&aempty[j], 1);
     }
     mbar_init(accum, 1);
     s_abort = 0;
@@ -220,29 +251,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q0)) : "memory");
       if (NA == 2) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q1)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
-      constexpr uint32_t kTx = NA * C::kQTileBytes + C::kBTileBytes;
-      const int npre = nk < S ? nk : S;
+      constexpr uint32_t kTx = NA * C::kQTileBytes + C::kXTileBytes;
+      const int npre = nk < SL ? nk : SL;
       // weights do not depend on the previous kernel: start them before the wait
+      for (int i = npre; i < nk && i < npre + kPrefetchStages; ++i) {
+        tma_prefetch_2d(&tm_q0, (kb0 + i) * kQBox, tile_n * BM);
+        if (NA == 2) tma_prefetch_2d(&tm_q1, (kb0 + i) * kQBox, tile_n * BM);
+      }
       for (int i = 0; i < npre; ++i) {
-        mbar_arrive_expect_tx(&full[i], kTx);
-        tma_load_2d(qtile(i, 0), &tm_q0, (kb0 + i) * kQBox, tile_n * BM, &full[i]);
-        if (NA == 2) tma_load_2d(qtile(i, 1), &tm_q1, (kb0 + i) * kQBox, tile_n * BM, &full[i]);
+        mbar_arrive_expect_tx(&lfull[i], kTx);
+        tma_load_2d(qtile(i, 0), &tm_q0, (kb0 + i) * kQBox, tile_n * BM, &lfull[i]);
+        if (NA == 2) tma_load_2d(qtile(i, 1), &tm_q1, (kb0 + i) * kQBox, tile_n * BM, &lfull[i]);
       }
       pdl_wait();
-      for (int i = 0; i < npre; ++i) tma_load_2d(btile(i), &tm_x, (kb0 + i) * BK, tile_m * N, &full[i]);
+      for (int i = 0; i < npre; ++i) tma_load_2d(xtile(i), &tm_x, (kb0 + i) * BK, tile_m * N, &lfull[i]);
       issued = npre;
       for (int i = npre; i < nk; ++i) {
-        const int s = i % S;
+        const int s = i % SL;
         // after any timed-out wait in this CTA, issue nothing more
-        if (*reinterpret_cast<volatile int *>(&s_abort) || !mbar_wait(&empty[s], ((i / S) + 1) & 1)) {
+        if (*reinterpret_cast<volatile int *>(&s_abort) || !mbar_wait(&lempty[s], ((i / SL) + 1) & 1)) {
           s_abort = 1;
           break;
         }
-        mbar_arrive_expect_tx(&full[s], kTx);
-        tma_load_2d(qtile(s, 0), &tm_q0, (kb0 + i) * kQBox, tile_n * BM, &full[s]);
-        if (NA == 2) tma_load_2d(qtile(s, 1), &tm_q1, (kb0 + i) * kQBox, tile_n * BM, &full[s]);
-        tma_load_2d(btile(s), &tm_x, (kb0 + i) * BK, tile_m * N, &full[s]);
+        mbar_arrive_expect_tx(&lfull[s], kTx);
+        tma_load_2d(qtile(s, 0), &tm_q0, (kb0 + i) * kQBox, tile_n * BM, &lfull[s]);
+        if (NA == 2) tma_load_2d(qtile(s, 1), &tm_q1, (kb0 + i) * kQBox, tile_n * BM, &lfull[s]);
+        tma_load_2d(xtile(s), &tm_x, (kb0 + i) * BK, tile_m * N, &lfull[s]);
         issued = i + 1;
+        if (i + kPrefetchStages < nk) {
+          tma_prefetch_2d(&tm_q0, (kb0 + i + kPrefetchStages) * kQBox, tile_n * BM);
+          if (NA == 2) tma_prefetch_2d(&tm_q1, (kb0 + i + kPrefetchStages) * kQBox, tile_n * BM);
+        }
       }
     } else {
       pdl_wait();
@@ -253,22 +292,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(BM, N);
       for (int i = 0; i < nk; ++i) {
-        const int s = i % S;
-        if (!mbar_wait(&aready[s], (i / S) & 1) || !mbar_wait(&full[s], (i / S) & 1)) {
+        const int s = i % SL, j = i % SA;
+        if (!mbar_wait(&aready[j], (i / SA) & 1) || !mbar_wait(&lfull[s], (i / SL) & 1)) {
           s_abort = 1;
           break;
         }
         tc_fence_after();
-        const uint32_t b_base = smem_u32(btile(s));
+        const uint32_t b_base = smem_u32(btile(i));
 #pragma unroll
         for (int a = 0; a < NA; ++a) {
-          const uint32_t a_base = smem_u32(atile(s, a));
+          const uint32_t a_base = smem_u32(atile(j, a));
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             umma_bf16(tmem + uint32_t(a * N), desc_kmajor_sw128(a_base + 32 * k), desc_kmajor_sw128(b_base + 32 * k),
                       idesc, (i | k) != 0);
         }
-        umma_commit(&empty[s]);
+        umma_commit(&aempty[j]);  // the A slot (and the B tile in it) is free once these MMAs are done
+        umma_commit(&lempty[s]);  // so is the load slot
       }
       umma_commit(accum);
     }
@@ -277,6 +317,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The weights do not depend on the previous kernel, so dequantisation starts
     // at once; only the epilogue (which writes Y) waits for it.
     bool ok = true;
+    // stage i may overwrite A slot i % SA once the MMAs of stage i - SA are done
+    auto wait_slots = [&](int i) {
+      if (!mbar_wait(&lfull[i % SL], (i / SL) & 1)) return false;
+      return i < SA || mbar_wait(&aempty[i % SA], ((i / SA) - 1) & 1);
+    };
+    // kXF: X rows of the stage (f32, 256 bytes each) -> the bf16 B tile in the
+    // 128-byte-swizzled K-major layout; one 16-byte chunk (8 values) per thread
+    auto convert_x = [&](int i) {
+      if constexpr (C::kXF) {
+        const float *xs = reinterpret_cast<const float *>(xtile(i % SL));
+        uint8_t *bt = btile(i);
+        for (int t = threadIdx.x; t < N * 8; t += kDequantWarps * 32) {
+          const int r = t >> 3, c = t & 7;
+          const float4 v0 = *reinterpret_cast<const float4 *>(xs + r * BK + 8 * c);
+          const float4 v1 = *reinterpret_cast<const float4 *>(xs + r * BK + 8 * c + 4);
+          *reinterpret_cast<uint4 *>(bt + r * 128 + ((c ^ (r & 7)) << 4)) =
+              make_uint4(pack_bf16x2(f2(v0.x, v0.y)), pack_bf16x2(f2(v0.z, v0.w)), pack_bf16x2(f2(v1.x, v1.y)),
+                         pack_bf16x2(f2(v1.z, v1.w)));
+        }
+      }
+    };
     if constexpr (FMT == kWQ8) {
       const int row = threadIdx.x & (BM - 1);  // weight row within the tile
       const int part = threadIdx.x >> 7;       // which 16 of the row's 64 quants
@@ -293,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int a = 0; a < NA; ++a) dqa[t][a] = t < nk ? __ldg(d32[a] + kb0 + t) : 0u;
       for (int i = 0; i < nk; ++i) {
-        const int s = i % S;
+        const int s = i % SL, j = i % SA;
         uint32_t dq[NA];
 #pragma unroll
         for (int a = 0; a < NA; ++a) {
@@ -303,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           dqa[2][a] = dqa[3][a];
           dqa[3][a] = i + 4 < nk ? __ldg(d32[a] + kb0 + i + 4) : 0u;
         }
-        if (!mbar_wait(&full[s], (i / S) & 1)) {
+        if (!wait_slots(i)) {
           s_abort = 1;
           ok = false;
           break;
@@ -311,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int a = 0; a < NA; ++a) {
           const uint8_t *qt = qtile(s, a);
-          uint8_t *at = atile(s, a);
+          uint8_t *at = atile(j, a);
           const __half2 dh = *reinterpret_cast<const __half2 *>(&dq[a]);
           const float dsc = part < 2 ? __low2float(dh) : __high2float(dh);  // block scale of K 32*(part/2)..
           const float2 dpair = f2(dsc, dsc);
@@ -331,8 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4 *>(at + row * 128 + (((2 * part + 1) ^ (row & 7)) << 4)) =
               make_uint4(packed[4], packed[5], packed[6], packed[7]);
         }
+        convert_x(i);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(&aready[s]);
+        mbar_arrive(&aready[j]);
       }
     } else {
       // Q4_K: warp w takes rows 8w..8w+7, four threads per row, 16 nibbles (8 bytes) each:
@@ -354,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         hnext[a] = cur_sb + 1 < nsb ? __ldg(hdr[a] + cur_sb + 1) : hcur[a];
       }
       for (int i = 0; i < nk; ++i) {
-        const int s = i % S;
+        const int s = i % SL, jj = i % SA;
         const int kb = kb0 + i;
         if ((kb >> 2) != cur_sb) {  // entering the next superblock
           ++cur_sb;
@@ -368,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float2 dm[NA];                             // (d*sc_j, dmin*m_j)
 #pragma unroll
         for (int a = 0; a < NA; ++a) dm[a] = q4k_header_scale(hcur[a], j);
-        if (!mbar_wait(&full[s], (i / S) & 1)) {
+        if (!wait_slots(i)) {
           s_abort = 1;
           ok = false;
           break;
@@ -376,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int a = 0; a < NA; ++a) {
           const uint2 qv = *reinterpret_cast<const uint2 *>(qtile(s, a) + row * 32 + part * 8);
-          uint8_t *at = atile(s, a);
+          uint8_t *at = atile(jj, a);
           const float2 D = f2(dm[a].x, dm[a].x), Dm = f2(-dm[a].y, -dm[a].y);
           uint32_t packed[8];
 #pragma unroll
@@ -391,8 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4 *>(at + row * 128 + (((2 * part + 1) ^ (row & 7)) << 4)) =
               make_uint4(packed[4], packed[5], packed[6], packed[7]);
         }
+        convert_x(i);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(&aready[s]);
+        mbar_arrive(&aready[jj]);
       }
     }
     pdl_wait();
@@ -493,8 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool drained = true;
   if (warp == kDequantWarps + 1 && lane == 0) drained = mbar_wait(accum, 0);
   if (warp == kDequantWarps && lane == 0)
-    for (int i = issued - S < 0 ? 0 : issued - S; i < issued; ++i)
-      drained = mbar_wait(&full[i % S], (i / S) & 1) && drained;
+    for (int i = issued - SL < 0 ? 0 : issued - SL; i < issued; ++i)
+      drained = mbar_wait(&lfull[i % SL], (i / SL) & 1) && drained;
   if (!drained) atomicAdd(&g_pipeline_timeouts, 1u);
   if (threadIdx.x == 0 && s_abort) atomicAdd(&g_pipeline_timeouts, 1u);
   if (warp == kDequantWarps + 1) {
@@ -547,10 +610,15 @@ bool encode_2d(CUtensorMap *tm, CUtensorMapDataType dt, void *base, uint64_t inn
 // The token tile for M tokens.
 int token_tile(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256; }
 
-// Launch shape and workspace layout of one GEMM call.
+// Launch shape and workspace layout of one GEMM call.  The workspace starts
+// with kTicketBytes of split-K tile counters (zero between calls: the last CTA
+// of a tile resets its counter), then the bf16 copy of X (token tiles above
+// 64 only), then the split-K partial tiles.
+constexpr size_t kTicketBytes = 65536;
+constexpr int kMaxTiles = int(kTicketBytes / sizeof(int));
 struct GemmPlan {
   int N, ntile_n, ntile_m, nkb, split, kb_per;
-  size_t xb_bytes, part_bytes, ticket_bytes;
+  size_t xb_bytes, part_bytes;
 };
 GemmPlan plan_gemm(int M, int n_out, int n_in, int na, int sm_count) {
   GemmPlan p;
@@ -564,9 +632,8 @@ GemmPlan plan_gemm(int M, int n_out, int n_in, int na, int sm_count) {
   if (split > p.nkb) split = p.nkb;
   p.kb_per = (p.nkb + split - 1) / split;
   p.split = (p.nkb + p.kb_per - 1) / p.kb_per;  // every split gets at least one K block
-  p.xb_bytes = (size_t(M) * n_in * 2 + 255) / 256 * 256;
+  p.xb_bytes = p.N <= 64 ? 0 : (size_t(M) * n_in * 2 + 255) / 256 * 256;
   p.part_bytes = p.split > 1 ? size_t(p.split) * na * M * n_out * 4 : 0;
-  p.ticket_bytes = (size_t(tiles) * 4 + 255) / 256 * 256;
   return p;
 }
 
@@ -585,34 +652,44 @@ int launch_tile(const uint8_t *const W[2], const float *X, float *Y, void *ws, i
                                      CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!okq) return QDQ_ERR_UNSUPPORTED;
   }
-  if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws, uint64_t(n_in), uint64_t(M), uint64_t(n_in) * 2, BK, N,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
-    return QDQ_ERR_UNSUPPORTED;
 
   uint8_t *wsb = static_cast<uint8_t *>(ws);
   GemmArgs g{};
   g.W[0] = W[0];
   g.W[1] = W[NA - 1];
   g.Y = Y;
-  g.partials = reinterpret_cast<float *>(wsb + p.xb_bytes);
-  g.tickets = reinterpret_cast<int *>(wsb + p.xb_bytes + p.part_bytes);
+  g.tickets = reinterpret_cast<int *>(wsb);
+  g.partials = reinterpret_cast<float *>(wsb + kTicketBytes + p.xb_bytes);
   g.n_out = n_out;
   g.n_in = n_in;
   g.M = M;
   g.kb_per_split = p.kb_per;
   g.split = p.split;
+  if (p.split > 1 && p.ntile_n * p.ntile_m > kMaxTiles) return QDQ_ERR_UNSUPPORTED;
 
-  // conversion of X, and zeroing of the split-K tickets
-  const int64_t n4 = int64_t(M) * n_in / 4;
-  int cgrid = int((n4 + 255) / 256);
-  if (cgrid > di.sm_count * 8) cgrid = di.sm_count * 8;
-  if (cgrid < 1) cgrid = 1;
-  cudaError_t e = launch(x_to_bf16_kernel, dim3(cgrid), dim3(256), 0, s, reinterpret_cast<const float4 *>(X),
-                         reinterpret_cast<uint2 *>(wsb), n4, g.tickets, p.split > 1 ? p.ntile_n * p.ntile_m : 0);
-  if (e != cudaSuccess) return fail_cuda(e);
+  cudaError_t e;
+  if (C::kXF) {
+    // X is read as f32 and rounded to bf16 inside the GEMM
+    if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, const_cast<float *>(X), uint64_t(n_in), uint64_t(M),
+                   uint64_t(n_in) * 4, BK, N, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return QDQ_ERR_UNSUPPORTED;
+  } else {
+    // conversion of X into the workspace, and zeroing of the split-K tickets
+    uint8_t *xb = wsb + kTicketBytes;
+    if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xb, uint64_t(n_in), uint64_t(M), uint64_t(n_in) * 2, BK,
+                   N, CU_TENSOR_MAP_SWIZZLE_128B))
+      return QDQ_ERR_UNSUPPORTED;
+    const int64_t n4 = int64_t(M) * n_in / 4;
+    int cgrid = int((n4 + 255) / 256);
+    if (cgrid > di.sm_count * 8) cgrid = di.sm_count * 8;
+    if (cgrid < 1) cgrid = 1;
+    e = launch(x_to_bf16_kernel, dim3(cgrid), dim3(256), 0, s, reinterpret_cast<const float4 *>(X),
+               reinterpret_cast<uint2 *>(xb), n4, g.tickets, p.split > 1 ? p.ntile_n * p.ntile_m : 0);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
 
   auto kern = gemm_tc_kernel<FMT, N, NA>;
-  e = allow_dynamic_smem(reinterpret_cast<const void *>(kern), int(C::kSmemBytes));
+  e = allow_dynamic_smem(reinterpret_cast<const void *>(kern), int(C::kSmemBytes));  // once per kernel
   if (e != cudaSuccess) return fail_cuda(e);
   e = launch(kern, dim3(p.ntile_n, p.ntile_m, p.split), dim3(kThreads), C::kSmemBytes, s, tm_q[0], tm_q[1], tm_x, g,
              make_magic());
@@ -643,7 +720,7 @@ size_t gemm_workspace_bytes(int M, int n_out, int n_in, int na) {
   DeviceInfo di;
   if (device_info(&di) != cudaSuccess) return 0;
   const GemmPlan p = plan_gemm(M, n_out, n_in, na, di.sm_count);
-  return p.xb_bytes + p.part_bytes + p.ticket_bytes;
+  return kTicketBytes + p.xb_bytes + p.part_bytes;
 }
 
 int launch_q8_0_gemm_batch(const void *W, const float *X, float *Y, void *ws, int n_out, int n_in, int M,

@@ -13,27 +13,30 @@
 // owns half l & 1 of blocks 32 s + (l >> 1) and 32 s + 16 + (l >> 1), so that
 // each of its two 16-byte loads is one contiguous 512-byte span for the warp
 // (a whole 32-byte block per lane would touch every sector twice).  WPR =
-// ceil(n_in / 1024) slice warps
-// cover a row; G groups of slice warps take contiguous shares of the CTA's rows
-// (one CTA per SM).  A warp handles 4 (virtual) rows per stage: each lane loads
-// its block of the 4 rows with 128-bit loads into registers, multiplies, and a
-// recursive-halving butterfly leaves row k's warp total in lane 8k; the slice
-// totals of a row are added in fixed order at the end (deterministic results).
+// ceil(n_in / 1024) slice warps cover a row.  Rows are dealt out in whole
+// stages; by default a CTA is one group of slice warps, and as many CTAs as fit
+// share an SM (QDQ_OPT_XS_GROUPS / QDQ_OPT_CTAS_PER_SM override both).  A warp
+// handles 4 (virtual) rows per stage: each lane loads its part of the 4 rows
+// with 128-bit loads into registers, multiplies, and a recursive-halving
+// butterfly leaves row k's warp total in lane 8k; the slice totals of a row are
+// added in fixed order at the end (deterministic results).
 //
 // Loads in flight: with DEPTH = 2 a warp holds two stages of registers and
 // loads stage t + 2 as soon as it has used stage t, so a stage's loads are in
-// flight during the previous stage's arithmetic (12 warps, about 160 registers
-// a thread); DEPTH = 1 (rows of more than 12 slices) loads the next stage after
-// the arithmetic of the current one.  The first stages are loaded before the
-// wait for the previous kernel, and a bulk L2 prefetch of the CTA's rows is
-// issued first when the call's weights fit in half the L2.
+// flight during the previous stage's arithmetic (about 166 registers a thread:
+// four 3-warp CTAs fill an SM); DEPTH = 1 (rows of more than 4 slices) loads the
+// next stage after the arithmetic of the current one, at up to 128 registers, so
+// that two 8-warp CTAs share an SM.  The first stages are loaded before the wait
+// for the previous kernel.  Small CTAs are the point: the SM's CTAs finish at
+// different times, and each one that finishes lets a CTA of the next kernel in
+// the stream start its weight loads while the rest of this kernel completes
+// (one SM-sized CTA per kernel measured 8.1 us per 3072 <-> 8192 Q8_0 matrix
+// in the decode chain, the split shapes 6.9 us).
 //
-// Against the co-resident ring kernel (a producer warp streaming into a
-// shared-memory ring sized to half an SM, so that the next kernel's CTA fits
-// beside it, with 6-9 computing warps): here the whole SM computes and the
-// registers of two stages keep the memory pipe busy.  A variant with per-warp
-// bulk-copy rings in shared memory measured slower than this one (1 KB and
-// 64-byte copies per row and warp).
+// A variant with per-warp bulk-copy rings in shared memory measured slower than
+// registers (1 KB and 64-byte copies per row and warp), and so did a bulk L2
+// prefetch of the CTA's rows at its start (QDQ_OPT_L2_PREFETCH = 1 still issues
+// it).
 //
 // Arithmetic: f32 (weights converted exactly, packed f32x2 FMAs; Q4_K with the
 // sub-block shift q4k_mu), within 1e-5 sum |w||x| for every finite input.
@@ -417,29 +420,42 @@ template <int FMT, int EPI, int DEPTH>
 int launch_dl_depth(DlArgs a, cudaStream_t s, const DeviceInfo &di) {
   constexpr int kV = EPI == kSwiglu ? 2 : 1;
   constexpr int kCap = DEPTH == 2 ? kMaxWarpsDepth2 : kMaxWarps;
-  a.groups = opt_xs_groups() > 0 ? opt_xs_groups() : kCap / a.wpr;
-  if (a.groups < 1) a.groups = 1;
+  // default: one group of slice warps per CTA, and as many CTAs per SM as fit, so
+  // that a CTA that finishes early frees room for the next kernel's CTA (its
+  // weight loads then overlap this kernel's tail)
+  a.groups = opt_xs_groups() > 0 ? opt_xs_groups() : 1;
   if (a.wpr * a.groups > kCap) return QDQ_ERR_UNSUPPORTED;
+  const int threads = 32 * a.wpr * a.groups;
   constexpr int kRowsPerStage = 4 / kV;
   const int units = (a.n_out + kRowsPerStage - 1) / kRowsPerStage;
-  int grid = di.sm_count * ctas_per_sm_or(1);
-  if (grid > units) grid = units;
-  const int max_rows = (units + grid - 1) / grid * kRowsPerStage;
-  const size_t smem = size_t(max_rows) * kV * a.wpr * sizeof(float);
-  a.psum_cap = int(smem / sizeof(float));
-  // L2 prefetch of the CTA's rows: on by default when this call's weights fit in half the L2
-  const int64_t w_bytes = int64_t(a.n_out) * (FMT == kQ8 ? int64_t(a.n_in) / 32 * 34
-                                              : FMT == kQ4 ? int64_t(a.n_in) / 256 * 144
-                                                           : q6k_row_bytes(a.n_in)) * kV;
-  const int pf = opt_l2_prefetch();
-  a.prefetch = pf == 3 ? 0 : pf == 1 ? 1 : (w_bytes <= int64_t(di.l2_bytes) / 2 ? 1 : 0);
   auto kern = gemv_dl_kernel<FMT, EPI, DEPTH>;
+  auto psum_bytes = [&](int grid) { return size_t((units + grid - 1) / grid * kRowsPerStage) * kV * a.wpr * 4; };
+  int per_sm = ctas_per_sm_or(0);
+  if (per_sm == 0) {
+    // shared memory of the largest CTA share at one CTA per SM bounds every other shape's
+    const size_t smem0 = psum_bytes(units < di.sm_count ? units : di.sm_count);
+    if (smem0 > 48 * 1024) {
+      if (smem0 > size_t(di.max_smem_optin)) return QDQ_ERR_UNSUPPORTED;
+      const cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(kern), int(smem0));
+      if (e != cudaSuccess) return fail_cuda(e);
+    }
+    int nb = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, threads, smem0);
+    if (e != cudaSuccess) return fail_cuda(e);
+    per_sm = nb < 1 ? 1 : nb > 16 ? 16 : nb;
+  }
+  int grid = di.sm_count * per_sm;
+  if (grid > units) grid = units;
+  const size_t smem = psum_bytes(grid);
+  a.psum_cap = int(smem / sizeof(float));
+  // L2 prefetch of the CTA's rows: off unless QDQ_OPT_L2_PREFETCH = 1 (measured no faster here)
+  a.prefetch = opt_l2_prefetch() == 1 ? 1 : 0;
   if (smem > 48 * 1024) {
     if (smem > size_t(di.max_smem_optin)) return QDQ_ERR_UNSUPPORTED;
     const cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(kern), int(smem));
     if (e != cudaSuccess) return fail_cuda(e);
   }
-  const cudaError_t e = launch(kern, dim3(grid), dim3(32 * a.wpr * a.groups), smem, s, a, make_magic());
+  const cudaError_t e = launch(kern, dim3(grid), dim3(threads), smem, s, a, make_magic());
   return e == cudaSuccess ? QDQ_OK : fail_cuda(e);
 }
 
@@ -450,12 +466,12 @@ int launch_dl(DlArgs a, cudaStream_t s) {
   if (e0 != cudaSuccess) return fail_cuda(e0);
   a.wpr = ((a.n_in >> 5) + 31) / 32;
   if (a.wpr > kMaxWarps) return QDQ_ERR_UNSUPPORTED;
-  // two stages of registers in flight unless a row needs more than 12 slice warps
-  // (QDQ_OPT_XS_STAGES = 1 or 2 picks the depth)
-  int depth = a.wpr <= kMaxWarpsDepth2 ? 2 : 1;
+  // two stages of registers in flight for rows of up to 4 slice warps (several
+  // such CTAs share an SM); wider rows run one stage deep, which lets two of
+  // their CTAs share an SM (QDQ_OPT_XS_STAGES = 1 or 2 picks the depth)
+  int depth = a.wpr <= 4 ? 2 : 1;
   if (opt_xs_stages() == 1 || opt_xs_stages() == 2) depth = opt_xs_stages();
-  // more warps than two stages of registers allow (a wide row, or a forced group
-  // count) run one stage deep
+  // more warps than two stages of registers allow (a forced group count) run one stage deep
   const int warps = a.wpr * (opt_xs_groups() > 0 ? opt_xs_groups() : 1);
   if (warps > kMaxWarpsDepth2) depth = 1;
   return depth == 2 ? launch_dl_depth<FMT, EPI, 2>(a, s, di) : launch_dl_depth<FMT, EPI, 1>(a, s, di);

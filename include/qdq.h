@@ -266,8 +266,11 @@ int qdq_q4k_ffn_residual_noalloc(const void *Wg, const void *Wu, const void *Wd,
  * Y: M x n_out f32 (16-byte aligned), must not overlap W, X or workspace.
  * workspace: caller-owned scratch of qdq_gemm_batch_workspace_bytes(M, n_out,
  * n_in) bytes (the size depends on the current device's SM count, 0 when it
- * cannot be queried), 256-byte aligned, overwritten: X rounded to bf16, the
- * split-K partial tiles, one counter per output tile.
+ * cannot be queried), 256-byte aligned.  Its first 64 KiB hold one split-K
+ * counter per output tile and must be zero when a call starts: zero-fill the
+ * workspace once after allocating it; every call leaves the counters at zero
+ * again (also across calls of other shapes).  The rest is overwritten: X
+ * rounded to bf16 (M > 64 only), the split-K partial tiles.
  * Requires n_in % 64 == 0 (Q4_K: % 256) and n_out % 128 == 0; M >= 1 (tail
  * masked).  Results do not depend on the order in which CTAs run (split-K
  * partials are added in a fixed order).

@@ -59,7 +59,7 @@ def _nan(*shape):
 
 def _ws(nbytes):
     import torch
-    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=_dev())
+    return torch.zeros(max(int(nbytes), 1), dtype=torch.uint8, device=_dev())
 
 
 def _same(qdq, dbg, run):

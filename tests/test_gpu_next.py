@@ -225,7 +225,7 @@ def _gemm_q4k(qdq, wb, X, n_out, n_in, M):
     import torch
     W = qdq.upload_q4k(wb, n_out, n_in)
     Y = _nan(M, n_out)
-    ws = torch.empty(qdq.gemm_batch_workspace_bytes(M, n_out, n_in), dtype=torch.uint8, device=_dev())
+    ws = torch.zeros(qdq.gemm_batch_workspace_bytes(M, n_out, n_in), dtype=torch.uint8, device=_dev())
     qdq.q4k_gemm_batch(W, _t(X), Y, ws, n_out, n_in, M)
     return _np(Y)
 
@@ -289,7 +289,7 @@ def test_gemm_batch_split_k_is_deterministic(cuda_lib, fmt):
         W, f = qdq.upload_q8_0(synth.q8_0_blocks(rng, n_out, n_in), n_out, n_in), qdq.q8_0_gemm_batch
     else:
         W, f = qdq.upload_q4k(synth.q4k_blocks(rng, n_out, n_in), n_out, n_in), qdq.q4k_gemm_batch
-    ws = torch.empty(qdq.gemm_batch_workspace_bytes(M, n_out, n_in), dtype=torch.uint8, device=_dev())
+    ws = torch.zeros(qdq.gemm_batch_workspace_bytes(M, n_out, n_in), dtype=torch.uint8, device=_dev())
     outs = []
     for _ in range(3):
         Y = _nan(M, n_out)
@@ -297,6 +297,28 @@ def test_gemm_batch_split_k_is_deterministic(cuda_lib, fmt):
         outs.append(_np(Y))
     assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
     assert np.array_equal(outs[0].view(np.uint32), outs[2].view(np.uint32))
+
+
+def test_gemm_batch_workspace_reused_across_shapes(cuda_lib):
+    # one workspace, zero-filled once, serves calls of different shapes and token counts
+    # (different split-K plans): every call must leave its tile counters at zero
+    import torch
+    qdq = cuda_lib
+    rng = np.random.default_rng(74)
+    cases = [(3072, 8192, 16), (8192, 3072, 16), (3072, 8192, 40), (384, 1024, 33), (3072, 8192, 64),
+             (1024, 2048, 130), (3072, 8192, 16)]
+    size = max(qdq.gemm_batch_workspace_bytes(M, n_out, n_in) for n_out, n_in, M in cases)
+    ws = torch.zeros(size, dtype=torch.uint8, device=_dev())
+    for n_out, n_in, M in cases:
+        wb, X = synth.q8_0_blocks(rng, n_out, n_in), synth.activations(rng, M, n_in)
+        W = qdq.upload_q8_0(wb, n_out, n_in)
+        Y = _nan(M, n_out)
+        qdq.q8_0_gemm_batch(W, _t(X), Y, ws, n_out, n_in, M)
+        rows = np.arange(0, M, max(1, M // 8))
+        Y_ref, A = oracle.gemm_batch(oracle.q8_0_dequant(wb, n_out, n_in), X[rows])
+        assert gemv_excess(_np(Y)[rows], Y_ref, A, rel=4e-3) <= 1.0, (n_out, n_in, M)
+    assert int(ws[:65536].count_nonzero()) == 0
+    assert qdq.pipeline_timeouts() == 0
 
 
 def _swiglu_batch_bound(s, rel=4e-3):
@@ -314,7 +336,7 @@ def test_q4k_swiglu_batch_parity(cuda_lib, n_ff, n_embd, M):
     X = synth.activations(rng, M, n_embd)
     Wg, Wu = qdq.upload_q4k(g, n_ff, n_embd), qdq.upload_q4k(u, n_ff, n_embd)
     mid = _nan(M, n_ff)
-    ws = torch.empty(qdq.q4k_swiglu_batch_workspace_bytes(M, n_ff, n_embd), dtype=torch.uint8, device=_dev())
+    ws = torch.zeros(qdq.q4k_swiglu_batch_workspace_bytes(M, n_ff, n_embd), dtype=torch.uint8, device=_dev())
     qdq.q4k_swiglu_batch(Wg, Wu, _t(X), mid, ws, n_ff, n_embd, M)
     rows = _tile_sample(M, 5)[:16]
     s = oracle.swiglu(oracle.q4k_dequant(g, n_ff, n_embd), oracle.q4k_dequant(u, n_ff, n_embd), X[rows])

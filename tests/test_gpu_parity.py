@@ -254,7 +254,7 @@ def _gemm_case(qdq, n_out, n_in, M, wb=None, X=None, sample_rows=None, seed=0):
         X = synth.activations(rng, M, n_in)
     W = qdq.upload_q8_0(wb, n_out, n_in)
     Y = _nan(M, n_out)
-    ws = torch.empty(qdq.gemm_batch_workspace_bytes(M, n_out, n_in), dtype=torch.uint8, device=_dev())
+    ws = torch.zeros(qdq.gemm_batch_workspace_bytes(M, n_out, n_in), dtype=torch.uint8, device=_dev())
     qdq.q8_0_gemm_batch(W, _t(X), Y, ws, n_out, n_in, M)
     Yh = _np(Y)
     rows = np.arange(M) if sample_rows is None else sample_rows
@@ -294,7 +294,7 @@ def test_q8_0_gemm_batch_m1_matches_gemv_within_bf16_bound(cuda_lib):
     y = _nan(1, 256)
     Y = _nan(1, 256)
     qdq.q8_0_gemv(W, _t(x), y, 256, 512, 1)
-    ws = torch.empty(qdq.gemm_batch_workspace_bytes(1, 256, 512), dtype=torch.uint8, device=_dev())
+    ws = torch.zeros(qdq.gemm_batch_workspace_bytes(1, 256, 512), dtype=torch.uint8, device=_dev())
     qdq.q8_0_gemm_batch(W, _t(x), Y, ws, 256, 512, 1)
     _, a = oracle.gemv(oracle.q8_0_dequant(wb, 256, 512), x)
     assert np.all(np.abs(_np(Y) - _np(y)) <= 4e-3 * a)
