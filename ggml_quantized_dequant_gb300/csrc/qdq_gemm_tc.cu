@@ -28,18 +28,25 @@
 //
 // Warp roles (576 threads):
 //   warps 0-15 dequantise the weight tile(s) into bf16 A tiles in the
-//              128-byte-swizzled K-major layout the tensor core reads (Q8_0:
-//              four threads per row, 16 quants each, from a 64-byte-swizzled
-//              int8 TMA tile; Q4_K: a warp per 8 rows, four threads per row,
-//              16 nibbles each, from a dense 32-byte-row TMA tile, with the
-//              row's superblock header fetched once per superblock); after the
-//              last stage the same warps read the accumulators out of TMEM and
-//              store Y (warp w reads TMEM lanes 32*(w%4).. and every fourth
-//              16-column chunk);
-//   warp 16    TMA producer: weight tile(s) and the bf16 activation tile
-//              (N x 64, 128-byte swizzle) per stage;
+//              128-byte-swizzled K-major layout the tensor core reads, as two
+//              groups of 8 warps taking alternate K stages (Q8_0: two threads
+//              per row, 32 quants and one block scale each, from a
+//              64-byte-swizzled int8 TMA tile; Q4_K: two threads per row, one
+//              32-weight sub-block each, from a dense 32-byte-row TMA tile, with
+//              the row's superblock header fetched once per superblock); for
+//              token tiles up to 64 the same warps round the stage's f32 X tile
+//              to the bf16 B tile.  After the last stage the 16 warps read the
+//              accumulators out of TMEM and store Y (warp w reads TMEM lanes
+//              32*(w%4).. and every fourth 16-column chunk);
+//   warp 16    TMA producer: weight tile(s) and the activation tile (f32, or
+//              bf16 with the 128-byte swizzle for larger token tiles) per stage,
+//              into a load ring as deep as shared memory allows;
 //   warp 17    allocates TMEM, and one lane issues tcgen05.mma (K = 16 each)
-//              and tcgen05.commit to release each stage.
+//              and tcgen05.commit to release each stage's A slot and load slot.
+// A per-CTA timeline (%globaltimer stamps per stage) showed why the groups: with
+// one group of 16 warps every stage cost ~0.5 us of dequantisation latency (the
+// tiles were already in shared memory, the tensor core idle), at M = 16 and at
+// M = 512 alike.
 // Every mbarrier wait is bounded by a wall-clock limit; a wait that runs out
 // counts a pipeline timeout (qdq_pipeline_timeouts) and the CTA winds down
 // instead of hanging.
@@ -58,10 +65,11 @@ __device__ unsigned int g_pipeline_timeouts = 0;
 namespace {
 
 constexpr int BM = 128;  // weight rows per tile (MMA M)
-constexpr int BK = 64;   // K per stage (128 bytes of bf16: one swizzle span)
-constexpr int kDequantWarps = 16;  // 4 per SM sub-partition: hides ALU latency
+constexpr int BK = 64;   // K per sub-block (128 bytes of bf16: one swizzle span); a stage holds KB sub-blocks
+constexpr int kDequantWarps = 16;  // two groups of 8, taking alternate stages
+constexpr int kGroupThreads = 32 * kDequantWarps / 2;
 constexpr int kThreads = 32 * (kDequantWarps + 2);
-constexpr uint32_t kATileBytes = BM * BK * 2;  // bf16 weight tile
+constexpr uint32_t kATileBytes = BM * BK * 2;  // bf16 weight tile of one sub-block
 enum WFmt { kWQ8 = 0, kWQ4 = 1 };
 
 // ---- TMA ----------------------------------------------------------------------
@@ -72,16 +80,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, in
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
-
-// L2 prefetch of one TMA tile (no shared memory, no completion): issued well ahead
-// of the tile's load, so that many more weight rows are in flight from HBM than
-// the shared-memory ring alone could hold.
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *tm, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tm)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-constexpr int kPrefetchStages = 16;  // how far ahead of the loads the weight tiles are prefetched into L2
 
 // ---- tcgen05 --------------------------------------------------------------------
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -139,22 +137,29 @@ constexpr uint32_t round1k(uint32_t v) { return (v + 1023u) & ~1023u; }
 // Two rings in shared memory, every tile on a 1024-byte boundary (the 128-byte
 // swizzle atom):
 //   load ring, kSL slots, filled by TMA:  [ NA weight tiles as stored | X tile ]
-//     (X tile: the f32 activations, N x 64, when kXF; else the bf16 B tile);
+//     (X tile: the f32 activations, N x 64 KB, when kXF; else the bf16 B tile);
 //   A ring, kSA slots, filled by the dequantising warps:  [ NA bf16 A tiles |
-//     the bf16 B tile when kXF ].
-// The load ring is as deep as shared memory allows (up to 16 slots), so that
-// many weight tiles are in flight per SM; the A ring only needs to keep the
-// tensor core fed.  kXF (token tiles of 64 or fewer): X arrives as f32 and is
-// rounded to bf16 in the kernel, so no conversion kernel runs before it.
-template <int FMT, int N, int NA>
+//     the bf16 B tile when kXF ]  (each A / B tile is KB sub-tiles of 64 K).
+// The load ring is as deep as shared memory allows (up to 16 slots); the A ring
+// only needs to keep the tensor core fed.  kXF (token tiles of 64 or fewer): X
+// arrives as f32 and is rounded to bf16 in the kernel, so no conversion kernel
+// runs before it.  KB = 2 (token tiles of 64 or fewer, n_in % 128 == 0): 128 K
+// per stage, which halves the per-stage barrier and MMA-issue overhead that
+// bounds the small-token pipeline.
+template <int FMT, int N, int NA, int KB>
 struct GemmCfg {
   static constexpr bool kXF = N <= 64;
-  static constexpr uint32_t kQTileBytes = FMT == kWQ8 ? BM * BK : BM * BK / 2;
-  static constexpr uint32_t kBTileBytes = uint32_t(N) * 128;
-  static constexpr uint32_t kXTileBytes = kXF ? uint32_t(N) * BK * 4 : kBTileBytes;
+  static_assert(KB == 1 || kXF, "two sub-blocks per stage only with the in-kernel X conversion");
+  static constexpr uint32_t kQRowBytes = uint32_t(FMT == kWQ8 ? BK : BK / 2) * KB;  // a weight row's bytes per stage
+  static constexpr uint32_t kQTileBytes = BM * kQRowBytes;
+  static constexpr uint32_t kBSub = uint32_t(N) * 128;  // bf16 B tile of one sub-block
+  static constexpr uint32_t kBTileBytes = KB * kBSub;
+  static constexpr uint32_t kXTileBytes = kXF ? uint32_t(N) * BK * 4 * KB : kBTileBytes;
+  static constexpr uint32_t kATile = KB * kATileBytes;
   static constexpr uint32_t kLoadSlot = round1k(NA * kQTileBytes + kXTileBytes);
-  static constexpr uint32_t kASlot = round1k(NA * kATileBytes + (kXF ? kBTileBytes : 0u));
-  static constexpr int kSA = (NA == 1 && N <= 32) ? 3 : 2;
+  static constexpr uint32_t kASlot = round1k(NA * kATile + (kXF ? kBTileBytes : 0u));
+  // the two dequantising groups and the tensor core each hold a slot (two when they are large)
+  static constexpr int kSA = kASlot > 40u * 1024u ? 2 : 3;
   static constexpr int kFit = int((227u * 1024u - 2048u - uint32_t(kSA) * kASlot) / kLoadSlot);
   static constexpr int kSL = kFit > 16 ? 16 : kFit;
   static constexpr uint32_t kCols = uint32_t(NA * N);
@@ -170,7 +175,7 @@ struct GemmArgs {
   float *partials;      // [split][NA][M][n_out] when split > 1
   int *tickets;         // one per (row tile, token tile), zero on entry
   int n_out, n_in, M;
-  int kb_per_split, split;
+  int st_per_split, split;  // K stages per split, splits
 };
 
 // One Q4_K sub-block's (d*sc_j, dmin*m_j) from a 16-byte header record.
@@ -191,11 +196,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float2 v) {
   return *reinterpret_cast<const uint32_t *>(&p);
 }
 
-template <int FMT, int N, int NA>
+template <int FMT, int N, int NA, int KB>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_q0, const __grid_constant__ CUtensorMap tm_q1,
                    const __grid_constant__ CUtensorMap tm_x, const GemmArgs g, const Magic mg_param) {
-  using C = GemmCfg<FMT, N, NA>;
+  using C = GemmCfg<FMT, N, NA, KB>;
   const Magic mg = lane_magic(mg_param);
   constexpr int SL = C::kSL, SA = C::kSA;
   extern __shared__ uint8_t smem_raw[];
@@ -213,24 +218,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   int issued = 0;  // TMA stages the producer issued (drained before the CTA exits)
   const int tile_n = blockIdx.x, tile_m = blockIdx.y;
   const int n_in = g.n_in, n_out = g.n_out, M = g.M;
-  const int nkb = n_in / BK;
-  const int kb0 = blockIdx.z * g.kb_per_split;
-  const int kb1 = min(kb0 + g.kb_per_split, nkb);
+  const int nst = n_in / (BK * KB);  // K stages of the whole row
+  const int kb0 = blockIdx.z * g.st_per_split;  // this split's first stage
+  const int kb1 = min(kb0 + g.st_per_split, nst);
   const int nk = kb1 - kb0;
   auto qtile = [&](int s, int a) { return smem + s * C::kLoadSlot + a * C::kQTileBytes; };
   auto xtile = [&](int s) { return smem + s * C::kLoadSlot + NA * C::kQTileBytes; };
-  auto atile = [&](int j, int a) { return aring + j * C::kASlot + a * kATileBytes; };
+  auto atile = [&](int j, int a) { return aring + j * C::kASlot + a * C::kATile; };
   // the MMA's B operand of stage i: in the A slot (converted here) or the load slot (TMA)
-  auto btile = [&](int i) { return C::kXF ? aring + (i % SA) * C::kASlot + NA * kATileBytes : xtile(i % SL); };
-  constexpr int kQBox = FMT == kWQ8 ? BK : BK / 2;  // inner TMA coordinate step of a weight tile per stage
+  auto btile = [&](int i) { return C::kXF ? aring + (i % SA) * C::kASlot + NA * C::kATile : xtile(i % SL); };
+  constexpr int kQBox = int(C::kQRowBytes);  // inner TMA coordinate step of a weight tile per stage
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < SL; ++i) {
       mbar_init(&lfull[i], 1);
-      mbar_init(&lempty[i], 1);
+      // kXF: only the dequantising group reads a load slot (one arrival per warp);
+      // else the tensor core reads its B tile (one commit)
+      mbar_init(&lempty[i], C::kXF ? kDequantWarps / 2 : 1);
     }
     for (int j = 0; j < SA; ++j) {
-      mbar_init(&aready[j], kDequantWarps * 32);
+      mbar_init(&aready[j], kDequantWarps / 2);  // one arrival per warp of the stage's group
       mbar_init(&aempty[j], 1);
     }
     mbar_init(accum, 1);
@@ -254,17 +261,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kTx = NA * C::kQTileBytes + C::kXTileBytes;
       const int npre = nk < SL ? nk : SL;
       // weights do not depend on the previous kernel: start them before the wait
-      for (int i = npre; i < nk && i < npre + kPrefetchStages; ++i) {
-        tma_prefetch_2d(&tm_q0, (kb0 + i) * kQBox, tile_n * BM);
-        if (NA == 2) tma_prefetch_2d(&tm_q1, (kb0 + i) * kQBox, tile_n * BM);
-      }
       for (int i = 0; i < npre; ++i) {
         mbar_arrive_expect_tx(&lfull[i], kTx);
         tma_load_2d(qtile(i, 0), &tm_q0, (kb0 + i) * kQBox, tile_n * BM, &lfull[i]);
         if (NA == 2) tma_load_2d(qtile(i, 1), &tm_q1, (kb0 + i) * kQBox, tile_n * BM, &lfull[i]);
       }
       pdl_wait();
-      for (int i = 0; i < npre; ++i) tma_load_2d(xtile(i), &tm_x, (kb0 + i) * BK, tile_m * N, &lfull[i]);
+      for (int i = 0; i < npre; ++i) tma_load_2d(xtile(i), &tm_x, (kb0 + i) * BK * KB, tile_m * N, &lfull[i]);
       issued = npre;
       for (int i = npre; i < nk; ++i) {
         const int s = i % SL;
@@ -276,12 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&lfull[s], kTx);
         tma_load_2d(qtile(s, 0), &tm_q0, (kb0 + i) * kQBox, tile_n * BM, &lfull[s]);
         if (NA == 2) tma_load_2d(qtile(s, 1), &tm_q1, (kb0 + i) * kQBox, tile_n * BM, &lfull[s]);
-        tma_load_2d(xtile(s), &tm_x, (kb0 + i) * BK, tile_m * N, &lfull[s]);
+        tma_load_2d(xtile(s), &tm_x, (kb0 + i) * BK * KB, tile_m * N, &lfull[s]);
         issued = i + 1;
-        if (i + kPrefetchStages < nk) {
-          tma_prefetch_2d(&tm_q0, (kb0 + i + kPrefetchStages) * kQBox, tile_n * BM);
-          if (NA == 2) tma_prefetch_2d(&tm_q1, (kb0 + i + kPrefetchStages) * kQBox, tile_n * BM);
-        }
       }
     } else {
       pdl_wait();
@@ -293,7 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(BM, N);
       for (int i = 0; i < nk; ++i) {
         const int s = i % SL, j = i % SA;
-        if (!mbar_wait(&aready[j], (i / SA) & 1) || !mbar_wait(&lfull[s], (i / SL) & 1)) {
+        // kXF: A and B are both written by the dequantising group (aready covers them)
+        if (!mbar_wait(&aready[j], (i / SA) & 1) || (!C::kXF && !mbar_wait(&lfull[s], (i / SL) & 1))) {
           s_abort = 1;
           break;
         }
@@ -303,20 +303,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int a = 0; a < NA; ++a) {
           const uint32_t a_base = smem_u32(atile(j, a));
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            umma_bf16(tmem + uint32_t(a * N), desc_kmajor_sw128(a_base + 32 * k), desc_kmajor_sw128(b_base + 32 * k),
-                      idesc, (i | k) != 0);
+          for (int kb = 0; kb < KB; ++kb)
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+              umma_bf16(tmem + uint32_t(a * N), desc_kmajor_sw128(a_base + kb * kATileBytes + 32 * k),
+                        desc_kmajor_sw128(b_base + kb * C::kBSub + 32 * k), idesc, (i | kb | k) != 0);
         }
         umma_commit(&aempty[j]);  // the A slot (and the B tile in it) is free once these MMAs are done
-        umma_commit(&lempty[s]);  // so is the load slot
+        if (!C::kXF) umma_commit(&lempty[s]);  // so is the load slot (its B tile)
       }
       umma_commit(accum);
     }
   } else {
     // ---------------- dequantise, then epilogue ----------------
-    // The weights do not depend on the previous kernel, so dequantisation starts
-    // at once; only the epilogue (which writes Y) waits for it.
+    // Two groups of 8 warps take alternate stages (group g: stages g, g + 2, ...), so
+    // that one group's dequantisation overlaps the other's: a stage's work is a short
+    // dependent chain (shared-memory load, conversion, store, proxy fence), and one
+    // group alone leaves most issue slots empty.  The weights do not depend on the
+    // previous kernel, so dequantisation starts at once; only the epilogue (which
+    // writes Y) waits for it.
     bool ok = true;
+    const int grp = warp >> 3;                        // dequantising group
+    const int gt = threadIdx.x & (kGroupThreads - 1);  // thread within the group
     // stage i may overwrite A slot i % SA once the MMAs of stage i - SA are done
     auto wait_slots = [&](int i) {
       if (!mbar_wait(&lfull[i % SL], (i / SL) & 1)) return false;
@@ -327,81 +335,112 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto convert_x = [&](int i) {
       if constexpr (C::kXF) {
         const float *xs = reinterpret_cast<const float *>(xtile(i % SL));
-        uint8_t *bt = btile(i);
-        for (int t = threadIdx.x; t < N * 8; t += kDequantWarps * 32) {
-          const int r = t >> 3, c = t & 7;
-          const float4 v0 = *reinterpret_cast<const float4 *>(xs + r * BK + 8 * c);
-          const float4 v1 = *reinterpret_cast<const float4 *>(xs + r * BK + 8 * c + 4);
+        for (int t = gt; t < N * 8 * KB; t += kGroupThreads) {
+          const int kb = t / (N * 8), r = (t >> 3) % N, c = t & 7;
+          uint8_t *bt = btile(i) + kb * C::kBSub;
+          const float4 v0 = *reinterpret_cast<const float4 *>(xs + r * BK * KB + kb * BK + 8 * c);
+          const float4 v1 = *reinterpret_cast<const float4 *>(xs + r * BK * KB + kb * BK + 8 * c + 4);
           *reinterpret_cast<uint4 *>(bt + r * 128 + ((c ^ (r & 7)) << 4)) =
               make_uint4(pack_bf16x2(f2(v0.x, v0.y)), pack_bf16x2(f2(v0.z, v0.w)), pack_bf16x2(f2(v1.x, v1.y)),
                          pack_bf16x2(f2(v1.z, v1.w)));
         }
       }
     };
+    // the end of a stage: every write of the warp fenced for the tensor core, then one arrival
+    auto finish_stage = [&](int i) {
+      convert_x(i);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&aready[i % SA]);
+        if (C::kXF) mbar_arrive(&lempty[i % SL]);  // the warp has read its part of the load slot
+      }
+    };
     if constexpr (FMT == kWQ8) {
-      const int row = threadIdx.x & (BM - 1);  // weight row within the tile
-      const int part = threadIdx.x >> 7;       // which 16 of the row's 64 quants
+      // thread: weight row gt % 128, block half = gt / 128 of each 64-K sub-block (32 quants,
+      // one block scale)
+      const int row = gt & (BM - 1);
+      const int half = gt >> 7;
       const int grow = tile_n * BM + row;
-      const uint32_t *d32[NA];
+      const unsigned short *d16[NA];
 #pragma unroll
       for (int a = 0; a < NA; ++a)
-        d32[a] = reinterpret_cast<const uint32_t *>(g.W[a] + int64_t(n_out) * n_in) + int64_t(grow) * (n_in / BK);
-      const int qsw = (row >> 1) & 3;  // 64-byte swizzle of the TMA-written int8 tile
-      // the row's two block scales per stage (an fp16 pair), fetched four stages ahead
-      uint32_t dqa[4][NA];
+        d16[a] = reinterpret_cast<const unsigned short *>(g.W[a] + int64_t(n_out) * n_in) + int64_t(grow) * (n_in / 32) +
+                 half;
+      // 16-byte chunk c of the row as the TMA swizzle stored it (64-byte rows: 64-byte
+      // swizzle; 128-byte rows: 128-byte swizzle)
+      auto qchunk = [&](int c) { return KB == 1 ? c ^ ((row >> 1) & 3) : c ^ (row & 7); };
+      // block scales fetched four of this group's stages ahead into slot u, which the
+      // stage four later reads (unrolled by 4: no register copy waits for a load);
+      // sub-block kb of stage i is 64-K block (kb0 + i) * KB + kb, blocks 2 x + half
+      auto scale_at = [&](int a, int i, int kb) { return __ldg(d16[a] + 2 * ((kb0 + i) * KB + kb)); };
+      unsigned short dqa[4][NA][KB];
 #pragma unroll
-      for (int t = 0; t < 4; ++t)
+      for (int u = 0; u < 4; ++u)
 #pragma unroll
-        for (int a = 0; a < NA; ++a) dqa[t][a] = t < nk ? __ldg(d32[a] + kb0 + t) : 0u;
-      for (int i = 0; i < nk; ++i) {
-        const int s = i % SL, j = i % SA;
-        uint32_t dq[NA];
+        for (int a = 0; a < NA; ++a)
 #pragma unroll
-        for (int a = 0; a < NA; ++a) {
-          dq[a] = dqa[0][a];
-          dqa[0][a] = dqa[1][a];
-          dqa[1][a] = dqa[2][a];
-          dqa[2][a] = dqa[3][a];
-          dqa[3][a] = i + 4 < nk ? __ldg(d32[a] + kb0 + i + 4) : 0u;
-        }
-        if (!wait_slots(i)) {
-          s_abort = 1;
-          ok = false;
-          break;
-        }
+          for (int kb = 0; kb < KB; ++kb) dqa[u][a][kb] = grp + 2 * u < nk ? scale_at(a, grp + 2 * u, kb) : 0;
+      for (int i0 = grp; i0 < nk && ok; i0 += 8)
 #pragma unroll
-        for (int a = 0; a < NA; ++a) {
-          const uint8_t *qt = qtile(s, a);
-          uint8_t *at = atile(j, a);
-          const __half2 dh = *reinterpret_cast<const __half2 *>(&dq[a]);
-          const float dsc = part < 2 ? __low2float(dh) : __high2float(dh);  // block scale of K 32*(part/2)..
-          const float2 dpair = f2(dsc, dsc);
-          const uint4 qv = *reinterpret_cast<const uint4 *>(qt + row * 64 + ((part ^ qsw) << 4));
-          const uint32_t words[4] = {qv.x, qv.y, qv.z, qv.w};
-          uint32_t packed[8];
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + 2 * u;
+          if (i >= nk) break;
+          const int s = i % SL, j = i % SA;
+          float dsc[NA][KB];
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            float2 q01, q23;
-            s8x4_to_f2(words[w], mg, q01, q23);
-            packed[2 * w] = pack_bf16x2(__fmul2_rn(q01, dpair));  // d*q exact in f32, rounded once
-            packed[2 * w + 1] = pack_bf16x2(__fmul2_rn(q23, dpair));
+          for (int a = 0; a < NA; ++a)
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb) {
+              dsc[a][kb] = __half2float(__ushort_as_half(dqa[u][a][kb]));
+              dqa[u][a][kb] = i + 8 < nk ? scale_at(a, i + 8, kb) : 0;
+            }
+          // warp-uniform: the warp's lanes arrive together (one arrival per warp)
+          if (!__all_sync(0xffffffffu, wait_slots(i))) {
+            s_abort = 1;
+            ok = false;
+            break;
           }
-          // 16 quants -> two 16-byte bf16 chunks (K 16p..16p+7 and 16p+8..16p+15)
-          *reinterpret_cast<uint4 *>(at + row * 128 + (((2 * part) ^ (row & 7)) << 4)) =
-              make_uint4(packed[0], packed[1], packed[2], packed[3]);
-          *reinterpret_cast<uint4 *>(at + row * 128 + (((2 * part + 1) ^ (row & 7)) << 4)) =
-              make_uint4(packed[4], packed[5], packed[6], packed[7]);
+#pragma unroll
+          for (int a = 0; a < NA; ++a)
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb) {
+              const uint8_t *qt = qtile(s, a);
+              uint8_t *at = atile(j, a) + kb * kATileBytes;
+              const float2 dpair = f2(dsc[a][kb], dsc[a][kb]);
+#pragma unroll
+              for (int pp = 0; pp < 2; ++pp) {
+                const int part = 2 * half + pp;  // 16 quants: K 16 part .. 16 part + 15 of the sub-block
+                const uint4 qv =
+                    *reinterpret_cast<const uint4 *>(qt + row * C::kQRowBytes + (qchunk(4 * kb + part) << 4));
+                const uint32_t words[4] = {qv.x, qv.y, qv.z, qv.w};
+                uint32_t packed[8];
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                  float2 q01, q23;
+                  s8x4_to_f2(words[w], mg, q01, q23);
+                  packed[2 * w] = pack_bf16x2(__fmul2_rn(q01, dpair));  // d*q exact in f32, rounded once
+                  packed[2 * w + 1] = pack_bf16x2(__fmul2_rn(q23, dpair));
+                }
+                // two 16-byte bf16 chunks (K 16p..16p+7 and 16p+8..16p+15)
+                *reinterpret_cast<uint4 *>(at + row * 128 + (((2 * part) ^ (row & 7)) << 4)) =
+                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                *reinterpret_cast<uint4 *>(at + row * 128 + (((2 * part + 1) ^ (row & 7)) << 4)) =
+                    make_uint4(packed[4], packed[5], packed[6], packed[7]);
+              }
+            }
+          finish_stage(i);
         }
-        convert_x(i);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(&aready[j]);
-      }
     } else {
-      // Q4_K: warp w takes rows 8w..8w+7, four threads per row, 16 nibbles (8 bytes) each:
-      // a warp reads 256 contiguous bytes of the dense tile
-      const int row = warp * 8 + (lane >> 2);
-      const int part = lane & 3;
+      // Q4_K: warp w of the group takes rows 16w..16w+15, two threads per row, one
+      // 32-weight sub-block (16 bytes) of each 64-K block: a warp reads 512 bytes of
+      // the tile per 64-K block
+      const int row = (warp & 7) * 16 + (lane >> 1);
+      const int part = lane & 1;
       const int grow = tile_n * BM + row;
+      // 16-byte chunk c of the row as stored (32-byte rows: no swizzle; 64-byte rows:
+      // 64-byte swizzle)
+      auto qchunk = [&](int c) { return KB == 1 ? c : c ^ ((row >> 1) & 3); };
       const uint4 *hdr[NA];  // the row's superblock headers
 #pragma unroll
       for (int a = 0; a < NA; ++a)
@@ -409,16 +448,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the header of the current superblock, and of the next one fetched ahead
       const int nsb = n_in / 256;
       uint4 hcur[NA], hnext[NA];
-      int cur_sb = kb0 >> 2;
+      int cur_sb = ((kb0 + grp) * KB) >> 2;
 #pragma unroll
       for (int a = 0; a < NA; ++a) {
         hcur[a] = __ldg(hdr[a] + cur_sb);
         hnext[a] = cur_sb + 1 < nsb ? __ldg(hdr[a] + cur_sb + 1) : hcur[a];
       }
-      for (int i = 0; i < nk; ++i) {
+      for (int i = grp; i < nk; i += 2) {
         const int s = i % SL, jj = i % SA;
-        const int kb = kb0 + i;
-        if ((kb >> 2) != cur_sb) {  // entering the next superblock
+        const int k64 = (kb0 + i) * KB;  // the stage's first 64-K block (a stage stays in one superblock)
+        if ((k64 >> 2) != cur_sb) {      // entering the next superblock
           ++cur_sb;
 #pragma unroll
           for (int a = 0; a < NA; ++a) {
@@ -426,36 +465,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             hnext[a] = cur_sb + 1 < nsb ? __ldg(hdr[a] + cur_sb + 1) : hcur[a];
           }
         }
-        const int j = 2 * (kb & 3) + (part >> 1);  // sub-block of these 16 weights in the superblock
-        float2 dm[NA];                             // (d*sc_j, dmin*m_j)
+        float2 dm[NA][KB];  // (d*sc_j, dmin*m_j) of sub-block j = 2 (64-K block % 4) + part
 #pragma unroll
-        for (int a = 0; a < NA; ++a) dm[a] = q4k_header_scale(hcur[a], j);
-        if (!wait_slots(i)) {
+        for (int a = 0; a < NA; ++a)
+#pragma unroll
+          for (int kb = 0; kb < KB; ++kb) dm[a][kb] = q4k_header_scale(hcur[a], 2 * ((k64 + kb) & 3) + part);
+        if (!__all_sync(0xffffffffu, wait_slots(i))) {
           s_abort = 1;
           ok = false;
           break;
         }
 #pragma unroll
-        for (int a = 0; a < NA; ++a) {
-          const uint2 qv = *reinterpret_cast<const uint2 *>(qtile(s, a) + row * 32 + part * 8);
-          uint8_t *at = atile(jj, a);
-          const float2 D = f2(dm[a].x, dm[a].x), Dm = f2(-dm[a].y, -dm[a].y);
-          uint32_t packed[8];
+        for (int a = 0; a < NA; ++a)
 #pragma unroll
-          for (int w = 0; w < 2; ++w) {
-            float2 q[4];
-            u4x8_to_f2(w == 0 ? qv.x : qv.y, mg, q);
+          for (int kb = 0; kb < KB; ++kb) {
+            const uint4 qv =
+                *reinterpret_cast<const uint4 *>(qtile(s, a) + row * C::kQRowBytes + (qchunk(2 * kb + part) << 4));
+            uint8_t *at = atile(jj, a) + kb * kATileBytes;
+            const float2 D = f2(dm[a][kb].x, dm[a][kb].x), Dm = f2(-dm[a][kb].y, -dm[a][kb].y);
+            const uint32_t words[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-            for (int p = 0; p < 4; ++p) packed[4 * w + p] = pack_bf16x2(__ffma2_rn(D, q[p], Dm));  // RN(D q - Dm)
+            for (int h = 0; h < 2; ++h) {  // 16 weights -> two 16-byte chunks of the A row
+              uint32_t packed[8];
+#pragma unroll
+              for (int w = 0; w < 2; ++w) {
+                float2 q[4];
+                u4x8_to_f2(words[2 * h + w], mg, q);
+#pragma unroll
+                for (int p = 0; p < 4; ++p) packed[4 * w + p] = pack_bf16x2(__ffma2_rn(D, q[p], Dm));  // RN(D q - Dm)
+              }
+              const int c = 4 * part + 2 * h;  // 16-byte chunk of K 8c .. 8c + 15
+              *reinterpret_cast<uint4 *>(at + row * 128 + ((c ^ (row & 7)) << 4)) =
+                  make_uint4(packed[0], packed[1], packed[2], packed[3]);
+              *reinterpret_cast<uint4 *>(at + row * 128 + (((c + 1) ^ (row & 7)) << 4)) =
+                  make_uint4(packed[4], packed[5], packed[6], packed[7]);
+            }
           }
-          *reinterpret_cast<uint4 *>(at + row * 128 + (((2 * part) ^ (row & 7)) << 4)) =
-              make_uint4(packed[0], packed[1], packed[2], packed[3]);
-          *reinterpret_cast<uint4 *>(at + row * 128 + (((2 * part + 1) ^ (row & 7)) << 4)) =
-              make_uint4(packed[4], packed[5], packed[6], packed[7]);
-        }
-        convert_x(i);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(&aready[jj]);
+        finish_stage(i);
       }
     }
     pdl_wait();
@@ -508,34 +554,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(1, 32 * kDequantWarps);
         if (s_last) {
           __threadfence();
-          // the tile's partials, added in split order: every load of a 16-column chunk is
-          // issued before any is used, so the reads overlap instead of queueing
+          // the tile's partials, added in split order, by all 16 warps: thread t takes
+          // weight row t % 128 and every fourth token from t / 128, 8 tokens at a time; the
+          // loads of two splits are issued before either is added, so the reads overlap
+          const int rrow = tile_n * BM + (threadIdx.x & (BM - 1));
+          const int tq = threadIdx.x >> 7;
+          constexpr int kTok = N / 4;                   // tokens per thread
+          constexpr int kChunk = kTok < 8 ? kTok : 8;  // tokens per pass
 #pragma unroll 1
-          for (int c0 = (warp >> 2) * 16; c0 < N; c0 += 16 * (kDequantWarps / 4)) {
-#pragma unroll 1
-            for (int h = 0; h < 16; h += 8) {  // 8 columns at a time
-              float acc[NA][8];
+          for (int t0 = 0; t0 < kTok; t0 += kChunk) {
+            float acc[NA][kChunk];
+#pragma unroll
+            for (int a = 0; a < NA; ++a)
+#pragma unroll
+              for (int jj = 0; jj < kChunk; ++jj) acc[a][jj] = 0.f;
+            for (int zz = 0; zz < g.split; zz += 2) {
+              float v0[NA][kChunk], v1[NA][kChunk];
 #pragma unroll
               for (int a = 0; a < NA; ++a)
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) acc[a][jj] = 0.f;
-              for (int zz = 0; zz < g.split; ++zz) {
-#pragma unroll
-                for (int a = 0; a < NA; ++a)
-#pragma unroll
-                  for (int jj = 0; jj < 8; ++jj) {
-                    const int m = m0 + c0 + h + jj;
-                    if (m < M) acc[a][jj] += __ldcg(&g.partials[((int64_t(zz) * NA + a) * M + m) * n_out + erow]);
-                  }
-              }
-#pragma unroll
-              for (int jj = 0; jj < 8; ++jj) {
-                const int m = m0 + c0 + h + jj;
-                if (m < M) {
-                  float v = acc[0][jj];
-                  if (NA == 2) v = v / (1.0f + expf(-v)) * acc[NA - 1][jj];
-                  g.Y[int64_t(m) * n_out + erow] = v;
+                for (int jj = 0; jj < kChunk; ++jj) {
+                  const int m = m0 + tq + 4 * (t0 + jj);
+                  v0[a][jj] = m < M ? __ldcg(&g.partials[((int64_t(zz) * NA + a) * M + m) * n_out + rrow]) : 0.f;
+                  v1[a][jj] = m < M && zz + 1 < g.split
+                                  ? __ldcg(&g.partials[((int64_t(zz + 1) * NA + a) * M + m) * n_out + rrow])
+                                  : 0.f;
                 }
+#pragma unroll
+              for (int a = 0; a < NA; ++a)
+#pragma unroll
+                for (int jj = 0; jj < kChunk; ++jj) {
+                  acc[a][jj] += v0[a][jj];
+                  if (zz + 1 < g.split) acc[a][jj] += v1[a][jj];
+                }
+            }
+#pragma unroll
+            for (int jj = 0; jj < kChunk; ++jj) {
+              const int m = m0 + tq + 4 * (t0 + jj);
+              if (m < M && QDQ_GUARD(rrow < n_out, QDQ_CHECK_OUT)) {
+                float v = acc[0][jj];
+                if (NA == 2) v = v / (1.0f + expf(-v)) * acc[NA - 1][jj];
+                g.Y[int64_t(m) * n_out + rrow] = v;
               }
             }
           }
@@ -617,39 +676,43 @@ int token_tile(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <=
 constexpr size_t kTicketBytes = 65536;
 constexpr int kMaxTiles = int(kTicketBytes / sizeof(int));
 struct GemmPlan {
-  int N, ntile_n, ntile_m, nkb, split, kb_per;
+  int N, KB, ntile_n, ntile_m, nst, split, st_per;
   size_t xb_bytes, part_bytes;
 };
 GemmPlan plan_gemm(int M, int n_out, int n_in, int na, int sm_count) {
   GemmPlan p;
   p.N = token_tile(M);
+  // 64-K sub-blocks per stage: two for token tiles up to 32 (at 64 the larger stage
+  // leaves too few load slots and measured slower)
+  p.KB = p.N <= 32 && n_in % (2 * BK) == 0 ? 2 : 1;
   p.ntile_n = n_out / BM;
   p.ntile_m = (M + p.N - 1) / p.N;
-  p.nkb = n_in / BK;
+  p.nst = n_in / (BK * p.KB);
   const int tiles = p.ntile_n * p.ntile_m;
   int split = sm_count / tiles;
   if (split < 1) split = 1;
-  if (split > p.nkb) split = p.nkb;
-  p.kb_per = (p.nkb + split - 1) / split;
-  p.split = (p.nkb + p.kb_per - 1) / p.kb_per;  // every split gets at least one K block
+  if (split > p.nst) split = p.nst;
+  p.st_per = (p.nst + split - 1) / split;
+  p.split = (p.nst + p.st_per - 1) / p.st_per;  // every split gets at least one stage
   p.xb_bytes = p.N <= 64 ? 0 : (size_t(M) * n_in * 2 + 255) / 256 * 256;
   p.part_bytes = p.split > 1 ? size_t(p.split) * na * M * n_out * 4 : 0;
   return p;
 }
 
-template <int FMT, int N, int NA>
+template <int FMT, int N, int NA, int KB>
 int launch_tile(const uint8_t *const W[2], const float *X, float *Y, void *ws, int n_out, int n_in, int M,
                 const GemmPlan &p, cudaStream_t s, const DeviceInfo &di) {
-  using C = GemmCfg<FMT, N, NA>;
+  using C = GemmCfg<FMT, N, NA, KB>;
   CUtensorMap tm_q[2], tm_x;
   for (int a = 0; a < 2; ++a) {
     const uint8_t *w = W[a < NA ? a : 0];
-    const bool okq = FMT == kWQ8
-                         ? encode_2d(&tm_q[a], CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t *>(w), uint64_t(n_in),
-                                     uint64_t(n_out), uint64_t(n_in), BK, BM, CU_TENSOR_MAP_SWIZZLE_64B)
-                         : encode_2d(&tm_q[a], CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t *>(w),
-                                     uint64_t(n_in / 2), uint64_t(n_out), uint64_t(n_in / 2), BK / 2, BM,
-                                     CU_TENSOR_MAP_SWIZZLE_NONE);
+    // weight tile rows of kQRowBytes (Q8_0: 64 or 128; Q4_K: 32 or 64), swizzled to match
+    const uint64_t row_bytes = FMT == kWQ8 ? uint64_t(n_in) : uint64_t(n_in / 2);
+    const CUtensorMapSwizzle sw = C::kQRowBytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : C::kQRowBytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                        : CU_TENSOR_MAP_SWIZZLE_NONE;
+    const bool okq = encode_2d(&tm_q[a], CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t *>(w), row_bytes,
+                               uint64_t(n_out), row_bytes, C::kQRowBytes, BM, sw);
     if (!okq) return QDQ_ERR_UNSUPPORTED;
   }
 
@@ -663,7 +726,7 @@ int launch_tile(const uint8_t *const W[2], const float *X, float *Y, void *ws, i
   g.n_out = n_out;
   g.n_in = n_in;
   g.M = M;
-  g.kb_per_split = p.kb_per;
+  g.st_per_split = p.st_per;
   g.split = p.split;
   if (p.split > 1 && p.ntile_n * p.ntile_m > kMaxTiles) return QDQ_ERR_UNSUPPORTED;
 
@@ -671,7 +734,7 @@ int launch_tile(const uint8_t *const W[2], const float *X, float *Y, void *ws, i
   if (C::kXF) {
     // X is read as f32 and rounded to bf16 inside the GEMM
     if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, const_cast<float *>(X), uint64_t(n_in), uint64_t(M),
-                   uint64_t(n_in) * 4, BK, N, CU_TENSOR_MAP_SWIZZLE_NONE))
+                   uint64_t(n_in) * 4, BK * KB, N, CU_TENSOR_MAP_SWIZZLE_NONE))
       return QDQ_ERR_UNSUPPORTED;
   } else {
     // conversion of X into the workspace, and zeroing of the split-K tickets
@@ -688,7 +751,7 @@ int launch_tile(const uint8_t *const W[2], const float *X, float *Y, void *ws, i
     if (e != cudaSuccess) return fail_cuda(e);
   }
 
-  auto kern = gemm_tc_kernel<FMT, N, NA>;
+  auto kern = gemm_tc_kernel<FMT, N, NA, KB>;
   e = allow_dynamic_smem(reinterpret_cast<const void *>(kern), int(C::kSmemBytes));  // once per kernel
   if (e != cudaSuccess) return fail_cuda(e);
   e = launch(kern, dim3(p.ntile_n, p.ntile_m, p.split), dim3(kThreads), C::kSmemBytes, s, tm_q[0], tm_q[1], tm_x, g,
@@ -705,12 +768,14 @@ int launch_gemm(const uint8_t *const W[2], const float *X, float *Y, void *ws, i
   e = get_encoder();
   if (e != cudaSuccess) return fail_cuda(e);
   const GemmPlan p = plan_gemm(M, n_out, n_in, NA, di.sm_count);
-  switch (p.N) {
-    case 16: return launch_tile<FMT, 16, NA>(W, X, Y, ws, n_out, n_in, M, p, s, di);
-    case 32: return launch_tile<FMT, 32, NA>(W, X, Y, ws, n_out, n_in, M, p, s, di);
-    case 64: return launch_tile<FMT, 64, NA>(W, X, Y, ws, n_out, n_in, M, p, s, di);
-    case 128: return launch_tile<FMT, 128, NA>(W, X, Y, ws, n_out, n_in, M, p, s, di);
-    default: return launch_tile<FMT, 256, NA>(W, X, Y, ws, n_out, n_in, M, p, s, di);
+  switch (p.N * 2 + p.KB - 1) {
+    case 32: return launch_tile<FMT, 16, NA, 1>(W, X, Y, ws, n_out, n_in, M, p, s, di);
+    case 33: return launch_tile<FMT, 16, NA, 2>(W, X, Y, ws, n_out, n_in, M, p, s, di);
+    case 64: return launch_tile<FMT, 32, NA, 1>(W, X, Y, ws, n_out, n_in, M, p, s, di);
+    case 65: return launch_tile<FMT, 32, NA, 2>(W, X, Y, ws, n_out, n_in, M, p, s, di);
+    case 128: return launch_tile<FMT, 64, NA, 1>(W, X, Y, ws, n_out, n_in, M, p, s, di);
+    case 256: return launch_tile<FMT, 128, NA, 1>(W, X, Y, ws, n_out, n_in, M, p, s, di);
+    default: return launch_tile<FMT, 256, NA, 1>(W, X, Y, ws, n_out, n_in, M, p, s, di);
   }
 }
 
