@@ -249,11 +249,7 @@ def q8_0_logits_topk(W, x, logits, workspace, index, value, n_vocab: int, n_in: 
 
 
 def gemm_batch_workspace_bytes(M: int, n_out: int, n_in: int) -> int:
-    """Workspace bytes of the tensor-core batch GEMMs on the current device.
-
-    Zero-fill the workspace once after allocating it (its split-K counters must start at
-    zero; every call leaves them at zero again).
-    """
+    """Workspace bytes of the tensor-core batch GEMMs on the current device (the bf16 copy of X)."""
     return int(lib().qdq_gemm_batch_workspace_bytes(M, n_out, n_in))
 
 

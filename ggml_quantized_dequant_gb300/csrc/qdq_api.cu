@@ -426,7 +426,8 @@ int check_gemm_batch(const void *W, const void *W2, const float *X, const float 
   if (!aligned(W, 16) || (W2 && !aligned(W2, 16)) || !aligned(X, 16) || !aligned(Y, 16) || !aligned(ws, 256))
     return QDQ_ERR_ALIGN;
   const size_t xb = size_t(M) * n_in * 4, yb = size_t(M) * n_out * 4;
-  const size_t wsb = size_t(M) * n_in * 2;  // at least the bf16 activations (the exact size needs the device)
+  // the workspace bytes the call uses: the bf16 activations above 64 tokens, else none (256 reserved)
+  const size_t wsb = M > 64 ? size_t(M) * n_in * 2 : 256;
   if (overlaps(Y, yb, W, w_bytes) || (W2 && overlaps(Y, yb, W2, w_bytes)) || overlaps(Y, yb, X, xb) ||
       overlaps(Y, yb, ws, wsb) || overlaps(ws, wsb, W, w_bytes) || (W2 && overlaps(ws, wsb, W2, w_bytes)) ||
       overlaps(ws, wsb, X, xb))

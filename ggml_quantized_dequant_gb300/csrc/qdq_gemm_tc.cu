@@ -16,15 +16,17 @@
 // Computation (per output element):  Y[m, r] = sum_k bf16(X[m, k]) * bf16(w[r, k])
 // with f32 accumulation, w the exact f32 dequantised weight (Q8_0: d*q;
 // Q4_K: RN(d*sc*q - dmin*m), one FMA) rounded once to bf16; X is rounded once to
-// bf16 by a small conversion kernel that runs first.
+// bf16 (inside the GEMM for token tiles up to 64, else by a small conversion
+// kernel that runs first).
 //
 // Tiling ("swap AB"): the MMA's M dimension is 128 weight rows (n_out), its N
-// dimension is the token tile (16..256), K steps by 64 per pipeline stage.
-// One CTA = one (128-row, token-tile, K-range) tile; K is split across CTAs
-// when the tile count alone cannot fill the SMs.  Split partial tiles go to a
-// workspace; the CTA that finishes a tile last (an atomic ticket per tile, no
-// waiting) adds the partials in split order and writes Y, so results do not
-// depend on which CTA ran first.
+// dimension is the token tile (16..256), K steps by 64 or 128 per pipeline
+// stage.  One CTA = one (128-row, token-tile, K-range) tile; K is split across
+// the CTAs of a (1, 1, split) thread-block cluster when the tile count alone
+// cannot fill the SMs: each split leaves its partial tile in its own shared
+// memory, and after a cluster barrier split z adds the partials of its share of
+// the tile's tokens in split order through distributed shared memory and
+// writes Y, so results do not depend on which CTA ran first.
 //
 // Warp roles (576 threads):
 //   warps 0-15 dequantise the weight tile(s) into bf16 A tiles in the
@@ -54,6 +56,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "qdq_internal.cuh"
@@ -164,7 +167,9 @@ struct GemmCfg {
   static constexpr int kSL = kFit > 16 ? 16 : kFit;
   static constexpr uint32_t kCols = uint32_t(NA * N);
   static constexpr uint32_t kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
-  static constexpr size_t kSmemBytes = 1024 + size_t(kSL) * kLoadSlot + size_t(kSA) * kASlot + 512;
+  static constexpr size_t kRingBytes = size_t(kSL) * kLoadSlot + size_t(kSA) * kASlot;
+  static constexpr size_t kPBytes = size_t(NA) * N * BM * 4;  // a split's partial tile (f32)
+  static constexpr size_t kSmemBytes = 1024 + kRingBytes + 512;
   static_assert(kSL >= 2, "the load ring needs two slots");
   static_assert(kSmemBytes <= 227u * 1024u, "shared memory");
 };
@@ -172,11 +177,28 @@ struct GemmCfg {
 struct GemmArgs {
   const uint8_t *W[2];  // packed weights (gate and up for the SwiGLU)
   float *Y;
-  float *partials;      // [split][NA][M][n_out] when split > 1
-  int *tickets;         // one per (row tile, token tile), zero on entry
   int n_out, n_in, M;
-  int st_per_split, split;  // K stages per split, splits
+  int st_per_split, split;  // K stages per split, splits (= the cluster size along z)
 };
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_addr(const void *p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+  return a;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_cluster_s32(uint32_t a) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
 
 // One Q4_K sub-block's (d*sc_j, dmin*m_j) from a 16-byte header record.
 __device__ __forceinline__ float2 q4k_header_scale(const uint4 h, int j) {
@@ -212,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *aempty = aready + SA;
   uint64_t *accum = aempty + SA;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
-  __shared__ int s_abort, s_last;
+  __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int issued = 0;  // TMA stages the producer issued (drained before the CTA exits)
@@ -510,7 +532,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
       const int m0 = tile_m * N;
       const int erow = tile_n * BM + (warp & 3) * 32 + lane;  // this thread's output row (TMEM lane)
-      const int tile_id = tile_m * gridDim.x + tile_n;
       if (g.split == 1) {
 #pragma unroll 1
         for (int c0 = (warp >> 2) * 16; c0 < N; c0 += 16 * (kDequantWarps / 4)) {
@@ -531,79 +552,74 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        // split-K: store this split's partial tile, take a ticket; the last of the
-        // tile's splits adds all partials in split order and writes Y
-        const int z = blockIdx.z;
+        // split-K: this split's partial tile goes to its own shared memory (the rings
+        // are idle now: every stage was consumed and every MMA completed), [a][token][row]
+        if constexpr (C::kPBytes <= C::kRingBytes) {  // else the host never splits K
+          float *P = reinterpret_cast<float *>(smem);
+          const int prow = (warp & 3) * 32 + lane;
 #pragma unroll 1
-        for (int c0 = (warp >> 2) * 16; c0 < N; c0 += 16 * (kDequantWarps / 4)) {
-          uint32_t r[NA][16];
+          for (int c0 = (warp >> 2) * 16; c0 < N; c0 += 16 * (kDequantWarps / 4)) {
+            uint32_t r[NA][16];
 #pragma unroll
-          for (int a = 0; a < NA; ++a) tmem_ld16(tmem + lane_base + uint32_t(a * N + c0), r[a]);
-#pragma unroll
-          for (int a = 0; a < NA; ++a)
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              const int m = m0 + c0 + jj;
-              if (m < M && QDQ_GUARD(erow < n_out, QDQ_CHECK_OUT))
-                g.partials[((int64_t(z) * NA + a) * M + m) * n_out + erow] = __uint_as_float(r[a][jj]);
-            }
-        }
-        __threadfence();
-        named_bar_sync(1, 32 * kDequantWarps);
-        if (threadIdx.x == 0) s_last = atomicAdd(&g.tickets[tile_id], 1) == g.split - 1;
-        named_bar_sync(1, 32 * kDequantWarps);
-        if (s_last) {
-          __threadfence();
-          // the tile's partials, added in split order, by all 16 warps: thread t takes
-          // weight row t % 128 and every fourth token from t / 128, 8 tokens at a time; the
-          // loads of two splits are issued before either is added, so the reads overlap
-          const int rrow = tile_n * BM + (threadIdx.x & (BM - 1));
-          const int tq = threadIdx.x >> 7;
-          constexpr int kTok = N / 4;                   // tokens per thread
-          constexpr int kChunk = kTok < 8 ? kTok : 8;  // tokens per pass
-#pragma unroll 1
-          for (int t0 = 0; t0 < kTok; t0 += kChunk) {
-            float acc[NA][kChunk];
+            for (int a = 0; a < NA; ++a) tmem_ld16(tmem + lane_base + uint32_t(a * N + c0), r[a]);
 #pragma unroll
             for (int a = 0; a < NA; ++a)
 #pragma unroll
-              for (int jj = 0; jj < kChunk; ++jj) acc[a][jj] = 0.f;
-            for (int zz = 0; zz < g.split; zz += 2) {
-              float v0[NA][kChunk], v1[NA][kChunk];
-#pragma unroll
-              for (int a = 0; a < NA; ++a)
-#pragma unroll
-                for (int jj = 0; jj < kChunk; ++jj) {
-                  const int m = m0 + tq + 4 * (t0 + jj);
-                  v0[a][jj] = m < M ? __ldcg(&g.partials[((int64_t(zz) * NA + a) * M + m) * n_out + rrow]) : 0.f;
-                  v1[a][jj] = m < M && zz + 1 < g.split
-                                  ? __ldcg(&g.partials[((int64_t(zz + 1) * NA + a) * M + m) * n_out + rrow])
-                                  : 0.f;
-                }
-#pragma unroll
-              for (int a = 0; a < NA; ++a)
-#pragma unroll
-                for (int jj = 0; jj < kChunk; ++jj) {
-                  acc[a][jj] += v0[a][jj];
-                  if (zz + 1 < g.split) acc[a][jj] += v1[a][jj];
-                }
-            }
-#pragma unroll
-            for (int jj = 0; jj < kChunk; ++jj) {
-              const int m = m0 + tq + 4 * (t0 + jj);
-              if (m < M && QDQ_GUARD(rrow < n_out, QDQ_CHECK_OUT)) {
-                float v = acc[0][jj];
-                if (NA == 2) v = v / (1.0f + expf(-v)) * acc[NA - 1][jj];
-                g.Y[int64_t(m) * n_out + rrow] = v;
-              }
-            }
+              for (int jj = 0; jj < 16; ++jj) P[(a * N + c0 + jj) * BM + prow] = __uint_as_float(r[a][jj]);
           }
-          if (threadIdx.x == 0) g.tickets[tile_id] = 0;  // ready for the next call
         }
       }
     } else {
       s_abort = 1;
     }
+  }
+
+  if (g.split > 1) {
+    // The K splits of a tile form one thread-block cluster: after a cluster barrier every
+    // split's partial tile is readable through distributed shared memory, and split z
+    // writes its share of the tile's tokens, adding the partials in split order (so the
+    // result does not depend on which CTA finished first).  Every thread of every CTA
+    // takes both barriers, also after an abort; then no Y is written for the tile.
+    cluster_sync_all();
+    if (warp < kDequantWarps) {
+      const int split = g.split, z = blockIdx.z;
+      bool all_ok = true;
+      for (int r = 0; r < split; ++r) all_ok = all_ok && ld_cluster_s32(cluster_addr(&s_abort, uint32_t(r))) == 0;
+      if (all_ok && C::kPBytes <= C::kRingBytes) {
+        const float *P = reinterpret_cast<const float *>(smem);
+        const int c_lo = N * z / split, c_hi = N * (z + 1) / split;  // this split's tokens of the tile
+        const int prow = threadIdx.x & (BM - 1);
+        const int erow = tile_n * BM + prow;
+        const int m0 = tile_m * N;
+        uint32_t base[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) base[r] = cluster_addr(P, uint32_t(r < split ? r : 0));
+#pragma unroll 1
+        for (int c = c_lo + (threadIdx.x >> 7); c < c_hi; c += kDequantWarps * 32 / BM) {
+          float acc[NA];
+#pragma unroll
+          for (int a = 0; a < NA; ++a) {
+            float v[8];
+            const uint32_t off = uint32_t(((a * N + c) * BM + prow) * 4);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) v[r] = r < split ? ld_cluster_f32(base[r] + off) : 0.f;
+            acc[a] = 0.f;
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+              if (r < split) acc[a] += v[r];
+          }
+          const int m = m0 + c;
+          if (m < M && QDQ_GUARD(erow < n_out, QDQ_CHECK_OUT)) {
+            float y = acc[0];
+            if (NA == 2) y = y / (1.0f + expf(-y)) * acc[NA - 1];
+            g.Y[int64_t(m) * n_out + erow] = y;
+          }
+        }
+      } else if (threadIdx.x == 0) {
+        s_abort = 1;
+      }
+    }
+    cluster_sync_all();  // no CTA leaves while another may still read its shared memory
   }
 
   tc_fence_before();
@@ -626,9 +642,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// X (f32, M x n_in) -> bf16 workspace; zero the split-K tickets.
+// X (f32, M x n_in) -> bf16 workspace.
 __global__ void __launch_bounds__(256) x_to_bf16_kernel(const float4 *__restrict__ X, uint2 *__restrict__ xb,
-                                                        int64_t n4, int *tickets, int n_tickets) {
+                                                        int64_t n4) {
   pdl_launch_dependents();
   pdl_wait();  // the workspace may still be in use by the previous kernel
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
@@ -638,7 +654,6 @@ __global__ void __launch_bounds__(256) x_to_bf16_kernel(const float4 *__restrict
     const __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
     xb[i] = make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
   }
-  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n_tickets; i += stride) tickets[i] = 0;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -669,17 +684,13 @@ bool encode_2d(CUtensorMap *tm, CUtensorMapDataType dt, void *base, uint64_t inn
 // The token tile for M tokens.
 int token_tile(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256; }
 
-// Launch shape and workspace layout of one GEMM call.  The workspace starts
-// with kTicketBytes of split-K tile counters (zero between calls: the last CTA
-// of a tile resets its counter), then the bf16 copy of X (token tiles above
-// 64 only), then the split-K partial tiles.
-constexpr size_t kTicketBytes = 65536;
-constexpr int kMaxTiles = int(kTicketBytes / sizeof(int));
+// Launch shape and workspace of one GEMM call (the workspace holds only the bf16
+// copy of X, for token tiles above 64).
 struct GemmPlan {
-  int N, KB, ntile_n, ntile_m, nst, split, st_per;
-  size_t xb_bytes, part_bytes;
+  int N, KB, ntile_n, ntile_m, nst;
+  size_t xb_bytes;
 };
-GemmPlan plan_gemm(int M, int n_out, int n_in, int na, int sm_count) {
+GemmPlan plan_gemm(int M, int n_out, int n_in) {
   GemmPlan p;
   p.N = token_tile(M);
   // 64-K sub-blocks per stage: two for token tiles up to 32 (at 64 the larger stage
@@ -688,21 +699,73 @@ GemmPlan plan_gemm(int M, int n_out, int n_in, int na, int sm_count) {
   p.ntile_n = n_out / BM;
   p.ntile_m = (M + p.N - 1) / p.N;
   p.nst = n_in / (BK * p.KB);
-  const int tiles = p.ntile_n * p.ntile_m;
-  int split = sm_count / tiles;
-  if (split < 1) split = 1;
-  if (split > p.nst) split = p.nst;
-  p.st_per = (p.nst + split - 1) / split;
-  p.split = (p.nst + p.st_per - 1) / p.st_per;  // every split gets at least one stage
   p.xb_bytes = p.N <= 64 ? 0 : (size_t(M) * n_in * 2 + 255) / 256 * 256;
-  p.part_bytes = p.split > 1 ? size_t(p.split) * na * M * n_out * 4 : 0;
   return p;
+}
+
+// Launch with programmatic dependent launch and a (1, 1, cz) thread-block cluster.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_cluster_z(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, int cz,
+                             Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = opt_pdl() ? 1 : 0;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = unsigned(cz);
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 template <int FMT, int N, int NA, int KB>
 int launch_tile(const uint8_t *const W[2], const float *X, float *Y, void *ws, int n_out, int n_in, int M,
                 const GemmPlan &p, cudaStream_t s, const DeviceInfo &di) {
   using C = GemmCfg<FMT, N, NA, KB>;
+  auto kern = gemm_tc_kernel<FMT, N, NA, KB>;
+  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(kern), int(C::kSmemBytes));
+  if (e != cudaSuccess) return fail_cuda(e);
+
+  // K splits, when the tiles alone cannot fill the SMs: at most 8 (a portable cluster),
+  // and only as many as keep every tile's cluster resident at once (one wave)
+  const int tiles = p.ntile_n * p.ntile_m;
+  int split = di.sm_count / tiles;
+  if (split > 8) split = 8;
+  if (split > p.nst) split = p.nst;
+  if (C::kPBytes > C::kRingBytes) split = 1;
+  static std::atomic<int> max_clusters[9];  // per cluster size, measured once (0: not yet)
+  while (split > 1) {
+    int mc = max_clusters[split].load(std::memory_order_relaxed);
+    if (mc == 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(p.ntile_n, p.ntile_m, split);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = C::kSmemBytes;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 1;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = unsigned(split);
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&mc, kern, &cfg) != cudaSuccess || mc < 1) {
+        (void)cudaGetLastError();
+        mc = -1;
+      }
+      max_clusters[split].store(mc, std::memory_order_relaxed);
+    }
+    if (mc >= tiles) break;
+    --split;
+  }
+  int st_per = (p.nst + split - 1) / split;
+  split = (p.nst + st_per - 1) / st_per;  // every split gets at least one stage
+
   CUtensorMap tm_q[2], tm_x;
   for (int a = 0; a < 2; ++a) {
     const uint8_t *w = W[a < NA ? a : 0];
@@ -716,29 +779,24 @@ int launch_tile(const uint8_t *const W[2], const float *X, float *Y, void *ws, i
     if (!okq) return QDQ_ERR_UNSUPPORTED;
   }
 
-  uint8_t *wsb = static_cast<uint8_t *>(ws);
   GemmArgs g{};
   g.W[0] = W[0];
   g.W[1] = W[NA - 1];
   g.Y = Y;
-  g.tickets = reinterpret_cast<int *>(wsb);
-  g.partials = reinterpret_cast<float *>(wsb + kTicketBytes + p.xb_bytes);
   g.n_out = n_out;
   g.n_in = n_in;
   g.M = M;
-  g.st_per_split = p.st_per;
-  g.split = p.split;
-  if (p.split > 1 && p.ntile_n * p.ntile_m > kMaxTiles) return QDQ_ERR_UNSUPPORTED;
+  g.st_per_split = st_per;
+  g.split = split;
 
-  cudaError_t e;
   if (C::kXF) {
     // X is read as f32 and rounded to bf16 inside the GEMM
     if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, const_cast<float *>(X), uint64_t(n_in), uint64_t(M),
                    uint64_t(n_in) * 4, BK * KB, N, CU_TENSOR_MAP_SWIZZLE_NONE))
       return QDQ_ERR_UNSUPPORTED;
   } else {
-    // conversion of X into the workspace, and zeroing of the split-K tickets
-    uint8_t *xb = wsb + kTicketBytes;
+    // conversion of X into the workspace
+    uint8_t *xb = static_cast<uint8_t *>(ws);
     if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xb, uint64_t(n_in), uint64_t(M), uint64_t(n_in) * 2, BK,
                    N, CU_TENSOR_MAP_SWIZZLE_128B))
       return QDQ_ERR_UNSUPPORTED;
@@ -747,15 +805,14 @@ int launch_tile(const uint8_t *const W[2], const float *X, float *Y, void *ws, i
     if (cgrid > di.sm_count * 8) cgrid = di.sm_count * 8;
     if (cgrid < 1) cgrid = 1;
     e = launch(x_to_bf16_kernel, dim3(cgrid), dim3(256), 0, s, reinterpret_cast<const float4 *>(X),
-               reinterpret_cast<uint2 *>(xb), n4, g.tickets, p.split > 1 ? p.ntile_n * p.ntile_m : 0);
+               reinterpret_cast<uint2 *>(xb), n4);
     if (e != cudaSuccess) return fail_cuda(e);
   }
 
-  auto kern = gemm_tc_kernel<FMT, N, NA, KB>;
-  e = allow_dynamic_smem(reinterpret_cast<const void *>(kern), int(C::kSmemBytes));  // once per kernel
-  if (e != cudaSuccess) return fail_cuda(e);
-  e = launch(kern, dim3(p.ntile_n, p.ntile_m, p.split), dim3(kThreads), C::kSmemBytes, s, tm_q[0], tm_q[1], tm_x, g,
-             make_magic());
+  const dim3 grid(p.ntile_n, p.ntile_m, split);
+  e = split > 1 ? launch_cluster_z(kern, grid, dim3(kThreads), C::kSmemBytes, s, split, tm_q[0], tm_q[1], tm_x, g,
+                                   make_magic())
+                : launch(kern, grid, dim3(kThreads), C::kSmemBytes, s, tm_q[0], tm_q[1], tm_x, g, make_magic());
   return e == cudaSuccess ? QDQ_OK : fail_cuda(e);
 }
 
@@ -767,7 +824,7 @@ int launch_gemm(const uint8_t *const W[2], const float *X, float *Y, void *ws, i
   if (e != cudaSuccess) return fail_cuda(e);
   e = get_encoder();
   if (e != cudaSuccess) return fail_cuda(e);
-  const GemmPlan p = plan_gemm(M, n_out, n_in, NA, di.sm_count);
+  const GemmPlan p = plan_gemm(M, n_out, n_in);
   switch (p.N * 2 + p.KB - 1) {
     case 32: return launch_tile<FMT, 16, NA, 1>(W, X, Y, ws, n_out, n_in, M, p, s, di);
     case 33: return launch_tile<FMT, 16, NA, 2>(W, X, Y, ws, n_out, n_in, M, p, s, di);
@@ -784,8 +841,9 @@ int launch_gemm(const uint8_t *const W[2], const float *X, float *Y, void *ws, i
 size_t gemm_workspace_bytes(int M, int n_out, int n_in, int na) {
   DeviceInfo di;
   if (device_info(&di) != cudaSuccess) return 0;
-  const GemmPlan p = plan_gemm(M, n_out, n_in, na, di.sm_count);
-  return kTicketBytes + p.xb_bytes + p.part_bytes;
+  (void)na;
+  const GemmPlan p = plan_gemm(M, n_out, n_in);
+  return p.xb_bytes > 256 ? p.xb_bytes : 256;
 }
 
 int launch_q8_0_gemm_batch(const void *W, const float *X, float *Y, void *ws, int n_out, int n_in, int M,

@@ -265,12 +265,11 @@ int qdq_q4k_ffn_residual_noalloc(const void *Wg, const void *Wu, const void *Wd,
  * W: packed Q8_0 / Q4_K (16-byte aligned).  X: M x n_in f32 (16-byte aligned).
  * Y: M x n_out f32 (16-byte aligned), must not overlap W, X or workspace.
  * workspace: caller-owned scratch of qdq_gemm_batch_workspace_bytes(M, n_out,
- * n_in) bytes (the size depends on the current device's SM count, 0 when it
- * cannot be queried), 256-byte aligned.  Its first 64 KiB hold one split-K
- * counter per output tile and must be zero when a call starts: zero-fill the
- * workspace once after allocating it; every call leaves the counters at zero
- * again (also across calls of other shapes).  The rest is overwritten: X
- * rounded to bf16 (M > 64 only), the split-K partial tiles.
+ * n_in) bytes (0 when no device can be queried), 256-byte aligned, overwritten
+ * with X rounded to bf16 when M > 64 (unused for M <= 64, where the kernel
+ * rounds X itself).  K is split across the CTAs of a thread-block cluster when
+ * the output tiles alone cannot fill the SMs; the splits' partial tiles are
+ * added in shared memory, in a fixed order.
  * Requires n_in % 64 == 0 (Q4_K: % 256) and n_out % 128 == 0; M >= 1 (tail
  * masked).  Results do not depend on the order in which CTAs run (split-K
  * partials are added in a fixed order).

@@ -300,8 +300,8 @@ def test_gemm_batch_split_k_is_deterministic(cuda_lib, fmt):
 
 
 def test_gemm_batch_workspace_reused_across_shapes(cuda_lib):
-    # one workspace, zero-filled once, serves calls of different shapes and token counts
-    # (different split-K plans): every call must leave its tile counters at zero
+    # one workspace serves calls of different shapes and token counts (different split-K
+    # cluster sizes, in-kernel or separate X conversion) back to back
     import torch
     qdq = cuda_lib
     rng = np.random.default_rng(74)
@@ -317,7 +317,6 @@ def test_gemm_batch_workspace_reused_across_shapes(cuda_lib):
         rows = np.arange(0, M, max(1, M // 8))
         Y_ref, A = oracle.gemm_batch(oracle.q8_0_dequant(wb, n_out, n_in), X[rows])
         assert gemv_excess(_np(Y)[rows], Y_ref, A, rel=4e-3) <= 1.0, (n_out, n_in, M)
-    assert int(ws[:65536].count_nonzero()) == 0
     assert qdq.pipeline_timeouts() == 0
 
 
