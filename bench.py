@@ -60,6 +60,7 @@ KERNEL_SOURCES = {
     "q8_0_gemv": _DL, "q4k_gemv": _DL, "q4k_ffn": _DL, "q4k_qkv": _DL, "q8_0_vocab": _DL, "q6k_gemv": _DL,
     "q8_0_gemm_M16": _TC, "q8_0_gemm_M64": _TC, "q8_0_gemm_M512": _TC,
     "q4k_gemm_M16": _TC, "q4k_gemm_M64": _TC, "q4k_gemm_M512": _TC,
+    "q4k_swiglu_M16": _TC, "q4k_swiglu_M64": _TC, "q4k_swiglu_M512": _TC,
 }
 
 
@@ -524,7 +525,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roofline("hbm", bytes_per_launch, launch_s, peaks["hbm_gbs"], "GB/s",
                              args.traffic if args.traffic is not None else recorded_traffic("q8_0_gemv"),
-                             "gemv_dl_kernel<0, 0> (Q8_0 batch-1 GEMV, f32 arithmetic)", peaks["source"]),
+                             "gemv_dl_kernel<0, 0, 2> (up) + <0, 0, 1> (down): Q8_0 batch-1 GEMV, f32 arithmetic", peaks["source"]),
         "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": N_EMBD * 4, "d2h_bytes_per_step": N_EMBD * 4,
                 "steps": e2e_steps, "ms_per_step": e2e_dt / e2e_steps * 1e3,
                 "path": "Python binding -> C ABI per GEMV (no graph), pinned H2D of x and D2H of y each step"},
@@ -569,7 +570,7 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
     ls, dist = time_calls(torch, timer, lambda t: qdq.q4k_gemv(W2[t], x2, y2, N_FF, N_EMBD, 1), N_LAYERS, iters)
     b = Q4_W_BYTES + (N_EMBD + N_FF) * 4
     rows["q4k_gemv_3072x8192"] = _row(ls, dist, roofline("hbm", b, ls, hbm, "GB/s", recorded_traffic("q4k_gemv"),
-                                                         "gemv_dl_kernel<1, 0>", src))
+                                                         "gemv_dl_kernel<1, 0, 2>", src))
     del W2
 
     # config 3: fused Q4_K FFN block with residual, 28 layers
@@ -586,7 +587,7 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
     b = 3 * Q4_W_BYTES + N_EMBD * 4 + N_FF * 4 * 2 + N_EMBD * 4 * 2
     rows["q4k_ffn_residual_3072x8192"] = _row(
         ls, dist, roofline("hbm", b, ls, hbm, "GB/s", recorded_traffic("q4k_ffn"),
-                           "gemv_dl_kernel<1, 1> + gemv_dl_kernel<1, 2> (2 launches per block)", src),
+                           "gemv_dl_kernel<1, 1, 2> + gemv_dl_kernel<1, 2, 1> (2 launches per block)", src),
         launches_per_block=2)
     # FFN e2e: per block, one pinned H2D of x and one D2H of out, through the public call
     xp = torch.from_numpy(xh).pin_memory()
@@ -625,7 +626,7 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
     rows_q = synth.N_Q + 2 * synth.N_KV
     b = rows_q * (N_EMBD // 256) * 144 + N_EMBD * 4 + rows_q * 4
     rows["q4k_qkv_3072_q3072_kv1024"] = _row(ls, dist, roofline("hbm", b, ls, hbm, "GB/s", recorded_traffic("q4k_qkv"),
-                                                                "gemv_dl_kernel<1, 3>", src))
+                                                                "gemv_dl_kernel<1, 3, 2>", src))
     del LQ
 
     # output projection 3072 -> 128256 (Q8_0, 418 MB: larger than L2) with the on-device argmax / top-40
@@ -640,11 +641,12 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
     bw = synth.N_VOCAB * (N_EMBD // 32) * 34 + N_EMBD * 4 + synth.N_VOCAB * 4
     ls, dist = time_calls(torch, timer, lambda i: qdq.q8_0_gemv(WO, xo, lo, synth.N_VOCAB, N_EMBD, 1), 4, it4)
     rows["q8_0_gemv_3072x128256"] = _row(ls, dist, roofline("hbm", bw, ls, hbm, "GB/s",
-                                                            recorded_traffic("q8_0_vocab"), "gemv_dl_kernel<0, 0>", src))
+                                                            recorded_traffic("q8_0_vocab"), "gemv_dl_kernel<0, 0, 2>", src))
     ls, dist = time_calls(torch, timer, lambda i: qdq.q8_0_logits_argmax(WO, xo, lo, io, vo, synth.N_VOCAB, N_EMBD, 1),
                           4, it4)
     rows["q8_0_logits_argmax_3072x128256"] = _row(
-        ls, dist, roofline("hbm", bw + 8, ls, hbm, "GB/s", None, "gemv_dl_kernel<0, 0> + argmax", src),
+        ls, dist, roofline("hbm", bw + 8, ls, hbm, "GB/s", recorded_traffic("q8_0_vocab"),
+                           "gemv_dl_kernel<0, 0, 2> + argmax_rows_kernel", src),
         launches_per_call=2)
     K = 40
     wsk = torch.empty(qdq.topk_workspace_bytes(synth.N_VOCAB, 1, K), dtype=torch.uint8, device=dev)
@@ -653,7 +655,8 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
     ls, dist = time_calls(torch, timer, lambda i: qdq.q8_0_logits_topk(WO, xo, lo, wsk, ik, vk, synth.N_VOCAB, N_EMBD,
                                                                         1, K), 4, it4)
     rows["q8_0_logits_top40_3072x128256"] = _row(
-        ls, dist, roofline("hbm", bw + 8 * K, ls, hbm, "GB/s", None, "gemv_dl_kernel<0, 0> + top-k", src))
+        ls, dist, roofline("hbm", bw + 8 * K, ls, hbm, "GB/s", recorded_traffic("q8_0_vocab"),
+                           "gemv_dl_kernel<0, 0, 2> + top-k kernels", src))
     ls, dist = time_calls(torch, timer, lambda i: qdq.topk_rows(lo, synth.N_VOCAB, 1, K, wsk, ik, vk), 4, it4)
     rows["top40_128256"] = {"us_per_call": ls * 1e6, "us_dist": dist,
                             "roofline": "n/a (L2-resident logits, latency-bound sort)"}
@@ -668,7 +671,7 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
     ls, dist = time_calls(torch, timer, lambda i: qdq.q6k_gemv(W6, xq6, y6, synth.N_VOCAB, N_EMBD, 1), 4, it4)
     b = synth.N_VOCAB * (N_EMBD // 256) * 210 + N_EMBD * 4 + synth.N_VOCAB * 4
     rows["q6k_gemv_3072x128256"] = _row(ls, dist, roofline("hbm", b, ls, hbm, "GB/s", recorded_traffic("q6k_gemv"),
-                                                           "gemv_dl_kernel<2, 0>", src))
+                                                           "gemv_dl_kernel<2, 0, 2>", src))
     del W6
 
     # config 4 and the Q4_K prefill shapes: tensor-core batch GEMMs, 8 copies of each shape cycled
@@ -694,12 +697,13 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
                 b = wbytes + M * n_in * 4 + M * n_out * 4
                 flops = 2.0 * M * n_out * n_in
                 shape = "3072x8192" if kind == 0 else "8192x3072"
-                kern = "gemm_tc_kernel<%d, %d, 1>" % (0 if fmt == "q8_0" else 1, min(256, max(16, 1 << (M - 1).bit_length())))
+                kern = "gemm_tc_kernel<%d, %d, 1, *>" % (0 if fmt == "q8_0" else 1, min(256, max(16, 1 << (M - 1).bit_length())))
+                # ncu traffic was captured on the 3072 -> 8192 shape; the other shape reports none
+                tr = recorded_traffic("%s_gemm_M%d" % (fmt, M)) if kind == 0 else None
                 if M >= 256:
-                    rl = roofline("tensor", flops, ls, peaks["bf16_tflops"], "TFLOP/s",
-                                  recorded_traffic("%s_gemm_M%d" % (fmt, M)), kern, src)
+                    rl = roofline("tensor", flops, ls, peaks["bf16_tflops"], "TFLOP/s", tr, kern, src)
                 else:
-                    rl = roofline("hbm", b, ls, hbm, "GB/s", recorded_traffic("%s_gemm_M%d" % (fmt, M)), kern, src)
+                    rl = roofline("hbm", b, ls, hbm, "GB/s", tr, kern, src)
                 rows["%s_gemm_%s_M%d" % (fmt, shape, M)] = _row(ls, dist, rl, gbs=b / ls / 1e9,
                                                                tflops=flops / ls / 1e12, bytes_per_call=b,
                                                                flop_per_call=flops)
@@ -714,9 +718,10 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
                         pairs[t][0], pairs[t][1], X, midb, wsp, n_out, n_in, M), len(pairs), max(10, iters // 2))
                     b = 2 * Q4_W_BYTES + M * n_in * 4 + M * n_out * 4
                     flops = 4.0 * M * n_out * n_in
-                    kern = "gemm_tc_kernel<1, %d, 2>" % min(256, max(16, 1 << (M - 1).bit_length()))
-                    rl = (roofline("tensor", flops, ls, peaks["bf16_tflops"], "TFLOP/s", None, kern, src) if M >= 256
-                          else roofline("hbm", b, ls, hbm, "GB/s", None, kern, src))
+                    kern = "gemm_tc_kernel<1, %d, 2, *>" % min(256, max(16, 1 << (M - 1).bit_length()))
+                    tr = recorded_traffic("q4k_swiglu_M%d" % M)
+                    rl = (roofline("tensor", flops, ls, peaks["bf16_tflops"], "TFLOP/s", tr, kern, src) if M >= 256
+                          else roofline("hbm", b, ls, hbm, "GB/s", tr, kern, src))
                     rows["q4k_swiglu_batch_3072x8192_M%d" % M] = _row(ls, dist, rl, gbs=b / ls / 1e9,
                                                                      tflops=flops / ls / 1e12, bytes_per_call=b,
                                                                      flop_per_call=flops)
@@ -792,6 +797,14 @@ def run_profile_case(case: str):
         Y = torch.empty((M, N_FF), device=dev)
         ws = torch.zeros(qdq.gemm_batch_workspace_bytes(M, N_FF, N_EMBD), dtype=torch.uint8, device=dev)
         fn = lambda: f(W, X, Y, ws, N_FF, N_EMBD, M)
+    elif case.startswith("q4k_swiglu_M"):
+        M = int(case.split("_M")[1])
+        Wg = qdq.upload_q4k(synth.q4k_blocks(synth.rng_for(8, 0, 0), N_FF, N_EMBD), N_FF, N_EMBD, device=dev)
+        Wu = qdq.upload_q4k(synth.q4k_blocks(synth.rng_for(8, 0, 1), N_FF, N_EMBD), N_FF, N_EMBD, device=dev)
+        X = torch.from_numpy(synth.activations(synth.rng_for(8, 4, M), M, N_EMBD)).to(dev)
+        mid = torch.empty((M, N_FF), device=dev)
+        ws = torch.zeros(qdq.q4k_swiglu_batch_workspace_bytes(M, N_FF, N_EMBD), dtype=torch.uint8, device=dev)
+        fn = lambda: qdq.q4k_swiglu_batch(Wg, Wu, X, mid, ws, N_FF, N_EMBD, M)
     else:
         raise SystemExit("unknown --profile case %r" % case)
     for _ in range(calls):

@@ -319,12 +319,16 @@ int qdq_noop(cudaStream_t stream);
 
 /* ---- launch options (same work, different launch shape; for measurement) -- */
 #define QDQ_OPT_PDL          1  /* 1 (default): programmatic dependent launch on; 0: plain launches */
-#define QDQ_OPT_L2_PREFETCH  2  /* L2 prefetch of weight rows.  0 (default): automatic -- the batch-1 Q8_0 GEMV prefetches the rows its first ring fill
-                                   leaves out, nothing else prefetches; 1: every GEMV CTA prefetches all its rows first; 2: every batch-1 CTA
-                                   prefetches the rows its first ring fill leaves out; 3: no prefetch */
-#define QDQ_OPT_CTAS_PER_SM  3  /* GEMV-family CTAs per SM, 1..4; 0 (default): automatic (2 for the FFN kernels, else 1) */
-#define QDQ_OPT_XS_GROUPS    4  /* batch-1 GEMV consumer groups per CTA, 0 = automatic (default), 1..16 */
-#define QDQ_OPT_XS_STAGES    5  /* batch-1 GEMV weight-ring slots per consumer group (4-row stages), 0 = automatic (default), 1..16 */
+#define QDQ_OPT_L2_PREFETCH  2  /* L2 prefetch of weight rows.  0 (default): automatic -- the batch-1 direct-load kernel
+                                   prefetches nothing, the ring kernel's Q8_0 GEMV prefetches the rows its first ring fill
+                                   leaves out when they fit in half the L2; 1: every GEMV CTA prefetches all its rows first;
+                                   2: every ring-kernel CTA prefetches the rows its first ring fill leaves out; 3: no prefetch */
+#define QDQ_OPT_CTAS_PER_SM  3  /* GEMV-family CTAs per SM, 1..4; 0 (default): automatic (batch-1 direct-load kernel: as
+                                   many as fit; ring kernel: 2 for the FFN kernels, else 1; batch 2..8: 1) */
+#define QDQ_OPT_XS_GROUPS    4  /* batch-1 GEMV groups of slice warps per CTA, 0 = automatic (default: 1 in the
+                                   direct-load kernel), 1..16 */
+#define QDQ_OPT_XS_STAGES    5  /* batch-1 GEMV: ring slots per consumer group (ring kernel), or the register depth
+                                   1 / 2 (direct-load kernel); 0 = automatic (default), 1..16 */
 /* Arithmetic of the batch-1 kernels (qdq_q8_0_gemv and qdq_q4k_gemv at batch 1,
  * qdq_q4k_swiglu, qdq_q4k_qkv, the output projections and both FFN calls at batch 1):
  *   1 (default): weights converted exactly to f32 and multiplied with f32 FMAs
@@ -340,10 +344,10 @@ int qdq_noop(cudaStream_t stream);
  *     activation gives NaN outputs. */
 #define QDQ_OPT_XS_FLOAT_X   6
 /* Batch-1 kernel of the f32 arithmetic: 0 (default) the direct-load kernel (weights straight into
- * registers after an L2 prefetch of each CTA's rows, every warp of the SM computing); 1 the
- * shared-memory ring kernel (a producer warp streams weights into a ring sized to half an SM, so
- * that the next kernel's CTA can start streaming beside it).  Same results within the stated
- * bound; the fixed-point arithmetic always runs in the ring kernel. */
+ * registers, small CTAs of one group of slice warps, as many per SM as fit); 1 the shared-memory
+ * ring kernel (a producer warp streams weights into a ring sized to half an SM, so that the next
+ * kernel's CTA can start streaming beside it).  Same results within the stated bound; the
+ * fixed-point arithmetic always runs in the ring kernel. */
 #define QDQ_OPT_BATCH1_KERNEL 7
 /* Sets a process-wide option; returns the previous value, or QDQ_ERR_DIMS for a bad key/value. */
 int qdq_set_option(int key, int value);

@@ -341,3 +341,48 @@ def test_q4k_swiglu_batch_parity(cuda_lib, n_ff, n_embd, M):
     s = oracle.swiglu(oracle.q4k_dequant(g, n_ff, n_embd), oracle.q4k_dequant(u, n_ff, n_embd), X[rows])
     assert np.all(np.abs(_np(mid)[rows] - s["mid"]) <= _swiglu_batch_bound(s))
     assert qdq.pipeline_timeouts() == 0
+
+
+def _topk_direct(qdq, lg, k):
+    import torch
+    batch, n = lg.shape
+    ws = torch.empty(qdq.topk_workspace_bytes(n, batch, k), dtype=torch.uint8, device=_dev())
+    idx = torch.full((batch, k), -1, dtype=torch.int32, device=_dev())
+    val = _nan(batch, k)
+    qdq.topk_rows(_t(lg), n, batch, k, ws, idx, val)
+    ix, vl = _np(idx), _np(val)
+    for b in range(batch):
+        order = _stable_topk(lg[b], k)
+        assert np.array_equal(ix[b], order), b
+        assert np.array_equal(vl[b].view(np.uint32), lg[b, order].view(np.uint32)), b
+
+
+def test_topk_adversarial_rows(cuda_lib):
+    # full-vocabulary rows whose top values cluster in one 1024-logit chunk, ascending and descending
+    # rows (every chunk's candidates matter / none do), all equal (ties broken by index), NaNs spread
+    # over every chunk, runs of equal values across chunk borders
+    n, k = 128256, 64
+    rng = np.random.default_rng(31)
+    rows = []
+    r = rng.standard_normal(n).astype(np.float32)
+    lo7 = 7 * n // 8
+    r[lo7 + 5 + 64 * np.arange(15)] = 100.0 + np.arange(15, dtype=np.float32)  # one chunk
+    rows.append(r)
+    rows.append(np.arange(n, dtype=np.float32))            # ascending: every CTA's threshold differs
+    rows.append(-np.arange(n, dtype=np.float32))           # descending
+    rows.append(np.full(n, 2.5, dtype=np.float32))         # all equal: ties broken by index
+    r = rng.standard_normal(n).astype(np.float32)
+    r[::997] = np.nan
+    rows.append(r)
+    r = np.repeat(rng.integers(-3, 4, size=n // 64 + 1), 64)[:n].astype(np.float32)  # runs of equal values
+    rows.append(r)
+    _topk_direct(cuda_lib, np.stack(rows), k)
+    _topk_direct(cuda_lib, np.ascontiguousarray(np.stack(rows)[:, :100000]), 33)
+
+
+def test_topk_long_rows(cuda_lib):
+    # 300001 logits: three merge rounds (1024-logit chunks, 2048-key merges), a ragged last chunk
+    rng = np.random.default_rng(32)
+    lg = rng.standard_normal((2, 300001)).astype(np.float32)
+    lg[1, 5::50000] = np.nan
+    _topk_direct(cuda_lib, lg, 40)
