@@ -99,7 +99,7 @@ __device__ __forceinline__ void sort_desc(uint64_t &a, uint64_t &b, uint64_t *sm
   }
 }
 
-// Round 1: chunk blockIdx.x of batch row blockIdx.y -> its k best keys at
+// First pass: chunk blockIdx.x of batch row blockIdx.y -> its k best keys at
 // out[(row * gridDim.x + chunk) * k ...].
 __global__ void __launch_bounds__(kChunk1 / 2) topk_chunk_kernel(const float *logits, int n, int k, uint64_t *out) {
   __shared__ uint64_t sm[kChunk1];
