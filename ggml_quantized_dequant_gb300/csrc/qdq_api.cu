@@ -371,6 +371,14 @@ int qdq_q8_0_logits_topk(const void *W, const float *x, float *logits, void *wor
   if (overlaps(workspace, sb, W, wb) || overlaps(workspace, sb, x, xb) || overlaps(index, rb, W, wb) ||
       overlaps(index, rb, x, xb) || overlaps(value, rb, W, wb) || overlaps(value, rb, x, xb))
     return QDQ_ERR_ALIAS;
+  if (batch == 1 && gemv_xs_supported(n_in, 1, 0) && opt_batch1_kernel() == 0 && opt_xs_float_x()) {
+    // batch 1: the projection's CTAs write their rows' k best keys as they finish, so the
+    // logits are not read back for the first selection; then the merge rounds
+    int n_cand = 0;
+    rc = launch_gemv_dl_topk(W, x, logits, n_vocab, n_in, static_cast<uint64_t *>(workspace), k, &n_cand, stream);
+    if (rc != QDQ_OK) return rc;
+    return launch_topk_merge(n_cand, k, workspace, logits, n_vocab, index, value, stream);
+  }
   rc = launch_q8_0_gemv(W, x, logits, n_vocab, n_in, batch, stream);
   if (rc != QDQ_OK) return rc;
   return launch_topk_rows(logits, n_vocab, batch, k, workspace, index, value, stream);

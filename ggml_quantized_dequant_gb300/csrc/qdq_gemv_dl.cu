@@ -48,7 +48,7 @@ namespace {
 constexpr int kMaxWarps = 16;
 constexpr int kMaxWarpsDepth2 = 12;  // two stages of registers: about 160 a thread
 enum Fmt { kQ8 = 0, kQ4 = 1, kQ6 = 2 };
-enum Epi { kPlain = 0, kSwiglu = 1, kResidual = 2, kQkv = 3 };
+enum Epi { kPlain = 0, kSwiglu = 1, kResidual = 2, kQkv = 3, kTopk = 4 };
 
 struct DlArgs {
   const uint8_t *W, *W2, *W3;  // matrix (gate / W_q), up / W_k, W_v
@@ -58,7 +58,59 @@ struct DlArgs {
   int seg1, seg2;              // QKV: rows [0, seg1) W_q, [seg1, seg2) W_k, [seg2, n_out) W_v
   int n_out, n_in, wpr, groups, prefetch;
   int psum_cap;  // floats of the row-total buffer in shared memory
+  uint64_t *cand;  // kTopk: the k best keys of each CTA's rows, at cand[cta * k ...]
+  int k;
+  int key_off;     // kTopk: floats from the start of shared memory to the rows' keys (8-byte aligned)
 };
+
+// Warp-wide bitonic sort of 64 keys, descending: lane l holds positions l (a) and
+// 32 + l (b).  Strides below 32 are shuffles, the 32 stride a register swap.
+__device__ __forceinline__ uint64_t shfl_xor_key(uint64_t v, int m) {
+  const uint32_t lo = __shfl_xor_sync(0xffffffffu, uint32_t(v), m);
+  const uint32_t hi = __shfl_xor_sync(0xffffffffu, uint32_t(v >> 32), m);
+  return (uint64_t(hi) << 32) | lo;
+}
+__device__ __forceinline__ uint64_t key_cmpx(uint64_t mine, uint64_t other, int p, int j, int k) {
+  const bool take_max = ((p & j) == 0) == ((p & k) == 0);  // lower position of a descending run keeps the max
+  return take_max ? (mine > other ? mine : other) : (mine < other ? mine : other);
+}
+__device__ __forceinline__ void warp_merge_desc(uint64_t &a, uint64_t &b, int lane, int k) {
+  // the bitonic merge steps of stage k (k = 64: a bitonic sequence -> descending)
+  int j = k >> 1;
+  if (j == 32) {
+    const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+    a = hi;
+    b = lo;
+    j = 16;
+  }
+  for (; j > 0; j >>= 1) {
+    const uint64_t oa = shfl_xor_key(a, j), ob = shfl_xor_key(b, j);
+    a = key_cmpx(a, oa, lane, j, k);
+    b = key_cmpx(b, ob, lane + 32, j, k);
+  }
+}
+__device__ __forceinline__ void warp_sort64_desc(uint64_t &a, uint64_t &b, int lane) {
+#pragma unroll 1
+  for (int k = 2; k <= 64; k <<= 1) {
+    if (k == 64) {
+      warp_merge_desc(a, b, lane, 64);
+    } else {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const uint64_t oa = shfl_xor_key(a, j), ob = shfl_xor_key(b, j);
+        a = key_cmpx(a, oa, lane, j, k);
+        b = key_cmpx(b, ob, lane + 32, j, k);
+      }
+    }
+  }
+}
+// (ta, tb) <- the 64 largest of two descending 64-key lists (ta, tb) and (a, b), descending:
+// the element-wise maximum of one list and the other reversed is bitonic and holds them.
+__device__ __forceinline__ void warp_top64_merge(uint64_t &ta, uint64_t &tb, uint64_t a, uint64_t b, int lane) {
+  const uint64_t ra = shfl_xor_key(b, 31), rb = shfl_xor_key(a, 31);  // positions 63 - l and 31 - l of (a, b)
+  ta = ta > ra ? ta : ra;
+  tb = tb > rb ? tb : rb;
+  warp_merge_desc(ta, tb, lane, 64);
+}
 
 // The columns one lane owns: Q4_K / Q6_K block `bq`; Q8_0 half `h` of blocks qa and qb.
 struct LaneCols {
@@ -412,12 +464,30 @@ __global__ void __launch_bounds__(32 * (DEPTH == 2 ? kMaxWarpsDepth2 : kMaxWarps
       } else {
         a.y[R] = EPI == kResidual ? a.residual[R] + v : v;
       }
+      if (EPI == kTopk) reinterpret_cast<uint64_t *>(psum + a.key_off)[r] = topk_key(v, uint32_t(R));
+    }
+  }
+  if constexpr (EPI == kTopk) {
+    // the k best keys of this CTA's rows (warp 0: a running top 64 over chunks of 64)
+    __syncthreads();
+    if (warp == 0) {
+      const uint64_t *keys = reinterpret_cast<const uint64_t *>(psum + a.key_off);
+      uint64_t ta = 0, tb = 0;
+      for (int c0 = 0; c0 < nreal; c0 += 64) {
+        uint64_t ka = c0 + lane < nreal ? keys[c0 + lane] : 0ull;
+        uint64_t kb = c0 + 32 + lane < nreal ? keys[c0 + 32 + lane] : 0ull;
+        warp_sort64_desc(ka, kb, lane);
+        warp_top64_merge(ta, tb, ka, kb, lane);
+      }
+      uint64_t *o = a.cand + int64_t(blockIdx.x) * a.k;
+      if (lane < a.k) o[lane] = ta;
+      if (lane + 32 < a.k) o[lane + 32] = tb;
     }
   }
 }
 
 template <int FMT, int EPI, int DEPTH>
-int launch_dl_depth(DlArgs a, cudaStream_t s, const DeviceInfo &di) {
+int launch_dl_depth(DlArgs a, cudaStream_t s, const DeviceInfo &di, int *grid_out) {
   constexpr int kV = EPI == kSwiglu ? 2 : 1;
   constexpr int kCap = DEPTH == 2 ? kMaxWarpsDepth2 : kMaxWarps;
   // default: one group of slice warps per CTA, and as many CTAs per SM as fit, so
@@ -430,10 +500,15 @@ int launch_dl_depth(DlArgs a, cudaStream_t s, const DeviceInfo &di) {
   const int units = (a.n_out + kRowsPerStage - 1) / kRowsPerStage;
   auto kern = gemv_dl_kernel<FMT, EPI, DEPTH>;
   auto psum_bytes = [&](int grid) { return size_t((units + grid - 1) / grid * kRowsPerStage) * kV * a.wpr * 4; };
+  // kTopk: the rows' keys after the row totals (8-byte aligned)
+  auto smem_bytes = [&](int grid) {
+    const size_t p = psum_bytes(grid);
+    return EPI == kTopk ? (p + 7) / 8 * 8 + size_t((units + grid - 1) / grid * kRowsPerStage) * 8 : p;
+  };
   int per_sm = ctas_per_sm_or(0);
   if (per_sm == 0) {
     // shared memory of the largest CTA share at one CTA per SM bounds every other shape's
-    const size_t smem0 = psum_bytes(units < di.sm_count ? units : di.sm_count);
+    const size_t smem0 = smem_bytes(units < di.sm_count ? units : di.sm_count);
     if (smem0 > 48 * 1024) {
       if (smem0 > size_t(di.max_smem_optin)) return QDQ_ERR_UNSUPPORTED;
       const cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(kern), int(smem0));
@@ -446,8 +521,10 @@ int launch_dl_depth(DlArgs a, cudaStream_t s, const DeviceInfo &di) {
   }
   int grid = di.sm_count * per_sm;
   if (grid > units) grid = units;
-  const size_t smem = psum_bytes(grid);
-  a.psum_cap = int(smem / sizeof(float));
+  const size_t smem = smem_bytes(grid);
+  a.psum_cap = int(psum_bytes(grid) / sizeof(float));
+  a.key_off = int((psum_bytes(grid) + 7) / 8 * 2);
+  if (grid_out) *grid_out = grid;
   // L2 prefetch of the CTA's rows: off unless QDQ_OPT_L2_PREFETCH = 1 (measured no faster here)
   a.prefetch = opt_l2_prefetch() == 1 ? 1 : 0;
   if (smem > 48 * 1024) {
@@ -460,7 +537,7 @@ int launch_dl_depth(DlArgs a, cudaStream_t s, const DeviceInfo &di) {
 }
 
 template <int FMT, int EPI>
-int launch_dl(DlArgs a, cudaStream_t s) {
+int launch_dl(DlArgs a, cudaStream_t s, int *grid_out = nullptr) {
   DeviceInfo di;
   const cudaError_t e0 = device_info(&di);
   if (e0 != cudaSuccess) return fail_cuda(e0);
@@ -474,7 +551,8 @@ int launch_dl(DlArgs a, cudaStream_t s) {
   // more warps than two stages of registers allow (a forced group count) run one stage deep
   const int warps = a.wpr * (opt_xs_groups() > 0 ? opt_xs_groups() : 1);
   if (warps > kMaxWarpsDepth2) depth = 1;
-  return depth == 2 ? launch_dl_depth<FMT, EPI, 2>(a, s, di) : launch_dl_depth<FMT, EPI, 1>(a, s, di);
+  return depth == 2 ? launch_dl_depth<FMT, EPI, 2>(a, s, di, grid_out)
+                    : launch_dl_depth<FMT, EPI, 1>(a, s, di, grid_out);
 }
 
 }  // namespace
@@ -494,6 +572,27 @@ int launch_gemv_dl(int fmt, int mode, const void *W, const void *W2, const float
   if (mode == 1) return launch_dl<kQ4, kSwiglu>(a, s);
   if (mode == 2) return launch_dl<kQ4, kResidual>(a, s);
   return launch_dl<kQ4, kPlain>(a, s);
+}
+
+int launch_gemv_dl_topk(const void *W, const float *x, float *y, int n_out, int n_in, uint64_t *cand, int k,
+                        int *n_cand, cudaStream_t s) {
+  DlArgs a{};
+  a.W = static_cast<const uint8_t *>(W);
+  a.x = x;
+  a.y = y;
+  a.n_out = n_out;
+  a.n_in = n_in;
+  a.cand = cand;
+  a.k = k;
+  int grid = 0;
+  const int rc = launch_dl<kQ8, kTopk>(a, s, &grid);
+  *n_cand = grid * k;
+  return rc;
+}
+
+int gemv_dl_max_ctas() {
+  DeviceInfo di;
+  return device_info(&di) == cudaSuccess ? di.sm_count * 16 : 0;
 }
 
 int read_dl_timeouts() { return 0; }  // the direct-load kernel has no waits

@@ -113,11 +113,21 @@ int launch_gemv_xs(int fmt, int mode, const void *W, const void *W2, const float
 size_t topk_workspace_bytes(int n, int batch, int k);
 int launch_topk_rows(const float *logits, int n, int batch, int k, void *workspace, int *index, float *value,
                      cudaStream_t s);
+// The merge rounds alone, for one row whose `count` candidate keys (each CTA's k best,
+// in any order) are at the start of the workspace (the batch-1 projection writes them).
+int launch_topk_merge(int count, int k, void *workspace, const float *logits, int n, int *index, float *value,
+                      cudaStream_t s);
 // Batch-1 direct-load GEMV (qdq_gemv_dl.cu), f32 arithmetic; same fmt / mode as launch_gemv_xs.
 int launch_gemv_dl(int fmt, int mode, const void *W, const void *W2, const float *x, const float *residual, float *y,
                    int n_out, int n_in, cudaStream_t s);
 int launch_gemv_dl_qkv(const void *Wq, const void *Wk, const void *Wv, const float *x, float *q, float *k, float *v,
                        int n_q, int n_kv, int n_in, cudaStream_t s);
+// Batch-1 Q8_0 GEMV whose CTAs also write the k best keys (topk_key) of their rows to
+// cand[cta * k ...]; *n_cand = CTAs * k.
+int launch_gemv_dl_topk(const void *W, const float *x, float *y, int n_out, int n_in, uint64_t *cand, int k,
+                        int *n_cand, cudaStream_t s);
+// Upper bound of the CTAs launch_gemv_dl_topk runs on the current device (0 on error).
+int gemv_dl_max_ctas();
 // Q6_K (qdq_q6k.cu): repack, dequantisation, embedding-row lookup, GEMV (batch 1..8).
 int launch_q6k_pack(const void *ggml, void *packed, int n_out, int n_in, cudaStream_t s);
 int launch_q6k_dequant(const void *W, float *out, int n_out, int n_in, cudaStream_t s);
@@ -170,6 +180,23 @@ int read_checks_xs();
 int read_checks_gemm();
 int read_checks_topk();
 int read_checks_q6k();
+
+// A logit and its index as a 64-bit key whose unsigned order is the top-k order: a
+// NaN above every number, then larger values, equal values (+0 = -0) by smaller
+// index.  The high word maps the float to an order-preserving integer (every NaN
+// to the largest), the low word is the complement of the index; key 0 is below
+// every real key.
+__device__ __forceinline__ uint64_t topk_key(float v, uint32_t index) {
+  uint32_t o;
+  if (v != v) {
+    o = 0xFFFFFFFFu;
+  } else {
+    uint32_t b = __float_as_uint(v);
+    if ((b & 0x7FFFFFFFu) == 0) b = 0;  // -0 sorts as +0
+    o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  }
+  return (uint64_t(o) << 32) | uint64_t(~index);
+}
 
 // Programmatic dependent launch: let the next grid on the stream start early.
 __device__ __forceinline__ void pdl_launch_dependents() {

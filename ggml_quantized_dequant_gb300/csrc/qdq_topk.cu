@@ -28,18 +28,6 @@ namespace {
 constexpr int kChunk1 = 1024;  // logits per first-round chunk
 constexpr int kChunk2 = 2048;  // candidate keys per merge chunk
 
-__device__ __forceinline__ uint64_t topk_key(float v, uint32_t index) {
-  uint32_t o;
-  if (v != v) {
-    o = 0xFFFFFFFFu;
-  } else {
-    uint32_t b = __float_as_uint(v);
-    if ((b & 0x7FFFFFFFu) == 0) b = 0;  // -0 sorts as +0
-    o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-  }
-  return (uint64_t(o) << 32) | uint64_t(~index);
-}
-
 __device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
   const uint32_t lo = __shfl_xor_sync(0xffffffffu, uint32_t(v), m);
   const uint32_t hi = __shfl_xor_sync(0xffffffffu, uint32_t(v >> 32), m);
@@ -176,18 +164,21 @@ cudaError_t launch_merge(int m, int batch, cudaStream_t s, const uint64_t *in, i
 QDQ_CHECK_READER(read_checks_topk)
 
 size_t topk_workspace_bytes(int n, int batch, int k) {
-  return 2 * size_t(batch) * size_t(chunks1(n)) * size_t(k) * sizeof(uint64_t);
+  // the chunked path: two rounds of ceil(n / 1024) * k keys per row; the batch-1 output
+  // projection: one key list per CTA of k keys, and the merge round after it
+  const size_t chunked = 2 * size_t(batch) * size_t(chunks1(n)) * size_t(k);
+  const size_t fused = 2 * size_t(gemv_dl_max_ctas()) * size_t(k);
+  return (chunked > fused ? chunked : fused) * sizeof(uint64_t);
 }
 
-int launch_topk_rows(const float *logits, int n, int batch, int k, void *workspace, int *index, float *value,
-                     cudaStream_t s) {
-  uint64_t *buf[2];
-  buf[0] = static_cast<uint64_t *>(workspace);
-  buf[1] = buf[0] + size_t(batch) * size_t(chunks1(n)) * size_t(k);
-  const int nch = int(chunks1(n));
-  cudaError_t e = launch(topk_chunk_kernel, dim3(nch, batch), dim3(kChunk1 / 2), 0, s, logits, n, k, buf[0]);
-  if (e != cudaSuccess) return fail_cuda(e);
-  int count = nch * k, cur = 0;  // candidate keys per batch row in buf[cur]
+namespace {
+// Merge rounds over `count` candidate keys per batch row in buf0 (buf1 the other
+// half of the ping-pong), then the last merge, sized to what is left.
+int merge_rounds(int count, int batch, int k, uint64_t *buf0, uint64_t *buf1, const float *logits, int n, int *index,
+                 float *value, cudaStream_t s) {
+  uint64_t *buf[2] = {buf0, buf1};
+  int cur = 0;
+  cudaError_t e = cudaSuccess;
   while (count > kChunk2) {
     const int m = (count + kChunk2 - 1) / kChunk2;
     e = launch_merge<kChunk2>(m, batch, s, buf[cur], count, k, buf[cur ^ 1], nullptr, 0, nullptr, nullptr);
@@ -204,6 +195,23 @@ int launch_topk_rows(const float *logits, int n, int batch, int k, void *workspa
   else if (count <= 1024) e = launch_merge<1024>(1, batch, s, in, count, k, nullptr, logits, n, index, value);
   else e = launch_merge<2048>(1, batch, s, in, count, k, nullptr, logits, n, index, value);
   return e == cudaSuccess ? QDQ_OK : fail_cuda(e);
+}
+}  // namespace
+
+int launch_topk_rows(const float *logits, int n, int batch, int k, void *workspace, int *index, float *value,
+                     cudaStream_t s) {
+  uint64_t *buf0 = static_cast<uint64_t *>(workspace);
+  uint64_t *buf1 = buf0 + size_t(batch) * size_t(chunks1(n)) * size_t(k);
+  const int nch = int(chunks1(n));
+  const cudaError_t e = launch(topk_chunk_kernel, dim3(nch, batch), dim3(kChunk1 / 2), 0, s, logits, n, k, buf0);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return merge_rounds(nch * k, batch, k, buf0, buf1, logits, n, index, value, s);
+}
+
+int launch_topk_merge(int count, int k, void *workspace, const float *logits, int n, int *index, float *value,
+                      cudaStream_t s) {
+  uint64_t *buf0 = static_cast<uint64_t *>(workspace);
+  return merge_rounds(count, 1, k, buf0, buf0 + count, logits, n, index, value, s);
 }
 
 }  // namespace qdq

@@ -196,10 +196,14 @@ int qdq_q8_0_logits_argmax(const void *W, const float *x, float *logits, int *in
  * of the order NaN first (the first NaN first), then larger logits first, equal
  * logits (+0 == -0) by smaller index; value holds the logit's exact bits.
  * 1 <= k <= min(n, QDQ_MAX_TOPK).  workspace: qdq_topk_workspace_bytes(n, batch,
- * k) bytes of caller scratch (16-byte aligned, overwritten).  Outputs and
- * workspace may overlap nothing.  Several kernels on `stream`.
+ * k) bytes of caller scratch (16-byte aligned, overwritten; the size depends on
+ * the current device).  Outputs and workspace may overlap nothing.  Several
+ * kernels on `stream`.
  * qdq_q8_0_logits_topk: the Q8_0 output projection (as qdq_q8_0_logits_argmax)
- * followed by the top-k; logits: batch x n_vocab scratch the caller owns.
+ * followed by the top-k; logits: batch x n_vocab scratch the caller owns (it
+ * receives the logits).  At batch 1 the projection's CTAs write the k best
+ * (logit, index) keys of their own rows as they finish, and only merge kernels
+ * follow; same results as the separate top-k.
  */
 #define QDQ_MAX_TOPK 64
 size_t qdq_topk_workspace_bytes(int n, int batch, int k);   /* 0 on bad arguments */

@@ -386,3 +386,22 @@ def test_topk_long_rows(cuda_lib):
     lg = rng.standard_normal((2, 300001)).astype(np.float32)
     lg[1, 5::50000] = np.nan
     _topk_direct(cuda_lib, lg, 40)
+
+
+@pytest.mark.parametrize("n_vocab,n_in,k", [(100, 256, 64), (1000, 512, 1), (5003, 2048, 40), (33333, 1024, 17),
+                                            (128256, 3072, 64)])
+def test_logits_topk_fused_equals_separate(cuda_lib, n_vocab, n_in, k):
+    # batch 1 selects from the projection's per-CTA candidates; the separate GEMV + top-k
+    # path must give the same indices and value bits (also for rows shorter than k per CTA)
+    qdq = cuda_lib
+    rng = np.random.default_rng(n_vocab + k)
+    wb, x = synth.q8_0_blocks(rng, n_vocab, n_in), synth.activations(rng, 1, n_in)
+    import torch
+    W = qdq.upload_q8_0(wb, n_vocab, n_in)
+    lg1, ix1, vl1 = _topk_case(qdq, W, x, n_vocab, n_in, 1, k, fused=True)
+    lg2, ix2, vl2 = _topk_case(qdq, W, x, n_vocab, n_in, 1, k, fused=False)
+    assert np.array_equal(lg1.view(np.uint32), lg2.view(np.uint32))
+    assert np.array_equal(ix1, ix2)
+    assert np.array_equal(vl1.view(np.uint32), vl2.view(np.uint32))
+    order = _stable_topk(lg1[0], k)
+    assert np.array_equal(ix1[0], order)
