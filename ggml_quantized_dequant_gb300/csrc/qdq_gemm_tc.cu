@@ -681,26 +681,108 @@ bool encode_2d(CUtensorMap *tm, CUtensorMapDataType dt, void *base, uint64_t inn
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The token tile for M tokens.
-int token_tile(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256; }
+// The token tile for up to 128 tokens; more tokens choose among 128, 192 and 256 (plan_gemm).
+int token_tile(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
+
+// Clusters of cz CTAs (one CTA per SM, as every GEMM instantiation takes) that can be
+// resident at once on the current device, measured once per size; 0 if unknown.
+int resident_clusters(int cz) {
+  static std::atomic<int> cache[9];  // per cluster size (0: not yet measured, -1: unknown)
+  if (cz < 2 || cz > 8) return 0;
+  int mc = cache[cz].load(std::memory_order_relaxed);
+  if (mc == 0) {
+    using C = GemmCfg<kWQ8, 256, 1, 1>;
+    auto kern = gemm_tc_kernel<kWQ8, 256, 1, 1>;
+    if (allow_dynamic_smem(reinterpret_cast<const void *>(kern), int(C::kSmemBytes)) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, unsigned(cz));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = unsigned(cz);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&mc, kern, &cfg) != cudaSuccess || mc < 1) {
+      (void)cudaGetLastError();
+      mc = -1;
+    }
+    cache[cz].store(mc, std::memory_order_relaxed);
+  }
+  return mc > 0 ? mc : 0;
+}
+
+// Whether the split-K partial tile fits the CTA's rings (else K is never split).
+template <int FMT, int NA>
+bool splittable(int N) {
+  switch (N) {
+    case 16: return GemmCfg<FMT, 16, NA, 2>::kPBytes <= GemmCfg<FMT, 16, NA, 2>::kRingBytes;
+    case 32: return GemmCfg<FMT, 32, NA, 2>::kPBytes <= GemmCfg<FMT, 32, NA, 2>::kRingBytes;
+    case 64: return GemmCfg<FMT, 64, NA, 1>::kPBytes <= GemmCfg<FMT, 64, NA, 1>::kRingBytes;
+    case 128: return GemmCfg<FMT, 128, NA, 1>::kPBytes <= GemmCfg<FMT, 128, NA, 1>::kRingBytes;
+    case 192: return GemmCfg<FMT, 192, NA, 1>::kPBytes <= GemmCfg<FMT, 192, NA, 1>::kRingBytes;
+    default: return GemmCfg<FMT, 256, NA, 1>::kPBytes <= GemmCfg<FMT, 256, NA, 1>::kRingBytes;
+  }
+}
 
 // Launch shape and workspace of one GEMM call (the workspace holds only the bf16
 // copy of X, for token tiles above 64).
 struct GemmPlan {
   int N, KB, ntile_n, ntile_m, nst;
+  int split, st_per;  // K splits (the cluster size along z) and K stages per split
   size_t xb_bytes;
 };
-GemmPlan plan_gemm(int M, int n_out, int n_in) {
+// The shape for token tile N: K is split when the tiles alone cannot fill the SMs, at
+// most 8 ways (a portable cluster) and only as far as every tile's cluster stays
+// resident at once (one wave).
+template <int FMT, int NA>
+GemmPlan plan_for(int N, int M, int n_out, int n_in, int sm_count) {
   GemmPlan p;
-  p.N = token_tile(M);
+  p.N = N;
   // 64-K sub-blocks per stage: two for token tiles up to 32 (at 64 the larger stage
   // leaves too few load slots and measured slower)
   p.KB = p.N <= 32 && n_in % (2 * BK) == 0 ? 2 : 1;
   p.ntile_n = n_out / BM;
   p.ntile_m = (M + p.N - 1) / p.N;
   p.nst = n_in / (BK * p.KB);
+  const int tiles = p.ntile_n * p.ntile_m;
+  int split = sm_count / tiles;
+  if (split > 8) split = 8;
+  if (split > p.nst) split = p.nst;
+  if (split < 1 || !splittable<FMT, NA>(p.N)) split = 1;
+  while (split > 1 && resident_clusters(split) < tiles) --split;
+  p.st_per = (p.nst + split - 1) / split;
+  p.split = (p.nst + p.st_per - 1) / p.st_per;  // every split gets at least one stage
   p.xb_bytes = p.N <= 64 ? 0 : (size_t(M) * n_in * 2 + 255) / 256 * 256;
   return p;
+}
+// Above 128 tokens the token tile is the one of 128, 192 and 256 with the least
+// estimated time: waves of CTAs x K stages per CTA x a stage's time, which the
+// measurements put at about 0.35 us + 1.2 ns per token of the tile.  (8192 -> 3072
+// at 512 tokens: 24 row tiles, so 256-token tiles leave 96 CTAs and 192-token tiles
+// 144; 3072 -> 8192 at 512 tokens: 64 row tiles, where 192-token tiles would take
+// two waves.)
+template <int FMT, int NA>
+GemmPlan plan_gemm(int M, int n_out, int n_in, int sm_count) {
+  if (M <= 128) return plan_for<FMT, NA>(token_tile(M), M, n_out, n_in, sm_count);
+  GemmPlan best{};
+  double best_cost = 0.0;
+  for (const int N : {256, 192, 128}) {
+    const GemmPlan p = plan_for<FMT, NA>(N, M, n_out, n_in, sm_count);
+    const int ctas = p.ntile_n * p.ntile_m * p.split;
+    const int waves = (ctas + sm_count - 1) / sm_count;
+    const double cost = double(waves) * p.st_per * (0.35 + 0.0012 * N);
+    if (best.N == 0 || cost < best_cost * (1.0 - 1e-9)) {
+      best = p;
+      best_cost = cost;
+    }
+  }
+  return best;
 }
 
 // Launch with programmatic dependent launch and a (1, 1, cz) thread-block cluster.
@@ -732,39 +814,7 @@ int launch_tile(const uint8_t *const W[2], const float *X, float *Y, void *ws, i
   cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(kern), int(C::kSmemBytes));
   if (e != cudaSuccess) return fail_cuda(e);
 
-  // K splits, when the tiles alone cannot fill the SMs: at most 8 (a portable cluster),
-  // and only as many as keep every tile's cluster resident at once (one wave)
-  const int tiles = p.ntile_n * p.ntile_m;
-  int split = di.sm_count / tiles;
-  if (split > 8) split = 8;
-  if (split > p.nst) split = p.nst;
-  if (C::kPBytes > C::kRingBytes) split = 1;
-  static std::atomic<int> max_clusters[9];  // per cluster size, measured once (0: not yet)
-  while (split > 1) {
-    int mc = max_clusters[split].load(std::memory_order_relaxed);
-    if (mc == 0) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(p.ntile_n, p.ntile_m, split);
-      cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = C::kSmemBytes;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = 1;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = unsigned(split);
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&mc, kern, &cfg) != cudaSuccess || mc < 1) {
-        (void)cudaGetLastError();
-        mc = -1;
-      }
-      max_clusters[split].store(mc, std::memory_order_relaxed);
-    }
-    if (mc >= tiles) break;
-    --split;
-  }
-  int st_per = (p.nst + split - 1) / split;
-  split = (p.nst + st_per - 1) / st_per;  // every split gets at least one stage
+  const int split = p.split, st_per = p.st_per;
 
   CUtensorMap tm_q[2], tm_x;
   for (int a = 0; a < 2; ++a) {
@@ -824,7 +874,7 @@ int launch_gemm(const uint8_t *const W[2], const float *X, float *Y, void *ws, i
   if (e != cudaSuccess) return fail_cuda(e);
   e = get_encoder();
   if (e != cudaSuccess) return fail_cuda(e);
-  const GemmPlan p = plan_gemm(M, n_out, n_in);
+  const GemmPlan p = plan_gemm<FMT, NA>(M, n_out, n_in, di.sm_count);
   switch (p.N * 2 + p.KB - 1) {
     case 32: return launch_tile<FMT, 16, NA, 1>(W, X, Y, ws, n_out, n_in, M, p, s, di);
     case 33: return launch_tile<FMT, 16, NA, 2>(W, X, Y, ws, n_out, n_in, M, p, s, di);
@@ -832,6 +882,7 @@ int launch_gemm(const uint8_t *const W[2], const float *X, float *Y, void *ws, i
     case 65: return launch_tile<FMT, 32, NA, 2>(W, X, Y, ws, n_out, n_in, M, p, s, di);
     case 128: return launch_tile<FMT, 64, NA, 1>(W, X, Y, ws, n_out, n_in, M, p, s, di);
     case 256: return launch_tile<FMT, 128, NA, 1>(W, X, Y, ws, n_out, n_in, M, p, s, di);
+    case 384: return launch_tile<FMT, 192, NA, 1>(W, X, Y, ws, n_out, n_in, M, p, s, di);
     default: return launch_tile<FMT, 256, NA, 1>(W, X, Y, ws, n_out, n_in, M, p, s, di);
   }
 }
@@ -839,11 +890,11 @@ int launch_gemm(const uint8_t *const W[2], const float *X, float *Y, void *ws, i
 }  // namespace
 
 size_t gemm_workspace_bytes(int M, int n_out, int n_in, int na) {
-  DeviceInfo di;
-  if (device_info(&di) != cudaSuccess) return 0;
+  // the bf16 copy of X (token tiles above 64, which every M > 128 takes), else 256 bytes reserved
+  (void)n_out;
   (void)na;
-  const GemmPlan p = plan_gemm(M, n_out, n_in);
-  return p.xb_bytes > 256 ? p.xb_bytes : 256;
+  const size_t xb = M > 64 ? (size_t(M) * n_in * 2 + 255) / 256 * 256 : 0;
+  return xb > 256 ? xb : 256;
 }
 
 int launch_q8_0_gemm_batch(const void *W, const float *X, float *Y, void *ws, int n_out, int n_in, int M,

@@ -264,6 +264,18 @@ def test_q4k_gemm_batch_full_size(cuda_lib, kind, M):
     assert gemv_excess(Y[rows], Y_ref, A, rel=4e-3) <= 1.0
 
 
+@pytest.mark.parametrize("n_out,n_in,M", [(8192, 3072, 600), (3072, 8192, 384)])
+def test_q4k_gemm_batch_token_tiles(cuda_lib, n_out, n_in, M):
+    # 8192 x 600: more output tiles than SMs (no K split, two waves); 3072 x 384: 192-token tiles
+    rng = np.random.default_rng(n_out + M)
+    wb, X = synth.q4k_blocks(rng, n_out, n_in), synth.activations(rng, M, n_in)
+    Y = _gemm_q4k(cuda_lib, wb, X, n_out, n_in, M)
+    rows = np.sort(rng.choice(M, 24, replace=False))
+    Y_ref, A = oracle.gemm_batch(oracle.q4k_dequant(wb, n_out, n_in), X[rows])
+    assert gemv_excess(Y[rows], Y_ref, A, rel=4e-3) <= 1.0
+    assert cuda_lib.pipeline_timeouts() == 0
+
+
 def test_q4k_gemm_batch_m1_matches_gemv_within_bf16_bound(cuda_lib):
     qdq = cuda_lib
     rng = np.random.default_rng(72)
@@ -326,7 +338,8 @@ def _swiglu_batch_bound(s, rel=4e-3):
             + 1e-6 * np.abs(s["mid"]))
 
 
-@pytest.mark.parametrize("n_ff,n_embd,M", [(512, 256, 20), (1024, 512, 130), (256, 1024, 1), (8192, 3072, 64)])
+@pytest.mark.parametrize("n_ff,n_embd,M", [(512, 256, 20), (1024, 512, 130), (256, 1024, 1), (8192, 3072, 64),
+                                           (1024, 512, 192), (3072, 1024, 600)])
 def test_q4k_swiglu_batch_parity(cuda_lib, n_ff, n_embd, M):
     import torch
     qdq = cuda_lib

@@ -286,6 +286,16 @@ def test_q8_0_gemm_batch_full_size_config4(cuda_lib, kind, M):
                sample_rows=sample)
 
 
+@pytest.mark.parametrize("n_out,n_in,M", [(8192, 3072, 600), (3072, 8192, 384), (1024, 1024, 160)])
+def test_q8_0_gemm_batch_token_tiles(cuda_lib, n_out, n_in, M):
+    # above 128 tokens the token tile is 128, 192 or 256, whichever the launch plan
+    # estimates fastest: 8192 x 600 has more output tiles than SMs (no K split, two
+    # waves), 3072 x 384 takes 192-token tiles, 160 tokens one partial 192-token tile.
+    # 24 sampled rows spread over the tokens
+    sample = np.sort(np.random.default_rng(M).choice(M, min(M, 24), replace=False))
+    _gemm_case(cuda_lib, n_out, n_in, M, sample_rows=sample, seed=n_out + M)
+
+
 def test_q8_0_gemm_batch_m1_matches_gemv_within_bf16_bound(cuda_lib):
     qdq = cuda_lib
     import torch
