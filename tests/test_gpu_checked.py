@@ -151,14 +151,16 @@ def test_checked_q6k(cuda_lib, checked):
     _same(qdq, checked, run)
 
 
+@pytest.mark.parametrize("n_in", [1024, 3072])
 @pytest.mark.parametrize("batch", [1, 2])
 @pytest.mark.parametrize("k", [1, 40, 64])
-def test_checked_topk_and_argmax(cuda_lib, checked, k, batch):
-    # batch 1: the projection writes per-CTA candidates, then merges; batch 2: the chunked path
+def test_checked_topk_and_argmax(cuda_lib, checked, k, batch, n_in):
+    # batch 1: the projection writes per-CTA candidates (CTAs of fewer than k rows at
+    # n_in = 1024, of more at 3072), then the merge rounds; batch 2: the chunked path
     import torch
     qdq = cuda_lib
     rng = np.random.default_rng(40 + k)
-    n_vocab, n_in = 50003, 1024
+    n_vocab = 50003
     W = qdq.upload_q8_0(synth.q8_0_blocks(rng, n_vocab, n_in), n_vocab, n_in)
     x = _t(synth.activations(rng, batch, n_in))
 

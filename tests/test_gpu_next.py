@@ -402,7 +402,7 @@ def test_topk_long_rows(cuda_lib):
 
 
 @pytest.mark.parametrize("n_vocab,n_in,k", [(100, 256, 64), (1000, 512, 1), (5003, 2048, 40), (33333, 1024, 17),
-                                            (128256, 3072, 64)])
+                                            (40000, 3072, 40), (128256, 3072, 64)])
 def test_logits_topk_fused_equals_separate(cuda_lib, n_vocab, n_in, k):
     # batch 1 selects from the projection's per-CTA candidates; the separate GEMV + top-k
     # path must give the same indices and value bits (also for rows shorter than k per CTA)
@@ -418,3 +418,25 @@ def test_logits_topk_fused_equals_separate(cuda_lib, n_vocab, n_in, k):
     assert np.array_equal(vl1.view(np.uint32), vl2.view(np.uint32))
     order = _stable_topk(lg1[0], k)
     assert np.array_equal(ix1[0], order)
+
+
+@pytest.mark.parametrize("k", [40, 64])
+def test_logits_topk_fused_many_candidates(cuda_lib, k):
+    # every third row has a large logit, so that each CTA of the projection holds fewer
+    # than k large rows and every CTA's candidate list mixes large and small logits; the
+    # merge of the lists and the separate GEMV + top-k path must agree bit for bit
+    qdq = cuda_lib
+    n_vocab, n_in = 40000, 3072
+    rng = np.random.default_rng(91 + k)
+    wb = synth.q8_0_blocks(rng, n_vocab, n_in).reshape(n_vocab, n_in // 32, 34)
+    wb[0::3, :, 2:] = 127  # int8 quants 127 on every third row
+    wb = wb.reshape(n_vocab, -1)
+    x = np.abs(synth.activations(rng, 1, n_in))
+    W = qdq.upload_q8_0(wb, n_vocab, n_in)
+    lg1, ix1, vl1 = _topk_case(qdq, W, x, n_vocab, n_in, 1, k, fused=True)
+    lg2, ix2, vl2 = _topk_case(qdq, W, x, n_vocab, n_in, 1, k, fused=False)
+    assert np.array_equal(ix1, ix2)
+    assert np.array_equal(vl1.view(np.uint32), vl2.view(np.uint32))
+    order = _stable_topk(lg1[0], k)
+    assert np.array_equal(ix1[0], order)
+    assert np.all(ix1[0] % 3 == 0)
