@@ -63,55 +63,6 @@ struct DlArgs {
   int key_off;     // kTopk: floats from the start of shared memory to the rows' keys (8-byte aligned)
 };
 
-// Warp-wide bitonic sort of 64 keys, descending: lane l holds positions l (a) and
-// 32 + l (b).  Strides below 32 are shuffles, the 32 stride a register swap.
-__device__ __forceinline__ uint64_t shfl_xor_key(uint64_t v, int m) {
-  const uint32_t lo = __shfl_xor_sync(0xffffffffu, uint32_t(v), m);
-  const uint32_t hi = __shfl_xor_sync(0xffffffffu, uint32_t(v >> 32), m);
-  return (uint64_t(hi) << 32) | lo;
-}
-__device__ __forceinline__ uint64_t key_cmpx(uint64_t mine, uint64_t other, int p, int j, int k) {
-  const bool take_max = ((p & j) == 0) == ((p & k) == 0);  // lower position of a descending run keeps the max
-  return take_max ? (mine > other ? mine : other) : (mine < other ? mine : other);
-}
-__device__ __forceinline__ void warp_merge_desc(uint64_t &a, uint64_t &b, int lane, int k) {
-  // the bitonic merge steps of stage k (k = 64: a bitonic sequence -> descending)
-  int j = k >> 1;
-  if (j == 32) {
-    const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
-    a = hi;
-    b = lo;
-    j = 16;
-  }
-  for (; j > 0; j >>= 1) {
-    const uint64_t oa = shfl_xor_key(a, j), ob = shfl_xor_key(b, j);
-    a = key_cmpx(a, oa, lane, j, k);
-    b = key_cmpx(b, ob, lane + 32, j, k);
-  }
-}
-__device__ __forceinline__ void warp_sort64_desc(uint64_t &a, uint64_t &b, int lane) {
-#pragma unroll 1
-  for (int k = 2; k <= 64; k <<= 1) {
-    if (k == 64) {
-      warp_merge_desc(a, b, lane, 64);
-    } else {
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        const uint64_t oa = shfl_xor_key(a, j), ob = shfl_xor_key(b, j);
-        a = key_cmpx(a, oa, lane, j, k);
-        b = key_cmpx(b, ob, lane + 32, j, k);
-      }
-    }
-  }
-}
-// (ta, tb) <- the 64 largest of two descending 64-key lists (ta, tb) and (a, b), descending:
-// the element-wise maximum of one list and the other reversed is bitonic and holds them.
-__device__ __forceinline__ void warp_top64_merge(uint64_t &ta, uint64_t &tb, uint64_t a, uint64_t b, int lane) {
-  const uint64_t ra = shfl_xor_key(b, 31), rb = shfl_xor_key(a, 31);  // positions 63 - l and 31 - l of (a, b)
-  ta = ta > ra ? ta : ra;
-  tb = tb > rb ? tb : rb;
-  warp_merge_desc(ta, tb, lane, 64);
-}
-
 // The columns one lane owns: Q4_K / Q6_K block `bq`; Q8_0 half `h` of blocks qa and qb.
 struct LaneCols {
   int bq;            // Q4_K / Q6_K: the column block

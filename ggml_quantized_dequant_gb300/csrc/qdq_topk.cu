@@ -5,8 +5,8 @@
 // "QTensorEngine", dispatch_output_topk_chunked: the logits stay on the GPU, a
 // top-k kernel reduces them per chunk, and only the merged K candidates are read
 // back.  The same here: the row is cut into chunks of 1024 logits, each chunk is
-// sorted on chip and keeps its k best; the candidates are then merged by the
-// same sort, 2048 at a time, until one chunk holds them all.
+// sorted on chip and keeps its k best; the chunks' sorted lists are then folded
+// 32 at a time by bitonic merges until one list holds the row's k best.
 //
 // Order (the k = 1 case is the argmax epilogue): a NaN comes before every number
 // (the first NaN first), then larger values first, equal values (+0 and -0 are
@@ -26,7 +26,6 @@ namespace qdq {
 namespace {
 
 constexpr int kChunk1 = 1024;  // logits per first-round chunk
-constexpr int kChunk2 = 2048;  // candidate keys per merge chunk
 
 __device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
   const uint32_t lo = __shfl_xor_sync(0xffffffffu, uint32_t(v), m);
@@ -112,52 +111,59 @@ __global__ void __launch_bounds__(kChunk1 / 2) topk_chunk_kernel(const float *lo
   }
 }
 
-// Merge rounds: chunk blockIdx.x of the `count` candidate keys of batch row
-// blockIdx.y -> its k best.  With `index` non-NULL (one chunk left) writes the
-// final (index, value) pairs instead, the value read back from the logits so that
+// Merge rounds: the candidate lists (k keys each, sorted best first: the chunks' or the
+// projection CTAs' k best) of batch row blockIdx.y hold the row's k best, which are the
+// k best of their union.  They are folded with bitonic merges of sorted lists instead of
+// being sorted again (the element-wise maximum of one sorted list and the other reversed
+// is bitonic and holds the 64 largest of the two; one bitonic merge sorts it).  A round:
+// CTA b takes lists 32b .. 32b + 31, one per warp, and folds them pairwise through shared
+// memory into one sorted list of k keys; rounds repeat until one CTA per row is left,
+// which writes the (index, value) pairs, the value read back from the logits so that
 // its bits are exactly the logit's.
-template <int N>
-__global__ void __launch_bounds__(N / 2) topk_merge_kernel(const uint64_t *in, int count, int k, uint64_t *out,
-                                                           const float *logits, int n, int *index, float *value) {
-  __shared__ uint64_t sm[N];
+__global__ void __launch_bounds__(1024) topk_fold_kernel(const uint64_t *in, int nlists, int k, uint64_t *out,
+                                                         const float *logits, int n, int *index, float *value) {
+  __shared__ uint64_t sl[16][64];
   pdl_launch_dependents();
-  pdl_wait();
-  const int row = blockIdx.y;
-  const int64_t base = int64_t(blockIdx.x) * N;
-  const uint64_t *ir = in + int64_t(row) * count;
+  pdl_wait();  // the lists come from the previous kernel
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t ia = base + 64 * warp + lane, ib = ia + 32;
-  uint64_t a = 0, b = 0;
-  if (ia < count) asm volatile("ld.global.u64 %0, [%1];" : "=l"(a) : "l"(ir + ia) : "memory");
-  if (ib < count) asm volatile("ld.global.u64 %0, [%1];" : "=l"(b) : "l"(ir + ib) : "memory");
-  sort_desc<N>(a, b, sm);
-  if (warp != 0) return;
-  if (index != nullptr) {
-    for (int h = 0; h < 2; ++h) {
-      const int j = lane + 32 * h;
-      if (j >= k) break;
-      const uint64_t key = h ? b : a;
-      const uint32_t id = ~uint32_t(key & 0xFFFFFFFFull);
-      float v = __int_as_float(0x7fffffff);
-      if (QDQ_GUARD(id < uint32_t(n), QDQ_CHECK_ROW))
-        asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(logits + int64_t(row) * n + id) : "memory");
-      index[int64_t(row) * k + j] = int(id);
-      value[int64_t(row) * k + j] = v;
+  const int row = blockIdx.y;
+  const int c = blockIdx.x * 32 + warp;  // this warp's list: positions lane, lane + 32 (key 0 past k)
+  uint64_t ta = 0ull, tb = 0ull;
+  if (c < nlists) {
+    const uint64_t *p = in + (int64_t(row) * nlists + c) * k;
+    if (lane < k) asm volatile("ld.global.u64 %0, [%1];" : "=l"(ta) : "l"(p + lane) : "memory");
+    if (lane + 32 < k) asm volatile("ld.global.u64 %0, [%1];" : "=l"(tb) : "l"(p + lane + 32) : "memory");
+  }
+  for (int half = 16; half >= 1; half >>= 1) {
+    if (warp >= half && warp < 2 * half) {
+      sl[warp - half][lane] = ta;
+      sl[warp - half][lane + 32] = tb;
     }
-  } else {
+    __syncthreads();
+    if (warp < half) warp_top64_merge(ta, tb, sl[warp][lane], sl[warp][lane + 32], lane);
+    __syncthreads();
+  }
+  if (warp != 0) return;
+  if (index == nullptr) {
     uint64_t *o = out + (int64_t(row) * gridDim.x + blockIdx.x) * k;
-    if (lane < k) o[lane] = a;
-    if (lane + 32 < k) o[lane + 32] = b;
+    if (lane < k) o[lane] = ta;
+    if (lane + 32 < k) o[lane + 32] = tb;
+    return;
+  }
+  for (int h = 0; h < 2; ++h) {
+    const int j = lane + 32 * h;
+    if (j >= k) break;
+    const uint64_t key = h ? tb : ta;
+    const uint32_t id = ~uint32_t(key & 0xFFFFFFFFull);
+    float v = __int_as_float(0x7fffffff);
+    if (QDQ_GUARD(id < uint32_t(n), QDQ_CHECK_ROW))
+      asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(logits + int64_t(row) * n + id) : "memory");
+    index[int64_t(row) * k + j] = int(id);
+    value[int64_t(row) * k + j] = v;
   }
 }
 
 int64_t chunks1(int n) { return (int64_t(n) + kChunk1 - 1) / kChunk1; }
-
-template <int N>
-cudaError_t launch_merge(int m, int batch, cudaStream_t s, const uint64_t *in, int count, int k, uint64_t *out,
-                         const float *logits, int n, int *index, float *value) {
-  return launch(topk_merge_kernel<N>, dim3(m, batch), dim3(N / 2), 0, s, in, count, k, out, logits, n, index, value);
-}
 
 }  // namespace
 
@@ -172,28 +178,23 @@ size_t topk_workspace_bytes(int n, int batch, int k) {
 }
 
 namespace {
-// Merge rounds over `count` candidate keys per batch row in buf0 (buf1 the other
-// half of the ping-pong), then the last merge, sized to what is left.
+// Fold rounds over `count` candidate keys (count / k lists) per batch row in buf0, buf1
+// the other half of the ping-pong, down to one CTA per row, which writes the pairs.
 int merge_rounds(int count, int batch, int k, uint64_t *buf0, uint64_t *buf1, const float *logits, int n, int *index,
                  float *value, cudaStream_t s) {
   uint64_t *buf[2] = {buf0, buf1};
-  int cur = 0;
+  int cur = 0, nlists = count / k;
   cudaError_t e = cudaSuccess;
-  while (count > kChunk2) {
-    const int m = (count + kChunk2 - 1) / kChunk2;
-    e = launch_merge<kChunk2>(m, batch, s, buf[cur], count, k, buf[cur ^ 1], nullptr, 0, nullptr, nullptr);
+  while (nlists > 32) {
+    const int m = (nlists + 31) / 32;
+    e = launch(topk_fold_kernel, dim3(m, batch), dim3(1024), 0, s, buf[cur], nlists, k, buf[cur ^ 1],
+               static_cast<const float *>(nullptr), 0, static_cast<int *>(nullptr), static_cast<float *>(nullptr));
     if (e != cudaSuccess) return fail_cuda(e);
-    count = m * k;
+    nlists = m;
     cur ^= 1;
   }
-  // the last merge, sized to the candidates left (at least 64 keys: one warp)
-  const uint64_t *in = buf[cur];
-  if (count <= 64) e = launch_merge<64>(1, batch, s, in, count, k, nullptr, logits, n, index, value);
-  else if (count <= 128) e = launch_merge<128>(1, batch, s, in, count, k, nullptr, logits, n, index, value);
-  else if (count <= 256) e = launch_merge<256>(1, batch, s, in, count, k, nullptr, logits, n, index, value);
-  else if (count <= 512) e = launch_merge<512>(1, batch, s, in, count, k, nullptr, logits, n, index, value);
-  else if (count <= 1024) e = launch_merge<1024>(1, batch, s, in, count, k, nullptr, logits, n, index, value);
-  else e = launch_merge<2048>(1, batch, s, in, count, k, nullptr, logits, n, index, value);
+  e = launch(topk_fold_kernel, dim3(1, batch), dim3(1024), 0, s, buf[cur], nlists, k, static_cast<uint64_t *>(nullptr),
+             logits, n, index, value);
   return e == cudaSuccess ? QDQ_OK : fail_cuda(e);
 }
 }  // namespace
