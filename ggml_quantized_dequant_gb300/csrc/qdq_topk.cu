@@ -4,9 +4,9 @@
 //
 // "QTensorEngine", dispatch_output_topk_chunked: the logits stay on the GPU, a
 // top-k kernel reduces them per chunk, and only the merged K candidates are read
-// back.  The same here: the row is cut into chunks of 1024 logits, each chunk is
-// sorted on chip and keeps its k best; the chunks' sorted lists are then folded
-// 32 at a time by bitonic merges until one list holds the row's k best.
+// back.  The same here: the row is cut into chunks of 1024 logits, each chunk keeps
+// its k best (sorted); the chunks' sorted lists are then folded 32 at a time by
+// bitonic merges until one list holds the row's k best.
 //
 // Order (the k = 1 case is the argmax epilogue): a NaN comes before every number
 // (the first NaN first), then larger values first, equal values (+0 and -0 are
@@ -15,11 +15,10 @@
 // (every NaN to the largest), the low word is the complement of the index.  A
 // chunk past the row's end is padded with key 0, below every real key.
 //
-// The sort is a bitonic network over N keys held two per thread (warp w holds
-// keys 64w .. 64w+63: lane l has 64w + l and 64w + 32 + l).  Exchanges between
-// keys less than 32 apart are warp shuffles, the 32-apart exchange is between a
-// thread's two registers, and only the longer strides go through shared memory
-// with a block barrier: for N = 1024 that is 10 of the network's 55 steps.
+// Sorting is warp-wide only: bitonic networks over 64 keys held two per lane (lane l
+// has positions l and 32 + l; strides below 32 are shuffles, the 32 stride a swap
+// between a lane's two registers), and sorted 64-key lists are combined by bitonic
+// merges, never by a block-wide sort.
 #include "qdq_internal.cuh"
 
 namespace qdq {
@@ -27,69 +26,12 @@ namespace {
 
 constexpr int kChunk1 = 1024;  // logits per first-round chunk
 
-__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
-  const uint32_t lo = __shfl_xor_sync(0xffffffffu, uint32_t(v), m);
-  const uint32_t hi = __shfl_xor_sync(0xffffffffu, uint32_t(v >> 32), m);
-  return (uint64_t(hi) << 32) | lo;
-}
-
-// Compare-exchange of the key at position p with its partner p ^ j in a stage whose
-// direction is descending where (p & k) == 0: the lower position keeps the larger
-// key in a descending run (the smaller in an ascending one).
-__device__ __forceinline__ uint64_t cmpx(uint64_t mine, uint64_t other, int p, int j, int k) {
-  const bool lower = (p & j) == 0, desc = (p & k) == 0;
-  const bool take_max = lower == desc;
-  return take_max ? (mine > other ? mine : other) : (mine < other ? mine : other);
-}
-
-// Sorts the N keys held in (a, b) by the CTA's N / 2 threads into descending
-// order; `sm` is N keys of shared memory.  Every thread of the CTA calls it.
-template <int N>
-__device__ __forceinline__ void sort_desc(uint64_t &a, uint64_t &b, uint64_t *sm) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pa = 64 * warp + lane, pb = pa + 32;  // positions of a and b
-  for (int k = 2; k <= N; k <<= 1) {
-    int j = k >> 1;
-    if (j >= 64) {  // strides across warps: through shared memory
-      sm[pa] = a;
-      sm[pb] = b;
-      __syncthreads();
-      for (; j >= 64; j >>= 1) {
-        for (int i = threadIdx.x; i < N / 2; i += N / 2) {
-          const int x = 2 * i - (i & (j - 1));  // i with a zero bit inserted at bit log2(j)
-          const int y = x + j;
-          const uint64_t kx = sm[x], ky = sm[y];
-          const bool desc = (x & k) == 0;
-          if ((kx < ky) == desc) {
-            sm[x] = ky;
-            sm[y] = kx;
-          }
-        }
-        __syncthreads();
-      }
-      a = sm[pa];
-      b = sm[pb];
-      __syncthreads();  // the buffer is free again
-    }
-    if (j == 32) {  // between the two registers of a thread
-      const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
-      const bool desc = (pa & k) == 0;
-      a = desc ? hi : lo;
-      b = desc ? lo : hi;
-      j = 16;
-    }
-    for (; j > 0; j >>= 1) {  // within a warp
-      const uint64_t oa = shfl_xor_u64(a, j), ob = shfl_xor_u64(b, j);
-      a = cmpx(a, oa, pa, j, k);
-      b = cmpx(b, ob, pb, j, k);
-    }
-  }
-}
-
-// First pass: chunk blockIdx.x of batch row blockIdx.y -> its k best keys at
-// out[(row * gridDim.x + chunk) * k ...].
+// First pass: chunk blockIdx.x of batch row blockIdx.y -> its k best keys, sorted best
+// first, at out[(row * gridDim.x + chunk) * k ...].  Each of the 16 warps sorts its 64
+// logits (a warp-wide bitonic sort), and the warps' sorted lists are folded pairwise
+// through shared memory as in the merge rounds.
 __global__ void __launch_bounds__(kChunk1 / 2) topk_chunk_kernel(const float *logits, int n, int k, uint64_t *out) {
-  __shared__ uint64_t sm[kChunk1];
+  __shared__ uint64_t sl[kChunk1 / 128][64];
   pdl_launch_dependents();
   pdl_wait();  // the logits come from the previous kernel
   const int row = blockIdx.y;
@@ -102,10 +44,18 @@ __global__ void __launch_bounds__(kChunk1 / 2) topk_chunk_kernel(const float *lo
   if (ib < n) asm volatile("ld.global.f32 %0, [%1];" : "=f"(vb) : "l"(lr + ib) : "memory");
   uint64_t a = ia < n ? topk_key(va, uint32_t(ia)) : 0ull;
   uint64_t b = ib < n ? topk_key(vb, uint32_t(ib)) : 0ull;
-  sort_desc<kChunk1>(a, b, sm);
-  // the k best are positions 0..k-1: warp 0 holds 0..63
-  uint64_t *o = out + (int64_t(row) * gridDim.x + blockIdx.x) * k;
-  if (warp == 0) {
+  warp_sort64_desc(a, b, lane);
+  for (int half = kChunk1 / 128; half >= 1; half >>= 1) {
+    if (warp >= half && warp < 2 * half) {
+      sl[warp - half][lane] = a;
+      sl[warp - half][lane + 32] = b;
+    }
+    __syncthreads();
+    if (warp < half) warp_top64_merge(a, b, sl[warp][lane], sl[warp][lane + 32], lane);
+    __syncthreads();
+  }
+  if (warp == 0) {  // the k best are positions 0..k-1 of warp 0's list
+    uint64_t *o = out + (int64_t(row) * gridDim.x + blockIdx.x) * k;
     if (lane < k) o[lane] = a;
     if (lane + 32 < k) o[lane + 32] = b;
   }
