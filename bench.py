@@ -656,10 +656,10 @@ def measure_rows(torch, qdq, synth, dev, timer, peaks, args):
                                                                         1, K), 4, it4)
     rows["q8_0_logits_top40_3072x128256"] = _row(
         ls, dist, roofline("hbm", bw + 8 * K, ls, hbm, "GB/s", recorded_traffic("q8_0_vocab"),
-                           "gemv_dl_kernel<0, 0, 2> + top-k kernels", src))
+                           "gemv_dl_kernel<0, 4, 2> (top-k epilogue) + topk_fold_kernel rounds", src))
     ls, dist = time_calls(torch, timer, lambda i: qdq.topk_rows(lo, synth.N_VOCAB, 1, K, wsk, ik, vk), 4, it4)
     rows["top40_128256"] = {"us_per_call": ls * 1e6, "us_dist": dist,
-                            "roofline": "n/a (L2-resident logits, latency-bound sort)"}
+                            "roofline": "n/a (L2-resident logits, latency-bound warp sorts and folds)"}
     del WO
 
     # Q6_K output projection 3072 -> 128256 (323 MB, larger than L2)
