@@ -35,9 +35,10 @@
 //              per row, 32 quants and one block scale each, from a
 //              64-byte-swizzled int8 TMA tile; Q4_K: two threads per row, one
 //              32-weight sub-block each, from a dense 32-byte-row TMA tile, with
-//              the row's superblock header fetched once per superblock); for
-//              token tiles up to 64 the same warps round the stage's f32 X tile
-//              to the bf16 B tile.  After the last stage the 16 warps read the
+//              the row's superblock header fetched once per superblock); Q8_0
+//              with token tiles above 64 writes the A tiles into TMEM instead
+//              (tcgen05.st; the MMA reads A from there); for token tiles up to 64
+//              the same warps round the stage's f32 X tile to the bf16 B tile.  After the last stage the 16 warps read the
 //              accumulators out of TMEM and store Y (warp w reads TMEM lanes
 //              32*(w%4).. and every fourth 16-column chunk);
 //   warp 16    TMA producer: weight tile(s) and the activation tile (f32, or
@@ -104,6 +105,25 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// As umma_bf16 with the A operand in TMEM (a_tmem: its first column, lane 0).
+__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// 16 consecutive TMEM columns of this thread's lane (a warp writes its 32 lanes).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
@@ -160,12 +180,18 @@ struct GemmCfg {
   static constexpr uint32_t kXTileBytes = kXF ? uint32_t(N) * BK * 4 * KB : kBTileBytes;
   static constexpr uint32_t kATile = KB * kATileBytes;
   static constexpr uint32_t kLoadSlot = round1k(NA * kQTileBytes + kXTileBytes);
-  static constexpr uint32_t kASlot = round1k(NA * kATile + (kXF ? kBTileBytes : 0u));
+  // Q8_0, token tiles above 64, one weight matrix: the bf16 A tiles live in TMEM, written by
+  // the dequantising warps with tcgen05.st, which leaves shared memory to the load ring (one
+  // more slot at 256-token tiles) and takes the A tiles' traffic off shared memory.  (The
+  // same for Q4_K measured no faster: its rows then need one header load per thread.)
+  static constexpr bool kTA = FMT == kWQ8 && !kXF && NA == 1 && KB == 1;
+  static constexpr uint32_t kASlot = kTA ? 0u : round1k(NA * kATile + (kXF ? kBTileBytes : 0u));
   // the two dequantising groups and the tensor core each hold a slot (two when they are large)
-  static constexpr int kSA = kASlot > 40u * 1024u ? 2 : 3;
+  static constexpr int kSA = kTA ? 3 : (kASlot > 40u * 1024u ? 2 : 3);
   static constexpr int kFit = int((227u * 1024u - 2048u - uint32_t(kSA) * kASlot) / kLoadSlot);
   static constexpr int kSL = kFit > 16 ? 16 : kFit;
-  static constexpr uint32_t kCols = uint32_t(NA * N);
+  static constexpr uint32_t kACol = uint32_t(NA * N);  // kTA: A slot j at columns kACol + 32 j
+  static constexpr uint32_t kCols = kACol + (kTA ? uint32_t(kSA) * 32u : 0u);
   static constexpr uint32_t kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
   static constexpr size_t kRingBytes = size_t(kSL) * kLoadSlot + size_t(kSA) * kASlot;
   static constexpr size_t kPBytes = size_t(NA) * N * BM * 4;  // a split's partial tile (f32)
@@ -321,15 +347,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t b_base = smem_u32(btile(i));
+        if constexpr (C::kTA) {
 #pragma unroll
-        for (int a = 0; a < NA; ++a) {
-          const uint32_t a_base = smem_u32(atile(j, a));
+          for (int k = 0; k < BK / 16; ++k)  // K 16 k .. 16 k + 15: 8 columns of the A slot
+            umma_bf16_ta(tmem, tmem + C::kACol + uint32_t(32 * j + 8 * k), desc_kmajor_sw128(b_base + 32 * k), idesc,
+                         (i | k) != 0);
+        } else {
 #pragma unroll
-          for (int kb = 0; kb < KB; ++kb)
+          for (int a = 0; a < NA; ++a) {
+            const uint32_t a_base = smem_u32(atile(j, a));
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k)
-              umma_bf16(tmem + uint32_t(a * N), desc_kmajor_sw128(a_base + kb * kATileBytes + 32 * k),
-                        desc_kmajor_sw128(b_base + kb * C::kBSub + 32 * k), idesc, (i | kb | k) != 0);
+            for (int kb = 0; kb < KB; ++kb)
+#pragma unroll
+              for (int k = 0; k < BK / 16; ++k)
+                umma_bf16(tmem + uint32_t(a * N), desc_kmajor_sw128(a_base + kb * kATileBytes + 32 * k),
+                          desc_kmajor_sw128(b_base + kb * C::kBSub + 32 * k), idesc, (i | kb | k) != 0);
+          }
         }
         umma_commit(&aempty[j]);  // the A slot (and the B tile in it) is free once these MMAs are done
         if (!C::kXF) umma_commit(&lempty[s]);  // so is the load slot (its B tile)
@@ -371,7 +404,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the end of a stage: every write of the warp fenced for the tensor core, then one arrival
     auto finish_stage = [&](int i) {
       convert_x(i);
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      if constexpr (C::kTA) {
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");  // this thread's A writes are done
+        tc_fence_before();
+      } else {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&aready[i % SA]);
@@ -423,13 +461,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          if constexpr (C::kTA) tc_fence_after();
 #pragma unroll
           for (int a = 0; a < NA; ++a)
 #pragma unroll
             for (int kb = 0; kb < KB; ++kb) {
               const uint8_t *qt = qtile(s, a);
-              uint8_t *at = atile(j, a) + kb * kATileBytes;
+              uint8_t *at = C::kTA ? nullptr : atile(j, a) + kb * kATileBytes;
               const float2 dpair = f2(dsc[a][kb], dsc[a][kb]);
+              uint32_t tw[16];  // kTA: the half's 32 bf16 weights, K order, two per column
 #pragma unroll
               for (int pp = 0; pp < 2; ++pp) {
                 const int part = 2 * half + pp;  // 16 quants: K 16 part .. 16 part + 15 of the sub-block
@@ -444,12 +484,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                   packed[2 * w] = pack_bf16x2(__fmul2_rn(q01, dpair));  // d*q exact in f32, rounded once
                   packed[2 * w + 1] = pack_bf16x2(__fmul2_rn(q23, dpair));
                 }
-                // two 16-byte bf16 chunks (K 16p..16p+7 and 16p+8..16p+15)
-                *reinterpret_cast<uint4 *>(at + row * 128 + (((2 * part) ^ (row & 7)) << 4)) =
-                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                *reinterpret_cast<uint4 *>(at + row * 128 + (((2 * part + 1) ^ (row & 7)) << 4)) =
-                    make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                if constexpr (C::kTA) {
+#pragma unroll
+                  for (int w = 0; w < 8; ++w) tw[8 * pp + w] = packed[w];
+                } else {
+                  // two 16-byte bf16 chunks (K 16p..16p+7 and 16p+8..16p+15)
+                  *reinterpret_cast<uint4 *>(at + row * 128 + (((2 * part) ^ (row & 7)) << 4)) =
+                      make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                  *reinterpret_cast<uint4 *>(at + row * 128 + (((2 * part + 1) ^ (row & 7)) << 4)) =
+                      make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                }
               }
+              // kTA: row = TMEM lane 32 (warp % 4) + lane; K 32 half .. at column 16 half of the slot
+              if constexpr (C::kTA)
+                tmem_st16(tmem + (uint32_t((warp & 3) * 32) << 16) + C::kACol + uint32_t(32 * j + 16 * half), tw);
             }
           finish_stage(i);
         }
