@@ -36,9 +36,9 @@
 //              64-byte-swizzled int8 TMA tile; Q4_K: two threads per row, one
 //              32-weight sub-block each, from a dense 32-byte-row TMA tile, with
 //              the row's superblock header fetched once per superblock); Q8_0
-//              with token tiles above 64 writes the A tiles into TMEM instead
-//              (tcgen05.st; the MMA reads A from there); for token tiles up to 64
-//              the same warps round the stage's f32 X tile to the bf16 B tile.  After the last stage the 16 warps read the
+//              with token tiles of 64 and above writes the A tiles into TMEM
+//              instead (tcgen05.st; the MMA reads A from there); for token tiles up
+//              to 64 the same warps round the stage's f32 X tile to the bf16 B tile.  After the last stage the 16 warps read the
 //              accumulators out of TMEM and store Y (warp w reads TMEM lanes
 //              32*(w%4).. and every fourth 16-column chunk);
 //   warp 16    TMA producer: weight tile(s) and the activation tile (f32, or
@@ -180,12 +180,13 @@ struct GemmCfg {
   static constexpr uint32_t kXTileBytes = kXF ? uint32_t(N) * BK * 4 * KB : kBTileBytes;
   static constexpr uint32_t kATile = KB * kATileBytes;
   static constexpr uint32_t kLoadSlot = round1k(NA * kQTileBytes + kXTileBytes);
-  // Q8_0, token tiles above 64, one weight matrix: the bf16 A tiles live in TMEM, written by
-  // the dequantising warps with tcgen05.st, which leaves shared memory to the load ring (one
-  // more slot at 256-token tiles) and takes the A tiles' traffic off shared memory.  (The
-  // same for Q4_K measured no faster: its rows then need one header load per thread.)
-  static constexpr bool kTA = FMT == kWQ8 && !kXF && NA == 1 && KB == 1;
-  static constexpr uint32_t kASlot = kTA ? 0u : round1k(NA * kATile + (kXF ? kBTileBytes : 0u));
+  // Q8_0, one weight matrix, 64 K per stage (token tiles of 64 and above): the bf16 A tiles
+  // live in TMEM, written by the dequantising warps with tcgen05.st, which leaves shared
+  // memory to the load ring (one more slot at 256-token tiles) and takes the A tiles'
+  // traffic off shared memory.  (The same for Q4_K measured no faster: its rows then need
+  // one header load per thread; at 16 and 32 tokens, 128 K per stage, it measured slower.)
+  static constexpr bool kTA = FMT == kWQ8 && NA == 1 && KB == 1 && (!kXF || N == 64);
+  static constexpr uint32_t kASlot = kTA ? (kXF ? round1k(kBTileBytes) : 0u) : round1k(NA * kATile + (kXF ? kBTileBytes : 0u));
   // the two dequantising groups and the tensor core each hold a slot (two when they are large)
   static constexpr int kSA = kTA ? 3 : (kASlot > 40u * 1024u ? 2 : 3);
   static constexpr int kFit = int((227u * 1024u - 2048u - uint32_t(kSA) * kASlot) / kLoadSlot);
@@ -274,7 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto xtile = [&](int s) { return smem + s * C::kLoadSlot + NA * C::kQTileBytes; };
   auto atile = [&](int j, int a) { return aring + j * C::kASlot + a * C::kATile; };
   // the MMA's B operand of stage i: in the A slot (converted here) or the load slot (TMA)
-  auto btile = [&](int i) { return C::kXF ? aring + (i % SA) * C::kASlot + NA * C::kATile : xtile(i % SL); };
+  auto btile = [&](int i) {
+    return C::kXF ? aring + (i % SA) * C::kASlot + (C::kTA ? 0u : NA * C::kATile) : xtile(i % SL);
+  };
   constexpr int kQBox = int(C::kQRowBytes);  // inner TMA coordinate step of a weight tile per stage
 
   if (threadIdx.x == 0) {
@@ -407,9 +410,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (C::kTA) {
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");  // this thread's A writes are done
         tc_fence_before();
-      } else {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
+      if constexpr (!C::kTA || C::kXF)  // the B tile written here (kXF) or the A tile, for the tensor core
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&aready[i % SA]);
