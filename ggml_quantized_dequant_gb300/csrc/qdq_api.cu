@@ -355,6 +355,8 @@ int qdq_topk_rows(const float *logits, int n, int batch, int k, void *workspace,
                   cudaStream_t stream) {
   const int rc = check_topk(logits, n, batch, k, workspace, index, value);
   if (rc != QDQ_OK) return rc;
+  // k = 1 is the argmax (the same order: NaN first, then larger, then smaller index)
+  if (k == 1) return launch_argmax_rows(logits, n, batch, index, value, stream);
   return launch_topk_rows(logits, n, batch, k, workspace, index, value, stream);
 }
 
@@ -371,6 +373,11 @@ int qdq_q8_0_logits_topk(const void *W, const float *x, float *logits, void *wor
   if (overlaps(workspace, sb, W, wb) || overlaps(workspace, sb, x, xb) || overlaps(index, rb, W, wb) ||
       overlaps(index, rb, x, xb) || overlaps(value, rb, W, wb) || overlaps(value, rb, x, xb))
     return QDQ_ERR_ALIAS;
+  if (k == 1) {  // the argmax epilogue (the same order)
+    rc = launch_q8_0_gemv(W, x, logits, n_vocab, n_in, batch, stream);
+    if (rc != QDQ_OK) return rc;
+    return launch_argmax_rows(logits, n_vocab, batch, index, value, stream);
+  }
   if (batch == 1 && gemv_xs_supported(n_in, 1, 0) && opt_batch1_kernel() == 0 && opt_xs_float_x()) {
     // batch 1: the projection's CTAs write their rows' k best keys as they finish, so the
     // logits are not read back for the first selection; then the merge rounds

@@ -198,12 +198,14 @@ int qdq_q8_0_logits_argmax(const void *W, const float *x, float *logits, int *in
  * 1 <= k <= min(n, QDQ_MAX_TOPK).  workspace: qdq_topk_workspace_bytes(n, batch,
  * k) bytes of caller scratch (16-byte aligned, overwritten; the size depends on
  * the current device).  Outputs and workspace may overlap nothing.  Several
- * kernels on `stream`.
+ * kernels on `stream`; k = 1 is the argmax kernel of qdq_q8_0_logits_argmax (the
+ * same order), one launch, the workspace untouched.
  * qdq_q8_0_logits_topk: the Q8_0 output projection (as qdq_q8_0_logits_argmax)
  * followed by the top-k; logits: batch x n_vocab scratch the caller owns (it
  * receives the logits).  At batch 1 the projection's CTAs write the k best
  * (logit, index) keys of their own rows as they finish, and only merge kernels
- * follow; same results as the separate top-k.
+ * follow; same results as the separate top-k.  k = 1 runs as
+ * qdq_q8_0_logits_argmax.
  */
 #define QDQ_MAX_TOPK 64
 size_t qdq_topk_workspace_bytes(int n, int batch, int k);   /* 0 on bad arguments */

@@ -391,6 +391,37 @@ def test_topk_adversarial_rows(cuda_lib):
     rows.append(r)
     _topk_direct(cuda_lib, np.stack(rows), k)
     _topk_direct(cuda_lib, np.ascontiguousarray(np.stack(rows)[:, :100000]), 33)
+    _topk_direct(cuda_lib, np.stack(rows), 1)
+
+
+def test_top1_is_the_argmax(cuda_lib):
+    # k = 1 takes the argmax kernel: same index and value bits as the argmax entry point and the
+    # stated order on rows whose best entries are NaNs, -0 before +0, ties and -inf only
+    import torch
+    qdq = cuda_lib
+    n = 70001
+    rng = np.random.default_rng(33)
+    rows = [rng.standard_normal(n).astype(np.float32) for _ in range(6)]
+    rows[0][[70000, 40000]] = np.nan
+    rows[1][:] = -1.0
+    rows[1][[5000, 3]] = -0.0
+    rows[1][[60000, 100]] = 0.0
+    rows[2][:] = -np.inf
+    rows[3][[12345, 54321]] = 9.0
+    rows[4][-1] = 50.0
+    lg = np.stack(rows)
+    _topk_direct(qdq, lg, 1)
+    # the fused projection + top-1 against the projection + argmax on the same weights
+    n_vocab, n_in, batch = 5003, 1024, 3
+    wb, x = synth.q8_0_blocks(rng, n_vocab, n_in), synth.activations(rng, batch, n_in)
+    W = qdq.upload_q8_0(wb, n_vocab, n_in)
+    lg1, ix1, vl1 = _topk_case(qdq, W, x, n_vocab, n_in, batch, 1, fused=True)
+    logits = _nan(batch, n_vocab)
+    idx = torch.full((batch,), -1, dtype=torch.int32, device=_dev())
+    val = _nan(batch)
+    qdq.q8_0_logits_argmax(W, _t(x), logits, idx, val, n_vocab, n_in, batch)
+    assert np.array_equal(_np(logits).view(np.uint32), lg1.view(np.uint32))
+    assert np.array_equal(_np(idx), ix1[:, 0]) and np.array_equal(_np(val).view(np.uint32), vl1[:, 0].view(np.uint32))
 
 
 def test_topk_long_rows(cuda_lib):
