@@ -206,19 +206,19 @@ struct GemmCfg {
   static constexpr uint32_t kXTileBytes = kXF ? uint32_t(N) * BK * 4 * KB : kBTileBytes;
   static constexpr uint32_t kATile = KB * kATileBytes;
   static constexpr uint32_t kLoadSlot = round1k(NA * kQTileBytes + kXTileBytes);
-  // Q8_0, one weight matrix, 64 K per stage (token tiles of 64 and above): the bf16 A tiles
-  // live in TMEM, written by the dequantising warps with tcgen05.st, which leaves shared
-  // memory to the load ring (one more slot at 256-token tiles) and takes the A tiles'
-  // traffic off shared memory.  (The same for Q4_K measured no faster: its rows then need
-  // one header load per thread; at 16 and 32 tokens, 128 K per stage, it measured slower.)
-  static constexpr bool kTA = FMT == kWQ8 && NA == 1 && KB == 1 && (!kXF || N == 64);
+  // Q8_0, one weight matrix, token tiles of 32 and of 64 and above: the bf16 A tiles live
+  // in TMEM, written by the dequantising warps with tcgen05.st, which leaves shared memory
+  // to the load ring (one more slot at 256-token tiles, twice the slots at 32) and takes
+  // the A tiles' traffic off shared memory.  (The same for Q4_K measured no faster: its
+  // rows then need one header load per thread; at 16 tokens it measured no faster either.)
+  static constexpr bool kTA = FMT == kWQ8 && NA == 1 && (KB == 1 ? !kXF || N == 64 : N == 32);
   static constexpr uint32_t kASlot = kTA ? (kXF ? round1k(kBTileBytes) : 0u) : round1k(NA * kATile + (kXF ? kBTileBytes : 0u));
   // the two dequantising groups and the tensor core each hold a slot (two when they are large)
   static constexpr int kSA = kTA ? 3 : (kASlot > 40u * 1024u ? 2 : 3);
   static constexpr int kFit = int((227u * 1024u - 2048u - uint32_t(kSA) * kASlot) / kLoadSlot);
   static constexpr int kSL = kFit > 16 ? 16 : kFit;
-  static constexpr uint32_t kACol = uint32_t(NA * N);  // kTA: A slot j at columns kACol + 32 j
-  static constexpr uint32_t kCols = kACol + (kTA ? uint32_t(kSA) * 32u : 0u);
+  static constexpr uint32_t kACol = uint32_t(NA * N);  // kTA: A slot j at columns kACol + 32 KB j
+  static constexpr uint32_t kCols = kACol + (kTA ? uint32_t(kSA) * 32u * KB : 0u);
   static constexpr uint32_t kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
   static constexpr size_t kRingBytes = size_t(kSL) * kLoadSlot + size_t(kSA) * kASlot;
   static constexpr size_t kPBytes = size_t(NA) * N * BM * 4;  // a split's partial tile (f32)
@@ -383,9 +383,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t b_base = smem_u32(btile(i));
         if constexpr (C::kTA) {
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)  // K 16 k .. 16 k + 15: 8 columns of the A slot
-            umma_bf16_ta_if(leader, tmem, tmem + C::kACol + uint32_t(32 * j + 8 * k), desc_kmajor_sw128(b_base + 32 * k),
-                            idesc, (i | k) != 0);
+          for (int kb = 0; kb < KB; ++kb)
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)  // K 16 k .. 16 k + 15 of sub-block kb: 8 columns of the A slot
+              umma_bf16_ta_if(leader, tmem, tmem + C::kACol + uint32_t(32 * KB * j + 32 * kb + 8 * k),
+                              desc_kmajor_sw128(b_base + kb * C::kBSub + 32 * k), idesc, (i | kb | k) != 0);
         } else {
 #pragma unroll
           for (int a = 0; a < NA; ++a) {
@@ -531,7 +533,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               // kTA: row = TMEM lane 32 (warp % 4) + lane; K 32 half .. at column 16 half of the slot
               if constexpr (C::kTA)
-                tmem_st16(tmem + (uint32_t((warp & 3) * 32) << 16) + C::kACol + uint32_t(32 * j + 16 * half), tw);
+                tmem_st16(tmem + (uint32_t((warp & 3) * 32) << 16) + C::kACol + uint32_t(32 * KB * j + 32 * kb + 16 * half),
+                          tw);
             }
           finish_stage(i);
         }

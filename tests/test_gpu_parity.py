@@ -263,7 +263,7 @@ def _gemm_case(qdq, n_out, n_in, M, wb=None, X=None, sample_rows=None, seed=0):
     assert qdq.pipeline_timeouts() == 0
 
 
-@pytest.mark.parametrize("M", [1, 16, 20, 64, 100, 200, 257, 512, 1000])
+@pytest.mark.parametrize("M", [1, 16, 20, 32, 64, 100, 200, 257, 512, 1000])
 def test_q8_0_gemm_batch_parity_small(cuda_lib, M):
     _gemm_case(cuda_lib, 256, 512, M, seed=M)
 
@@ -275,7 +275,7 @@ def test_q8_0_gemm_batch_parity_shapes(cuda_lib, n_out, n_in, M):
 
 
 @pytest.mark.parametrize("kind", [0, 1])
-@pytest.mark.parametrize("M", [16, 64, 512])
+@pytest.mark.parametrize("M", [16, 32, 64, 512])
 def test_q8_0_gemm_batch_full_size_config4(cuda_lib, kind, M):
     n_out, n_in = (8192, 3072) if kind == 0 else (3072, 8192)
     # M = 512: 32 rows from each 256-token tile (every output column, so every weight
