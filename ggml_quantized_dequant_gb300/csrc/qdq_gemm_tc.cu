@@ -247,6 +247,14 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t a) {
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
   return v;
 }
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a)
+               : "memory");
+  return v;
+}
 __device__ __forceinline__ int ld_cluster_s32(uint32_t a) {
   int v;
   asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
@@ -673,31 +681,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (all_ok && C::kPBytes <= C::kRingBytes) {
         const float *P = reinterpret_cast<const float *>(smem);
         const int c_lo = N * z / split, c_hi = N * (z + 1) / split;  // this split's tokens of the tile
-        const int prow = threadIdx.x & (BM - 1);
-        const int erow = tile_n * BM + prow;
+        // warp w takes tokens c_lo + w, c_lo + w + 16, ...; lane l rows 4 l .. 4 l + 3 of the
+        // tile (16-byte loads from every split, all in flight before the sums)
+        const int erow = tile_n * BM + 4 * lane;
         const int m0 = tile_m * N;
         uint32_t base[8];
 #pragma unroll
         for (int r = 0; r < 8; ++r) base[r] = cluster_addr(P, uint32_t(r < split ? r : 0));
 #pragma unroll 1
-        for (int c = c_lo + (threadIdx.x >> 7); c < c_hi; c += kDequantWarps * 32 / BM) {
-          float acc[NA];
+        for (int c = c_lo + warp; c < c_hi; c += kDequantWarps) {
+          float4 acc[NA];
 #pragma unroll
           for (int a = 0; a < NA; ++a) {
-            float v[8];
-            const uint32_t off = uint32_t(((a * N + c) * BM + prow) * 4);
+            float4 v[8];
+            const uint32_t off = uint32_t(((a * N + c) * BM + 4 * lane) * 4);
 #pragma unroll
-            for (int r = 0; r < 8; ++r) v[r] = r < split ? ld_cluster_f32(base[r] + off) : 0.f;
-            acc[a] = 0.f;
+            for (int r = 0; r < 8; ++r) v[r] = r < split ? ld_cluster_f32x4(base[r] + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+            acc[a] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int r = 0; r < 8; ++r)
-              if (r < split) acc[a] += v[r];
+              if (r < split) {
+                acc[a].x += v[r].x;
+                acc[a].y += v[r].y;
+                acc[a].z += v[r].z;
+                acc[a].w += v[r].w;
+              }
           }
           const int m = m0 + c;
-          if (m < M && QDQ_GUARD(erow < n_out, QDQ_CHECK_OUT)) {
-            float y = acc[0];
-            if (NA == 2) y = y / (1.0f + expf(-y)) * acc[NA - 1];
-            g.Y[int64_t(m) * n_out + erow] = y;
+          if (m < M && QDQ_GUARD(erow + 4 <= n_out, QDQ_CHECK_OUT)) {
+            float4 y = acc[0];
+            if (NA == 2) {
+              y.x = y.x / (1.0f + expf(-y.x)) * acc[NA - 1].x;
+              y.y = y.y / (1.0f + expf(-y.y)) * acc[NA - 1].y;
+              y.z = y.z / (1.0f + expf(-y.z)) * acc[NA - 1].z;
+              y.w = y.w / (1.0f + expf(-y.w)) * acc[NA - 1].w;
+            }
+            *reinterpret_cast<float4 *>(g.Y + int64_t(m) * n_out + erow) = y;  // n_out % 128 == 0, Y 16-byte aligned
           }
         }
       } else if (threadIdx.x == 0) {
