@@ -5,7 +5,7 @@
 // "QTensorEngine", dispatch_output_top1_chunked (the output projection plus a
 // GPU block argmax, k = 1, that saves the logits readback).  One cluster of
 // eight CTAs per batch row: each CTA scans an eighth of the row (the logits come
-// from L2, where the projection just wrote them) with eight loads in flight per
+// from L2, where the projection just wrote them) with sixteen loads in flight per
 // thread, reduces it, and CTA 0 of the cluster combines the eight results through
 // distributed shared memory after a cluster barrier.  The first maximal index
 // wins; a NaN counts as larger than every number (the first NaN wins), the
@@ -19,7 +19,7 @@ namespace {
 
 constexpr int kArgmaxThreads = 1024;
 constexpr int kArgmaxCluster = 8;
-constexpr int kUnroll = 8;
+constexpr int kUnroll = 16;
 
 // (value, index) that wins between two candidates
 __device__ __forceinline__ bool better(float a, int ia, float b, int ib) {

@@ -190,14 +190,20 @@ constexpr uint32_t round1k(uint32_t v) { return (v + 1023u) & ~1023u; }
 //   A ring, kSA slots, filled by the dequantising warps:  [ NA bf16 A tiles |
 //     the bf16 B tile when kXF ]  (each A / B tile is KB sub-tiles of 64 K).
 // The load ring is as deep as shared memory allows (up to 16 slots); the A ring
-// only needs to keep the tensor core fed.  kXF (token tiles of 64 or fewer): X
-// arrives as f32 and is rounded to bf16 in the kernel, so no conversion kernel
-// runs before it.  KB = 2 (token tiles of 64 or fewer, n_in % 128 == 0): 128 K
-// per stage, which halves the per-stage barrier and MMA-issue overhead that
-// bounds the small-token pipeline.
+// only needs to keep the tensor core fed.  kXF (token tiles of 16, and of 32 for one
+// weight matrix): X arrives as f32 and is rounded to bf16 in the kernel, so no
+// conversion kernel runs before it; the other tiles load the bf16 X a conversion
+// kernel wrote (at 64 tokens, and 32 for the SwiGLU, the dequantising warps' extra
+// rounding work cost more than that kernel: 6-8 % on those calls).  KB = 2 (the kXF
+// tiles, n_in % 128 == 0): 128 K per stage, which halves the per-stage barrier and
+// MMA-issue overhead that bounds the small-token pipeline.
+// Whether a token tile of N rounds X to bf16 in the kernel (else it loads the bf16 X
+// that x_to_bf16_kernel wrote into the workspace).
+__host__ __device__ constexpr bool x_in_kernel(int N, int NA) { return N == 16 || (N == 32 && NA == 1); }
+
 template <int FMT, int N, int NA, int KB>
 struct GemmCfg {
-  static constexpr bool kXF = N <= 64;
+  static constexpr bool kXF = x_in_kernel(N, NA);
   static_assert(KB == 1 || kXF, "two sub-blocks per stage only with the in-kernel X conversion");
   static constexpr uint32_t kQRowBytes = uint32_t(FMT == kWQ8 ? BK : BK / 2) * KB;  // a weight row's bytes per stage
   static constexpr uint32_t kQTileBytes = BM * kQRowBytes;
@@ -826,7 +832,10 @@ template <int FMT, int NA>
 bool splittable(int N) {
   switch (N) {
     case 16: return GemmCfg<FMT, 16, NA, 2>::kPBytes <= GemmCfg<FMT, 16, NA, 2>::kRingBytes;
-    case 32: return GemmCfg<FMT, 32, NA, 2>::kPBytes <= GemmCfg<FMT, 32, NA, 2>::kRingBytes;
+    case 32: {
+      using C32 = GemmCfg<FMT, 32, NA, x_in_kernel(32, NA) ? 2 : 1>;
+      return C32::kPBytes <= C32::kRingBytes;
+    }
     case 64: return GemmCfg<FMT, 64, NA, 1>::kPBytes <= GemmCfg<FMT, 64, NA, 1>::kRingBytes;
     case 128: return GemmCfg<FMT, 128, NA, 1>::kPBytes <= GemmCfg<FMT, 128, NA, 1>::kRingBytes;
     case 192: return GemmCfg<FMT, 192, NA, 1>::kPBytes <= GemmCfg<FMT, 192, NA, 1>::kRingBytes;
@@ -835,7 +844,7 @@ bool splittable(int N) {
 }
 
 // Launch shape and workspace of one GEMM call (the workspace holds only the bf16
-// copy of X, for token tiles above 64).
+// copy of X, for the token tiles that do not round X in the kernel).
 struct GemmPlan {
   int N, KB, ntile_n, ntile_m, nst;
   int split, st_per;  // K splits (the cluster size along z) and K stages per split
@@ -850,7 +859,7 @@ GemmPlan plan_for(int N, int M, int n_out, int n_in, int sm_count) {
   p.N = N;
   // 64-K sub-blocks per stage: two for token tiles up to 32 (at 64 the larger stage
   // leaves too few load slots and measured slower)
-  p.KB = p.N <= 32 && n_in % (2 * BK) == 0 ? 2 : 1;
+  p.KB = x_in_kernel(p.N, NA) && n_in % (2 * BK) == 0 ? 2 : 1;
   p.ntile_n = n_out / BM;
   p.ntile_m = (M + p.N - 1) / p.N;
   p.nst = n_in / (BK * p.KB);
@@ -862,7 +871,7 @@ GemmPlan plan_for(int N, int M, int n_out, int n_in, int sm_count) {
   while (split > 1 && resident_clusters(split) < tiles) --split;
   p.st_per = (p.nst + split - 1) / split;
   p.split = (p.nst + p.st_per - 1) / p.st_per;  // every split gets at least one stage
-  p.xb_bytes = p.N <= 64 ? 0 : (size_t(M) * n_in * 2 + 255) / 256 * 256;
+  p.xb_bytes = x_in_kernel(p.N, NA) ? 0 : (size_t(M) * n_in * 2 + 255) / 256 * 256;
   return p;
 }
 // Above 128 tokens the token tile is the one of 128, 192 and 256 with the least
@@ -983,7 +992,9 @@ int launch_gemm(const uint8_t *const W[2], const float *X, float *Y, void *ws, i
     case 32: return launch_tile<FMT, 16, NA, 1>(W, X, Y, ws, n_out, n_in, M, p, s, di);
     case 33: return launch_tile<FMT, 16, NA, 2>(W, X, Y, ws, n_out, n_in, M, p, s, di);
     case 64: return launch_tile<FMT, 32, NA, 1>(W, X, Y, ws, n_out, n_in, M, p, s, di);
-    case 65: return launch_tile<FMT, 32, NA, 2>(W, X, Y, ws, n_out, n_in, M, p, s, di);
+    case 65:
+      if constexpr (x_in_kernel(32, NA)) return launch_tile<FMT, 32, NA, 2>(W, X, Y, ws, n_out, n_in, M, p, s, di);
+      return QDQ_ERR_UNSUPPORTED;  // not planned
     case 128: return launch_tile<FMT, 64, NA, 1>(W, X, Y, ws, n_out, n_in, M, p, s, di);
     case 256: return launch_tile<FMT, 128, NA, 1>(W, X, Y, ws, n_out, n_in, M, p, s, di);
     case 384: return launch_tile<FMT, 192, NA, 1>(W, X, Y, ws, n_out, n_in, M, p, s, di);
@@ -994,10 +1005,11 @@ int launch_gemm(const uint8_t *const W[2], const float *X, float *Y, void *ws, i
 }  // namespace
 
 size_t gemm_workspace_bytes(int M, int n_out, int n_in, int na) {
-  // the bf16 copy of X (token tiles above 64, which every M > 128 takes), else 256 bytes reserved
+  // the bf16 copy of X (every token tile but those that round X in the kernel: token_tile(M)
+  // is 16 up to 16 tokens and 32 up to 32), else 256 bytes reserved
   (void)n_out;
-  (void)na;
-  const size_t xb = M > 64 ? (size_t(M) * n_in * 2 + 255) / 256 * 256 : 0;
+  const bool conv = !x_in_kernel(token_tile(M), na);
+  const size_t xb = conv ? (size_t(M) * n_in * 2 + 255) / 256 * 256 : 0;
   return xb > 256 ? xb : 256;
 }
 

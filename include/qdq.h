@@ -272,8 +272,8 @@ int qdq_q4k_ffn_residual_noalloc(const void *Wg, const void *Wu, const void *Wd,
  * Y: M x n_out f32 (16-byte aligned), must not overlap W, X or workspace.
  * workspace: caller-owned scratch of qdq_gemm_batch_workspace_bytes(M, n_out,
  * n_in) bytes (0 when no device can be queried), 256-byte aligned, overwritten
- * with X rounded to bf16 when M > 64 (unused for M <= 64, where the kernel
- * rounds X itself).  K is split across the CTAs of a thread-block cluster when
+ * with X rounded to bf16 when M > 32 (unused for M <= 32, where the kernel
+ * rounds X itself; qdq_q4k_swiglu_batch: M > 16 and M <= 16).  K is split across the CTAs of a thread-block cluster when
  * the output tiles alone cannot fill the SMs; the splits' partial tiles are
  * added in shared memory, in a fixed order.
  * Requires n_in % 64 == 0 (Q4_K: % 256) and n_out % 128 == 0; M >= 1 (tail

@@ -60,9 +60,15 @@ def test_packed_sizes(lib):
     assert lib.qdq_q4k_packed_bytes(4, 300) == 0
     assert lib.qdq_q8_0_packed_bytes(0, 32) == 0
     # the GEMM workspace size needs a device to query: 0 without one, else X in bf16 above
-    # 64 tokens (and a token 256 bytes below)
+    # 32 tokens (the SwiGLU: above 16), and a token 256 bytes below
     ws = lib.qdq_gemm_batch_workspace_bytes(16, 8192, 3072)
     assert ws == 0 or ws == 256
+    ws = lib.qdq_gemm_batch_workspace_bytes(32, 8192, 3072)
+    assert ws == 0 or ws == 256
+    ws = lib.qdq_gemm_batch_workspace_bytes(33, 8192, 3072)
+    assert ws == 0 or ws >= 33 * 3072 * 2
+    ws = lib.qdq_q4k_swiglu_batch_workspace_bytes(17, 8192, 3072)
+    assert ws == 0 or ws >= 17 * 3072 * 2
     ws = lib.qdq_gemm_batch_workspace_bytes(512, 8192, 3072)
     assert ws == 0 or ws >= 512 * 3072 * 2
     assert lib.qdq_gemm_batch_workspace_bytes(0, 8192, 3072) == 0
