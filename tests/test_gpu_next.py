@@ -424,6 +424,44 @@ def test_top1_is_the_argmax(cuda_lib):
     assert np.array_equal(_np(idx), ix1[:, 0]) and np.array_equal(_np(val).view(np.uint32), vl1[:, 0].view(np.uint32))
 
 
+def test_topk_very_long_row(cuda_lib):
+    # 1.5 M logits: 1465 chunk lists, so three merge rounds (46 CTAs, 2, 1); a second row of
+    # equal values (ties by index)
+    rng = np.random.default_rng(34)
+    lg = rng.standard_normal((2, 1_500_001)).astype(np.float32)
+    lg[0, 7::300000] = np.nan
+    lg[1, :] = 1.0
+    _topk_direct(cuda_lib, lg, 64)
+    _topk_direct(cuda_lib, lg, 7)
+
+
+def test_topk_repeated_calls_reuse_the_workspace(cuda_lib):
+    # back-to-back calls (fused projection and separate top-k, different k and row counts)
+    # on one workspace stay exact
+    import torch
+    qdq = cuda_lib
+    rng = np.random.default_rng(35)
+    n_vocab, n_in = 40000, 1024
+    wb, x = synth.q8_0_blocks(rng, n_vocab, n_in), synth.activations(rng, 1, n_in)
+    W = qdq.upload_q8_0(wb, n_vocab, n_in)
+    ws = torch.empty(max(qdq.topk_workspace_bytes(n_vocab, 3, 64), qdq.topk_workspace_bytes(n_vocab, 1, 64)),
+                     dtype=torch.uint8, device=_dev())
+    ws.fill_(0xAB)  # arbitrary scratch contents before the first call
+    lg3 = rng.standard_normal((3, n_vocab)).astype(np.float32)
+    for k in (40, 64, 3, 40):
+        logits = _nan(1, n_vocab)
+        idx = torch.full((1, k), -1, dtype=torch.int32, device=_dev())
+        val = _nan(1, k)
+        qdq.q8_0_logits_topk(W, _t(x), logits, ws, idx, val, n_vocab, n_in, 1, k)
+        lg = _np(logits)
+        assert np.array_equal(_np(idx)[0], _stable_topk(lg[0], k))
+        idx3 = torch.full((3, k), -1, dtype=torch.int32, device=_dev())
+        val3 = _nan(3, k)
+        qdq.topk_rows(_t(lg3), n_vocab, 3, k, ws, idx3, val3)
+        for b in range(3):
+            assert np.array_equal(_np(idx3)[b], _stable_topk(lg3[b], k))
+
+
 def test_topk_long_rows(cuda_lib):
     # 300001 logits: three merge rounds (1024-logit chunks, 2048-key merges), a ragged last chunk
     rng = np.random.default_rng(32)
