@@ -61,6 +61,7 @@ struct DlArgs {
   uint64_t *cand;  // kTopk: the k best keys of each CTA's rows, at cand[cta * k ...]
   int k;
   int key_off;     // kTopk: floats from the start of shared memory to the rows' keys (8-byte aligned)
+  int fold_off;    // kTopk: ... to the warps' candidate lists (64 keys for each warp but the first)
 };
 
 // The columns one lane owns: Q4_K / Q6_K block `bq`; Q8_0 half `h` of blocks qa and qb.
@@ -419,17 +420,27 @@ __global__ void __launch_bounds__(32 * (DEPTH == 2 ? kMaxWarpsDepth2 : kMaxWarps
     }
   }
   if constexpr (EPI == kTopk) {
-    // the k best keys of this CTA's rows (warp 0: a running top 64 over chunks of 64)
+    // the k best keys of this CTA's rows: warp w keeps a running top 64 over chunks w,
+    // w + warps, ... of 64 keys; warp 0 then merges the other warps' lists
+    __syncthreads();
+    const int nw = int(blockDim.x >> 5);
+    const uint64_t *keys = reinterpret_cast<const uint64_t *>(psum + a.key_off);
+    uint64_t *fold = reinterpret_cast<uint64_t *>(psum + a.fold_off);
+    uint64_t ta = 0, tb = 0;
+    for (int c0 = 64 * warp; c0 < nreal; c0 += 64 * nw) {
+      uint64_t ka = c0 + lane < nreal ? keys[c0 + lane] : 0ull;
+      uint64_t kb = c0 + 32 + lane < nreal ? keys[c0 + 32 + lane] : 0ull;
+      warp_sort64_desc(ka, kb, lane);
+      warp_top64_merge(ta, tb, ka, kb, lane);
+    }
+    if (warp > 0) {
+      fold[(warp - 1) * 64 + lane] = ta;
+      fold[(warp - 1) * 64 + lane + 32] = tb;
+    }
     __syncthreads();
     if (warp == 0) {
-      const uint64_t *keys = reinterpret_cast<const uint64_t *>(psum + a.key_off);
-      uint64_t ta = 0, tb = 0;
-      for (int c0 = 0; c0 < nreal; c0 += 64) {
-        uint64_t ka = c0 + lane < nreal ? keys[c0 + lane] : 0ull;
-        uint64_t kb = c0 + 32 + lane < nreal ? keys[c0 + 32 + lane] : 0ull;
-        warp_sort64_desc(ka, kb, lane);
-        warp_top64_merge(ta, tb, ka, kb, lane);
-      }
+      for (int w = 1; w < nw && 64 * w < nreal; ++w)
+        warp_top64_merge(ta, tb, fold[(w - 1) * 64 + lane], fold[(w - 1) * 64 + lane + 32], lane);
       uint64_t *o = a.cand + int64_t(blockIdx.x) * a.k;
       if (lane < a.k) o[lane] = ta;
       if (lane + 32 < a.k) o[lane + 32] = tb;
@@ -451,10 +462,12 @@ int launch_dl_depth(DlArgs a, cudaStream_t s, const DeviceInfo &di, int *grid_ou
   const int units = (a.n_out + kRowsPerStage - 1) / kRowsPerStage;
   auto kern = gemv_dl_kernel<FMT, EPI, DEPTH>;
   auto psum_bytes = [&](int grid) { return size_t((units + grid - 1) / grid * kRowsPerStage) * kV * a.wpr * 4; };
-  // kTopk: the rows' keys after the row totals (8-byte aligned)
+  // kTopk: the rows' keys after the row totals (8-byte aligned), then the warps' lists
   auto smem_bytes = [&](int grid) {
     const size_t p = psum_bytes(grid);
-    return EPI == kTopk ? (p + 7) / 8 * 8 + size_t((units + grid - 1) / grid * kRowsPerStage) * 8 : p;
+    return EPI == kTopk ? (p + 7) / 8 * 8 + size_t((units + grid - 1) / grid * kRowsPerStage) * 8 +
+                              size_t(threads / 32 - 1) * 64 * 8
+                        : p;
   };
   int per_sm = ctas_per_sm_or(0);
   if (per_sm == 0) {
@@ -475,6 +488,7 @@ int launch_dl_depth(DlArgs a, cudaStream_t s, const DeviceInfo &di, int *grid_ou
   const size_t smem = smem_bytes(grid);
   a.psum_cap = int(psum_bytes(grid) / sizeof(float));
   a.key_off = int((psum_bytes(grid) + 7) / 8 * 2);
+  a.fold_off = a.key_off + (units + grid - 1) / grid * kRowsPerStage * 2;
   if (grid_out) *grid_out = grid;
   // L2 prefetch of the CTA's rows: off unless QDQ_OPT_L2_PREFETCH = 1 (measured no faster here)
   a.prefetch = opt_l2_prefetch() == 1 ? 1 : 0;
