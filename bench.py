@@ -65,14 +65,19 @@ KERNEL_SOURCES = {
 
 
 def kernel_sources_digest(case: str) -> str:
-    """sha256 over the CUDA sources of one profiled kernel, in the listed order."""
+    """sha256 over the code of the CUDA sources of one profiled kernel, in the listed order:
+    comments and layout are left out, so that a comment edit keeps the recorded counters."""
     import hashlib
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ggml_quantized_dequant_gb300", "csrc")
     for name in KERNEL_SOURCES[case]:
         h.update(name.encode())
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()
 
 

@@ -16,8 +16,8 @@
 // Computation (per output element):  Y[m, r] = sum_k bf16(X[m, k]) * bf16(w[r, k])
 // with f32 accumulation, w the exact f32 dequantised weight (Q8_0: d*q;
 // Q4_K: RN(d*sc*q - dmin*m), one FMA) rounded once to bf16; X is rounded once to
-// bf16 (inside the GEMM for token tiles up to 64, else by a small conversion
-// kernel that runs first).
+// bf16 (inside the GEMM for token tiles of 16, and of 32 with one weight matrix,
+// else by a small conversion kernel that runs first).
 //
 // Tiling ("swap AB"): the MMA's M dimension is 128 weight rows (n_out), its N
 // dimension is the token tile (16..256), K steps by 64 or 128 per pipeline
@@ -36,11 +36,12 @@
 //              64-byte-swizzled int8 TMA tile; Q4_K: two threads per row, one
 //              32-weight sub-block each, from a dense 32-byte-row TMA tile, with
 //              the row's superblock header fetched once per superblock); Q8_0
-//              with token tiles of 64 and above writes the A tiles into TMEM
-//              instead (tcgen05.st; the MMA reads A from there); for token tiles up
-//              to 64 the same warps round the stage's f32 X tile to the bf16 B tile.  After the last stage the 16 warps read the
-//              accumulators out of TMEM and store Y (warp w reads TMEM lanes
-//              32*(w%4).. and every fourth 16-column chunk);
+//              with token tiles of 32 and of 64 and above writes the A tiles into
+//              TMEM instead (tcgen05.st; the MMA reads A from there); for the
+//              tiles that round X in the kernel the same warps round the stage's
+//              f32 X tile to the bf16 B tile.  After the last stage the 16 warps
+//              read the accumulators out of TMEM and store Y (warp w reads TMEM
+//              lanes 32*(w%4).. and every fourth 16-column chunk);
 //   warp 16    TMA producer: weight tile(s) and the activation tile (f32, or
 //              bf16 with the 128-byte swizzle for larger token tiles) per stage,
 //              into a load ring as deep as shared memory allows;
