@@ -241,7 +241,7 @@ def _tile_sample(M, seed):
 
 @pytest.mark.parametrize("n_out,n_in,M", [(256, 512, 1), (256, 512, 16), (256, 512, 20), (256, 512, 64),
                                           (256, 512, 100), (256, 512, 257), (384, 1024, 33), (128, 256, 16),
-                                          (1024, 2048, 130), (512, 768, 300)])
+                                          (1024, 2048, 130), (512, 768, 300), (128, 256, 40), (128, 768, 32)])
 def test_q4k_gemm_batch_parity(cuda_lib, n_out, n_in, M):
     rng = np.random.default_rng(n_out + n_in + M)
     wb, X = synth.q4k_blocks(rng, n_out, n_in), synth.activations(rng, M, n_in)
@@ -339,7 +339,8 @@ def _swiglu_batch_bound(s, rel=4e-3):
 
 
 @pytest.mark.parametrize("n_ff,n_embd,M", [(512, 256, 20), (1024, 512, 130), (256, 1024, 1), (8192, 3072, 64),
-                                           (1024, 512, 192), (3072, 1024, 600)])
+                                           (1024, 512, 192), (3072, 1024, 600), (256, 256, 17), (384, 768, 32),
+                                           (128, 256, 16)])
 def test_q4k_swiglu_batch_parity(cuda_lib, n_ff, n_embd, M):
     import torch
     qdq = cuda_lib

@@ -269,7 +269,7 @@ def test_q8_0_gemm_batch_parity_small(cuda_lib, M):
 
 
 @pytest.mark.parametrize("n_out,n_in,M", [(384, 1024, 33), (128, 64, 16), (1024, 2048, 130), (256, 320, 40),
-                                           (128, 448, 17), (512, 192, 300)])
+                                           (128, 448, 17), (512, 192, 300), (128, 64, 40), (256, 192, 48)])
 def test_q8_0_gemm_batch_parity_shapes(cuda_lib, n_out, n_in, M):
     _gemm_case(cuda_lib, n_out, n_in, M, seed=n_out + M)
 
