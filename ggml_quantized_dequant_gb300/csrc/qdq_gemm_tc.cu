@@ -531,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
                   float2 q01, q23;
-                  s8x4_to_f2(words[w], mg, q01, q23);
+                  s8x4_to_f2_sel(words[w], mg, q01, q23);
                   packed[2 * w] = pack_bf16x2(__fmul2_rn(q01, dpair));  // d*q exact in f32, rounded once
                   packed[2 * w + 1] = pack_bf16x2(__fmul2_rn(q23, dpair));
                 }
